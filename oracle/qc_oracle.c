@@ -1,0 +1,512 @@
+/*
+ * qc_oracle.c -- plain, slow, scalar CPU oracle for the communication codec.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header, table or constant generator with the CUDA
+ * library; the two are independent restatements of the same method.
+ *
+ * Sources (web pages on quantized communication for distributed training):
+ *   [p1] "Quantized Communication for Distributed Training" (edmondo-vault),
+ *        sections "Where Quantization Sits" and "Numeric Example":
+ *        quantize for the wire, dequantize on the receiver, FP32 -> FP8 payloads
+ *        of embedding lookups (1,000,000 x 128 values).
+ *   [p2] "Gradient quantization for communication" (chipfoundryservices),
+ *        sections "How Gradient Quantization Works" and "Quantization Schemes".
+ *   [p3] "Quantization for Communication" (chipfoundryservices), sections
+ *        "Quantization Schemes" (uniform min/max formulas, stochastic rounding),
+ *        "Quantized SGD Algorithms" (TernGrad, SignSGD majority vote),
+ *        "Error Feedback for Quantization", "Quantization-Aware All-Reduce"
+ *        (accumulate in higher precision), "Hardware Acceleration" (packed words).
+ *   [p4] "Gradient Compression and Quantised Collectives" (praveentn.live),
+ *        sections "Why sparsification fights the all-reduce" (signSGD majority
+ *        vote) and "Error feedback is the component that makes it work".
+ *
+ * Arithmetic: IEEE-754 binary32, round-to-nearest-even, one rounding per
+ * operation as written (build with -ffp-contract=off, never -ffast-math); fp64
+ * only for the sign scheme's mean, as stated there.  Each function takes the
+ * steps of the method in the order the pages give them, element by element in
+ * index order.  Readings taken where the pages are silent are stated at each
+ * step.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_API __attribute__((visibility("default")))
+
+enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2 };
+enum { ORC_ROUND_NEAREST = 0, ORC_ROUND_STOCHASTIC = 1 };
+enum { ORC_DTYPE_F32 = 0, ORC_DTYPE_BF16 = 1 };
+enum { ORC_OUT_MEAN = 1, ORC_ACCUMULATE_INTO_OUT = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10, written from Salmon, Moraes, Dror and Shaw, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3" (SC'11): a 4-word counter and a 2-word key,
+ * ten rounds.  Each round multiplies counter words 0 and 2 by the two round
+ * constants, and builds the new counter from the high halves xor-ed with the
+ * other two counter words and the key, and from the low halves.  Between
+ * rounds the key is bumped by the two Weyl constants (golden ratio and
+ * sqrt(3)-1 in 32-bit fixed point). */
+
+static void orc_mul_hi_lo(uint32_t a, uint32_t b, uint32_t *hi, uint32_t *lo)
+{
+    uint64_t product = (uint64_t)a * (uint64_t)b;
+    *hi = (uint32_t)(product >> 32);
+    *lo = (uint32_t)product;
+}
+
+ORC_API void oracle_philox4x32_10(const uint32_t counter[4], const uint32_t key[2],
+                                  uint32_t out[4])
+{
+    uint32_t x0 = counter[0], x1 = counter[1], x2 = counter[2], x3 = counter[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u; /* Weyl increment, key word 0 */
+            k1 += 0xBB67AE85u; /* Weyl increment, key word 1 */
+        }
+        uint32_t hi0, lo0, hi2, lo2;
+        orc_mul_hi_lo(0xD2511F53u, x0, &hi0, &lo0);
+        orc_mul_hi_lo(0xCD9E8D57u, x2, &hi2, &lo2);
+        uint32_t y0 = hi2 ^ x1 ^ k0;
+        uint32_t y1 = lo2;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0;
+        x1 = y1;
+        x2 = y2;
+        x3 = y3;
+    }
+    out[0] = x0;
+    out[1] = x1;
+    out[2] = x2;
+    out[3] = x3;
+}
+
+/* The uniform draw u_i in [0, 1) used for stochastic rounding of element i.
+ * The pages only say "probabilistic rounding"; the reading taken here is:
+ *   key     = (low 32 bits of seed, high 32 bits of seed)
+ *   counter = (low 32 of i/4, high 32 of i/4, step, 0)
+ *   u_i     = (word (i mod 4) of the Philox output >> 8) * 2^-24   (exact)
+ * so one Philox call serves four consecutive elements and the draw depends only
+ * on (seed, step, global element index). */
+ORC_API float oracle_uniform(uint64_t seed, uint32_t step, uint64_t index)
+{
+    uint64_t block = index >> 2;
+    uint32_t counter[4] = {(uint32_t)block, (uint32_t)(block >> 32), step, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    oracle_philox4x32_10(counter, key, r);
+    return (float)(r[index & 3u] >> 8) * 0x1p-24f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Helpers with no codec arithmetic in them. */
+
+static float orc_load_grad(const void *grad, int dtype, size_t i)
+{
+    if (dtype == ORC_DTYPE_F32)
+        return ((const float *)grad)[i];
+    /* bf16 -> fp32 is an exact widening: the 16 bits are the top half. */
+    uint32_t bits = (uint32_t)((const uint16_t *)grad)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* After a min/max reduction a zero result is taken as +0 (the pages are
+ * silent on signed zero; this makes the reduction's result unique). */
+static float orc_positive_zero(float r)
+{
+    return (r == 0.0f) ? 0.0f : r;
+}
+
+static int orc_valid_bucket(size_t bucket)
+{
+    return bucket >= 32 && bucket % 32 == 0;
+}
+
+/* Packing (p3 "Hardware Acceleration", packed formats): code i of a b-bit
+ * stream goes to word i / (32/b) at bit offset (i mod (32/b)) * b, least
+ * significant bits first (bit order within a word: a reading). */
+static void orc_put_code(uint32_t *words, size_t i, int bits, uint32_t code)
+{
+    size_t per_word = (size_t)(32 / bits);
+    words[i / per_word] |= code << ((i % per_word) * (size_t)bits);
+}
+
+static uint32_t orc_get_code(const uint32_t *words, size_t i, int bits)
+{
+    size_t per_word = (size_t)(32 / bits);
+    uint32_t mask = (bits == 32) ? 0xFFFFFFFFu : ((1u << bits) - 1u);
+    return (words[i / per_word] >> ((i % per_word) * (size_t)bits)) & mask;
+}
+
+ORC_API size_t oracle_code_words(size_t n, int bits)
+{
+    return (n * (size_t)bits + 31) / 32;
+}
+
+ORC_API size_t oracle_num_buckets(size_t n, size_t bucket)
+{
+    return (n + bucket - 1) / bucket;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Uniform min/max quantization with optional error feedback.
+ *
+ * p3 "Quantization Schemes": scale = (max - min) / (2^bits - 1),
+ * q = round((x - min) / scale), x ~= q * scale + min; stochastic rounding takes
+ * floor((x - min)/scale) with probability 1 - frac and the ceiling with
+ * probability frac.  p3 "Error Feedback for Quantization" and p4 "Error
+ * feedback ...": e = e + grad; q = quantize(e); e = e - dequantize(q).
+ *
+ * Per bucket k of `bucket` elements (the last may be partial):
+ *   p_i   = e_i + g_i                 (or g_i without error feedback)
+ *   mn, mx = min p, max p             (zero taken as +0)
+ *   scale = (mx - mn) / L,  L = 2^bits - 1          (IEEE division)
+ *   scale == 0  -> q_i = 0            (constant bucket: a reading)
+ *   t_i   = (p_i - mn) / scale
+ *   nearest:    q_i = min(rint(t_i), L)             (ties to even: a reading)
+ *   stochastic: q_i = min(floor(t_i) + [u_i < t_i - floor(t_i)], L)
+ *   deq_i = fma(q_i, scale, mn)       (one rounding: a reading)
+ *   e_i   = p_i - deq_i
+ * Outputs: packed codes, scale[k], offset[k] = mn.
+ *
+ * `index_base` is the global index of element 0 of this slice (it must start
+ * on a bucket boundary); the stochastic draw uses global indices, so a slice
+ * reproduces exactly the corresponding part of a whole-array call. */
+ORC_API int oracle_encode_uniform(const void *grad, int dtype, float *err, size_t n,
+                                  uint64_t index_base, int bits, size_t bucket, int mode,
+                                  uint64_t seed, uint32_t step, uint32_t *codes,
+                                  float *scale_out, float *offset_out)
+{
+    if (!(bits == 1 || bits == 2 || bits == 4 || bits == 8) || !orc_valid_bucket(bucket))
+        return -1;
+    const uint32_t L = (1u << bits) - 1u;
+    const float Lf = (float)L;
+    memset(codes, 0, oracle_code_words(n, bits) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    if (!p)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+        }
+        float mn = p[0], mx = p[0];
+        for (size_t j = 1; j < cnt; ++j) {
+            if (p[j] < mn)
+                mn = p[j];
+            if (p[j] > mx)
+                mx = p[j];
+        }
+        mn = orc_positive_zero(mn);
+        mx = orc_positive_zero(mx);
+        float range = mx - mn;
+        float scale = range / Lf;
+        for (size_t j = 0; j < cnt; ++j) {
+            uint32_t q = 0;
+            if (scale != 0.0f) {
+                float diff = p[j] - mn;
+                float t = diff / scale;
+                float level;
+                if (mode == ORC_ROUND_NEAREST) {
+                    level = rintf(t);
+                } else {
+                    float f = floorf(t);
+                    float frac = t - f;
+                    float u = oracle_uniform(seed, step, index_base + lo + j);
+                    level = (u < frac) ? f + 1.0f : f;
+                }
+                if (!(level >= 0.0f)) /* non-finite input: unspecified, never UB */
+                    level = 0.0f;
+                q = (level > Lf) ? L : (uint32_t)level;
+            }
+            orc_put_code(codes, lo + j, bits, q);
+            if (err) {
+                float deq = fmaf((float)q, scale, mn);
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = scale;
+        offset_out[k] = mn;
+    }
+    free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scaled sign (1-bit) with error feedback.
+ *
+ * p3 "Quantized SGD Algorithms" (SignSGD: the sign only) and "Bit-Width
+ * Selection" (1-bit with error feedback); p4 (signSGD, error feedback).
+ * The per-bucket magnitude s is the mean of |p| (a reading: the scaled-sign
+ * form whose dequantized bucket keeps the l1 mass):
+ *   p_i  = e_i + g_i
+ *   s    = (sum over the bucket of |p_i|, in fp64, index order) / cnt,
+ *          rounded once to fp32
+ *   bit_i = [p_i >= 0]                 (sign(0) = +1: a reading)
+ *   deq_i = bit_i ? s : -s ;  e_i = p_i - deq_i
+ * Outputs: 32 sign bits per word, scale[k] = s. */
+ORC_API int oracle_encode_sign(const void *grad, int dtype, float *err, size_t n, size_t bucket,
+                               uint32_t *codes, float *scale_out)
+{
+    if (!orc_valid_bucket(bucket))
+        return -1;
+    memset(codes, 0, oracle_code_words(n, 1) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    if (!p)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+        }
+        double sum = 0.0;
+        for (size_t j = 0; j < cnt; ++j)
+            sum += fabs((double)p[j]);
+        float s = (float)(sum / (double)cnt);
+        for (size_t j = 0; j < cnt; ++j) {
+            uint32_t bit = (p[j] >= 0.0f) ? 1u : 0u;
+            orc_put_code(codes, lo + j, 1, bit);
+            if (err) {
+                float deq = bit ? s : -s;
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = s;
+    }
+    free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* TernGrad ternary {-1, 0, +1} with a per-bucket scale.
+ *
+ * p3 "Quantized SGD Algorithms": TernGrad quantizes to {-1, 0, +1} with a scale
+ * factor.  The stochastic rule is the named method's (keep the sign with
+ * probability |p|/s, s = max |p|); the deterministic variant keeps it when
+ * |p|/s > 1/2.  Codes {-1, 0, +1} -> {0, 1, 2} in 2 bits (a reading).
+ *   s = max |p| (+0 for an all-zero bucket; then every code is 1)
+ *   pr_i = |p_i| / s ;  keep_i = stochastic ? [u_i < pr_i] : [pr_i > 1/2]
+ *   code_i = keep_i ? (p_i > 0 ? 2 : 0) : 1 ;  deq_i = (code_i - 1) * s
+ *   e_i = p_i - deq_i (with error feedback)
+ * Outputs: 16 codes per word, scale[k] = s. */
+ORC_API int oracle_encode_ternary(const void *grad, int dtype, float *err, size_t n,
+                                  uint64_t index_base, size_t bucket, int mode, uint64_t seed,
+                                  uint32_t step, uint32_t *codes, float *scale_out)
+{
+    if (!orc_valid_bucket(bucket))
+        return -1;
+    memset(codes, 0, oracle_code_words(n, 2) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    if (!p)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+        }
+        float s = 0.0f;
+        for (size_t j = 0; j < cnt; ++j) {
+            float a = fabsf(p[j]);
+            if (a > s)
+                s = a;
+        }
+        s = orc_positive_zero(s);
+        for (size_t j = 0; j < cnt; ++j) {
+            uint32_t code = 1;
+            if (s != 0.0f) {
+                float pr = fabsf(p[j]) / s;
+                int keep;
+                if (mode == ORC_ROUND_NEAREST)
+                    keep = pr > 0.5f;
+                else
+                    keep = oracle_uniform(seed, step, index_base + lo + j) < pr;
+                if (keep)
+                    code = (p[j] > 0.0f) ? 2u : 0u;
+            }
+            orc_put_code(codes, lo + j, 2, code);
+            if (err) {
+                float deq = (float)((int)code - 1) * s;
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = s;
+    }
+    free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Receiver side: dequantize M workers' payloads and accumulate in fp32.
+ *
+ * p1 "Where Quantization Sits" (receive, dequantize, continue); p2 "How
+ * Gradient Quantization Works" (dequantize, then average or sum); p3
+ * "Quantization-Aware All-Reduce" (dequantize after the exchange; accumulate
+ * in higher precision).  For every element i (bucket k = i / bucket):
+ *   acc = +0
+ *   for w = 0 .. M-1 in this order:
+ *       d = uniform: fma(q, scale_w[k], offset_w[k])
+ *           sign:    bit ? s_w[k] : -s_w[k]
+ *           ternary: (code - 1) * s_w[k]
+ *       acc = acc + d
+ *   r = mean ? acc / M : acc ;  out_i = accumulate ? out_i + r : r
+ * Worker w's codes start at codes + w*codes_stride_words and its metadata at
+ * scale/offset + w*meta_stride. */
+ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
+                                     const float *scale, const float *offset,
+                                     size_t meta_stride, int M, size_t n, int bits,
+                                     size_t bucket, int scheme, float *out, int flags)
+{
+    if (M < 1 || !orc_valid_bucket(bucket))
+        return -1;
+    if (scheme == ORC_SCHEME_UNIFORM && !(bits == 1 || bits == 2 || bits == 4 || bits == 8))
+        return -1;
+    if (scheme == ORC_SCHEME_SIGN && bits != 1)
+        return -1;
+    if (scheme == ORC_SCHEME_TERNARY && bits != 2)
+        return -1;
+    for (size_t i = 0; i < n; ++i) {
+        size_t k = i / bucket;
+        float acc = 0.0f;
+        for (int w = 0; w < M; ++w) {
+            const uint32_t *cw = codes + (size_t)w * codes_stride_words;
+            uint32_t q = orc_get_code(cw, i, bits);
+            float s = scale[(size_t)w * meta_stride + k];
+            float d;
+            if (scheme == ORC_SCHEME_UNIFORM)
+                d = fmaf((float)q, s, offset[(size_t)w * meta_stride + k]);
+            else if (scheme == ORC_SCHEME_SIGN)
+                d = q ? s : -s;
+            else
+                d = (float)((int)q - 1) * s;
+            acc = acc + d;
+        }
+        float r = (flags & ORC_OUT_MEAN) ? acc / (float)M : acc;
+        out[i] = (flags & ORC_ACCUMULATE_INTO_OUT) ? out[i] + r : r;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* signSGD majority vote (p3 "Quantized SGD Algorithms"; p4 "Why sparsification
+ * fights the all-reduce"): out bit i = [2 * (number of workers with bit i set)
+ * >= M].  A tie (even M) gives 1, matching sign(0) = +1 (a reading).  Bits past
+ * n in the last word are 0. */
+ORC_API int oracle_sign_vote(const uint32_t *signs, size_t stride_words, int M, size_t n,
+                             uint32_t *out)
+{
+    if (M < 1)
+        return -1;
+    memset(out, 0, oracle_code_words(n, 1) * sizeof(uint32_t));
+    for (size_t i = 0; i < n; ++i) {
+        long count = 0;
+        for (int w = 0; w < M; ++w)
+            count += (long)orc_get_code(signs + (size_t)w * stride_words, i, 1);
+        if (2 * count >= (long)M)
+            orc_put_code(out, i, 1, 1u);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 (OCP 8-bit floating point, E4M3 variant): sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; the
+ * largest finite magnitude is 1.75 * 2^8 = 448; exponent field 0 encodes the
+ * subnormals m * 2^-9. */
+
+ORC_API float oracle_e4m3_to_f32(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    float v;
+    if (e == 0xF && m == 0x7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexpf((float)m, -9);
+    else
+        v = ldexpf((float)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* fp32 -> E4M3 with round-to-nearest-even and saturation to +-448 for finite
+ * values beyond range ("satfinite"); NaN -> NaN.  The magnitude is written as
+ * a multiple of its binade's quantum (2^(E-3) for normal binades, 2^-9 below
+ * 2^-6), rounded to the nearest even multiple; a rounding carry into the next
+ * binade lands on the next code because codes are ordered like magnitudes. */
+ORC_API uint8_t oracle_e4m3_from_f32(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x))
+        return (uint8_t)(sign | 0x7F);
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    frexp(a, &e2); /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;
+    if (E < -6) {
+        double m = rint(a / ldexp(1.0, -9)); /* 0 .. 8 */
+        return (uint8_t)(sign | (int)m);
+    }
+    double m = rint(a / ldexp(1.0, E - 3)); /* 8 .. 16 */
+    int code = ((E + 7) << 3) + ((int)m - 8);
+    if (code > 0x7E)
+        code = 0x7E;
+    return (uint8_t)(sign | code);
+}
+
+/* Row-wise FP8 quantization of an N x D fp32 payload (p1 "Numeric Example" and
+ * "Pinterest QComms Example": embedding lookup payloads go FP32 -> FP8 before
+ * the collective).  Per row r (a reading: absmax scaling onto E4M3's range):
+ *   a = max |x_rj| (+0)   sc = a / 448
+ *   sc == 0 -> codes 0, row_scale = 0
+ *   else code_rj = e4m3(x_rj / sc), row_scale = sc
+ * Codes are row-major bytes; the fp32 scales are a separate array. */
+ORC_API int oracle_rowwise_fp8(const float *x, size_t rows, size_t dim, uint8_t *codes,
+                               float *row_scale)
+{
+    for (size_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * dim;
+        float a = 0.0f;
+        for (size_t j = 0; j < dim; ++j) {
+            float v = fabsf(xr[j]);
+            if (v > a)
+                a = v;
+        }
+        a = orc_positive_zero(a);
+        float sc = a / 448.0f;
+        for (size_t j = 0; j < dim; ++j)
+            codes[r * dim + j] = (sc == 0.0f) ? 0 : oracle_e4m3_from_f32(xr[j] / sc);
+        row_scale[r] = sc;
+    }
+    return 0;
+}
+
+/* Receiver side of the FP8 payload: x_rj ~= e4m3_value(code_rj) * sc_r
+ * (p1 "Where Quantization Sits": dequantize on receipt). */
+ORC_API int oracle_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, size_t rows,
+                                       size_t dim, float *out)
+{
+    for (size_t r = 0; r < rows; ++r)
+        for (size_t j = 0; j < dim; ++j)
+            out[r * dim + j] = oracle_e4m3_to_f32(codes[r * dim + j]) * row_scale[r];
+    return 0;
+}

@@ -1,0 +1,566 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No GPU.  Every check here is independent of the oracle's own code: published
+known-answer vectors, the pages' byte counts and ratios, closed forms on hand-built
+buckets, exact rational arithmetic, brute force on tiny inputs, invariants and
+statistical tests of unbiasedness.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as orc
+import workloads as wl
+from tests._exact import dist_to_half_integer, frac, round_half_even, to_f32, ulp32
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _read_golden(golden_dir, name):
+    rows = []
+    with open(os.path.join(golden_dir, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _unpack(words, n, bits):
+    per = 32 // bits
+    out = []
+    for i in range(n):
+        out.append((int(words[i // per]) >> ((i % per) * bits)) & ((1 << bits) - 1))
+    return out
+
+
+def _pack(codes, bits):
+    per = 32 // bits
+    words = [0] * ((len(codes) * bits + 31) // 32)
+    for i, c in enumerate(codes):
+        words[i // per] |= int(c) << ((i % per) * bits)
+    return np.array(words, dtype=np.uint32)
+
+
+# --------------------------------------------------------------------------- Philox
+
+def test_philox_known_answers(golden_dir):
+    rows = _read_golden(golden_dir, "philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(x, 16) for x in r]
+        got = orc.philox4x32_10(v[0:4], v[4:6])
+        assert [int(x) for x in got] == v[6:10]
+
+
+def test_uniform_draw_layout():
+    # The reading: key = seed words, counter = (i/4 low, i/4 high, step, 0),
+    # element i takes output word i mod 4, u = (word >> 8) * 2^-24.
+    for seed, step, idx in [(0, 0, 0), (0, 0, 3), (7, 2, 5), (2 | (5 << 32), 9, (1 << 33) + 6)]:
+        blk = idx >> 2
+        r = orc.philox4x32_10([blk & 0xFFFFFFFF, blk >> 32, step, 0],
+                              [seed & 0xFFFFFFFF, seed >> 32])
+        want = float(int(r[idx & 3]) >> 8) * 2.0 ** -24
+        assert orc.uniform(seed, step, idx) == want
+
+
+def test_uniform_draw_statistics():
+    n = 1 << 16
+    u = np.array([orc.uniform(11, 3, i) for i in range(n)])
+    assert u.min() >= 0.0 and u.max() < 1.0
+    counts, _ = np.histogram(u, bins=64, range=(0.0, 1.0))
+    expected = n / 64
+    chi2 = float(((counts - expected) ** 2 / expected).sum())
+    # 63 degrees of freedom: mean 63, sd ~11.2; 130 is beyond 6 sd.
+    assert chi2 < 130.0
+    # neighbouring draws are uncorrelated
+    c = np.corrcoef(u[:-1], u[1:])[0, 1]
+    assert abs(c) < 5.0 / math.sqrt(n)
+
+
+# --------------------------------------------------------------- sizes and ratios
+
+def test_compression_ratios_pages(golden_dir):
+    rows = _read_golden(golden_dir, "compression_ratios.txt")
+    ratios = {int(r[0]): int(r[1]) for r in rows if r[0].isdigit()}
+    n = 1 << 16
+    for bits, ratio in ratios.items():
+        words = orc.code_words(n, bits)
+        assert (n * 4) / (words * 4) == ratio
+    per_word = [r for r in rows if r[0] == "codes_per_word_4bit"][0]
+    assert 32 // 4 == int(per_word[1])
+    # with one fp32 scale + one fp32 offset per bucket the ratio is slightly lower
+    for bits, ratio in ratios.items():
+        for bucket in (512, 1024, 2048):
+            eff = 32.0 * bucket / (bits * bucket + 64)
+            assert ratio * 0.85 < eff < ratio
+
+
+def test_code_words_and_buckets():
+    assert orc.code_words(0, 8) == 0
+    assert orc.code_words(1, 1) == 1
+    assert orc.code_words(33, 1) == 2
+    assert orc.code_words(250_000_000, 4) == 125_000_000 // 4
+    assert orc.num_buckets(250_000_000, 512) == 488_282
+    assert orc.num_buckets(1 << 20, 2048) == 512
+
+
+# ------------------------------------------------------------ uniform, nearest
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_uniform_ramp_closed_form(bits):
+    L = (1 << bits) - 1
+    bucket = max(32, L + 1)
+    c = 2.0 ** -10
+    base = -3.0
+    levels = [j % (L + 1) for j in range(bucket)]
+    g = np.array([base + lv * c for lv in levels], dtype=np.float32)
+    err = np.zeros_like(g)
+    codes, scale, offset = orc.encode_uniform(g, err, bits=bits, bucket=bucket)
+    assert scale[0] == np.float32(c)
+    assert offset[0] == np.float32(base)
+    assert _unpack(codes, bucket, bits) == levels
+    assert np.array_equal(codes, _pack(levels, bits))
+    assert np.all(err == 0.0)
+
+
+def test_uniform_ties_to_even():
+    bucket = 32
+    vals = [0.0, 255.0, 2.5, 3.5, 100.5, 101.5, 0.5, 254.5] + [7.0] * 24
+    g = np.array(vals, dtype=np.float32)
+    codes, scale, offset = orc.encode_uniform(g, None, bits=8, bucket=bucket)
+    assert scale[0] == 1.0 and offset[0] == 0.0
+    q = _unpack(codes, bucket, 8)
+    assert q[:8] == [0, 255, 2, 4, 100, 102, 0, 254]
+
+
+def test_uniform_constant_bucket():
+    g = np.full(96, np.float32(0.125), dtype=np.float32)
+    g[64:] = np.float32(-2.0)
+    err = np.zeros_like(g)
+    codes, scale, offset = orc.encode_uniform(g, err, bits=4, bucket=64)
+    assert scale[0] == 0.0 and offset[0] == np.float32(0.125)
+    assert scale[1] == 0.0 and offset[1] == np.float32(-2.0)
+    assert not codes.any()
+    assert np.all(err == 0.0)
+
+
+def _tiny_buckets(seed, n, scale=1e-3):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal(n) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_uniform_nearest_level_exact(bits):
+    """Each code is the level nearest to the exact (p - min)/scale."""
+    L = (1 << bits) - 1
+    bucket = 64
+    g = _tiny_buckets(bits, 4 * bucket + 40)   # ragged last bucket
+    n = g.size
+    codes, scale, offset = orc.encode_uniform(g, None, bits=bits, bucket=bucket)
+    q = _unpack(codes, n, bits)
+    for k in range(orc.num_buckets(n, bucket)):
+        seg = g[k * bucket:(k + 1) * bucket]
+        mn, mx = seg.min(), seg.max()
+        assert offset[k] == mn
+        # scale is the binary32 rounding of the binary32 range over L
+        rng32 = to_f32(frac(mx) - frac(mn))
+        assert scale[k] == to_f32(frac(rng32) / L)
+        for j, p in enumerate(seg):
+            t = (frac(p) - frac(mn)) / frac(scale[k])
+            want = min(round_half_even(t), L)
+            got = q[k * bucket + j]
+            if got != want:
+                # only allowed within two roundings of a half-integer
+                assert dist_to_half_integer(t) <= t * Fraction(1, 1 << 22)
+                assert abs(got - want) == 1
+
+
+def test_uniform_invariants_outlier_workload():
+    n, bucket, bits = 1 << 14, 2048, 8
+    g = wl.outlier_gradient(n, seed=0)
+    e0 = np.zeros(n, dtype=np.float32)
+    err = e0.copy()
+    codes, scale, offset = orc.encode_uniform(g, err, bits=bits, bucket=bucket)
+    q = np.array(_unpack(codes, n, bits))
+    for k in range(n // bucket):
+        s = slice(k * bucket, (k + 1) * bucket)
+        seg = g[s]
+        assert q[s][np.argmin(seg)] == 0
+        assert q[s][np.argmax(seg)] == 255
+        deq = np.float32(offset[k]) + q[s].astype(np.float64) * np.float64(scale[k])
+        # |p - deq| <= scale/2 up to rounding
+        bound = 0.5 * float(scale[k]) * (1 + 2.0 ** -20) + 2 * ulp32(np.abs(seg).max())
+        assert np.all(np.abs(seg.astype(np.float64) - deq) <= bound)
+        # error feedback keeps exactly what was dropped (up to one rounding)
+        assert np.all(np.abs(err[s].astype(np.float64) - (seg - deq)) <= bound)
+
+
+def test_uniform_ef_identity_and_monotone():
+    n, bucket = 3000, 512
+    g = _tiny_buckets(5, n)
+    e_old = _tiny_buckets(6, n, scale=1e-4)
+    err = e_old.copy()
+    codes, scale, offset = orc.encode_uniform(g, err, bits=4, bucket=bucket)
+    q = np.array(_unpack(codes, n, 4))
+    p = (e_old + g).astype(np.float32)         # one binary32 rounding of e + g
+    for k in range(orc.num_buckets(n, bucket)):
+        s = slice(k * bucket, min(n, (k + 1) * bucket))
+        deq = np.array([float(np.float32(frac(qq) * frac(scale[k]) + frac(offset[k])))
+                        for qq in q[s]])
+        lhs = err[s].astype(np.float64) + deq
+        tol = np.array([ulp32(max(abs(a), abs(b))) for a, b in zip(p[s], deq)])
+        assert np.all(np.abs(lhs - p[s].astype(np.float64)) <= tol)
+        order = np.argsort(p[s], kind="stable")
+        assert np.all(np.diff(q[s][order]) >= 0)
+
+
+# ------------------------------------------------------------- uniform, stochastic
+
+def test_stochastic_floor_or_ceil_and_unbiased():
+    bits, bucket = 4, 32
+    L = 15
+    fracs = [0.0, 0.1, 0.25, 0.5, 0.7, 0.9, 0.99]
+    vals = [0.0, 15.0] + [3 + f for f in fracs] + [8 + f for f in fracs]
+    vals += [1.0] * (bucket - len(vals))
+    g = np.array(vals, dtype=np.float32) * np.float32(2.0 ** -7)
+    K = 6000
+    acc = np.zeros(bucket)
+    ceil_count = np.zeros(bucket)
+    t_exact = [(frac(v) - frac(g.min())) / frac(np.float32(2.0 ** -7)) for v in g]
+    for step in range(K):
+        codes, scale, offset = orc.encode_uniform(g, None, bits=bits, bucket=bucket,
+                                                  mode=orc.ROUND_STOCHASTIC, seed=17,
+                                                  step=step)
+        assert scale[0] == np.float32(2.0 ** -7)
+        q = np.array(_unpack(codes, bucket, bits))
+        fl = np.array([math.floor(t) for t in t_exact])
+        assert np.all((q == fl) | (q == np.minimum(fl + 1, L)))
+        ceil_count += (q > fl)
+        acc += offset[0] + q * float(scale[0])
+    mean = acc / K
+    for j in range(bucket):
+        fr = float(t_exact[j] - math.floor(t_exact[j]))
+        sd = math.sqrt(max(fr * (1 - fr), 1e-12) / K)
+        assert abs(ceil_count[j] / K - fr) <= 5 * sd + 1e-12
+        assert abs(mean[j] - float(g[j])) <= 5 * float(scale[0]) * sd + 1e-12
+
+
+def test_stochastic_deterministic_and_global_index():
+    n, bucket = 4096 + 96, 512
+    g = _tiny_buckets(9, n)
+    a = orc.encode_uniform(g, None, bits=2, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                           seed=5, step=4)
+    b = orc.encode_uniform(g, None, bits=2, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                           seed=5, step=4)
+    c = orc.encode_uniform(g, None, bits=2, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                           seed=5, step=5)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert not np.array_equal(a[0], c[0])
+    # a slice starting on a bucket boundary reproduces its part of the whole
+    lo = 2 * bucket
+    part = orc.encode_uniform(g[lo:], None, bits=2, bucket=bucket,
+                              mode=orc.ROUND_STOCHASTIC, seed=5, step=4, index_base=lo)
+    assert np.array_equal(part[0], a[0][lo * 2 // 32:])
+    assert np.array_equal(part[1], a[1][2:])
+
+
+def test_ef_chain_delays_not_loses():
+    """Sum of transmitted values + final residual = sum of gradients (p4: the
+    dropped signal is only delayed)."""
+    n, bucket, steps = 2048 + 128, 512, 10
+    sig = wl.bucket_sigmas(n, bucket, seed=2)
+    err = np.zeros(n, dtype=np.float32)
+    sent = np.zeros(n)
+    gsum = np.zeros(n)
+    bound = np.zeros(n)
+    for t in range(steps):
+        g = wl.bucket_sigma_gradient(n, bucket, t, seed=2, sigmas=sig)
+        codes, scale, offset = orc.encode_uniform(g, err, bits=4, bucket=bucket,
+                                                  mode=orc.ROUND_STOCHASTIC, seed=2, step=t)
+        out = orc.decode_accumulate(codes, scale, offset, M=1, n=n, bits=4, bucket=bucket,
+                                    scheme=orc.SCHEME_UNIFORM)
+        sent += out
+        gsum += g
+        bound += 4 * np.spacing(np.abs(out).astype(np.float32) + np.abs(g) + 1e-30)
+    assert np.all(np.abs(sent + err - gsum) <= bound)
+
+
+# -------------------------------------------------------------------------- sign
+
+def test_sign_bits_scale_and_partial_bucket():
+    n, bucket = 64 * 3 + 16, 64
+    g = _tiny_buckets(21, n)
+    g[3] = np.float32(0.0)
+    g[4] = np.float32(-0.0)
+    g[-16:] = np.float32(1.0)                 # partial last bucket: mean over 16
+    e_old = np.zeros(n, dtype=np.float32)
+    err = e_old.copy()
+    codes, scale = orc.encode_sign(g, err, bucket=bucket)
+    bits = _unpack(codes, n, 1)
+    assert bits == [1 if v >= 0 else 0 for v in g]   # sign(+-0) = +1
+    assert scale[-1] == 1.0
+    for k in range(orc.num_buckets(n, bucket)):
+        seg = g[k * bucket:(k + 1) * bucket]
+        exact = sum(abs(frac(v)) for v in seg) / len(seg)
+        assert abs(frac(scale[k]) - exact) <= Fraction(ulp32(scale[k]))
+        deq = np.where(np.array(bits[k * bucket:k * bucket + len(seg)]) == 1,
+                       scale[k], -scale[k]).astype(np.float32)
+        assert np.all(err[k * bucket:k * bucket + len(seg)] == (seg - deq))
+        assert math.isclose(float(np.abs(deq.astype(np.float64)).sum()),
+                            len(seg) * float(scale[k]), rel_tol=1e-12)
+
+
+def test_sign_with_residual():
+    n, bucket = 4096 * 2, 4096
+    g = wl.shared_mean_gradients(n, 1, seed=3)[0]
+    e_old = _tiny_buckets(4, n, scale=5e-4)
+    err = e_old.copy()
+    codes, scale = orc.encode_sign(g, err, bucket=bucket)
+    p = (e_old + g).astype(np.float32)
+    assert _unpack(codes, n, 1) == [int(v >= 0) for v in p]
+    deq = np.where(p >= 0, np.repeat(scale, bucket), -np.repeat(scale, bucket))
+    lhs = err.astype(np.float64) + deq
+    assert np.all(np.abs(lhs - p) <= np.spacing(np.abs(p) + np.abs(deq).astype(np.float32)))
+
+
+# ----------------------------------------------------------------------- ternary
+
+def test_ternary_levels_and_nearest_rule():
+    n, bucket = 256 + 32, 128
+    g = _tiny_buckets(31, n)
+    g[200:232] = 0.0                          # part of a bucket at zero
+    codes, scale = orc.encode_ternary(g, None, bucket=bucket, mode=orc.ROUND_NEAREST)
+    c = np.array(_unpack(codes, n, 2))
+    assert set(np.unique(c)) <= {0, 1, 2}
+    for k in range(orc.num_buckets(n, bucket)):
+        seg = g[k * bucket:(k + 1) * bucket]
+        cs = c[k * bucket:k * bucket + len(seg)]
+        s = np.abs(seg).max()
+        assert scale[k] == s
+        am = np.argmax(np.abs(seg))
+        assert cs[am] == (2 if seg[am] > 0 else 0)
+        for v, code in zip(seg, cs):
+            r = abs(frac(v)) / frac(s)
+            if r > Fraction(1, 2) * (1 + Fraction(1, 1 << 22)):
+                assert code == (2 if v > 0 else 0)
+            elif r <= Fraction(1, 2):
+                assert code == 1
+
+
+def test_ternary_zero_bucket_and_unbiased():
+    g = np.zeros(64, dtype=np.float32)
+    codes, scale = orc.encode_ternary(g, None, bucket=32, mode=orc.ROUND_STOCHASTIC, seed=1)
+    assert scale.tolist() == [0.0, 0.0]
+    assert _unpack(codes, 64, 2) == [1] * 64
+
+    vals = np.array([1.0, -1.0, 0.5, -0.25, 0.1, 0.9, -0.75, 0.0] * 4, dtype=np.float32)
+    K = 5000
+    acc = np.zeros(vals.size)
+    for step in range(K):
+        codes, scale = orc.encode_ternary(vals, None, bucket=32, mode=orc.ROUND_STOCHASTIC,
+                                          seed=8, step=step)
+        c = np.array(_unpack(codes, vals.size, 2))
+        acc += (c - 1) * float(scale[0])
+    mean = acc / K
+    for j, v in enumerate(vals):
+        pr = abs(float(v))
+        sd = math.sqrt(max(pr * (1 - pr), 1e-12) / K)
+        assert abs(mean[j] - float(v)) <= 5 * sd + 1e-12
+
+
+# ------------------------------------------------------------------------ decode
+
+def test_decode_hand_built_exact():
+    """Three workers, two buckets, exact dyadic values: the sums are exact."""
+    n, bucket, M = 64, 32, 3
+    rng = np.random.default_rng(0)
+    for bits in (1, 2, 4, 8):
+        L = (1 << bits) - 1
+        q = rng.integers(0, L + 1, size=(M, n))
+        words = np.stack([_pack(q[w], bits) for w in range(M)])
+        scale = np.array([[0.5, 0.25], [2.0, 0.125], [1.0, 4.0]], dtype=np.float32)
+        off = np.array([[-1.0, 3.0], [0.0, -8.0], [16.0, 0.5]], dtype=np.float32)
+        out = orc.decode_accumulate(words, scale, off, M=M, n=n, bits=bits, bucket=bucket,
+                                    scheme=orc.SCHEME_UNIFORM)
+        want = [sum(q[w, i] * float(scale[w, i // bucket]) + float(off[w, i // bucket])
+                    for w in range(M)) for i in range(n)]
+        assert out.tolist() == want
+        # mean over M=4 (power of two: exact) and accumulate into out
+        words4 = np.concatenate([words, words[:1]])
+        sc4 = np.concatenate([scale, scale[:1]])
+        of4 = np.concatenate([off, off[:1]])
+        prior = np.full(n, 0.5, dtype=np.float32)
+        out4 = orc.decode_accumulate(words4, sc4, of4, M=4, n=n, bits=bits, bucket=bucket,
+                                     scheme=orc.SCHEME_UNIFORM,
+                                     flags=orc.OUT_MEAN | orc.ACCUMULATE_INTO_OUT,
+                                     out=prior.copy())
+        want4 = [0.5 + (want[i] + q[0, i] * float(scale[0, i // bucket])
+                        + float(off[0, i // bucket])) / 4 for i in range(n)]
+        assert out4.tolist() == want4
+
+
+def test_decode_sign_ternary_closed_form():
+    n, bucket = 96, 32
+    rng = np.random.default_rng(1)
+    bitsv = rng.integers(0, 2, size=(2, n))
+    s = np.array([[0.5, 1.0, 2.0], [0.25, 4.0, 8.0]], dtype=np.float32)
+    out = orc.decode_accumulate(np.stack([_pack(b, 1) for b in bitsv]), s, None, M=2, n=n,
+                                bits=1, bucket=bucket, scheme=orc.SCHEME_SIGN)
+    want = [sum((1 if bitsv[w, i] else -1) * float(s[w, i // bucket]) for w in range(2))
+            for i in range(n)]
+    assert out.tolist() == want
+    t = rng.integers(0, 3, size=(2, n))
+    out = orc.decode_accumulate(np.stack([_pack(c, 2) for c in t]), s, None, M=2, n=n, bits=2,
+                                bucket=bucket, scheme=orc.SCHEME_TERNARY)
+    want = [sum((int(t[w, i]) - 1) * float(s[w, i // bucket]) for w in range(2))
+            for i in range(n)]
+    assert out.tolist() == want
+
+
+def test_decode_fixed_worker_order():
+    """Accumulation runs over workers 0..M-1 in order: 1 + 2^-24 + 2^-24 = 1 under
+    round-to-nearest-even, while the reverse order would give 1 + 2^-23."""
+    n, bucket = 32, 32
+    codes = np.zeros((3, 1), dtype=np.uint32)
+    scale = np.zeros((3, 1), dtype=np.float32)
+    fwd = np.array([[1.0], [2.0 ** -24], [2.0 ** -24]], dtype=np.float32)
+    out = orc.decode_accumulate(codes, scale, fwd, M=3, n=n, bits=1, bucket=bucket,
+                                scheme=orc.SCHEME_UNIFORM)
+    assert np.all(out == 1.0)
+    out = orc.decode_accumulate(codes, scale, fwd[::-1].copy(), M=3, n=n, bits=1,
+                                bucket=bucket, scheme=orc.SCHEME_UNIFORM)
+    assert np.all(out == np.float32(1.0 + 2.0 ** -23))
+
+
+def test_decode_single_worker_matches_encoder():
+    n, bucket = 5000, 1024
+    g = wl.outlier_gradient(n, seed=3)
+    err = np.zeros(n, dtype=np.float32)
+    codes, scale, offset = orc.encode_uniform(g, err, bits=8, bucket=bucket)
+    out = orc.decode_accumulate(codes, scale, offset, M=1, n=n, bits=8, bucket=bucket,
+                                scheme=orc.SCHEME_UNIFORM)
+    # e = p - deq with one rounding, so deq + e recovers p to one ulp
+    assert np.all(np.abs(out.astype(np.float64) + err - g) <= np.spacing(np.abs(g) + np.abs(out)))
+
+
+# -------------------------------------------------------------------------- vote
+
+@pytest.mark.parametrize("M", list(range(1, 10)))
+def test_vote_brute_force(M):
+    patterns = 1 << M
+    reps = max(1, 96 // patterns)
+    n = patterns * reps + 5                  # ragged last word
+    bits = np.zeros((M, n), dtype=np.int64)
+    for i in range(n):
+        pat = i % patterns
+        for w in range(M):
+            bits[w, i] = (pat >> w) & 1
+    words = np.stack([_pack(bits[w], 1) for w in range(M)])
+    out = orc.sign_vote(words, M=M, n=n)
+    want = [1 if 2 * bin(i % patterns).count("1") >= M else 0 for i in range(n)]
+    assert _unpack(out, n, 1) == want
+    tail = n % 32
+    if tail:
+        assert int(out[-1]) >> tail == 0
+    if M % 2 == 1:                          # odd M: textbook strict majority
+        assert want == [1 if bin(i % patterns).count("1") > M // 2 else 0 for i in range(n)]
+
+
+# --------------------------------------------------------------------------- FP8
+
+def test_e4m3_spec_points(golden_dir):
+    for code, val in _read_golden(golden_dir, "e4m3_spec_points.txt"):
+        got = orc.e4m3_to_f32(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_e4m3_order_round_trip_and_ties():
+    vals = [orc.e4m3_to_f32(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        assert orc.e4m3_from_f32(orc.e4m3_to_f32(c)) == c
+    for c in range(0x7E):
+        lo, hi = vals[c], vals[c + 1]
+        mid = (Fraction(lo) + Fraction(hi)) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert orc.e4m3_from_f32(float(mid)) == even
+        assert orc.e4m3_from_f32(-float(mid)) == 0x80 | even
+        eps = (Fraction(hi) - Fraction(lo)) / 64
+        assert orc.e4m3_from_f32(float(mid - eps)) == c
+        assert orc.e4m3_from_f32(float(mid + eps)) == c + 1
+
+
+def test_e4m3_saturation_and_nan():
+    for x in (448.0, 449.0, 464.0, 479.0, 480.0, 1e6, 3.0e38, math.inf):
+        assert orc.e4m3_from_f32(x) == 0x7E
+        assert orc.e4m3_from_f32(-x) == 0xFE
+    assert orc.e4m3_from_f32(math.nan) & 0x7F == 0x7F
+    assert orc.e4m3_from_f32(2.0 ** -11) == 0x00      # below half the smallest subnormal
+    assert orc.e4m3_from_f32(-(2.0 ** -11)) == 0x80
+    assert orc.e4m3_from_f32(3 * 2.0 ** -11) == 0x01   # rounds up past the midpoint
+
+
+def test_rowwise_fp8_rows():
+    x = wl.embedding_rows(rows=257, dim=128, seed=1)
+    x[5] = 0.0
+    x[6, :] = np.float32(-1e-3)
+    codes, sc = orc.rowwise_fp8(x)
+    assert sc[5] == 0.0 and not codes[5].any()
+    for r in range(x.shape[0]):
+        if r == 5:
+            continue
+        a = np.abs(x[r]).max()
+        assert sc[r] == to_f32(frac(a) / 448)
+        j = int(np.argmax(np.abs(x[r])))
+        assert codes[r, j] == (0x7E if x[r, j] > 0 else 0xFE)
+    xh = orc.rowwise_fp8_dequant(codes, sc)
+    scb = sc[:, None].astype(np.float64)
+    t = np.abs(x / np.where(scb == 0, 1, scb))
+    err = np.abs(xh.astype(np.float64) - x)
+    normal = t >= 2.0 ** -6
+    assert np.all(err[normal] <= (2.0 ** -4) * np.abs(x[normal]) * (1 + 2.0 ** -20))
+    assert np.all(err[~normal] <= (2.0 ** -10) * np.broadcast_to(scb, x.shape)[~normal]
+                  * (1 + 2.0 ** -20) + 1e-45)
+
+
+@pytest.mark.slow
+def test_rowwise_fp8_numeric_example(golden_dir):
+    kv = {r[0]: int(r[1]) for r in _read_golden(golden_dir, "fp8_numeric_example.txt")}
+    rows, dim = kv["lookups"], kv["dim"]
+    x = wl.embedding_rows(rows=rows, dim=dim, seed=1)
+    assert x.nbytes == kv["fp32_payload_bytes"]
+    codes, sc = orc.rowwise_fp8(x)
+    assert codes.nbytes == kv["fp8_payload_bytes"]
+    assert sc.nbytes == 4 * rows
+    shrink = 1 - (codes.nbytes + sc.nbytes) / x.nbytes
+    assert 0.74 < shrink < 0.75
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_workload_distributions():
+    g = wl.outlier_gradient(1 << 20, seed=0)
+    big = np.abs(g) > 0.01
+    assert 0.0005 < big.mean() < 0.0015
+    assert 0.9e-3 < g[~big].std() < 1.1e-3
+    x = wl.embedding_rows(rows=1000, dim=128, seed=1)
+    assert 0.048 < x.std() < 0.052
+    sig = wl.bucket_sigmas(512 * 4000, 512, seed=2)
+    lg = np.log10(sig)
+    assert lg.min() >= -5 and lg.max() <= -2 and abs(lg.mean() + 3.5) < 0.05
+    gw = wl.shared_mean_gradients(1 << 16, 2, seed=3)
+    d = gw[0] - gw[1]
+    assert abs(d.std() - math.sqrt(2) * 1e-3) < 5e-5
+    b = wl.bf16_gradients(1 << 12, 2, seed=4)
+    assert b.dtype == np.uint16 and b.shape == (2, 1 << 12)
