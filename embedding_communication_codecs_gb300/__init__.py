@@ -1,0 +1,193 @@
+"""GB300-native communication codec (libqcodec) for data-parallel training.
+
+The encode half compresses a gradient for the wire with error feedback. The
+options are uniform min/max levels at 8/4/2/1 bits (round to nearest or Philox
+stochastic rounding), TernGrad ternary and scaled sign. FP32 -> FP8 e4m3
+row-wise quantization covers embedding payloads. The decode half dequantizes
+and accumulates M workers' payloads in fp32 in a fixed worker order. It also
+majority-votes signSGD sign vectors.
+
+Every step runs in hand-written CUDA kernels for sm_103a inside ``libqcodec.so``.
+The functions here only pass torch tensors' device pointers and the current
+stream through the C ABI declared in ``include/qcodec.h``, under the same names.
+There is no CPU fallback: importing this package fails if the library has not
+been built (``python -m embedding_communication_codecs_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+QC_OK, QC_ERR_NULL, QC_ERR_INVALID_ARG, QC_ERR_ALIGNMENT, QC_ERR_UNSUPPORTED, QC_ERR_CUDA = range(6)
+QC_SCHEME_UNIFORM, QC_SCHEME_SIGN, QC_SCHEME_TERNARY = 0, 1, 2
+QC_ROUND_NEAREST, QC_ROUND_STOCHASTIC = 0, 1
+QC_DTYPE_F32, QC_DTYPE_BF16 = 0, 1
+QC_OUT_SUM, QC_OUT_MEAN, QC_ACCUMULATE_INTO_OUT = 0, 1, 2
+QC_MAX_WORKERS = 1024
+QC_MAX_FP8_DIM = 4096
+
+STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ERR_ALIGNMENT",
+                4: "QC_ERR_UNSUPPORTED", 5: "QC_ERR_CUDA"}
+
+# Every symbol the C ABI exports, in header order.
+EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
+           "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_last_error",
+           "qc_version")
+
+
+class QCodecError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m embedding_communication_codecs_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    U64, U32 = ctypes.c_uint64, ctypes.c_uint32
+    lib.qc_code_words.argtypes, lib.qc_code_words.restype = [S, I], S
+    lib.qc_num_buckets.argtypes, lib.qc_num_buckets.restype = [S, S], S
+    lib.qc_encode_ef.argtypes = [P, I, P, S, I, S, I, I, U64, U32, P, P, P, P]
+    lib.qc_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I, P]
+    lib.qc_sign_vote.argtypes = [P, S, I, S, P, P]
+    lib.qc_rowwise_fp8.argtypes = [P, S, S, P, P, P]
+    lib.qc_rowwise_fp8_dequant.argtypes = [P, P, S, S, P, P]
+    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8",
+                 "qc_rowwise_fp8_dequant"):
+        getattr(lib, name).restype = I
+    lib.qc_last_error.argtypes, lib.qc_last_error.restype = [], ctypes.c_char_p
+    lib.qc_version.argtypes, lib.qc_version.restype = [], ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != QC_OK:
+        raise QCodecError(status, lib.qc_last_error().decode())
+
+
+def _ptr(t):
+    """Device address of a tensor (None -> NULL).  Integers pass through, so raw
+    addresses can be given too."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def qc_version() -> str:
+    return lib.qc_version().decode()
+
+
+def qc_code_words(n: int, bits: int) -> int:
+    return int(lib.qc_code_words(n, bits))
+
+
+def qc_num_buckets(n: int, bucket: int) -> int:
+    return int(lib.qc_num_buckets(n, bucket))
+
+
+def _dtype_code(grad, dtype):
+    if dtype is not None:
+        return dtype
+    import torch
+    if grad.dtype == torch.float32:
+        return QC_DTYPE_F32
+    if grad.dtype == torch.bfloat16:
+        return QC_DTYPE_BF16
+    raise TypeError(f"gradient dtype {grad.dtype} is not float32 or bfloat16")
+
+
+def qc_encode_ef(grad, err, n, bits, bucket, scheme, mode, seed, step, codes, scale, offset,
+                 stream=None, dtype=None):
+    """Sender half: error-feedback encode of ``n`` gradient elements.
+
+    ``err`` (fp32, in/out) may be None for no error feedback; ``offset`` may be
+    None unless ``scheme`` is uniform.  Raises QCodecError on a non-OK status."""
+    _check(lib.qc_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bits, bucket,
+                            scheme, mode, seed, step, _ptr(codes), _ptr(scale), _ptr(offset),
+                            _stream(stream)))
+
+
+def qc_decode_accumulate(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits,
+                         bucket, scheme, out, flags=QC_OUT_SUM, stream=None):
+    """Receiver half: ``out`` = fixed-order fp32 sum (or mean) of M decoded payloads."""
+    _check(lib.qc_decode_accumulate(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
+                                    meta_stride, M, n, bits, bucket, scheme, _ptr(out), flags,
+                                    _stream(stream)))
+
+
+def qc_sign_vote(signs, stride_words, M, n, out, stream=None):
+    """Majority vote over M packed sign vectors."""
+    _check(lib.qc_sign_vote(_ptr(signs), stride_words, M, n, _ptr(out), _stream(stream)))
+
+
+def qc_rowwise_fp8(x, rows, dim, codes, row_scale, stream=None):
+    """FP32 rows -> E4M3 codes + per-row fp32 scale."""
+    _check(lib.qc_rowwise_fp8(_ptr(x), rows, dim, _ptr(codes), _ptr(row_scale), _stream(stream)))
+
+
+def qc_rowwise_fp8_dequant(codes, row_scale, rows, dim, out, stream=None):
+    """E4M3 codes + per-row scale -> fp32 rows."""
+    _check(lib.qc_rowwise_fp8_dequant(_ptr(codes), _ptr(row_scale), rows, dim, _ptr(out),
+                                      _stream(stream)))
+
+
+# ---------------------------------------------------------------- conveniences
+
+def alloc_payload(n: int, bits: int, bucket: int, scheme: int, device="cuda", workers: int = 0):
+    """Empty (codes, scale, offset) device tensors for one payload, or for
+    ``workers`` payloads stacked along a leading dimension when workers > 0.
+    Offset is None except for the uniform scheme."""
+    import torch
+    words = qc_code_words(n, bits)
+    nb = qc_num_buckets(n, bucket)
+    lead = (workers,) if workers else ()
+    codes = torch.empty(lead + (words,), dtype=torch.int32, device=device)
+    scale = torch.empty(lead + (nb,), dtype=torch.float32, device=device)
+    offset = (torch.empty(lead + (nb,), dtype=torch.float32, device=device)
+              if scheme == QC_SCHEME_UNIFORM else None)
+    return codes, scale, offset
+
+
+def encode_ef(grad, err, *, bits, bucket, scheme=QC_SCHEME_UNIFORM, mode=QC_ROUND_NEAREST,
+              seed=0, step=0, out=None, stream=None):
+    """Encode a flat device tensor; returns (codes int32[words], scale, offset)."""
+    n = grad.numel()
+    codes, scale, offset = out if out is not None else alloc_payload(n, bits, bucket, scheme,
+                                                                     grad.device)
+    qc_encode_ef(grad, err, n, bits, bucket, scheme, mode, seed, step, codes, scale, offset,
+                 stream=stream)
+    return codes, scale, offset
+
+
+def decode_accumulate(codes, scale, offset, *, n, bits, bucket, scheme=QC_SCHEME_UNIFORM,
+                      flags=QC_OUT_SUM, out=None, stream=None):
+    """Decode stacked payloads ([M, words] codes, [M, nb] scale/offset) or a single
+    payload (1-D) into a fresh or given fp32 tensor of n elements."""
+    import torch
+    M = codes.shape[0] if codes.dim() == 2 else 1
+    cs = codes.stride(0) if codes.dim() == 2 else 0
+    ms = scale.stride(0) if scale.dim() == 2 else 0
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=codes.device)
+    qc_decode_accumulate(codes, cs, scale, offset, ms, M, n, bits, bucket, scheme, out, flags,
+                         stream=stream)
+    return out

@@ -1,0 +1,312 @@
+// qc_api.cu -- the C ABI of libqcodec (declared in include/qcodec.h): host-side
+// validation, dispatch to the kernels, and error reporting.  Validation touches
+// no CUDA API, so every argument error is reported without any device work.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/qcodec.h"
+#include "qc_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+qc_status fail(qc_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qc_status ok() {
+    g_last_error[0] = '\0';
+    return QC_OK;
+}
+
+qc_status from_cuda(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return ok();
+    return fail(QC_ERR_CUDA, "%s: CUDA error %d (%s)", what, static_cast<int>(e),
+                cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [a, a+na) and [b, b+nb) (bytes) share a byte.
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool valid_bucket(size_t bucket) { return bucket >= 32 && bucket % 32 == 0 && bucket <= (1u << 24); }
+
+// Team of W warps per bucket: the smallest power of two with 512 W >= bucket,
+// capped at the 8 warps of a block (larger buckets take two passes).
+int team_warps_for(size_t elems) {
+    int w = 1;
+    while (w < 8 && static_cast<size_t>(qc::kWindowPerWarp) * w < elems) w <<= 1;
+    return w;
+}
+
+}  // namespace
+
+namespace qc {
+
+int persistent_grid(const void *kernel, int block, uint64_t units) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;  // (device, kernel) -> blocks per SM
+    static std::unordered_map<int, int> sms;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t key = (static_cast<uint64_t>(dev) << 48) ^ reinterpret_cast<uintptr_t>(kernel);
+    int per_sm = 0, nsm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it == cache.end()) {
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, 0) != cudaSuccess ||
+                b < 1)
+                b = 1;
+            it = cache.emplace(key, b).first;
+        }
+        per_sm = it->second;
+        auto is = sms.find(dev);
+        if (is == sms.end()) {
+            int n = 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+                n = 1;
+            is = sms.emplace(dev, n).first;
+        }
+        nsm = is->second;
+    }
+    const uint64_t cap = static_cast<uint64_t>(per_sm) * static_cast<uint64_t>(nsm);
+    uint64_t g = units < cap ? units : cap;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+}  // namespace qc
+
+extern "C" {
+
+size_t qc_code_words(size_t n, int bits) {
+    if (bits <= 0) return 0;
+    return (n * static_cast<size_t>(bits) + 31) / 32;
+}
+
+size_t qc_num_buckets(size_t n, size_t bucket) {
+    if (bucket == 0) return 0;
+    return (n + bucket - 1) / bucket;
+}
+
+const char *qc_last_error(void) { return g_last_error; }
+
+const char *qc_version(void) { return "libqcodec 0.1.0 (sm_103a)"; }
+
+qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
+                       size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
+                       uint32_t step, uint32_t *codes, float *scale, float *offset,
+                       qc_stream_t stream) {
+    if (dtype != QC_DTYPE_F32 && dtype != QC_DTYPE_BF16)
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: dtype %d is not F32 or BF16", dtype);
+    if (scheme == QC_SCHEME_UNIFORM) {
+        if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: uniform bits must be 1, 2, 4 or 8 (got %d)", bits);
+    } else if (scheme == QC_SCHEME_SIGN) {
+        if (bits != 1) return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme needs bits == 1 (got %d)", bits);
+        if (mode != QC_ROUND_NEAREST)
+            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme is deterministic; mode must be NEAREST");
+    } else if (scheme == QC_SCHEME_TERNARY) {
+        if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: ternary scheme needs bits == 2 (got %d)", bits);
+    } else {
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown scheme %d", scheme);
+    }
+    if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown rounding mode %d", mode);
+    if (!valid_bucket(bucket))
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", bucket);
+    if (n == 0) return ok();
+    if (n > (static_cast<size_t>(1) << 40))
+        return fail(QC_ERR_UNSUPPORTED, "qc_encode_ef: n = %zu exceeds 2^40 elements", n);
+    if (!grad || !codes || !scale) return fail(QC_ERR_NULL, "qc_encode_ef: grad, codes and scale must be non-NULL");
+    if (scheme == QC_SCHEME_UNIFORM && !offset)
+        return fail(QC_ERR_NULL, "qc_encode_ef: the uniform scheme needs an offset array");
+    const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
+    if (!aligned(grad, dtype == QC_DTYPE_F32 ? 16 : 8))
+        return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: grad must be %d-byte aligned", dtype == QC_DTYPE_F32 ? 16 : 8);
+    if (err && !aligned(err, 16)) return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: err must be 16-byte aligned");
+    if (!aligned(codes, 4) || !aligned(scale, 4) || (offset && !aligned(offset, 4)))
+        return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: codes, scale and offset must be 4-byte aligned");
+    const size_t nb = qc_num_buckets(n, bucket);
+    const size_t cbytes = qc_code_words(n, bits) * 4, mbytes = nb * 4;
+    const void *outs[3] = {codes, scale, scheme == QC_SCHEME_UNIFORM ? offset : nullptr};
+    const size_t osz[3] = {cbytes, mbytes, mbytes};
+    for (int a = 0; a < 3; ++a) {
+        if (overlaps(outs[a], osz[a], grad, n * esize) || overlaps(outs[a], osz[a], err, n * 4))
+            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: an output overlaps grad or err");
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], osz[a], outs[b], osz[b]))
+                return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: outputs overlap each other");
+    }
+    if (overlaps(err, n * 4, grad, n * esize))
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: err overlaps grad");
+
+    qc::EncodeParams p{};
+    p.grad = grad;
+    p.err = err;
+    p.n = n;
+    p.bucket = static_cast<uint32_t>(bucket);
+    p.nbuckets = nb;
+    p.team_warps = team_warps_for(bucket);
+    p.two_pass = bucket > static_cast<size_t>(qc::kWindowPerWarp) * p.team_warps ? 1 : 0;
+    p.seed = seed;
+    p.step = step;
+    p.codes = codes;
+    p.scale = scale;
+    p.offset = offset;
+    return from_cuda(qc::launch_encode(p, scheme, bits, mode == QC_ROUND_STOCHASTIC,
+                                       dtype == QC_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                     "qc_encode_ef");
+}
+
+qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
+                               const float *scale, const float *offset, size_t meta_stride,
+                               int M, size_t n, int bits, size_t bucket, qc_scheme scheme,
+                               float *out, int flags, qc_stream_t stream) {
+    if (scheme == QC_SCHEME_UNIFORM) {
+        if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: uniform bits must be 1, 2, 4 or 8 (got %d)", bits);
+    } else if (scheme == QC_SCHEME_SIGN) {
+        if (bits != 1) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: sign scheme needs bits == 1");
+    } else if (scheme == QC_SCHEME_TERNARY) {
+        if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: ternary scheme needs bits == 2");
+    } else {
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: unknown scheme %d", scheme);
+    }
+    if (M < 1 || M > QC_MAX_WORKERS)
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: M must be in [1, %d] (got %d)", QC_MAX_WORKERS, M);
+    if (flags & ~(QC_OUT_MEAN | QC_ACCUMULATE_INTO_OUT))
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: unknown flag bits 0x%x", flags);
+    if (!valid_bucket(bucket))
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", bucket);
+    if (n == 0) return ok();
+    if (n > (static_cast<size_t>(1) << 40))
+        return fail(QC_ERR_UNSUPPORTED, "qc_decode_accumulate: n = %zu exceeds 2^40 elements", n);
+    const size_t words = qc_code_words(n, bits), nb = qc_num_buckets(n, bucket);
+    if (M > 1 && (codes_stride_words < words || meta_stride < nb))
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: strides (%zu words, %zu buckets) are shorter than one payload (%zu, %zu)",
+                    codes_stride_words, meta_stride, words, nb);
+    if (!codes || !scale || !out) return fail(QC_ERR_NULL, "qc_decode_accumulate: codes, scale and out must be non-NULL");
+    if (scheme == QC_SCHEME_UNIFORM && !offset)
+        return fail(QC_ERR_NULL, "qc_decode_accumulate: the uniform scheme needs offsets");
+    if (!aligned(out, 16)) return fail(QC_ERR_ALIGNMENT, "qc_decode_accumulate: out must be 16-byte aligned");
+    if (!aligned(codes, 4) || !aligned(scale, 4) || (offset && !aligned(offset, 4)))
+        return fail(QC_ERR_ALIGNMENT, "qc_decode_accumulate: codes, scale and offset must be 4-byte aligned");
+    const size_t span_c = ((M - 1) * (M > 1 ? codes_stride_words : 0) + words) * 4;
+    const size_t span_m = ((M - 1) * (M > 1 ? meta_stride : 0) + nb) * 4;
+    if (overlaps(out, n * 4, codes, span_c) || overlaps(out, n * 4, scale, span_m) ||
+        (scheme == QC_SCHEME_UNIFORM && overlaps(out, n * 4, offset, span_m)))
+        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: out overlaps an input");
+
+    qc::DecodeParams p{};
+    p.codes = codes;
+    p.codes_stride = M > 1 ? codes_stride_words : 0;
+    p.scale = scale;
+    p.offset = offset;
+    p.meta_stride = M > 1 ? meta_stride : 0;
+    p.M = M;
+    p.n = n;
+    p.bucket = static_cast<uint32_t>(bucket);
+    p.nbuckets = nb;
+    p.out = out;
+    p.flags = flags;
+    return from_cuda(qc::launch_decode(p, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),
+                     "qc_decode_accumulate");
+}
+
+qc_status qc_sign_vote(const uint32_t *signs, size_t stride_words, int M, size_t n,
+                       uint32_t *out, qc_stream_t stream) {
+    if (M < 1 || M > QC_MAX_WORKERS)
+        return fail(QC_ERR_INVALID_ARG, "qc_sign_vote: M must be in [1, %d] (got %d)", QC_MAX_WORKERS, M);
+    if (n == 0) return ok();
+    if (n > (static_cast<size_t>(1) << 40))
+        return fail(QC_ERR_UNSUPPORTED, "qc_sign_vote: n = %zu exceeds 2^40 elements", n);
+    const size_t words = qc_code_words(n, 1);
+    if (M > 1 && stride_words < words)
+        return fail(QC_ERR_INVALID_ARG, "qc_sign_vote: stride %zu words is shorter than one vector (%zu)", stride_words, words);
+    if (!signs || !out) return fail(QC_ERR_NULL, "qc_sign_vote: signs and out must be non-NULL");
+    if (!aligned(signs, 4) || !aligned(out, 4))
+        return fail(QC_ERR_ALIGNMENT, "qc_sign_vote: signs and out must be 4-byte aligned");
+    const size_t stride = M > 1 ? stride_words : 0;
+    if (overlaps(out, words * 4, signs, ((M - 1) * stride + words) * 4))
+        return fail(QC_ERR_INVALID_ARG, "qc_sign_vote: out overlaps the inputs");
+    qc::VoteParams p{};
+    p.signs = signs;
+    p.stride = stride;
+    p.M = M;
+    p.nwords = words;
+    p.threshold = static_cast<uint32_t>((M + 1) / 2);
+    p.last_mask = (n % 32) ? ((1u << (n % 32)) - 1u) : 0xFFFFFFFFu;
+    p.out = out;
+    const bool vec = aligned(signs, 16) && aligned(out, 16) && stride % 4 == 0;
+    return from_cuda(qc::launch_vote(p, vec, reinterpret_cast<cudaStream_t>(stream)), "qc_sign_vote");
+}
+
+static qc_status check_fp8(const char *fn, const void *in, const void *codes, const float *sc,
+                           size_t rows, size_t dim, const void *out_f32) {
+    if (dim < 4 || dim % 4 != 0)
+        return fail(QC_ERR_INVALID_ARG, "%s: dim must be a positive multiple of 4 (got %zu)", fn, dim);
+    if (dim > QC_MAX_FP8_DIM)
+        return fail(QC_ERR_UNSUPPORTED, "%s: dim %zu exceeds %d", fn, dim, QC_MAX_FP8_DIM);
+    if (rows == 0) return QC_OK;
+    if (rows > (static_cast<size_t>(1) << 40) / dim)
+        return fail(QC_ERR_UNSUPPORTED, "%s: rows x dim exceeds 2^40", fn);
+    if (!in || !codes || !sc) return fail(QC_ERR_NULL, "%s: a buffer pointer is NULL", fn);
+    if (!aligned(out_f32, 16)) return fail(QC_ERR_ALIGNMENT, "%s: the fp32 buffer must be 16-byte aligned", fn);
+    if (!aligned(codes, 4) || !aligned(sc, 4))
+        return fail(QC_ERR_ALIGNMENT, "%s: codes and row_scale must be 4-byte aligned", fn);
+    return QC_OK;
+}
+
+qc_status qc_rowwise_fp8(const float *x, size_t rows, size_t dim, uint8_t *codes,
+                         float *row_scale, qc_stream_t stream) {
+    qc_status st = check_fp8("qc_rowwise_fp8", x, codes, row_scale, rows, dim, x);
+    if (st != QC_OK) return st;
+    if (rows == 0) return ok();
+    if (overlaps(codes, rows * dim, x, rows * dim * 4) || overlaps(row_scale, rows * 4, x, rows * dim * 4) ||
+        overlaps(codes, rows * dim, row_scale, rows * 4))
+        return fail(QC_ERR_INVALID_ARG, "qc_rowwise_fp8: buffers overlap");
+    qc::Fp8Params p{};
+    p.x = x;
+    p.rows = rows;
+    p.dim = static_cast<uint32_t>(dim);
+    p.team_warps = team_warps_for(dim);
+    p.codes = codes;
+    p.row_scale = row_scale;
+    return from_cuda(qc::launch_fp8_quant(p, reinterpret_cast<cudaStream_t>(stream)), "qc_rowwise_fp8");
+}
+
+qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, size_t rows,
+                                 size_t dim, float *out, qc_stream_t stream) {
+    qc_status st = check_fp8("qc_rowwise_fp8_dequant", out, codes, row_scale, rows, dim, out);
+    if (st != QC_OK) return st;
+    if (rows == 0) return ok();
+    if (overlaps(out, rows * dim * 4, codes, rows * dim) || overlaps(out, rows * dim * 4, row_scale, rows * 4))
+        return fail(QC_ERR_INVALID_ARG, "qc_rowwise_fp8_dequant: out overlaps an input");
+    qc::Fp8Params p{};
+    p.codes_in = codes;
+    p.scale_in = row_scale;
+    p.rows = rows;
+    p.dim = static_cast<uint32_t>(dim);
+    p.team_warps = team_warps_for(dim);
+    p.out = out;
+    return from_cuda(qc::launch_fp8_dequant(p, reinterpret_cast<cudaStream_t>(stream)),
+                     "qc_rowwise_fp8_dequant");
+}
+
+}  // extern "C"

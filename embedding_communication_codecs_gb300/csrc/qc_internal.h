@@ -1,0 +1,80 @@
+// qc_internal.h -- launchers behind the C ABI (host side, C++ linkage).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qc {
+
+enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2 };
+
+// Elements a team of W warps covers per window: 4 float4 slots per lane.
+constexpr int kSlots = 4;
+constexpr int kBlock = 256;
+constexpr int kWindowPerWarp = kSlots * 4 * 32;  // 512
+
+struct EncodeParams {
+    const void *grad;
+    float *err;
+    uint64_t n;
+    uint32_t bucket;
+    uint64_t nbuckets;
+    int team_warps;   // 1, 2, 4 or 8 warps own one bucket
+    int two_pass;     // bucket > 512 * team_warps: statistics pass, then re-read
+    uint64_t seed;
+    uint32_t step;
+    uint32_t *codes;
+    float *scale;
+    float *offset;
+};
+
+struct DecodeParams {
+    const uint32_t *codes;
+    uint64_t codes_stride;  // words
+    const float *scale;
+    const float *offset;
+    uint64_t meta_stride;   // floats
+    int M;
+    uint64_t n;
+    uint32_t bucket;
+    uint64_t nbuckets;
+    float *out;
+    int flags;
+};
+
+struct VoteParams {
+    const uint32_t *signs;
+    uint64_t stride;        // words
+    int M;
+    uint64_t nwords;
+    uint32_t threshold;     // ceil(M / 2)
+    uint32_t last_mask;     // valid bits of the last word
+    uint32_t *out;
+};
+
+struct Fp8Params {
+    const float *x;
+    const uint8_t *codes_in;
+    uint64_t rows;
+    uint32_t dim;
+    int team_warps;         // warps per row when dim > 128
+    uint8_t *codes;
+    float *row_scale;
+    const float *scale_in;
+    float *out;
+};
+
+// Each launcher picks the template instance and a persistent grid, launches on
+// `stream` and returns cudaGetLastError().
+cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stochastic,
+                          int bf16, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
+cudaError_t launch_vote(const VoteParams &p, bool vectorised, cudaStream_t stream);
+cudaError_t launch_fp8_quant(const Fp8Params &p, cudaStream_t stream);
+cudaError_t launch_fp8_dequant(const Fp8Params &p, cudaStream_t stream);
+
+// Persistent grid: min(work units, SMs x resident blocks of `kernel`).
+int persistent_grid(const void *kernel, int block, uint64_t units);
+
+}  // namespace qc

@@ -1,0 +1,214 @@
+/*
+ * qcodec.h -- C ABI of libqcodec, the communication codec that wraps a collective
+ * in data-parallel training: the sender quantizes a tensor for the wire, the
+ * receiver dequantizes (and aggregates) what arrived.
+ *
+ * Sources, by page title and section:
+ *   "Quantized Communication for Distributed Training", "Where Quantization Sits"
+ *       (quantize for wire -> collective -> dequantize on receipt) and "Numeric
+ *       Example" / "Pinterest QComms Example" (FP32 -> FP8 embedding payloads).
+ *   "Quantization for Communication", "Quantization Schemes" (uniform min/max,
+ *       stochastic rounding), "Quantized SGD Algorithms" (TernGrad, SignSGD with
+ *       majority vote), "Error Feedback for Quantization", "Quantization-Aware
+ *       All-Reduce" (accumulate in higher precision), "Hardware Acceleration"
+ *       (several low-bit values packed per 32-bit word).
+ *   "Gradient Compression and Quantised Collectives", "Why sparsification fights
+ *       the all-reduce" (signSGD majority vote) and "Error feedback is the
+ *       component that makes it work".
+ *
+ * Conventions shared by every call:
+ *   - Every buffer pointer is a DEVICE pointer on the current CUDA device.  The
+ *     caller allocates and frees every buffer; the library never allocates,
+ *     frees, or synchronises, and keeps no device state between calls.
+ *   - Every compute call is asynchronous on `stream` (0 = legacy default stream).
+ *     Arguments are validated on the host before any launch; on a non-OK status
+ *     nothing was launched and nothing was written, and qc_last_error() holds a
+ *     message.  QC_ERR_CUDA reports a launch error (cudaGetLastError after the
+ *     launch); a fault inside a kernel surfaces at the caller's next
+ *     synchronisation, as with any CUDA launch.
+ *   - n == 0 (or rows == 0) is a valid no-op that returns QC_OK.
+ *   - Outputs must not overlap inputs (checked for the buffers named per call).
+ *   - Element i of a flat tensor belongs to bucket k = i / bucket; bucket k spans
+ *     [k*bucket, min((k+1)*bucket, n)), so the last bucket may be partial.
+ *   - Packed codes: code i of a b-bit stream sits in 32-bit word i / (32/b) at
+ *     bit offset (i mod (32/b)) * b, least significant bits first.  Because
+ *     bucket % 32 == 0 no word holds codes of two buckets.  Padding codes past n
+ *     in the last word are written as 0.
+ *   - Arithmetic is IEEE-754 binary32 with round-to-nearest-even, one rounding per
+ *     operation as listed for each call; results are deterministic and do not
+ *     depend on the launch shape.
+ */
+#ifndef QCODEC_H
+#define QCODEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st *qc_stream_t;
+
+typedef enum {
+    QC_OK = 0,
+    QC_ERR_NULL = 1,          /* a required pointer is NULL                        */
+    QC_ERR_INVALID_ARG = 2,   /* bad size, bits, bucket, scheme, flag or overlap    */
+    QC_ERR_ALIGNMENT = 3,     /* a pointer or stride breaks the stated alignment    */
+    QC_ERR_UNSUPPORTED = 4,   /* valid in principle, outside this build's limits    */
+    QC_ERR_CUDA = 5           /* the CUDA runtime reported an error at launch       */
+} qc_status;
+
+typedef enum {
+    QC_SCHEME_UNIFORM = 0,    /* per-bucket min/max, 2^bits levels, fp32 scale+offset */
+    QC_SCHEME_SIGN = 1,       /* 1 bit: sign, per-bucket fp32 scale = mean |p|        */
+    QC_SCHEME_TERNARY = 2     /* 2 bits: {-1,0,+1} -> codes {0,1,2}, scale = max |p|  */
+} qc_scheme;
+
+typedef enum {
+    QC_ROUND_NEAREST = 0,
+    QC_ROUND_STOCHASTIC = 1   /* Philox4x32-10 keyed on (seed, step, element index) */
+} qc_round;
+
+typedef enum { QC_DTYPE_F32 = 0, QC_DTYPE_BF16 = 1 } qc_dtype;
+
+enum {
+    QC_OUT_SUM = 0,
+    QC_OUT_MEAN = 1,                 /* divide the fixed-order sum by M             */
+    QC_ACCUMULATE_INTO_OUT = 2       /* out = out + result instead of out = result  */
+};
+
+/* Largest supported worker count for decode and vote, and largest FP8 row. */
+#define QC_MAX_WORKERS 1024
+#define QC_MAX_FP8_DIM 4096
+
+/* Number of 32-bit words holding n codes of `bits` bits: ceil(n*bits/32). */
+size_t qc_code_words(size_t n, int bits);
+
+/* Number of buckets of `bucket` elements covering n elements: ceil(n/bucket);
+ * 0 when bucket is 0. */
+size_t qc_num_buckets(size_t n, size_t bucket);
+
+/*
+ * qc_encode_ef -- sender half: error-feedback compression of one flat gradient.
+ *
+ * "Quantization for Communication", "Error Feedback for Quantization":
+ *   e = e + grad; q = quantize(e); e = e - dequantize(q); communicate q.
+ * With err == NULL there is no error feedback and p = grad.
+ *
+ * Per element:  p_i = fl(err_i + grad_i)    (bf16 grad is widened exactly)
+ * Per bucket k, by scheme:
+ *   UNIFORM ("Quantization Schemes"): mn = min p, mx = max p (a zero result is
+ *     taken as +0), L = 2^bits - 1, scale = fl(fl(mx - mn) / L).
+ *     scale == 0: q_i = 0.  Else t_i = fl(fl(p_i - mn) / scale) and
+ *       NEAREST:    q_i = min(rint(t_i), L)                 (ties to even)
+ *       STOCHASTIC: q_i = min(floor(t_i) + [u_i < t_i - floor(t_i)], L)
+ *     deq_i = fma(q_i, scale, mn) (one rounding); scale[k] = scale, offset[k] = mn.
+ *   SIGN ("Quantized SGD Algorithms", SignSGD; bits must be 1, mode NEAREST):
+ *     s = mean over the bucket's elements of |p_i|, rounded once to binary32
+ *     from a compensated (double-word) sum; bit_i = [p_i >= 0];
+ *     deq_i = bit_i ? s : -s; scale[k] = s.  Within 1e-6 * max|p| of the exact
+ *     mean (the sum's order of operations is the only freedom).
+ *   TERNARY ("Quantized SGD Algorithms", TernGrad; bits must be 2):
+ *     s = max |p| (+0 for an all-zero bucket, then every code is 1).
+ *       STOCHASTIC: keep_i = [u_i < fl(|p_i| / s)];  NEAREST: keep_i = [fl(|p_i|/s) > 0.5]
+ *     code_i = keep_i ? (p_i > 0 ? 2 : 0) : 1; deq_i = (code_i - 1) * s; scale[k] = s.
+ * Then, with error feedback, err_i = fl(p_i - deq_i) is written in place.
+ *
+ * Stochastic draw for element i (global index within this call):
+ *   Philox4x32-10 (Salmon et al., SC'11) with key = (seed low 32, seed high 32),
+ *   counter = (i/4 low 32, i/4 high 32, step, 0); u_i = (word (i mod 4) >> 8) * 2^-24.
+ *
+ * grad   : n elements of `dtype`; 16-byte aligned (f32) or 8-byte aligned (bf16).
+ * err    : n fp32, in/out, 16-byte aligned, or NULL for no error feedback.
+ * bits   : UNIFORM 1, 2, 4 or 8; SIGN 1; TERNARY 2.
+ * bucket : elements per bucket, a multiple of 32, 32 <= bucket <= 2^24.
+ * codes  : out, qc_code_words(n, bits) uint32 words, 4-byte aligned.
+ * scale  : out, qc_num_buckets(n, bucket) fp32.
+ * offset : out, qc_num_buckets(n, bucket) fp32 for UNIFORM; ignored otherwise
+ *          (may be NULL).
+ */
+qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
+                       size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
+                       uint32_t step, uint32_t *codes, float *scale, float *offset,
+                       qc_stream_t stream);
+
+/*
+ * qc_decode_accumulate -- receiver half: dequantize M workers' payloads and
+ * accumulate them in fp32.
+ *
+ * "Quantization for Communication", "Quantization-Aware All-Reduce" (dequantize
+ * after the exchange; accumulate in higher precision) and "Gradient quantization
+ * for communication", "How Gradient Quantization Works" (dequantize, then
+ * average or sum).  For every element i (bucket k = i / bucket):
+ *   acc = +0; for w = 0 .. M-1 in this order: acc = fl(acc + d_w,i) with
+ *     UNIFORM d = fma(q, scale_w[k], offset_w[k]); SIGN d = bit ? s_w[k] : -s_w[k];
+ *     TERNARY d = (code - 1) * s_w[k]
+ *   r = (flags & QC_OUT_MEAN) ? fl(acc / M) : acc
+ *   out_i = (flags & QC_ACCUMULATE_INTO_OUT) ? fl(out_i + r) : r
+ *
+ * codes  : worker w's packed codes start at codes + w * codes_stride_words
+ *          (codes_stride_words >= qc_code_words(n, bits) when M > 1); 4-byte aligned.
+ * scale  : worker w's per-bucket scales at scale + w * meta_stride
+ *          (meta_stride >= qc_num_buckets(n, bucket) when M > 1).
+ * offset : same layout as scale; UNIFORM only (ignored otherwise, may be NULL).
+ * M      : 1 .. QC_MAX_WORKERS.   bits/scheme as for qc_encode_ef.
+ * out    : n fp32, 16-byte aligned; read only with QC_ACCUMULATE_INTO_OUT.
+ */
+qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
+                               const float *scale, const float *offset, size_t meta_stride,
+                               int M, size_t n, int bits, size_t bucket, qc_scheme scheme,
+                               float *out, int flags, qc_stream_t stream);
+
+/*
+ * qc_sign_vote -- signSGD aggregation by majority vote ("Quantization for
+ * Communication", "Quantized SGD Algorithms"; "Gradient Compression and
+ * Quantised Collectives", "Why sparsification fights the all-reduce").
+ *   c_i = number of workers whose sign bit i is set;  out bit i = [2 * c_i >= M]
+ * (a tie, possible for even M, gives 1, matching sign(0) = +1).  Bits past n in
+ * the last word are written as 0.
+ *
+ * signs        : worker w's qc_code_words(n, 1) words at signs + w * stride_words,
+ *                stride_words >= qc_code_words(n, 1) when M > 1; 4-byte aligned.
+ * M            : 1 .. QC_MAX_WORKERS.
+ * out          : qc_code_words(n, 1) uint32, 4-byte aligned.
+ * The vectorised path is taken when signs, out and stride_words keep 16-byte
+ * alignment; otherwise a word-at-a-time path gives the same result.
+ */
+qc_status qc_sign_vote(const uint32_t *signs, size_t stride_words, int M, size_t n,
+                       uint32_t *out, qc_stream_t stream);
+
+/*
+ * qc_rowwise_fp8 -- FP32 -> FP8 (OCP E4M3) row-wise quantization of an
+ * embedding lookup payload ("Quantized Communication for Distributed Training",
+ * "Numeric Example" and "Pinterest QComms Example").  Per row r:
+ *   a = max_j |x_rj| (+0 if zero);  sc = fl(a / 448)
+ *   sc == 0: codes 0x00, row_scale = 0;  else code_rj = e4m3_rn_satfinite(fl(x_rj / sc))
+ * x         : rows x dim fp32, row-major, 16-byte aligned.
+ * dim       : a multiple of 4, 4 <= dim <= QC_MAX_FP8_DIM.
+ * codes     : out, rows x dim bytes, row-major, 4-byte aligned.
+ * row_scale : out, rows fp32.
+ */
+qc_status qc_rowwise_fp8(const float *x, size_t rows, size_t dim, uint8_t *codes,
+                         float *row_scale, qc_stream_t stream);
+
+/*
+ * qc_rowwise_fp8_dequant -- receiver side of the FP8 payload:
+ *   out_rj = fl(e4m3_value(code_rj) * row_scale_r)   (the e4m3 value is exact)
+ * Layouts and limits as for qc_rowwise_fp8; out is 16-byte aligned.
+ */
+qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, size_t rows,
+                                 size_t dim, float *out, qc_stream_t stream);
+
+/* Message for the last non-OK status returned on the calling thread ("" if none). */
+const char *qc_last_error(void);
+
+/* Library version string. */
+const char *qc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QCODEC_H */

@@ -1,0 +1,140 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/qcodec.h declares, and rejects bad arguments on the host.
+
+Every call here fails validation (or is an n == 0 no-op) before any CUDA API is
+touched, so nothing is launched; the pointers are fake addresses never
+dereferenced.
+"""
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from embedding_communication_codecs_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q():
+    qbuild.build_library()
+    import embedding_communication_codecs_gb300 as q
+    return q
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "qcodec.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(q):
+    declared = _declared()
+    assert set(declared) == set(q.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", qbuild.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (qc_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared:
+        assert name in exported, name
+        assert hasattr(q.lib, name)
+
+
+def test_size_helpers(q):
+    assert q.qc_code_words(0, 8) == 0
+    assert q.qc_code_words(1, 1) == 1
+    assert q.qc_code_words(250_000_000, 4) == 31_250_000
+    assert q.qc_code_words(25_600_000, 1) == 800_000
+    assert q.qc_num_buckets(250_000_000, 512) == 488_282
+    assert q.qc_num_buckets(10, 0) == 0
+    assert "sm_103a" in q.qc_version()
+
+
+A = 0x10000          # fake, 256-byte aligned device addresses (never dereferenced)
+B = 0x20000000
+C = 0x30000000
+D = 0x40000000
+
+
+def _enc(q, **kw):
+    args = dict(grad=A, dtype=q.QC_DTYPE_F32, err=B, n=4096, bits=8, bucket=2048,
+                scheme=q.QC_SCHEME_UNIFORM, mode=q.QC_ROUND_NEAREST, seed=0, step=0, codes=C,
+                scale=D, offset=D + 0x100000, stream=0)
+    args.update(kw)
+    return q.lib.qc_encode_ef(args["grad"], args["dtype"], args["err"], args["n"], args["bits"],
+                              args["bucket"], args["scheme"], args["mode"], args["seed"],
+                              args["step"], args["codes"], args["scale"], args["offset"],
+                              args["stream"])
+
+
+def test_encode_rejects(q):
+    assert _enc(q, bits=3) == q.QC_ERR_INVALID_ARG
+    assert b"bits" in q.lib.qc_last_error()
+    assert _enc(q, scheme=q.QC_SCHEME_SIGN, bits=8) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scheme=q.QC_SCHEME_SIGN, bits=1, mode=q.QC_ROUND_STOCHASTIC) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scheme=q.QC_SCHEME_TERNARY, bits=1) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scheme=7) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, mode=5) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, dtype=9) == q.QC_ERR_INVALID_ARG
+    for bucket in (0, 16, 48, 2050, (1 << 24) + 32):
+        assert _enc(q, bucket=bucket) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, grad=None) == q.QC_ERR_NULL
+    assert _enc(q, codes=None) == q.QC_ERR_NULL
+    assert _enc(q, offset=None) == q.QC_ERR_NULL
+    assert _enc(q, grad=A + 4) == q.QC_ERR_ALIGNMENT
+    assert _enc(q, dtype=q.QC_DTYPE_BF16, grad=A + 4) == q.QC_ERR_ALIGNMENT
+    assert _enc(q, err=B + 8) == q.QC_ERR_ALIGNMENT
+    assert _enc(q, codes=C + 2) == q.QC_ERR_ALIGNMENT
+    # outputs overlapping inputs or each other
+    assert _enc(q, codes=A + 64) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scale=C) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, err=A) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, n=1 << 41) == q.QC_ERR_UNSUPPORTED
+
+
+def test_encode_empty_is_noop(q):
+    assert _enc(q, n=0, grad=None, codes=None, scale=None, offset=None) == q.QC_OK
+    assert q.lib.qc_last_error() == b""
+
+
+def test_decode_rejects(q):
+    def dec(**kw):
+        a = dict(codes=C, cs=1024, scale=D, offset=D + 0x100000, ms=2, M=2, n=4096, bits=8,
+                 bucket=2048, scheme=q.QC_SCHEME_UNIFORM, out=A, flags=0)
+        a.update(kw)
+        return q.lib.qc_decode_accumulate(a["codes"], a["cs"], a["scale"], a["offset"], a["ms"],
+                                          a["M"], a["n"], a["bits"], a["bucket"], a["scheme"],
+                                          a["out"], a["flags"], 0)
+    assert dec(M=0) == q.QC_ERR_INVALID_ARG
+    assert dec(M=q.QC_MAX_WORKERS + 1) == q.QC_ERR_INVALID_ARG
+    assert dec(flags=4) == q.QC_ERR_INVALID_ARG
+    assert dec(cs=1023) == q.QC_ERR_INVALID_ARG
+    assert dec(ms=1) == q.QC_ERR_INVALID_ARG
+    assert dec(bits=3) == q.QC_ERR_INVALID_ARG
+    assert dec(scheme=q.QC_SCHEME_TERNARY, bits=8) == q.QC_ERR_INVALID_ARG
+    assert dec(out=None) == q.QC_ERR_NULL
+    assert dec(offset=None) == q.QC_ERR_NULL
+    assert dec(out=A + 4) == q.QC_ERR_ALIGNMENT
+    assert dec(out=C) == q.QC_ERR_INVALID_ARG
+    assert dec(n=0, codes=None, out=None) == q.QC_OK
+
+
+def test_vote_and_fp8_reject(q):
+    L = q.lib
+    assert L.qc_sign_vote(C, 8, 0, 256, A, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_sign_vote(C, 7, 2, 256, A, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_sign_vote(None, 8, 2, 256, A, 0) == q.QC_ERR_NULL
+    assert L.qc_sign_vote(C + 2, 8, 2, 256, A, 0) == q.QC_ERR_ALIGNMENT
+    assert L.qc_sign_vote(C, 8, 2, 256, C + 4, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_sign_vote(C, 8, 2, 0, None, 0) == q.QC_OK
+    assert L.qc_rowwise_fp8(A, 10, 6, C, D, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_rowwise_fp8(A, 10, 0, C, D, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_rowwise_fp8(A, 10, 8192, C, D, 0) == q.QC_ERR_UNSUPPORTED
+    assert L.qc_rowwise_fp8(A + 8, 10, 128, C, D, 0) == q.QC_ERR_ALIGNMENT
+    assert L.qc_rowwise_fp8(None, 10, 128, C, D, 0) == q.QC_ERR_NULL
+    assert L.qc_rowwise_fp8(A, 10, 128, A + 256, D, 0) == q.QC_ERR_INVALID_ARG
+    assert L.qc_rowwise_fp8(A, 0, 128, None, None, 0) == q.QC_OK
+    assert L.qc_rowwise_fp8_dequant(C, D, 10, 128, A + 4, 0) == q.QC_ERR_ALIGNMENT
+    assert L.qc_rowwise_fp8_dequant(C, D, 10, 128, C, 0) == q.QC_ERR_INVALID_ARG
