@@ -11,7 +11,7 @@ Every step runs in hand-written CUDA kernels for sm_103a inside ``libqcodec.so``
 The functions here only pass torch tensors' device pointers and the current
 stream through the C ABI declared in ``include/qcodec.h``, under the same names.
 There is no CPU fallback: importing this package fails if the library has not
-been built (``python -m embedding_communication_codecs_gb300.build``).
+been built (``python embedding_communication_codecs_gb300/build.py``).
 """
 from __future__ import annotations
 
@@ -46,7 +46,7 @@ class QCodecError(RuntimeError):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m embedding_communication_codecs_gb300.build`")
+                          "`python embedding_communication_codecs_gb300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P, S, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     U64, U32 = ctypes.c_uint64, ctypes.c_uint32

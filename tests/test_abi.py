@@ -13,9 +13,10 @@ import subprocess
 
 import pytest
 
-from embedding_communication_codecs_gb300 import build as qbuild
+import __graft_entry__
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+qbuild = __graft_entry__._build_module()
 
 
 @pytest.fixture(scope="module")
