@@ -33,8 +33,8 @@ STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ER
 
 # Every symbol the C ABI exports, in header order.
 EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
-           "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_last_error",
-           "qc_version")
+           "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
+           "qc_last_error", "qc_version")
 
 
 class QCodecError(RuntimeError):
@@ -60,6 +60,7 @@ def _load():
     for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8",
                  "qc_rowwise_fp8_dequant"):
         getattr(lib, name).restype = I
+    lib.qc_take_device_errors.argtypes, lib.qc_take_device_errors.restype = [P], I
     lib.qc_last_error.argtypes, lib.qc_last_error.restype = [], ctypes.c_char_p
     lib.qc_version.argtypes, lib.qc_version.restype = [], ctypes.c_char_p
     return lib
@@ -90,6 +91,14 @@ def _stream(stream):
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def qc_take_device_errors() -> int:
+    """Synchronise the device and return (and clear) the pipelined kernels'
+    device-side error flags; 0 means no wait ever timed out."""
+    flags = ctypes.c_uint32(0)
+    _check(lib.qc_take_device_errors(ctypes.byref(flags)))
+    return int(flags.value)
 
 
 def qc_version() -> str:

@@ -52,24 +52,50 @@ int team_warps_for(size_t elems) {
     return w;
 }
 
+// Tiling for the TMA-pipelined encode: whole buckets per tile, the bucket count
+// a multiple of the block's teams, at least 16 KB of input per stage and three
+// stages (two above 32 KB), so small stages leave room for 4 blocks per SM.  Buckets larger than one team window (4096) and
+// gradients whose base is not 16-byte aligned take the direct kernel.
+bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool grad16,
+                      qc::EncodeTiles &t) {
+    if (!grad16 || p.two_pass) return false;
+    const size_t per_elem = esize + (ef ? 4 : 0);
+    const uint32_t teams = (qc::kBlock / 32) / p.team_warps;
+    const size_t target = 16 * 1024;
+    uint32_t tb = static_cast<uint32_t>(target / (static_cast<size_t>(p.bucket) * per_elem));
+    tb = tb / teams * teams;
+    if (tb < teams) tb = teams;
+    const size_t stage = static_cast<size_t>(tb) * p.bucket * per_elem;
+    if (stage > 64 * 1024) return false;
+    const uint32_t stages = stage <= 32 * 1024 ? 3u : 2u;
+    t.tb = tb;
+    t.te = tb * p.bucket;
+    t.stages = stages;
+    t.stage_bytes = static_cast<uint32_t>(stage);
+    t.e_offset = static_cast<uint32_t>(static_cast<size_t>(t.te) * esize);
+    t.ntiles = (p.n + t.te - 1) / t.te;
+    return true;
+}
+
 }  // namespace
 
 namespace qc {
 
-int persistent_grid(const void *kernel, int block, uint64_t units) {
+int persistent_grid(const void *kernel, int block, uint64_t units, size_t smem) {
     static std::mutex mu;
-    static std::unordered_map<uint64_t, int> cache;  // (device, kernel) -> blocks per SM
+    static std::unordered_map<uint64_t, int> cache;  // (device, kernel, smem) -> blocks per SM
     static std::unordered_map<int, int> sms;
     int dev = 0;
     cudaGetDevice(&dev);
-    const uint64_t key = (static_cast<uint64_t>(dev) << 48) ^ reinterpret_cast<uintptr_t>(kernel);
+    const uint64_t key = (static_cast<uint64_t>(dev) << 56) ^ (static_cast<uint64_t>(smem) << 40) ^
+                         reinterpret_cast<uintptr_t>(kernel);
     int per_sm = 0, nsm = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
         if (it == cache.end()) {
             int b = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, 0) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, smem) != cudaSuccess ||
                 b < 1)
                 b = 1;
             it = cache.emplace(key, b).first;
@@ -90,6 +116,21 @@ int persistent_grid(const void *kernel, int block, uint64_t units) {
     return static_cast<int>(g);
 }
 
+cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, size_t> done;  // (device, kernel) -> limit set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t key = (static_cast<uint64_t>(dev) << 56) ^ reinterpret_cast<uintptr_t>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(bytes));
+    if (e == cudaSuccess) done[key] = bytes;
+    return e;
+}
+
 }  // namespace qc
 
 extern "C" {
@@ -106,7 +147,16 @@ size_t qc_num_buckets(size_t n, size_t bucket) {
 
 const char *qc_last_error(void) { return g_last_error; }
 
-const char *qc_version(void) { return "libqcodec 0.1.0 (sm_103a)"; }
+const char *qc_version(void) { return "libqcodec 0.2.0 (sm_103a)"; }
+
+qc_status qc_take_device_errors(uint32_t *flags) {
+    if (!flags) return fail(QC_ERR_NULL, "qc_take_device_errors: flags must be non-NULL");
+    *flags = 0;
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
+    *flags = qc::take_encode_errors();
+    return from_cuda(cudaGetLastError(), "qc_take_device_errors");
+}
 
 qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
                        size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
@@ -169,8 +219,14 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     p.codes = codes;
     p.scale = scale;
     p.offset = offset;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    qc::EncodeTiles tiles{};
+    if (encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))
+        return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
+                                               dtype == QC_DTYPE_BF16, st),
+                         "qc_encode_ef");
     return from_cuda(qc::launch_encode(p, scheme, bits, mode == QC_ROUND_STOCHASTIC,
-                                       dtype == QC_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                                       dtype == QC_DTYPE_BF16, st),
                      "qc_encode_ef");
 }
 

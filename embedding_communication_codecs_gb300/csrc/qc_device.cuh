@@ -19,17 +19,33 @@ constexpr unsigned kFull = 0xffffffffu;
 // the 32x32->64 products of counter words 0 and 2 with the two round
 // multipliers; the new words 0 and 2 are the high halves xor the other counter
 // word and a key word, the new words 1 and 3 are the low halves.  The key is
-// advanced by the two Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+// advanced by the two Weyl constants between rounds; the ten round keys depend
+// only on the seed and are computed once per thread.
+struct PhiloxKeys {
+    uint32_t a[10], b[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
     constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+    PhiloxKeys k;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        k.a[r] = k0;
+        k.b[r] = k1;
+        k0 += kWeylA;
+        k1 += kWeylB;
+    }
+    return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &k) {
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
         const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
-        c = make_uint4(hiB ^ c.y ^ k0, loB, hiA ^ c.w ^ k1, loA);
-        k0 += kWeylA;
-        k1 += kWeylB;
+        c = make_uint4(hiB ^ c.y ^ k.a[r], loB, hiA ^ c.w ^ k.b[r], loA);
     }
     return c;
 }
@@ -37,12 +53,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // Four uniform draws u in [0, 1) for elements i0 .. i0+3 (i0 % 4 == 0):
 // counter (i0/4 low, i0/4 high, step, 0), key (seed low, seed high),
 // u = (word >> 8) * 2^-24, exact in binary32.
-__device__ __forceinline__ void uniform4(uint64_t i0, uint64_t seed, uint32_t step,
+__device__ __forceinline__ void uniform4(uint64_t i0, uint32_t step, const PhiloxKeys &k,
                                          float u[4]) {
     const uint64_t blk = i0 >> 2;
     const uint4 r = philox4x32_10(
-        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), step, 0u),
-        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), step, 0u), k);
     u[0] = __fmul_rn(__uint2float_rn(r.x >> 8), 0x1p-24f);
     u[1] = __fmul_rn(__uint2float_rn(r.y >> 8), 0x1p-24f);
     u[2] = __fmul_rn(__uint2float_rn(r.z >> 8), 0x1p-24f);
@@ -158,12 +173,15 @@ struct GradLoad<float> {
     static __device__ __forceinline__ float one(const float *g, uint64_t i) { return __ldcs(g + i); }
 };
 
+__device__ __forceinline__ float4 unpack_bf16x4(uint2 v) {
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+}
+
 template <>
 struct GradLoad<uint16_t> {
     static __device__ __forceinline__ float4 full(const uint16_t *g, uint64_t i) {
-        const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(g + i));
-        return make_float4(bf16_bits_to_float(v.x & 0xFFFFu), bf16_bits_to_float(v.x >> 16),
-                           bf16_bits_to_float(v.y & 0xFFFFu), bf16_bits_to_float(v.y >> 16));
+        return unpack_bf16x4(__ldcs(reinterpret_cast<const uint2 *>(g + i)));
     }
     static __device__ __forceinline__ float one(const uint16_t *g, uint64_t i) {
         return bf16_bits_to_float(__ldcs(reinterpret_cast<const unsigned short *>(g + i)));

@@ -1,0 +1,325 @@
+// qc_encode_math.cuh -- per-bucket statistics, bucket parameters, per-element
+// quantization and the slot-level quantize/store step shared by the encode
+// kernels (direct and TMA-pipelined).
+//
+// "Quantization for Communication", "Quantization Schemes" (uniform min/max:
+// scale = (max - min) / (2^bits - 1), q = round((x - min) / scale), x ~ q * scale
+// + min; stochastic rounding takes the floor with probability 1 - frac and the
+// ceiling with probability frac), "Quantized SGD Algorithms" (TernGrad
+// {-1, 0, +1} with a scale; SignSGD), "Error Feedback for Quantization"
+// (e = e + g; q = quantize(e); e = e - dequantize(q)), "Hardware Acceleration"
+// (low-bit codes packed into 32-bit words).
+//
+// Team geometry: a team of W warps (team_threads = 32 W) owns one bucket; slot s
+// of team thread tt covers bucket elements j = (s * team_threads + tt) * 4 ..
+// j + 3, so each slot is one coalesced sweep over 128 W consecutive elements.
+#pragma once
+
+#include "qc_device.cuh"
+#include "qc_internal.h"
+
+namespace qc {
+
+// ------------------------------------------------------------------ statistics
+
+template <int SCHEME>
+struct Stats;
+
+template <>
+struct Stats<kUniform> {  // min and max of p
+    float mn, mx;
+    __device__ void init() { mn = __int_as_float(0x7f800000); mx = -mn; }
+    __device__ void add(float x) { mn = fminf(mn, x); mx = fmaxf(mx, x); }
+    __device__ void warp_reduce() { mn = warp_min(mn); mx = warp_max(mx); }
+    __device__ void merge(const Stats &o) { mn = fminf(mn, o.mn); mx = fmaxf(mx, o.mx); }
+};
+
+template <>
+struct Stats<kTernary> {  // max |p|
+    float amax;
+    __device__ void init() { amax = 0.0f; }
+    __device__ void add(float x) { amax = fmaxf(amax, fabsf(x)); }
+    __device__ void warp_reduce() { amax = warp_max(amax); }
+    __device__ void merge(const Stats &o) { amax = fmaxf(amax, o.amax); }
+};
+
+template <>
+struct Stats<kSign> {  // sum of |p| as a double word
+    DWord sum;
+    __device__ void init() { sum = DWord{0.0f, 0.0f}; }
+    __device__ void add(float x) { sum = dw_add(sum, fabsf(x)); }
+    __device__ void warp_reduce() { sum = warp_sum(sum); }
+    __device__ void merge(const Stats &o) { sum = dw_add(sum, o.sum); }
+};
+
+// Per-bucket quantization parameters derived from the statistics.
+struct BucketParams {
+    float a;      // UNIFORM: min (offset); SIGN / TERNARY: s
+    float scale;  // UNIFORM: (max - min) / L
+};
+
+template <int SCHEME, int BITS>
+struct Finish;
+
+template <int BITS>
+struct Finish<kUniform, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kUniform> &st, uint32_t) {
+        const float mn = positive_zero(st.mn), mx = positive_zero(st.mx);
+        constexpr float L = static_cast<float>((1u << BITS) - 1u);
+        return BucketParams{mn, __fdiv_rn(__fsub_rn(mx, mn), L)};
+    }
+};
+
+template <int BITS>
+struct Finish<kTernary, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kTernary> &st, uint32_t) {
+        return BucketParams{positive_zero(st.amax), 0.0f};
+    }
+};
+
+template <int BITS>
+struct Finish<kSign, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kSign> &st, uint32_t cnt) {
+        return BucketParams{dw_div(st.sum, static_cast<float>(cnt)), 0.0f};
+    }
+};
+
+// ------------------------------------------------------------- per element
+
+// Code and dequantized value of one element.
+template <int SCHEME, int BITS, bool SR>
+__device__ __forceinline__ uint32_t quantize(float p, float u, const BucketParams &bp,
+                                             float &deq) {
+    if constexpr (SCHEME == kUniform) {
+        constexpr uint32_t L = (1u << BITS) - 1u;
+        if (bp.scale == 0.0f) {
+            deq = bp.a;
+            return 0u;
+        }
+        const float t = __fdiv_rn(__fsub_rn(p, bp.a), bp.scale);
+        uint32_t q = rint_small(t);
+        if constexpr (SR) {
+            // floor(t) = rint(t) - [rint(t) > t]; frac = t - floor(t) is exact
+            if (small_uint_to_float(q) > t) q -= 1u;
+            const float fr = __fsub_rn(t, small_uint_to_float(q));
+            q += (u < fr) ? 1u : 0u;
+        }
+        q = min(q, L);
+        deq = __fmaf_rn(small_uint_to_float(q), bp.scale, bp.a);
+        return q;
+    } else if constexpr (SCHEME == kSign) {
+        const bool pos = p >= 0.0f;
+        deq = pos ? bp.a : -bp.a;
+        return pos ? 1u : 0u;
+    } else {  // ternary
+        const float s = bp.a;
+        if (s == 0.0f) {
+            deq = 0.0f;
+            return 1u;
+        }
+        const float pr = __fdiv_rn(fabsf(p), s);
+        const bool keep = SR ? (u < pr) : (pr > 0.5f);
+        if (!keep) {
+            deq = 0.0f;
+            return 1u;
+        }
+        deq = p > 0.0f ? s : -s;
+        return p > 0.0f ? 2u : 0u;
+    }
+}
+
+// ------------------------------------------------- division-free decisions
+//
+// The divisions t = (p - mn) / scale (uniform) and pr = |p| / s (ternary) only
+// decide an integer: a level, a floor, or a comparison with a draw u.  With
+// rinv = RN(1 / scale) the product ta = RN(d * rinv) is within
+// 3 * 2^-24 * (d / scale) of d / scale, hence within
+//   delta = (L + 1) * 2^-22        (uniform; d / scale <= L (1 + 2^-22))
+//   delta = 2^-22                  (ternary; |p| / s <= 1)
+// of the correctly rounded quotient t = RN(d / scale).  When ta is farther than
+// 2 * delta from every decision boundary (half-integers for nearest rounding;
+// integers and u for stochastic rounding; u or 1/2 for ternary) the decision
+// taken on ta is the decision on t, so the code is the one the IEEE division
+// gives.  Otherwise the element is recomputed with the division.  The bound
+// needs rinv to be a normal number: buckets whose scale lies outside
+// [2^-125, 2^125] (including scale == 0) use the division throughout.
+struct FastQ {
+    float rinv;
+    float delta2;  // twice the bound, covering the rounding of u - ta as well
+    bool usable;
+};
+
+template <int SCHEME, int BITS>
+__device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
+    const float d = (SCHEME == kUniform) ? bp.scale : bp.a;
+    FastQ f;
+    f.usable = (SCHEME != kSign) && d >= 0x1p-125f && d <= 0x1p125f;
+    f.rinv = f.usable ? __frcp_rn(d) : 0.0f;
+    f.delta2 = (SCHEME == kUniform) ? static_cast<float>(1u << BITS) * 0x1p-21f : 0x1p-21f;
+    return f;
+}
+
+// Code and dequantized value of one element from ta; sets redo when the
+// decision is within reach of the approximation error.
+template <int SCHEME, int BITS, bool SR>
+__device__ __forceinline__ uint32_t quantize_fast(float p, float u, const BucketParams &bp,
+                                                  const FastQ &fq, float &deq, bool &redo) {
+    if constexpr (SCHEME == kUniform) {
+        constexpr uint32_t L = (1u << BITS) - 1u;
+        const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
+        uint32_t q = rint_small(ta);
+        const float r = __fsub_rn(ta, small_uint_to_float(q));  // exact, in [-1/2, 1/2]
+        if constexpr (!SR) {
+            redo = fabsf(r) >= 0.5f - fq.delta2;
+        } else {
+            const bool below = r < 0.0f;
+            const float fr = below ? __fadd_rn(r, 1.0f) : r;  // ta - floor(ta), exact
+            q -= below ? 1u : 0u;
+            redo = (fr <= fq.delta2) | (fr >= 1.0f - fq.delta2) |
+                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
+            q += (u < fr) ? 1u : 0u;
+        }
+        q = min(q, L);
+        deq = __fmaf_rn(small_uint_to_float(q), bp.scale, bp.a);
+        return q;
+    } else if constexpr (SCHEME == kTernary) {
+        const float s = bp.a;
+        const float pa = __fmul_rn(fabsf(p), fq.rinv);
+        bool keep;
+        if constexpr (SR) {
+            keep = u < pa;
+            redo = fabsf(__fsub_rn(u, pa)) <= fq.delta2;
+        } else {
+            keep = pa > 0.5f;
+            redo = fabsf(__fsub_rn(pa, 0.5f)) <= fq.delta2;
+        }
+        if (!keep) {
+            deq = 0.0f;
+            return 1u;
+        }
+        deq = p > 0.0f ? s : -s;
+        return p > 0.0f ? 2u : 0u;
+    } else {
+        redo = false;
+        return quantize<SCHEME, BITS, SR>(p, u, bp, deq);
+    }
+}
+
+// ------------------------------------------------------------- slot level
+
+// Adds the valid elements of the lane's slots to the statistics.
+template <int SCHEME>
+__device__ __forceinline__ void accumulate_slots(Stats<SCHEME> &st, const float4 (&p)[kSlots],
+                                                 int tt, int team_threads, uint32_t cnt) {
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
+        if (j + 4u <= cnt) {
+            st.add(p[s].x);
+            st.add(p[s].y);
+            st.add(p[s].z);
+            st.add(p[s].w);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (j + c < cnt) st.add(get(p[s], c));
+        }
+    }
+}
+
+// Quantizes the lane's slots of bucket [b0, b0 + cnt), packs and stores the code
+// words, and (with error feedback) stores the new residual.  All 32 lanes of the
+// warp must call this together (the packing uses shuffles).
+template <int SCHEME, int BITS, bool SR, bool EF>
+__device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err, uint64_t b0,
+                                                     uint32_t cnt, int tt, int team_threads,
+                                                     int lane, const float4 (&p)[kSlots],
+                                                     const BucketParams &bp, uint32_t step,
+                                                     const PhiloxKeys &keys) {
+    const FastQ fq = fast_params<SCHEME, BITS>(bp);
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
+        const uint64_t i = b0 + j;
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (SR) {
+            if (j < cnt) uniform4(i, step, keys, u);
+        }
+        uint32_t field = 0;
+        float4 e;
+        if (j + 4u <= cnt && fq.usable) {
+            float d[4];
+            bool redo[4];
+            uint32_t q[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                q[c] = quantize_fast<SCHEME, BITS, SR>(get(p[s], c), u[c], bp, fq, d[c], redo[c]);
+            if (redo[0] | redo[1] | redo[2] | redo[3]) {  // rare: near a decision boundary
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (redo[c]) q[c] = quantize<SCHEME, BITS, SR>(get(p[s], c), u[c], bp, d[c]);
+            }
+            field = q[0] | (q[1] << BITS) | (q[2] << (2 * BITS)) | (q[3] << (3 * BITS));
+            e = make_float4(__fsub_rn(p[s].x, d[0]), __fsub_rn(p[s].y, d[1]),
+                            __fsub_rn(p[s].z, d[2]), __fsub_rn(p[s].w, d[3]));
+        } else if (j + 4u <= cnt) {
+            float d0, d1, d2, d3;
+            field = quantize<SCHEME, BITS, SR>(p[s].x, u[0], bp, d0) |
+                    (quantize<SCHEME, BITS, SR>(p[s].y, u[1], bp, d1) << BITS) |
+                    (quantize<SCHEME, BITS, SR>(p[s].z, u[2], bp, d2) << (2 * BITS)) |
+                    (quantize<SCHEME, BITS, SR>(p[s].w, u[3], bp, d3) << (3 * BITS));
+            e = make_float4(__fsub_rn(p[s].x, d0), __fsub_rn(p[s].y, d1), __fsub_rn(p[s].z, d2),
+                            __fsub_rn(p[s].w, d3));
+        } else {
+            e = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (j + c < cnt) {
+                    float deq;
+                    const float pc = get(p[s], c);
+                    field |= quantize<SCHEME, BITS, SR>(pc, u[c], bp, deq) << (c * BITS);
+                    set(e, c, __fsub_rn(pc, deq));
+                }
+            }
+        }
+        const uint32_t word = gather_word<BITS>(field);
+        if (j < cnt && stores_word<BITS>(lane)) __stcs(codes + (i * BITS) / 32u, word);
+        if constexpr (EF) {
+            if (j + 4u <= cnt) {
+                __stcs(reinterpret_cast<float4 *>(err + i), e);
+            } else if (j < cnt) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (j + c < cnt) err[i + c] = get(e, c);
+            }
+        }
+    }
+}
+
+template <int SCHEME>
+__device__ __forceinline__ void store_meta(float *scale, float *offset, uint64_t k,
+                                           const BucketParams &bp) {
+    if constexpr (SCHEME == kUniform) {
+        scale[k] = bp.scale;
+        offset[k] = bp.a;
+    } else {
+        scale[k] = bp.a;
+    }
+}
+
+// Team-wide reduction of the statistics: warp butterflies, then (W > 1) one
+// exchange through shared memory.  Every thread of the block must call it.
+template <int SCHEME>
+__device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
+                                            int &buf, int W, int warp, int lane, int team) {
+    st.warp_reduce();
+    if (W > 1) {
+        if (lane == 0) red[buf][warp] = st;
+        __syncthreads();
+        st = red[buf][team * W];
+        for (int w = 1; w < W; ++w) st.merge(red[buf][team * W + w]);
+        buf ^= 1;
+    }
+}
+
+}  // namespace qc

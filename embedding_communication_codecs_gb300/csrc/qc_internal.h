@@ -29,6 +29,22 @@ struct EncodeParams {
     float *offset;
 };
 
+// Tiling of the TMA-pipelined encode: TB whole buckets per tile (TE elements),
+// `stages` shared-memory stages of stage_bytes each; the residual's part of a
+// stage starts at e_offset.
+struct EncodeTiles {
+    uint32_t tb;
+    uint32_t te;
+    uint32_t stages;
+    uint32_t stage_bytes;
+    uint32_t e_offset;
+    uint64_t ntiles;
+};
+
+inline size_t encode_tiles_smem(const EncodeTiles &g, size_t stats_bytes) {
+    return static_cast<size_t>(g.stages) * g.stage_bytes + 8u * g.stages + 2u * 8u * stats_bytes;
+}
+
 struct DecodeParams {
     const uint32_t *codes;
     uint64_t codes_stride;  // words
@@ -69,12 +85,21 @@ struct Fp8Params {
 // `stream` and returns cudaGetLastError().
 cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stochastic,
                           int bf16, cudaStream_t stream);
+cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
+                              int stochastic, int bf16, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
 cudaError_t launch_vote(const VoteParams &p, bool vectorised, cudaStream_t stream);
 cudaError_t launch_fp8_quant(const Fp8Params &p, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const Fp8Params &p, cudaStream_t stream);
 
-// Persistent grid: min(work units, SMs x resident blocks of `kernel`).
-int persistent_grid(const void *kernel, int block, uint64_t units);
+// Persistent grid: min(work units, SMs x resident blocks of `kernel` with
+// `smem` bytes of dynamic shared memory).
+int persistent_grid(const void *kernel, int block, uint64_t units, size_t smem = 0);
+
+// Raises the kernel's dynamic shared memory limit to `bytes` (once per device).
+cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
+
+// Device-side error flags of the pipelined kernels (read and cleared).
+uint32_t take_encode_errors();
 
 }  // namespace qc

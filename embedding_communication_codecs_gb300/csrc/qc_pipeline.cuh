@@ -1,0 +1,91 @@
+// qc_pipeline.cuh -- multi-stage shared-memory pipeline fed by the Tensor Memory
+// Accelerator's bulk copies (cp.async.bulk, 1-D), with mbarrier completion.
+//
+// One thread of a block issues the bulk copies of a tile into a stage and arms
+// the stage's mbarrier with the byte count; every consumer thread waits on the
+// barrier's phase before reading the stage.  Small per-bucket metadata that has
+// no 16-byte alignment guarantee is fetched with 4-byte cp.async copies whose
+// completion is tracked on the same barrier (cp.async.mbarrier.arrive.noinc).
+//
+// Every wait is bounded: after kWaitRounds unsuccessful try_wait rounds the wait
+// gives up and reports failure, the block stops at its next block-wide
+// agreement point, and the kernel records the failure in a device flag that the
+// host reads with qc_take_device_errors().  Nothing spins forever.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qc {
+
+constexpr uint32_t kWaitRounds = 1u << 22;
+constexpr uint32_t kErrPipelineTimeout = 1u;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global memory into this block's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (no alignment beyond 4 bytes).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase with the given parity; false if it never completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t r = 0; r < kWaitRounds; ++r)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__host__ __device__ constexpr uint32_t floor16(uint64_t bytes) {
+    return static_cast<uint32_t>(bytes & ~static_cast<uint64_t>(15));
+}
+
+}  // namespace qc

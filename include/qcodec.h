@@ -19,7 +19,8 @@
  * Conventions shared by every call:
  *   - Every buffer pointer is a DEVICE pointer on the current CUDA device.  The
  *     caller allocates and frees every buffer; the library never allocates,
- *     frees, or synchronises, and keeps no device state between calls.
+ *     frees, or synchronises, and keeps no device state between calls apart from
+ *     the error flags that qc_take_device_errors() reads.
  *   - Every compute call is asynchronous on `stream` (0 = legacy default stream).
  *     Arguments are validated on the host before any launch; on a non-OK status
  *     nothing was launched and nothing was written, and qc_last_error() holds a
@@ -200,6 +201,19 @@ qc_status qc_rowwise_fp8(const float *x, size_t rows, size_t dim, uint8_t *codes
  */
 qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, size_t rows,
                                  size_t dim, float *out, qc_stream_t stream);
+
+/*
+ * qc_take_device_errors -- device-side failures of the pipelined kernels.
+ *
+ * The kernels that stream tiles through shared memory wait on mbarriers with
+ * an iteration limit; a wait that runs out stops its block and sets a flag in
+ * device memory instead of spinning forever.  This call synchronises the
+ * current device, stores the OR of the flags set since the previous call in
+ * *flags (bit 0: a pipeline wait timed out; the outputs of that launch are
+ * incomplete) and clears them.  It is a diagnostic call: it blocks the host and
+ * must not be used inside stream capture.
+ */
+qc_status qc_take_device_errors(uint32_t *flags);
 
 /* Message for the last non-OK status returned on the calling thread ("" if none). */
 const char *qc_last_error(void);

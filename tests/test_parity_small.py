@@ -31,6 +31,14 @@ def q():
     return q
 
 
+@pytest.fixture(autouse=True)
+def no_device_errors(q):
+    """No pipelined kernel may report a timed-out wait."""
+    q.qc_take_device_errors()
+    yield
+    assert q.qc_take_device_errors() == 0
+
+
 class Guarded:
     """A device tensor between canary regions."""
 
@@ -174,6 +182,82 @@ def test_encode_degenerate_buckets(q, bits):
         assert_bits_equal(scale, s_or, tag + " scale")
         assert_bits_equal(offset, o_or, tag + " offset")
         assert_bits_equal(err, e_or, tag + " err")
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_encode_decision_boundaries(q, bits):
+    """Elements exactly on, and one ulp either side of, every rounding decision:
+    half-integer levels (ties to even), integer levels (the floor of stochastic
+    rounding), and for the ternary scheme |p| / s = 1/2 and |p| = s."""
+    L = (1 << bits) - 1
+    bucket = 512
+    c = np.float32(2.0 ** -6)
+    vals = []
+    for k in range(L + 1):
+        for frac in (0.0, 0.5):
+            v = np.float32((k + frac) * c)
+            vals += [v, np.nextafter(v, np.float32(1e9)), np.nextafter(v, np.float32(-1e9))]
+    vals = np.array(vals, dtype=np.float32)
+    vals = vals[(vals >= 0) & (vals <= np.float32(L * c))]
+    reps = -(-bucket // vals.size)
+    g = np.tile(vals, reps * 6)[:6 * bucket].astype(np.float32)
+    for k in range(6):                         # pin min 0 and max L*c in every bucket
+        g[k * bucket] = 0.0
+        g[k * bucket + 1] = np.float32(L * c)
+    for mode in (0, 1):
+        for scheme, b in ((0, bits), (2, 2)):
+            if scheme == 2 and bits != 2:
+                continue
+            gg = g.copy()
+            if scheme == 2:
+                gg = np.where(np.arange(gg.size) % 3 == 0, np.float32(0.5), gg).astype(np.float32)
+                gg[::bucket] = 1.0
+            codes, scale, offset, err = _run_encode(q, gg, np.zeros_like(gg), gg.size, b, bucket,
+                                                    scheme, mode)
+            e_or = np.zeros_like(gg)
+            if scheme == 0:
+                c_or, s_or, o_or = orc.encode_uniform(gg, e_or, bits=b, bucket=bucket, mode=mode,
+                                                      seed=SEED, step=STEP)
+                assert s_or[0] == c
+            else:
+                c_or, s_or = orc.encode_ternary(gg, e_or, bucket=bucket, mode=mode, seed=SEED,
+                                                step=STEP)
+            tag = f"boundaries scheme={scheme} b={b} mode={mode}"
+            assert_bits_equal(codes, c_or, tag + " codes")
+            assert_bits_equal(scale, s_or, tag + " scale")
+            assert_bits_equal(err, e_or, tag + " err")
+
+
+@pytest.mark.parametrize("scheme,bits,mode", [(0, 8, 0), (0, 4, 1), (1, 1, 0), (2, 2, 1)])
+def test_encode_bf16_unaligned_base(q, scheme, bits, mode):
+    """A bf16 gradient that is 8- but not 16-byte aligned takes the direct kernel;
+    results are the same as the oracle's (and so as the pipelined kernel's)."""
+    bucket, n = 1024, 1024 * 9 + 20
+    g = wl.to_bf16_bits(wl.outlier_gradient(n, seed=21))
+    base = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    view = base[4:4 + n]
+    view.copy_(torch.from_numpy(g.view(np.int16)).cuda())
+    assert view.data_ptr() % 16 == 8
+    words, nb = q.qc_code_words(n, bits), q.qc_num_buckets(n, bucket)
+    codes = torch.empty(words, dtype=torch.int32, device="cuda")
+    scale = torch.empty(nb, device="cuda")
+    offset = torch.empty(nb, device="cuda") if scheme == 0 else None
+    err = torch.zeros(n, device="cuda")
+    q.qc_encode_ef(view, err, n, bits, bucket, scheme, mode, SEED, STEP, codes, scale, offset,
+                   dtype=q.QC_DTYPE_BF16)
+    e_or = np.zeros(n, dtype=np.float32)
+    if scheme == 0:
+        c_or, s_or, o_or = orc.encode_uniform(g, e_or, bits=bits, bucket=bucket, mode=mode,
+                                              seed=SEED, step=STEP)
+        assert_bits_equal(host(offset), o_or)
+    elif scheme == 1:
+        c_or, s_or = orc.encode_sign(g, e_or, bucket=bucket)
+    else:
+        c_or, s_or = orc.encode_ternary(g, e_or, bucket=bucket, mode=mode, seed=SEED, step=STEP)
+    assert_bits_equal(u32(codes), c_or, "codes")
+    if scheme != 1:
+        assert_bits_equal(host(scale), s_or, "scale")
+        assert_bits_equal(host(err), e_or, "err")
 
 
 @pytest.mark.parametrize("n", [1, 3, 31, 32, 33, 100, 511, 513])
