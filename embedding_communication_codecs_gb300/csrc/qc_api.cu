@@ -77,6 +77,72 @@ bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool gra
     return true;
 }
 
+// Tiling for the bf16 encode without error feedback: W = ceil(bucket / 1024)
+// warps per bucket (a power of two, at most 8), whole buckets per tile, about
+// 16 KB of bf16 per stage, three stages.
+bool bf16_tiles_for(const qc::EncodeParams &p, bool grad16, qc::EncodeTiles &t) {
+    if (!grad16 || p.err != nullptr || p.bucket > 8192) return false;
+    uint32_t w = 1;
+    while (w < 8 && 1024u * w < p.bucket) w <<= 1;
+    const uint32_t teams = (qc::kBlock / 32) / w;
+    uint32_t tb = static_cast<uint32_t>((16 * 1024) / (static_cast<size_t>(p.bucket) * 2));
+    tb = tb / teams * teams;
+    if (tb < teams) tb = teams;
+    t.warps = w;
+    t.tb = tb;
+    t.te = tb * p.bucket;
+    t.stage_bytes = t.te * 2;
+    t.stages = t.stage_bytes <= 32 * 1024 ? 3u : 2u;
+    t.e_offset = 0;
+    t.ntiles = (p.n + t.te - 1) / t.te;
+    return true;
+}
+
+uint64_t gcd_u64(uint64_t a, uint64_t b) {
+    while (b) {
+        const uint64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Tiling for the pipelined decode: tiles of whole buckets whose element count
+// is a multiple of 128 (so every worker's code slice starts on a 16-byte
+// boundary), about 32 KB of codes per stage, three stages.  Payloads whose
+// worker stride or base breaks 16-byte alignment, and worker counts whose
+// smallest tile does not fit, take the direct kernel.
+bool decode_tiles_for(const qc::DecodeParams &p, int bits, qc::DecodeTiles &t) {
+    // Few workers: the decode is dominated by its fp32 stores, which the direct
+    // kernel's higher occupancy serves better.
+    if (p.M < 4) return false;
+    if (!aligned(p.codes, 16) || p.codes_stride % 4 != 0) return false;
+    const uint64_t unit = static_cast<uint64_t>(p.bucket) / gcd_u64(p.bucket, 128) * 128;
+    const uint64_t bytes_per_elem_x8 = static_cast<uint64_t>(p.M) * bits;  // code bits per element
+    const uint64_t target = 32 * 1024;
+    uint64_t te = (target * 8 / bytes_per_elem_x8) / unit * unit;
+    if (te < unit) te = unit;
+    const uint64_t worker_bytes = te * bits / 8;
+    const uint64_t tb = te / p.bucket;
+    const uint64_t meta_bytes = 8 * static_cast<uint64_t>(p.M) * tb;
+    const uint64_t stage = (static_cast<uint64_t>(p.M) * worker_bytes + meta_bytes + 127) / 128 * 128;
+    if (stage > 64 * 1024 || te > (1u << 30)) return false;
+    t.tb = static_cast<uint32_t>(tb);
+    t.te = static_cast<uint32_t>(te);
+    t.worker_bytes = static_cast<uint32_t>(worker_bytes);
+    t.meta_offset = static_cast<uint32_t>(p.M * worker_bytes);
+    t.stage_bytes = static_cast<uint32_t>(stage);
+    t.stages = stage <= 36 * 1024 ? 3u : 2u;
+    int sh = -1;
+    if ((p.bucket & (p.bucket - 1)) == 0) {
+        sh = 0;
+        while ((1u << sh) < p.bucket) ++sh;
+    }
+    t.bucket_shift = sh;
+    t.ntiles = (p.n + te - 1) / te;
+    return true;
+}
+
 }  // namespace
 
 namespace qc {
@@ -125,8 +191,13 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes) {
     std::lock_guard<std::mutex> lock(mu);
     auto it = done.find(key);
     if (it != done.end() && it->second >= bytes) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(bytes));
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    // Prefer the largest shared-memory carveout so that several pipelined
+    // blocks fit on one SM.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) done[key] = bytes;
     return e;
 }
@@ -154,7 +225,7 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = 0;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors();
+    *flags = qc::take_encode_errors() | qc::take_encode_bf16_errors() | qc::take_decode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }
 
@@ -221,6 +292,9 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     p.offset = offset;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     qc::EncodeTiles tiles{};
+    if (dtype == QC_DTYPE_BF16 && bf16_tiles_for(p, aligned(grad, 16), tiles))
+        return from_cuda(qc::launch_encode_bf16(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC, st),
+                         "qc_encode_ef");
     if (encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))
         return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                                dtype == QC_DTYPE_BF16, st),
@@ -281,6 +355,10 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
     p.nbuckets = nb;
     p.out = out;
     p.flags = flags;
+    qc::DecodeTiles tiles{};
+    if (decode_tiles_for(p, bits, tiles))
+        return from_cuda(qc::launch_decode_tma(p, tiles, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),
+                         "qc_decode_accumulate");
     return from_cuda(qc::launch_decode(p, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),
                      "qc_decode_accumulate");
 }

@@ -11,8 +11,7 @@
 // of slot s covers elements (s * 32 + l) * 4 .. +3 of a 512-element window: the
 // fp32 output is written as lane-contiguous float4s (fully coalesced), and each
 // worker's codes for those four elements are one 4*b-bit field.
-#include "qc_device.cuh"
-#include "qc_internal.h"
+#include "qc_decode_math.cuh"
 
 namespace qc {
 namespace {
@@ -33,23 +32,9 @@ __device__ __forceinline__ uint32_t load_field(const uint32_t *words, uint64_t i
 }
 
 template <int SCHEME, int BITS>
-__device__ __forceinline__ float dequant(uint32_t code, float sc, float of) {
-    if constexpr (SCHEME == kUniform) {
-        return __fmaf_rn(small_uint_to_float(code), sc, of);
-    } else if constexpr (SCHEME == kSign) {
-        return code ? sc : -sc;
-    } else {
-        // (code - 1) * s as a select; code 1 gives +0, and a zero's sign never
-        // survives a sum that starts at +0.
-        return code == 2u ? sc : code == 0u ? -sc : code == 1u ? 0.0f : __fmul_rn(2.0f, sc);
-    }
-}
-
-template <int SCHEME, int BITS>
 __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeParams P) {
     const int lane = threadIdx.x & 31;
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kBlock / 32);
-    constexpr uint32_t kMask = (1u << BITS) - 1u;
     const float Mf = static_cast<float>(P.M);
 
     for (uint64_t k = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
@@ -80,9 +65,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeParams P) {
                 for (int s = 0; s < kSlots; ++s)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        acc[s][c] = __fadd_rn(
-                            acc[s][c],
-                            dequant<SCHEME, BITS>((field[s] >> (c * BITS)) & kMask, sc, of));
+                        acc[s][c] = __fadd_rn(acc[s][c], dequant_code<SCHEME, BITS>(field[s], c, sc, of));
             }
 
 #pragma unroll

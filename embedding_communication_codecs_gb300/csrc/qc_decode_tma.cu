@@ -1,0 +1,237 @@
+// qc_decode_tma.cu -- receiver half of the codec with the M workers' payloads
+// streamed into shared memory by a producer warp (TMA bulk copies for the code
+// words, 4-byte cp.async for the per-bucket scales and offsets), consumed by
+// eight warps that dequantize and accumulate in the fixed worker order.
+//
+// "Quantization for Communication", "Quantization-Aware All-Reduce" (dequantize
+// after the exchange, accumulate in higher precision); "Gradient quantization for
+// communication", "How Gradient Quantization Works" (dequantize, then average or
+// sum).  Per element: acc = +0; for w = 0 .. M-1: acc = fl(acc + d_w); then
+// optionally fl(acc / M) and fl(out + r).
+//
+// Tile = TB whole buckets (TE elements); one stage holds, for every worker, the
+// TE * b / 8 code bytes of the tile followed by the M x TB scales and offsets.
+// Warp specialisation: warp 8 is the producer; warps 0-7 consume.  A stage is
+// refilled only after all eight consumer warps have arrived on its "empty"
+// barrier, so consumer warps never wait for one another.  Every wait is bounded
+// and a timeout is recorded in a device flag.
+#include "qc_decode_math.cuh"
+#include "qc_pipeline.cuh"
+
+namespace qc {
+
+static __device__ unsigned int g_decode_errors;
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeBlock = (kConsumerWarps + 1) * 32;
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// The 4*BITS-bit field of the four codes of tile element e (e % 4 == 0) of one
+// worker: from the stage when staged, else from global memory (tile tail).
+template <int BITS>
+__device__ __forceinline__ uint32_t field4(const unsigned char *wstage, const uint32_t *wglob,
+                                           uint32_t e, uint32_t staged_bytes) {
+    const uint32_t byte = (e * BITS) / 8u;
+    if constexpr (BITS == 8) {
+        return byte + 4u <= staged_bytes ? *reinterpret_cast<const uint32_t *>(wstage + byte)
+                                         : __ldcs(wglob + e / 4u);
+    } else if constexpr (BITS == 4) {
+        return byte + 2u <= staged_bytes
+                   ? *reinterpret_cast<const unsigned short *>(wstage + byte)
+                   : __ldcs(reinterpret_cast<const unsigned short *>(wglob) + e / 4u);
+    } else if constexpr (BITS == 2) {
+        return byte < staged_bytes ? wstage[byte]
+                                   : __ldcs(reinterpret_cast<const unsigned char *>(wglob) + e / 4u);
+    } else {
+        const uint32_t b = byte < staged_bytes
+                               ? wstage[byte]
+                               : __ldcs(reinterpret_cast<const unsigned char *>(wglob) + e / 8u);
+        return (b >> ((e & 4u) ? 4u : 0u)) & 0xFu;
+    }
+}
+
+template <int SCHEME, int BITS>
+__global__ void __launch_bounds__(kDecodeBlock) decode_tma_kernel(const DecodeParams P,
+                                                                  const DecodeTiles G) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
+    uint64_t *empty = full + G.stages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr bool kOffset = SCHEME == kUniform;
+    const uint32_t meta_per_tile = static_cast<uint32_t>(P.M) * G.tb;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < G.stages; ++s) {
+            mbar_init(&full[s], 1 + 32);           // producer's expect_tx + 32 cp.async arrivals
+            mbar_init(&empty[s], kConsumerWarps);  // one arrival per consumer warp
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        bool ok = true;
+        uint32_t it = 0;
+        for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
+            const uint32_t s = it % G.stages;
+            if (it >= G.stages && !mbar_wait(&empty[s], ((it / G.stages) - 1u) & 1u)) {
+                ok = false;
+                break;
+            }
+            unsigned char *stage = smem + s * G.stage_bytes;
+            const uint64_t t0 = tile * G.te;
+            const uint64_t tcnt = min(static_cast<uint64_t>(G.te), P.n - t0);
+            const uint32_t wb = floor16((tcnt * BITS + 7u) / 8u);  // whole 16-byte units per worker
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], wb * static_cast<uint32_t>(P.M));
+                if (wb)
+                    for (int w = 0; w < P.M; ++w)
+                        bulk_load(stage + static_cast<size_t>(w) * G.worker_bytes,
+                                  P.codes + w * P.codes_stride + (t0 * BITS) / 32u, wb, &full[s]);
+            }
+            float *msc = reinterpret_cast<float *>(stage + G.meta_offset);  // (scale, offset) pairs
+            const uint64_t k0 = tile * G.tb;
+            for (uint32_t idx = lane; idx < meta_per_tile; idx += 32) {
+                const uint32_t w = idx / G.tb, kb = idx - w * G.tb;
+                if (k0 + kb < P.nbuckets) {
+                    cp_async4(msc + 2 * idx, P.scale + w * P.meta_stride + k0 + kb);
+                    if constexpr (kOffset)
+                        cp_async4(msc + 2 * idx + 1, P.offset + w * P.meta_stride + k0 + kb);
+                }
+            }
+            cp_async_arrive(&full[s]);
+        }
+        cp_async_wait_all();
+        if (!ok) {
+            if (lane == 0) atomicOr(&g_decode_errors, kErrPipelineTimeout);
+            // let copies already issued land (bounded)
+            for (uint32_t d = 0; d < G.stages; ++d) {
+                const uint32_t j = it >= G.stages ? it - G.stages + d : d;
+                const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+                if (j < it && tile < G.ntiles) mbar_wait(&full[j % G.stages], (j / G.stages) & 1u);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int ct = warp * 32 + lane;
+    const float Mf = static_cast<float>(P.M);
+    uint32_t it = 0;
+    for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
+        const uint32_t s = it % G.stages;
+        if (!mbar_wait(&full[s], (it / G.stages) & 1u)) {
+            if (lane == 0) atomicOr(&g_decode_errors, kErrPipelineTimeout);
+            break;
+        }
+        const unsigned char *stage = smem + s * G.stage_bytes;
+        const float *msc = reinterpret_cast<const float *>(stage + G.meta_offset);
+        const uint64_t t0 = tile * G.te;
+        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
+        const uint32_t wb = floor16((static_cast<uint64_t>(tcnt) * BITS + 7u) / 8u);
+        const uint32_t *gcodes = P.codes + (t0 * BITS) / 32u;
+
+        const bool whole_tile = tcnt == G.te;
+        for (uint32_t e = static_cast<uint32_t>(ct) * 4u; e < tcnt; e += kConsumerWarps * 32 * 4) {
+            const uint32_t kb = G.bucket_shift >= 0 ? (e >> G.bucket_shift) : (e / P.bucket);
+            const float2 *meta = reinterpret_cast<const float2 *>(msc) + kb;
+            const unsigned char *wst = stage + (e * BITS) / 8u;
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+            if (whole_tile) {
+#pragma unroll 8
+                for (int w = 0; w < P.M; ++w) {
+                    uint32_t f;
+                    if constexpr (BITS == 8) f = *reinterpret_cast<const uint32_t *>(wst);
+                    else if constexpr (BITS == 4) f = *reinterpret_cast<const unsigned short *>(wst);
+                    else if constexpr (BITS == 2) f = *wst;
+                    else f = (*wst >> (e & 4u)) & 0xFu;
+                    const float2 m = meta[w * G.tb];
+                    a0 = __fadd_rn(a0, dequant_code<SCHEME, BITS>(f, 0, m.x, m.y));
+                    a1 = __fadd_rn(a1, dequant_code<SCHEME, BITS>(f, 1, m.x, m.y));
+                    a2 = __fadd_rn(a2, dequant_code<SCHEME, BITS>(f, 2, m.x, m.y));
+                    a3 = __fadd_rn(a3, dequant_code<SCHEME, BITS>(f, 3, m.x, m.y));
+                    wst += G.worker_bytes;
+                }
+            } else {
+                for (int w = 0; w < P.M; ++w) {
+                    const uint32_t f = field4<BITS>(stage + static_cast<size_t>(w) * G.worker_bytes,
+                                                    gcodes + w * P.codes_stride, e, wb);
+                    const float2 m = meta[w * G.tb];
+                    a0 = __fadd_rn(a0, dequant_code<SCHEME, BITS>(f, 0, m.x, m.y));
+                    a1 = __fadd_rn(a1, dequant_code<SCHEME, BITS>(f, 1, m.x, m.y));
+                    a2 = __fadd_rn(a2, dequant_code<SCHEME, BITS>(f, 2, m.x, m.y));
+                    a3 = __fadd_rn(a3, dequant_code<SCHEME, BITS>(f, 3, m.x, m.y));
+                }
+            }
+            float4 r = make_float4(a0, a1, a2, a3);
+            if (P.flags & 1)
+                r = make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf), __fdiv_rn(r.z, Mf),
+                                __fdiv_rn(r.w, Mf));
+            const uint64_t i = t0 + e;
+            if (e + 4u <= tcnt) {
+                float4 *o = reinterpret_cast<float4 *>(P.out + i);
+                if (P.flags & 2) {
+                    const float4 prev = __ldcs(o);
+                    r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
+                                    __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
+                }
+                __stcs(o, r);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (e + c < tcnt) {
+                        float v = get(r, c);
+                        if (P.flags & 2) v = __fadd_rn(P.out[i + c], v);
+                        P.out[i + c] = v;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+template <int SCHEME, int BITS>
+cudaError_t launch_one(const DecodeParams &p, const DecodeTiles &g, cudaStream_t stream) {
+    auto fn = &decode_tma_kernel<SCHEME, BITS>;
+    const size_t smem = decode_tiles_smem(g);
+    cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kDecodeBlock, g.ntiles, smem);
+    fn<<<grid, kDecodeBlock, smem, stream>>>(p, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int scheme, int bits,
+                              cudaStream_t stream) {
+    if (scheme == kSign) return launch_one<kSign, 1>(p, g, stream);
+    if (scheme == kTernary) return launch_one<kTernary, 2>(p, g, stream);
+    switch (bits) {
+        case 1: return launch_one<kUniform, 1>(p, g, stream);
+        case 2: return launch_one<kUniform, 2>(p, g, stream);
+        case 4: return launch_one<kUniform, 4>(p, g, stream);
+        default: return launch_one<kUniform, 8>(p, g, stream);
+    }
+}
+
+uint32_t take_decode_errors() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_decode_errors, sizeof v);
+    cudaMemcpyToSymbol(g_decode_errors, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace qc

@@ -43,9 +43,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &k) {
     constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
-        const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
-        c = make_uint4(hiB ^ c.y ^ k.a[r], loB, hiA ^ c.w ^ k.b[r], loA);
+        const uint64_t pA = static_cast<uint64_t>(kMulA) * c.x;  // one wide multiply each
+        const uint64_t pB = static_cast<uint64_t>(kMulB) * c.z;
+        c = make_uint4(static_cast<uint32_t>(pB >> 32) ^ c.y ^ k.a[r], static_cast<uint32_t>(pB),
+                       static_cast<uint32_t>(pA >> 32) ^ c.w ^ k.b[r], static_cast<uint32_t>(pA));
     }
     return c;
 }

@@ -1,0 +1,310 @@
+// qc_encode_bf16.cu -- encode of a bf16 gradient without error feedback (the
+// receiver-side workload of a quantized all-reduce), streamed through the TMA
+// shared-memory pipeline with 8 elements per lane slot.
+//
+// "Quantization for Communication", "Quantization Schemes" and "Quantized SGD
+// Algorithms" (the arithmetic is the shared code in qc_encode_math.cuh);
+// "Gradient Compression and Quantised Collectives", "When it breaks": gradients
+// are already bf16 in a modern run.
+//
+// Without error feedback p = g exactly, so the bucket's min / max (uniform) or
+// max |p| (ternary) are taken on packed bf16 pairs (one min.bf16x2 and one
+// max.bf16x2 per two elements), and widened once at the end.  Lane slot s of
+// team thread tt holds elements (s * 32 W + tt) * 8 .. +7 as one 16-byte
+// shared-memory read; a team of W = ceil(bucket / 1024) warps owns a bucket, so
+// the common bucket of 1024 needs no block barrier at all.
+#include "qc_encode_math.cuh"
+#include "qc_pipeline.cuh"
+
+namespace qc {
+
+static __device__ unsigned int g_encode_bf16_errors;
+
+namespace {
+
+constexpr int kEps = 8;                       // elements per lane slot
+
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&v)[8]) {
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    v[4] = __uint_as_float(w.z << 16);
+    v[5] = __uint_as_float(w.z & 0xFFFF0000u);
+    v[6] = __uint_as_float(w.w << 16);
+    v[7] = __uint_as_float(w.w & 0xFFFF0000u);
+}
+
+// Packed statistics of full slots (bf16 pairs); partial slots go element-wise.
+template <int SCHEME>
+struct PackedStats {
+    uint32_t a, b;
+    __device__ void init() {
+        if constexpr (SCHEME == kUniform) {
+            a = 0x7F807F80u;  // +inf, +inf (running min)
+            b = 0xFF80FF80u;  // -inf, -inf (running max)
+        } else {
+            a = 0u;  // running max |p|
+            b = 0u;
+        }
+    }
+    __device__ void add(uint32_t w) {
+        if constexpr (SCHEME == kUniform) {
+            a = bf16x2_min(a, w);
+            b = bf16x2_max(b, w);
+        } else {
+            a = bf16x2_max(a, w & 0x7FFF7FFFu);
+        }
+    }
+    __device__ void fold_into(Stats<SCHEME> &st) const {
+        if constexpr (SCHEME == kUniform) {
+            st.mn = fminf(st.mn, fminf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)));
+            st.mx = fmaxf(st.mx, fmaxf(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
+        } else if constexpr (SCHEME == kTernary) {
+            st.add(__uint_as_float(a << 16));
+            st.add(__uint_as_float(a & 0xFFFF0000u));
+        }
+    }
+};
+
+// Packs the 8 codes of a lane slot (c0 lowest) and stores them; every lane of
+// the warp calls this together.
+template <int BITS>
+__device__ __forceinline__ void store_codes8(uint32_t *codes, uint64_t i0, bool valid, int lane,
+                                             uint32_t lo, uint32_t hi) {
+    if constexpr (BITS == 8) {
+        if (valid) __stcs(reinterpret_cast<uint2 *>(codes + i0 / 4u), make_uint2(lo, hi));
+    } else if constexpr (BITS == 4) {
+        if (valid) __stcs(codes + i0 / 8u, lo | (hi << 16));
+    } else if constexpr (BITS == 2) {
+        uint32_t f = lo | (hi << 8);
+        f |= __shfl_down_sync(kFull, f, 1) << 16;
+        if (valid && (lane & 1) == 0) __stcs(codes + i0 / 16u, f);
+    } else {
+        uint32_t f = lo | (hi << 4);
+        f |= __shfl_down_sync(kFull, f, 1) << 8;
+        f |= __shfl_down_sync(kFull, f, 2) << 16;
+        if (valid && (lane & 3) == 0) __stcs(codes + i0 / 32u, f);
+    }
+}
+
+__device__ __forceinline__ void issue_tile(const EncodeParams &P, const EncodeTiles &G,
+                                           uint64_t tile, unsigned char *stage, uint64_t *bar) {
+    const uint64_t t0 = tile * G.te;
+    const uint64_t tcnt = min(static_cast<uint64_t>(G.te), P.n - t0);
+    const uint32_t gb = floor16(tcnt * 2u);
+    mbar_arrive_expect_tx(bar, gb);
+    if (gb) bulk_load(stage, static_cast<const uint16_t *>(P.grad) + t0, gb, bar);
+}
+
+template <int SCHEME, int BITS, bool SR>
+__global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodeParams P,
+                                                             const EncodeTiles G) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
+    auto red = reinterpret_cast<Stats<SCHEME>(*)[kBlock / 32]>(full + G.stages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = G.warps;
+    const int teams = (kBlock / 32) / W;
+    const int team = warp / W;
+    const int tt = (warp % W) * 32 + lane;
+    const int team_threads = W * 32;
+    const uint16_t *gsrc = static_cast<const uint16_t *>(P.grad);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < G.stages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < G.stages; ++s) {
+            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
+            if (tile < G.ntiles) issue_tile(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+        }
+    }
+    PhiloxKeys keys{};
+    if constexpr (SR) keys = philox_keys(P.seed);
+
+    int buf = 0;
+    uint32_t it = 0;
+    bool failed = false;
+    for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
+        const uint32_t s = it % G.stages;
+        const uint32_t parity = (it / G.stages) & 1u;
+        const unsigned char *stage = smem + s * G.stage_bytes;
+        const bool ok = mbar_wait(&full[s], parity);
+
+        const uint64_t t0 = tile * G.te;
+        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
+        const uint32_t staged = floor16(static_cast<uint64_t>(tcnt) * 2u) / 2u;
+        for (uint32_t kb0 = 0; kb0 < G.tb; kb0 += teams) {
+            const uint32_t kb = kb0 + team;
+            const uint32_t b_off = kb * P.bucket;
+            const uint32_t cnt = (kb < G.tb && b_off < tcnt) ? min(P.bucket, tcnt - b_off) : 0u;
+            const uint64_t b0 = t0 + b_off;
+
+            // ---- load the lane's slots and take the statistics
+            uint4 raw[kSlots];
+            bool whole[kSlots];
+            Stats<SCHEME> st;
+            st.init();
+            PackedStats<SCHEME> ps;
+            ps.init();
+#pragma unroll
+            for (int sl = 0; sl < kSlots; ++sl) {
+                const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
+                const uint32_t e = b_off + j;
+                whole[sl] = j + kEps <= cnt && e + kEps <= staged;
+                raw[sl] = make_uint4(0u, 0u, 0u, 0u);
+                if (whole[sl]) {
+                    raw[sl] = *reinterpret_cast<const uint4 *>(stage + e * 2u);
+                    if constexpr (SCHEME == kSign) {
+                        float v[8];
+                        unpack8(raw[sl], v);
+#pragma unroll
+                        for (int c = 0; c < kEps; ++c) st.add(v[c]);
+                    } else {
+                        ps.add(raw[sl].x);
+                        ps.add(raw[sl].y);
+                        ps.add(raw[sl].z);
+                        ps.add(raw[sl].w);
+                    }
+                } else if (j < cnt) {  // ragged end: element-wise, from smem or global
+                    uint32_t h[kEps];
+#pragma unroll
+                    for (int c = 0; c < kEps; ++c) {
+                        h[c] = 0u;
+                        if (j + c < cnt) {
+                            h[c] = (e + c < staged)
+                                       ? *reinterpret_cast<const unsigned short *>(stage + (e + c) * 2u)
+                                       : __ldcs(reinterpret_cast<const unsigned short *>(gsrc + t0 + e + c));
+                            st.add(bf16_bits_to_float(h[c]));
+                        }
+                    }
+                    raw[sl] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                         h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                }
+            }
+            ps.fold_into(st);
+            team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
+            const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            const FastQ fq = fast_params<SCHEME, BITS>(bp);
+
+            // ---- quantize, pack and store
+#pragma unroll
+            for (int sl = 0; sl < kSlots; ++sl) {
+                const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
+                const uint64_t i0 = b0 + j;
+                float v[8];
+                unpack8(raw[sl], v);
+                float u[8];
+#pragma unroll
+                for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
+                if constexpr (SR) {
+                    if (j < cnt) {
+                        uniform4(i0, P.step, keys, u);
+                        uniform4(i0 + 4, P.step, keys, u + 4);
+                    }
+                }
+                uint32_t q[kEps];
+                if (j + kEps <= cnt && fq.usable) {
+                    bool redo[kEps];
+                    bool any = false;
+#pragma unroll
+                    for (int c = 0; c < kEps; ++c) {
+                        float d;
+                        q[c] = quantize_fast<SCHEME, BITS, SR>(v[c], u[c], bp, fq, d, redo[c]);
+                        any |= redo[c];
+                    }
+                    if (any) {  // rare: near a decision boundary
+#pragma unroll
+                        for (int c = 0; c < kEps; ++c) {
+                            float d;
+                            if (redo[c]) q[c] = quantize<SCHEME, BITS, SR>(v[c], u[c], bp, d);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kEps; ++c) {
+                        float d;
+                        q[c] = (j + c < cnt) ? quantize<SCHEME, BITS, SR>(v[c], u[c], bp, d) : 0u;
+                    }
+                }
+                const uint32_t lo = q[0] | (q[1] << BITS) | (q[2] << (2 * BITS)) | (q[3] << (3 * BITS));
+                const uint32_t hi = q[4] | (q[5] << BITS) | (q[6] << (2 * BITS)) | (q[7] << (3 * BITS));
+                store_codes8<BITS>(P.codes, i0, j < cnt, lane, lo, hi);
+            }
+            if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);
+        }
+        if (!__syncthreads_and(ok)) {
+            failed = true;
+            break;
+        }
+        if (threadIdx.x == 0) {
+            const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
+            if (next < G.ntiles) issue_tile(P, G, next, smem + s * G.stage_bytes, &full[s]);
+        }
+    }
+    if (failed && threadIdx.x == 0) {
+        atomicOr(&g_encode_bf16_errors, kErrPipelineTimeout);
+        for (uint32_t d = 0; d < G.stages; ++d) {
+            const uint32_t j = it + d;
+            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+            if (tile < G.ntiles) mbar_wait(&full[j % G.stages], (j / G.stages) & 1u);
+        }
+    }
+}
+
+template <int SCHEME, int BITS, bool SR>
+cudaError_t launch_one(const EncodeParams &p, const EncodeTiles &g, cudaStream_t stream) {
+    auto fn = &encode_bf16_kernel<SCHEME, BITS, SR>;
+    const size_t smem = encode_tiles_smem(g, sizeof(Stats<SCHEME>));
+    cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kBlock, g.ntiles, smem);
+    fn<<<grid, kBlock, smem, stream>>>(p, g);
+    return cudaGetLastError();
+}
+
+template <int SCHEME, int BITS>
+cudaError_t launch_round(const EncodeParams &p, const EncodeTiles &g, int stochastic,
+                         cudaStream_t stream) {
+    return stochastic ? launch_one<SCHEME, BITS, true>(p, g, stream)
+                      : launch_one<SCHEME, BITS, false>(p, g, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
+                               int stochastic, cudaStream_t stream) {
+    if (scheme == kSign) return launch_one<kSign, 1, false>(p, g, stream);
+    if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, stream);
+    switch (bits) {
+        case 1: return launch_round<kUniform, 1>(p, g, stochastic, stream);
+        case 2: return launch_round<kUniform, 2>(p, g, stochastic, stream);
+        case 4: return launch_round<kUniform, 4>(p, g, stochastic, stream);
+        default: return launch_round<kUniform, 8>(p, g, stochastic, stream);
+    }
+}
+
+uint32_t take_encode_bf16_errors() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_encode_bf16_errors, sizeof v);
+    cudaMemcpyToSymbol(g_encode_bf16_errors, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace qc

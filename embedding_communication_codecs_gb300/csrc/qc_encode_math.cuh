@@ -166,21 +166,30 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
                                                   const FastQ &fq, float &deq, bool &redo) {
     if constexpr (SCHEME == kUniform) {
         constexpr uint32_t L = (1u << BITS) - 1u;
+        constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
-        uint32_t q = rint_small(ta);
-        const float r = __fsub_rn(ta, small_uint_to_float(q));  // exact, in [-1/2, 1/2]
+        float qf;
+        uint32_t q;
         if constexpr (!SR) {
-            redo = fabsf(r) >= 0.5f - fq.delta2;
+            const float y = __fadd_rn(ta, kMagic);  // rint(ta) in the low mantissa bits
+            q = __float_as_uint(y) - 0x4B400000u;
+            qf = __fsub_rn(y, kMagic);
+            redo = fabsf(__fsub_rn(ta, qf)) >= 0.5f - fq.delta2;
         } else {
-            const bool below = r < 0.0f;
-            const float fr = below ? __fadd_rn(r, 1.0f) : r;  // ta - floor(ta), exact
-            q -= below ? 1u : 0u;
-            redo = (fr <= fq.delta2) | (fr >= 1.0f - fq.delta2) |
+            // floor(ta) = rint(ta - 1/2) unless ta is an integer, which the
+            // check below sends to the exact path anyway.
+            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            const float ff = __fsub_rn(y, kMagic);
+            const float fr = __fsub_rn(ta, ff);  // ta - floor(ta), exact
+            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
                    (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
-            q += (u < fr) ? 1u : 0u;
+            const bool up = u < fr;
+            q += up ? 1u : 0u;
+            qf = up ? __fadd_rn(ff, 1.0f) : ff;
         }
         q = min(q, L);
-        deq = __fmaf_rn(small_uint_to_float(q), bp.scale, bp.a);
+        deq = __fmaf_rn(fminf(qf, static_cast<float>(L)), bp.scale, bp.a);
         return q;
     } else if constexpr (SCHEME == kTernary) {
         const float s = bp.a;

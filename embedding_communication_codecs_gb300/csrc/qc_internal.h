@@ -33,6 +33,7 @@ struct EncodeParams {
 // `stages` shared-memory stages of stage_bytes each; the residual's part of a
 // stage starts at e_offset.
 struct EncodeTiles {
+    uint32_t warps;  // warps per bucket (the bf16 kernel's own team size)
     uint32_t tb;
     uint32_t te;
     uint32_t stages;
@@ -58,6 +59,25 @@ struct DecodeParams {
     float *out;
     int flags;
 };
+
+// Tiling of the pipelined decode: TB whole buckets (TE elements) per tile; a
+// stage holds M slices of worker_bytes code bytes, then M x TB scales and
+// M x TB offsets at meta_offset.  bucket_shift = log2(bucket) when the bucket
+// is a power of two, else -1.
+struct DecodeTiles {
+    uint32_t tb;
+    uint32_t te;
+    uint32_t stages;
+    uint32_t stage_bytes;
+    uint32_t worker_bytes;
+    uint32_t meta_offset;
+    int bucket_shift;
+    uint64_t ntiles;
+};
+
+inline size_t decode_tiles_smem(const DecodeTiles &g) {
+    return static_cast<size_t>(g.stages) * g.stage_bytes + 16u * g.stages;
+}
 
 struct VoteParams {
     const uint32_t *signs;
@@ -87,7 +107,11 @@ cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stoch
                           int bf16, cudaStream_t stream);
 cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                               int stochastic, int bf16, cudaStream_t stream);
+cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
+                               int stochastic, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
+cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int scheme, int bits,
+                              cudaStream_t stream);
 cudaError_t launch_vote(const VoteParams &p, bool vectorised, cudaStream_t stream);
 cudaError_t launch_fp8_quant(const Fp8Params &p, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const Fp8Params &p, cudaStream_t stream);
@@ -101,5 +125,7 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 
 // Device-side error flags of the pipelined kernels (read and cleared).
 uint32_t take_encode_errors();
+uint32_t take_encode_bf16_errors();
+uint32_t take_decode_errors();
 
 }  // namespace qc

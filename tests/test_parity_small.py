@@ -294,10 +294,14 @@ DEC_CASES = [(0, 1), (0, 2), (0, 4), (0, 8), (1, 1), (2, 2)]
 @pytest.mark.parametrize("M", [1, 3, 16])
 def test_decode_accumulate(q, scheme, bits, M):
     rng = np.random.default_rng(100 * M + bits)
-    for bucket in (32, 96, 512, 1024, 4096):
+    for bucket, aligned in ((32, True), (96, True), (512, True), (1024, True), (4096, True),
+                            (512, False), (1024, False)):
         n = max(3 * bucket, 3000) + 13
         words, nb = orc.code_words(n, bits), orc.num_buckets(n, bucket)
-        cstride, mstride = words + 5, nb + 3              # padded worker strides
+        # padded worker strides: a multiple of 4 words takes the pipelined
+        # kernel, an odd stride the direct one
+        cstride = words + (-words) % 4 + 4 if aligned else words + 5
+        mstride = nb + 3
         codes = rng.integers(0, 1 << 32, size=(M, cstride), dtype=np.uint64).astype(np.uint32)
         scale = (rng.random((M, mstride)) * 1e-3).astype(np.float32)
         offset = (rng.standard_normal((M, mstride)) * 1e-2).astype(np.float32)
@@ -311,7 +315,8 @@ def test_decode_accumulate(q, scheme, bits, M):
                                          bits=bits, bucket=bucket, scheme=scheme, flags=flags,
                                          codes_stride_words=cstride, meta_stride=mstride,
                                          out=prior.copy())
-            assert_bits_equal(host(out), want, f"decode s={scheme} b={bits} M={M} B={bucket} f={flags}")
+            assert_bits_equal(host(out), want,
+                              f"decode s={scheme} b={bits} M={M} B={bucket} f={flags} al={aligned}")
 
 
 def test_decode_guards(q):
