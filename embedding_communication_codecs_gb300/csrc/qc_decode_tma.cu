@@ -24,16 +24,7 @@ static __device__ unsigned int g_decode_errors;
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kDecodeBlock = (kConsumerWarps + 1) * 32;
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
+constexpr int kDecodeBlock = kProducerBlock;
 
 // The 4*BITS-bit field of the four codes of tile element e (e % 4 == 0) of one
 // worker: from the stage when staged, else from global memory (tile tail).

@@ -42,9 +42,14 @@ struct EncodeTiles {
     uint64_t ntiles;
 };
 
+// Stages, then the full and empty barriers, then the team-reduction buffer.
 inline size_t encode_tiles_smem(const EncodeTiles &g, size_t stats_bytes) {
-    return static_cast<size_t>(g.stages) * g.stage_bytes + 8u * g.stages + 2u * 8u * stats_bytes;
+    return static_cast<size_t>(g.stages) * g.stage_bytes + 16u * g.stages + 2u * 8u * stats_bytes;
 }
+
+// Warp-specialised blocks: 8 consumer warps and one producer warp.
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerBlock = (kConsumerWarps + 1) * 32;
 
 struct DecodeParams {
     const uint32_t *codes;
