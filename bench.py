@@ -80,6 +80,10 @@ class Component:
         fp32-equivalent elements it processes."""
         raise NotImplementedError
 
+    def kernel_units(self):
+        """Elements each launch of each kernel processes (for scaling counters)."""
+        return {}
+
 
 def _words(n, bits):
     return (n * bits + 31) // 32
@@ -119,6 +123,9 @@ class Fp8Rowwise(Component):
 
     def host_outputs(self):
         return [self.out]
+
+    def kernel_units(self):
+        return {"fp8_quant": self.rows * self.dim, "fp8_dequant": self.rows * self.dim}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -174,6 +181,9 @@ class UniformEF(Component):
     def host_outputs(self):
         return [self.out]
 
+    def kernel_units(self):
+        return {k: self.n for k in self.kernels}
+
     def oracle_sample(self, frac):
         import oracle as orc
         n = max(self.bucket, int(self.n * frac) // self.bucket * self.bucket)
@@ -223,6 +233,9 @@ class SignVote(Component):
 
     def host_outputs(self):
         return [self.vote]
+
+    def kernel_units(self):
+        return {"encode_sign_ef": self.n, "sign_vote": self.M * self.n}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -281,6 +294,9 @@ class Receiver(Component):
 
     def host_inputs(self):
         return [self.g] if self.h2d else []
+
+    def kernel_units(self):
+        return {self.enc_name: self.n, self.dec_name: self.M * self.n}
 
     def host_outputs(self):
         return [self.out]
@@ -451,40 +467,43 @@ def measured_peak():
         return PEAK_FALLBACK_GBS, "fallback"
 
 
-def ncu_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its hash is recorded beside the figure)."""
+def source_digest(files):
+    """Short hash over the named kernel source files (in csrc/)."""
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "embedding_communication_codecs_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, units_per_launch):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, scaled
+    from the captured launch to this launch by the units processed; None if
+    the summary is missing or was taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
+            ent = json.load(f).get(kernel)
+        if not ent or source_digest(ent["sources"]) != ent["digest"]:
+            return None
+    except (OSError, ValueError, KeyError):
         return None
-    ent = d.get(kernel)
-    if not ent:
-        return None
-    src = os.path.join(ROOT, "embedding_communication_codecs_gb300", "csrc", ent["source"])
-    try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        hd = hashlib.sha256(open(os.path.join(os.path.dirname(src), "qc_device.cuh"),
-                                 "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    if h != ent.get("sha") or hd != ent.get("device_sha"):
-        return None
-    return ent.get("bytes_per_launch")
+    return int(round(ent["dram_bytes"] * units_per_launch / ent["units"]))
 
 
 # ------------------------------------------------------------- distributed
 
-def dist_setup():
+def dist_setup(backend=None):
+    """Rank, world size and local rank from the launcher's environment; with
+    more than one rank, a process group (NCCL on GPUs unless told otherwise)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
         if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
@@ -565,9 +584,10 @@ def run_ours(args, world, rank, local):
     peak, peak_src = measured_peak()
     dom = max(kinfo, key=lambda k: kinfo[k]["total_ms"])
     achieved = kinfo[dom]["gbs"]
+    units_per_launch = {k: u for c in comps for k, u in c.kernel_units().items()}
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": ncu_traffic(dom),
+                "traffic": ncu_traffic(dom, units_per_launch.get(dom, 0)),
                 "bytes_per_launch": kinfo[dom]["bytes_per_launch"]}
     for k in kinfo:
         kinfo[k]["frac_of_peak"] = round(kinfo[k]["gbs"] / peak, 4)

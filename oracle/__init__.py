@@ -73,6 +73,8 @@ def _L():
         lib.oracle_e4m3_to_f32.restype = ctypes.c_float
         lib.oracle_e4m3_from_f32.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_from_f32.restype = ctypes.c_uint8
+        lib.oracle_e4m3_from_f32_array.argtypes = [P, S, P]
+        lib.oracle_e4m3_from_f32_array.restype = None
         lib.oracle_rowwise_fp8.argtypes = [P, S, S, P, P]
         lib.oracle_rowwise_fp8_dequant.argtypes = [P, P, S, S, P]
         for name in ("oracle_encode_uniform", "oracle_encode_sign", "oracle_encode_ternary",
@@ -198,6 +200,13 @@ def e4m3_to_f32(code: int) -> float:
 
 def e4m3_from_f32(x: float) -> int:
     return int(_L().oracle_e4m3_from_f32(x))
+
+
+def e4m3_from_f32_array(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _L().oracle_e4m3_from_f32_array(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def rowwise_fp8(x):

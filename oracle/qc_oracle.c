@@ -473,6 +473,13 @@ ORC_API uint8_t oracle_e4m3_from_f32(float x)
     return (uint8_t)(sign | code);
 }
 
+/* The conversion above applied to an array (a loop over the scalar function). */
+ORC_API void oracle_e4m3_from_f32_array(const float *x, size_t n, uint8_t *out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_from_f32(x[i]);
+}
+
 /* Row-wise FP8 quantization of an N x D fp32 payload (p1 "Numeric Example" and
  * "Pinterest QComms Example": embedding lookup payloads go FP32 -> FP8 before
  * the collective).  Per row r (a reading: absmax scaling onto E4M3's range):

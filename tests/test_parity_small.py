@@ -393,3 +393,40 @@ def test_fp8_dequant_all_codes(q):
     nan = np.isnan(want)
     assert np.array_equal(np.isnan(got), nan)
     assert_bits_equal(got[~nan], want[~nan])
+
+
+def test_encode_largest_bucket(q):
+    """bucket = 2^24, the largest accepted: one two-pass bucket plus a ragged one."""
+    bucket = 1 << 24
+    n = bucket + 4099
+    g = wl.outlier_gradient(n, seed=13)
+    err0 = np.zeros(n, dtype=np.float32)
+    codes, scale, offset, err = _run_encode(q, g, err0, n, 8, bucket, q.QC_SCHEME_UNIFORM, 1)
+    e_or = err0.copy()
+    c_or, s_or, o_or = orc.encode_uniform(g, e_or, bits=8, bucket=bucket, mode=1, seed=SEED,
+                                          step=STEP)
+    assert_bits_equal(codes, c_or, "codes")
+    assert_bits_equal(scale, s_or, "scale")
+    assert_bits_equal(offset, o_or, "offset")
+    assert_bits_equal(err, e_or, "err")
+
+
+def test_most_workers(q):
+    """M = 1024 (the largest accepted) for decode and vote."""
+    M, n, bucket = q.QC_MAX_WORKERS, 4096 + 32, 1024
+    rng = np.random.default_rng(5)
+    words, nb = orc.code_words(n, 8), orc.num_buckets(n, bucket)
+    codes = rng.integers(0, 1 << 32, size=(M, words), dtype=np.uint64).astype(np.uint32)
+    scale = (rng.random((M, nb)) * 1e-3).astype(np.float32)
+    offset = (rng.standard_normal((M, nb)) * 1e-3).astype(np.float32)
+    out = torch.empty(n, device="cuda")
+    q.qc_decode_accumulate(dev(codes), words, dev(scale), dev(offset), nb, M, n, 8, bucket, 0,
+                           out, 1)
+    want = orc.decode_accumulate(codes, scale, offset, M=M, n=n, bits=8, bucket=bucket,
+                                 scheme=0, flags=1)
+    assert_bits_equal(host(out), want, "decode M=1024")
+    sw = orc.code_words(n, 1)
+    signs = rng.integers(0, 1 << 32, size=(M, sw), dtype=np.uint64).astype(np.uint32)
+    vote = torch.empty(sw, dtype=torch.int32, device="cuda")
+    q.qc_sign_vote(dev(signs), sw, M, n, vote)
+    assert_bits_equal(u32(vote), orc.sign_vote(signs, M=M, n=n), "vote M=1024")
