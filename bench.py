@@ -358,6 +358,14 @@ def make_workload(name):
         "rx_ternary": lambda: [Receiver("rx_ternary", 2, 2)],
         "u8_ef_small": lambda: [UniformEF("u8_ef_small", 1 << 20, 8, 2048, False, 0, "outlier")],
         "u8_ef_large": lambda: [UniformEF("u8_ef_large", 1 << 28, 8, 2048, False, 0, "outlier")],
+        # smaller single-kernel cases (inputs still larger than L2) for profiler captures
+        "probe_sr4_ef": lambda: [UniformEF("sr4_ef", 1 << 26, 4, 512, True, 2, "bucket")],
+        "probe_sign": lambda: [SignVote(n=1 << 24, M=2)],
+        "probe_u8_bf16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 27, M=1)],
+        "probe_ternary_bf16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 27, M=1)],
+        "probe_decode_u8_m16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 24, M=16)],
+        "probe_decode_ternary_m16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 24, M=16)],
+        "probe_fp8": lambda: [Fp8Rowwise(rows=1 << 19)],
     }
     return table[name]()
 

@@ -40,9 +40,11 @@ def test_e4m3_all_values_in_range():
             cnt = min(CHUNK, hi - start)
             vals = np.arange(start, start + cnt, dtype=np.uint64).astype(np.uint32).view(np.float32)
             rows = -(-cnt // 127)
-            x = np.zeros((rows, dim), dtype=np.float32)
+            body = np.zeros(rows * 127, dtype=np.float32)
+            body[:cnt] = vals
+            x = np.empty((rows, dim), dtype=np.float32)
             x[:, 0] = 448.0
-            x[:, 1:].reshape(-1)[:cnt] = vals
+            x[:, 1:] = body.reshape(rows, 127)
             xd[:rows].copy_(torch.from_numpy(x))
             q.qc_rowwise_fp8(xd[:rows], rows, dim, codes[:rows], sc[:rows])
             assert bool((sc[:rows] == 1.0).all())
