@@ -287,6 +287,7 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     p.two_pass = bucket > static_cast<size_t>(qc::kWindowPerWarp) * p.team_warps ? 1 : 0;
     p.seed = seed;
     p.step = step;
+    p.keys = qc::philox_round_keys(seed);
     p.codes = codes;
     p.scale = scale;
     p.offset = offset;

@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "qc_internal.h"
+
 namespace qc {
 
 constexpr unsigned kFull = 0xffffffffu;
@@ -20,25 +22,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // multipliers; the new words 0 and 2 are the high halves xor the other counter
 // word and a key word, the new words 1 and 3 are the low halves.  The key is
 // advanced by the two Weyl constants between rounds; the ten round keys depend
-// only on the seed and are computed once per thread.
-struct PhiloxKeys {
-    uint32_t a[10], b[10];
-};
-
-__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
-    constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
-    PhiloxKeys k;
-    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        k.a[r] = k0;
-        k.b[r] = k1;
-        k0 += kWeylA;
-        k1 += kWeylB;
-    }
-    return k;
-}
-
+// only on the seed, so the host computes them once per launch (PhiloxKeys) and
+// the kernels read them from their constant parameter bank.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &k) {
     constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
 #pragma unroll

@@ -59,7 +59,7 @@ __device__ __forceinline__ void load_slots(const EncodeParams &P, uint64_t base,
 }
 
 template <int SCHEME, int BITS, bool SR, typename TIn, bool EF>
-__global__ void __launch_bounds__(kBlock) encode_kernel(const EncodeParams P) {
+__global__ void __launch_bounds__(kBlock) encode_kernel(const __grid_constant__ EncodeParams P) {
     __shared__ Stats<SCHEME> red[2][kBlock / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int W = P.team_warps;
@@ -69,8 +69,7 @@ __global__ void __launch_bounds__(kBlock) encode_kernel(const EncodeParams P) {
     const int team_threads = W * 32;
     const uint32_t window = static_cast<uint32_t>(kWindowPerWarp * W);
     const uint64_t ngroups = (P.nbuckets + teams - 1) / teams;
-    PhiloxKeys keys{};
-    if constexpr (SR) keys = philox_keys(P.seed);
+    const PhiloxKeys &keys = P.keys;
     int buf = 0;
 
     for (uint64_t grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {

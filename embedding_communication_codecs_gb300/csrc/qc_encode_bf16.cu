@@ -110,8 +110,8 @@ __device__ __forceinline__ void issue_tile(const EncodeParams &P, const EncodeTi
 }
 
 template <int SCHEME, int BITS, bool SR>
-__global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodeParams P,
-                                                             const EncodeTiles G) {
+__global__ void __launch_bounds__(kBlock, SR ? 3 : 4) encode_bf16_kernel(const __grid_constant__ EncodeParams P,
+                                                             const __grid_constant__ EncodeTiles G) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
     auto red = reinterpret_cast<Stats<SCHEME>(*)[kBlock / 32]>(full + G.stages);
@@ -135,8 +135,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodePara
             if (tile < G.ntiles) issue_tile(P, G, tile, smem + s * G.stage_bytes, &full[s]);
         }
     }
-    PhiloxKeys keys{};
-    if constexpr (SR) keys = philox_keys(P.seed);
+    const PhiloxKeys &keys = P.keys;
 
     int buf = 0;
     uint32_t it = 0;
@@ -158,7 +157,6 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodePara
 
             // ---- load the lane's slots and take the statistics
             uint4 raw[kSlots];
-            bool whole[kSlots];
             Stats<SCHEME> st;
             st.init();
             PackedStats<SCHEME> ps;
@@ -167,9 +165,8 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodePara
             for (int sl = 0; sl < kSlots; ++sl) {
                 const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
                 const uint32_t e = b_off + j;
-                whole[sl] = j + kEps <= cnt && e + kEps <= staged;
                 raw[sl] = make_uint4(0u, 0u, 0u, 0u);
-                if (whole[sl]) {
+                if (j + kEps <= cnt && e + kEps <= staged) {
                     raw[sl] = *reinterpret_cast<const uint4 *>(stage + e * 2u);
                     if constexpr (SCHEME == kSign) {
                         float v[8];
@@ -203,49 +200,65 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const EncodePara
             const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
             const FastQ fq = fast_params<SCHEME, BITS>(bp);
 
-            // ---- quantize, pack and store
+            // ---- quantize, pack and store, one slot at a time: a division-free
+            // pass, an exact recompute of the slot in the rare case that one of its
+            // elements lies near a decision boundary, then the store
+            const uint32_t jlast = static_cast<uint32_t>((kSlots - 1) * team_threads + tt) * kEps;
+            if (fq.usable && jlast + kEps <= cnt && b_off + jlast + kEps <= staged) {
+#pragma unroll 2
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
+                    const uint64_t i0 = b0 + j;
+                    float v[8], u[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(stage + (b_off + j) * 2u), v);
 #pragma unroll
-            for (int sl = 0; sl < kSlots; ++sl) {
-                const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
-                const uint64_t i0 = b0 + j;
-                float v[8];
-                unpack8(raw[sl], v);
-                float u[8];
-#pragma unroll
-                for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
-                if constexpr (SR) {
-                    if (j < cnt) {
+                    for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
+                    if constexpr (SR) {
                         uniform4(i0, P.step, keys, u);
                         uniform4(i0 + 4, P.step, keys, u + 4);
                     }
-                }
-                uint32_t q[kEps];
-                if (j + kEps <= cnt && fq.usable) {
-                    bool redo[kEps];
+                    uint32_t f0 = 0, f1 = 0;
                     bool any = false;
 #pragma unroll
-                    for (int c = 0; c < kEps; ++c) {
-                        float d;
-                        q[c] = quantize_fast<SCHEME, BITS, SR>(v[c], u[c], bp, fq, d, redo[c]);
-                        any |= redo[c];
+                    for (int c = 0; c < 4; ++c) {
+                        bool r0, r1;
+                        f0 |= code_fast<SCHEME, BITS, SR>(v[c], u[c], bp, fq, r0) << (c * BITS);
+                        f1 |= code_fast<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp, fq, r1) << (c * BITS);
+                        any |= r0 | r1;
                     }
-                    if (any) {  // rare: near a decision boundary
+                    if (any) {  // rare
+                        f0 = f1 = 0;
 #pragma unroll
-                        for (int c = 0; c < kEps; ++c) {
-                            float d;
-                            if (redo[c]) q[c] = quantize<SCHEME, BITS, SR>(v[c], u[c], bp, d);
+                        for (int c = 0; c < 4; ++c) {
+                            f0 |= code_exact<SCHEME, BITS, SR>(v[c], u[c], bp) << (c * BITS);
+                            f1 |= code_exact<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp) << (c * BITS);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kEps; ++c) {
-                        float d;
-                        q[c] = (j + c < cnt) ? quantize<SCHEME, BITS, SR>(v[c], u[c], bp, d) : 0u;
-                    }
+                    store_codes8<BITS>(P.codes, i0, true, lane, f0, f1);
                 }
-                const uint32_t lo = q[0] | (q[1] << BITS) | (q[2] << (2 * BITS)) | (q[3] << (3 * BITS));
-                const uint32_t hi = q[4] | (q[5] << BITS) | (q[6] << (2 * BITS)) | (q[7] << (3 * BITS));
-                store_codes8<BITS>(P.codes, i0, j < cnt, lane, lo, hi);
+            } else {  // partial slots or an extreme scale: element-wise with the division
+#pragma unroll
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
+                    float v[8], u[8];
+                    unpack8(raw[sl], v);
+#pragma unroll
+                    for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
+                    if constexpr (SR) {
+                        if (j < cnt) {
+                            uniform4(b0 + j, P.step, keys, u);
+                            uniform4(b0 + j + 4, P.step, keys, u + 4);
+                        }
+                    }
+                    uint32_t f0 = 0, f1 = 0;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (j + c < cnt) f0 |= code_exact<SCHEME, BITS, SR>(v[c], u[c], bp) << (c * BITS);
+                        if (j + c + 4 < cnt)
+                            f1 |= code_exact<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp) << (c * BITS);
+                    }
+                    store_codes8<BITS>(P.codes, b0 + j, j < cnt, lane, f0, f1);
+                }
             }
             if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);
         }

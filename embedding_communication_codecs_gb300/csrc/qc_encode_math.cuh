@@ -15,6 +15,7 @@
 // j + 3, so each slot is one coalesced sweep over 128 W consecutive elements.
 #pragma once
 
+#include "qc_decode_math.cuh"
 #include "qc_device.cuh"
 #include "qc_internal.h"
 
@@ -153,8 +154,9 @@ template <int SCHEME, int BITS>
 __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
     const float d = (SCHEME == kUniform) ? bp.scale : bp.a;
     FastQ f;
-    f.usable = (SCHEME != kSign) && d >= 0x1p-125f && d <= 0x1p125f;
-    f.rinv = f.usable ? __frcp_rn(d) : 0.0f;
+    const bool normal = d >= 0x1p-125f && d <= 0x1p125f;
+    f.usable = SCHEME == kSign || normal;  // the sign code needs no division
+    f.rinv = (SCHEME != kSign && normal) ? __frcp_rn(d) : 0.0f;
     f.delta2 = (SCHEME == kUniform) ? static_cast<float>(1u << BITS) * 0x1p-21f : 0x1p-21f;
     return f;
 }
@@ -212,6 +214,64 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
         redo = false;
         return quantize<SCHEME, BITS, SR>(p, u, bp, deq);
     }
+}
+
+// Code of one element from ta; sets redo when the decision is within reach of
+// the approximation error (the caller then recomputes it with the division).
+template <int SCHEME, int BITS, bool SR>
+__device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketParams &bp,
+                                              const FastQ &fq, bool &redo) {
+    if constexpr (SCHEME == kUniform) {
+        constexpr uint32_t L = (1u << BITS) - 1u;
+        constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+        const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
+        uint32_t q;
+        if constexpr (!SR) {
+            const float y = __fadd_rn(ta, kMagic);  // rint(ta) in the low mantissa bits
+            q = __float_as_uint(y) - 0x4B400000u;
+            redo = fabsf(__fsub_rn(ta, __fsub_rn(y, kMagic))) >= 0.5f - fq.delta2;
+        } else {
+            // floor(ta) = rint(ta - 1/2) unless ta is an integer, which the
+            // check below sends to the exact path anyway.
+            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            const float fr = __fsub_rn(ta, __fsub_rn(y, kMagic));  // ta - floor(ta), exact
+            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
+                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
+            q += (u < fr) ? 1u : 0u;
+        }
+        return min(q, L);
+    } else if constexpr (SCHEME == kTernary) {
+        const float pa = __fmul_rn(fabsf(p), fq.rinv);
+        bool keep;
+        if constexpr (SR) {
+            const float d = __fsub_rn(u, pa);
+            keep = d < 0.0f;
+            redo = fabsf(d) <= fq.delta2;
+        } else {
+            keep = pa > 0.5f;
+            redo = fabsf(__fsub_rn(pa, 0.5f)) <= fq.delta2;
+        }
+        // keep ? (p > 0 ? 2 : 0) : 1; a kept element is never zero
+        return keep ? ((__float_as_uint(p) >> 31) ? 0u : 2u) : 1u;
+    } else {
+        redo = false;
+        return p >= 0.0f ? 1u : 0u;
+    }
+}
+
+// Exact code of one element (the IEEE division path).
+template <int SCHEME, int BITS, bool SR>
+__device__ __forceinline__ uint32_t code_exact(float p, float u, const BucketParams &bp) {
+    float deq;
+    return quantize<SCHEME, BITS, SR>(p, u, bp, deq);
+}
+
+// Dequantized value of code c of a packed field, identical to the encoder's deq.
+template <int SCHEME, int BITS>
+__device__ __forceinline__ float deq_of(uint32_t field, int c, const BucketParams &bp) {
+    if constexpr (SCHEME == kUniform) return dequant_code<SCHEME, BITS>(field, c, bp.scale, bp.a);
+    else return dequant_code<SCHEME, BITS>(field, c, bp.a, bp.a);
 }
 
 // ------------------------------------------------------------- slot level

@@ -102,8 +102,8 @@ __device__ __forceinline__ void load_slots_staged(const EncodeParams &P, const E
 }
 
 template <int SCHEME, int BITS, bool SR, typename TIn, bool EF>
-__global__ void __launch_bounds__(kBlock) encode_tma_kernel(const EncodeParams P,
-                                                            const EncodeTiles G) {
+__global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constant__ EncodeParams P,
+                                                            const __grid_constant__ EncodeTiles G) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
     auto red = reinterpret_cast<Stats<SCHEME>(*)[kBlock / 32]>(full + G.stages);
@@ -127,8 +127,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const EncodeParams P
                 issue_tile<TIn, EF>(P, G, tile, smem + s * G.stage_bytes, &full[s]);
         }
     }
-    PhiloxKeys keys{};
-    if constexpr (SR) keys = philox_keys(P.seed);
+    const PhiloxKeys &keys = P.keys;
 
     int buf = 0;
     uint32_t it = 0;

@@ -14,6 +14,24 @@ constexpr int kSlots = 4;
 constexpr int kBlock = 256;
 constexpr int kWindowPerWarp = kSlots * 4 * 32;  // 512
 
+// Round keys of Philox4x32-10 for one seed: round r uses (a[r], b[r]) =
+// (seed low + r * 0x9E3779B9, seed high + r * 0xBB67AE85), mod 2^32.
+struct PhiloxKeys {
+    uint32_t a[10], b[10];
+};
+
+inline PhiloxKeys philox_round_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        k.a[r] = k0;
+        k.b[r] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return k;
+}
+
 struct EncodeParams {
     const void *grad;
     float *err;
@@ -24,6 +42,7 @@ struct EncodeParams {
     int two_pass;     // bucket > 512 * team_warps: statistics pass, then re-read
     uint64_t seed;
     uint32_t step;
+    PhiloxKeys keys;  // round keys of `seed`
     uint32_t *codes;
     float *scale;
     float *offset;
