@@ -356,6 +356,8 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
     p.nbuckets = nb;
     p.out = out;
     p.flags = flags;
+    // x / M and x * (1 / M) round the same exact value when M is a power of two.
+    p.inv_m = (M & (M - 1)) == 0 ? 1.0f / static_cast<float>(M) : 0.0f;
     qc::DecodeTiles tiles{};
     if (decode_tiles_for(p, bits, tiles))
         return from_cuda(qc::launch_decode_tma(p, tiles, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),

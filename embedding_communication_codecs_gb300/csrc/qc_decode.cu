@@ -32,7 +32,7 @@ __device__ __forceinline__ uint32_t load_field(const uint32_t *words, uint64_t i
 }
 
 template <int SCHEME, int BITS>
-__global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(kBlock) decode_kernel(const __grid_constant__ DecodeParams P) {
     const int lane = threadIdx.x & 31;
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kBlock / 32);
     const float Mf = static_cast<float>(P.M);
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeParams P) {
                 for (int s = 0; s < kSlots; ++s)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        acc[s][c] = __fadd_rn(acc[s][c], dequant_code<SCHEME, BITS>(field[s], c, sc, of));
+                        acc[s][c] = accumulate_code<SCHEME, BITS>(acc[s][c], field[s], c, sc, of);
             }
 
 #pragma unroll
@@ -75,8 +75,11 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeParams P) {
                 const uint64_t i = b0 + j;
                 float4 r = make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
                 if (P.flags & 1) {
-                    r = make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf), __fdiv_rn(r.z, Mf),
-                                    __fdiv_rn(r.w, Mf));
+                    r = P.inv_m != 0.0f
+                            ? make_float4(__fmul_rn(r.x, P.inv_m), __fmul_rn(r.y, P.inv_m),
+                                          __fmul_rn(r.z, P.inv_m), __fmul_rn(r.w, P.inv_m))
+                            : make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf),
+                                          __fdiv_rn(r.z, Mf), __fdiv_rn(r.w, Mf));
                 }
                 if (j + 4u <= cnt) {
                     float4 *o = reinterpret_cast<float4 *>(P.out + i);

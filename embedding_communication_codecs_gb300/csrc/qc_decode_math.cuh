@@ -38,4 +38,43 @@ __device__ __forceinline__ float dequant_code(uint32_t f, int c, float sc, float
     }
 }
 
+// acc + (dequantized code c of field f), rounded once as fl(acc + d).  The
+// ternary value d = (c - 1) * s is exact, so fl(acc + d) is the single rounding
+// of fma(c - 1, s, acc); c - 1 comes from the bit pattern of 2^23 + c minus
+// 2^23 + 1.  Uniform values are themselves rounded and need the separate add.
+template <int SCHEME, int BITS>
+__device__ __forceinline__ float accumulate_code(float acc, uint32_t f, int c, float sc, float of) {
+    if constexpr (SCHEME == kTernary) {
+        const uint32_t m = ((f >> (c * BITS)) & ((1u << BITS) - 1u)) | 0x4B000000u;
+        return __fmaf_rn(__fsub_rn(__uint_as_float(m), 8388609.0f), sc, acc);
+    } else {
+        return __fadd_rn(acc, dequant_code<SCHEME, BITS>(f, c, sc, of));
+    }
+}
+
+// The codes of 16 consecutive elements of one worker, read from shared memory
+// as 2 * BITS bytes (16-byte, 8-byte, 4-byte or 2-byte load).
+template <int BITS>
+__device__ __forceinline__ void load_codes16(const unsigned char *src, uint32_t (&f)[4]) {
+    if constexpr (BITS == 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    } else if constexpr (BITS == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        f[0] = v.x; f[1] = v.y; f[2] = 0u; f[3] = 0u;
+    } else if constexpr (BITS == 2) {
+        f[0] = *reinterpret_cast<const uint32_t *>(src); f[1] = f[2] = f[3] = 0u;
+    } else {
+        f[0] = *reinterpret_cast<const unsigned short *>(src); f[1] = f[2] = f[3] = 0u;
+    }
+}
+
+// acc + the dequantized code c (0..15) of a 16-code group.
+template <int SCHEME, int BITS>
+__device__ __forceinline__ float accumulate16(float acc, const uint32_t (&f)[4], int c, float sc,
+                                              float of) {
+    constexpr int kPerWord = 32 / BITS;
+    return accumulate_code<SCHEME, BITS>(acc, f[c / kPerWord], c % kPerWord, sc, of);
+}
+
 }  // namespace qc

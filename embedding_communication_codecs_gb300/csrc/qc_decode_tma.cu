@@ -51,8 +51,8 @@ __device__ __forceinline__ uint32_t field4(const unsigned char *wstage, const ui
 }
 
 template <int SCHEME, int BITS>
-__global__ void __launch_bounds__(kDecodeBlock) decode_tma_kernel(const DecodeParams P,
-                                                                  const DecodeTiles G) {
+__global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __grid_constant__ DecodeParams P,
+                                                                  const __grid_constant__ DecodeTiles G) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
     uint64_t *empty = full + G.stages;
@@ -132,58 +132,86 @@ __global__ void __launch_bounds__(kDecodeBlock) decode_tma_kernel(const DecodePa
         const uint32_t wb = floor16((static_cast<uint64_t>(tcnt) * BITS + 7u) / 8u);
         const uint32_t *gcodes = P.codes + (t0 * BITS) / 32u;
 
-        const bool whole_tile = tcnt == G.te;
-        for (uint32_t e = static_cast<uint32_t>(ct) * 4u; e < tcnt; e += kConsumerWarps * 32 * 4) {
-            const uint32_t kb = G.bucket_shift >= 0 ? (e >> G.bucket_shift) : (e / P.bucket);
-            const float2 *meta = reinterpret_cast<const float2 *>(msc) + kb;
-            const unsigned char *wst = stage + (e * BITS) / 8u;
-            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-            if (whole_tile) {
-#pragma unroll 8
+        if (tcnt == G.te) {
+            // Whole tile: each thread takes 16 consecutive outputs, which lie in
+            // one bucket (buckets are multiples of 32), so one wide load gives a
+            // worker's 16 codes and one 8-byte load its (scale, offset).
+            for (uint32_t g = static_cast<uint32_t>(ct); g < G.te / 16u; g += kConsumerWarps * 32) {
+                const uint32_t e = g * 16u;
+                const uint32_t kb = G.bucket_shift >= 0 ? (e >> G.bucket_shift) : (e / P.bucket);
+                const float2 *meta = reinterpret_cast<const float2 *>(msc) + kb;
+                const unsigned char *wst = stage + (e * BITS) / 8u;
+                float a[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) a[c] = 0.0f;
+#pragma unroll 4
                 for (int w = 0; w < P.M; ++w) {
-                    uint32_t f;
-                    if constexpr (BITS == 8) f = *reinterpret_cast<const uint32_t *>(wst);
-                    else if constexpr (BITS == 4) f = *reinterpret_cast<const unsigned short *>(wst);
-                    else if constexpr (BITS == 2) f = *wst;
-                    else f = (*wst >> (e & 4u)) & 0xFu;
+                    uint32_t f[4];
+                    load_codes16<BITS>(wst, f);
                     const float2 m = meta[w * G.tb];
-                    a0 = __fadd_rn(a0, dequant_code<SCHEME, BITS>(f, 0, m.x, m.y));
-                    a1 = __fadd_rn(a1, dequant_code<SCHEME, BITS>(f, 1, m.x, m.y));
-                    a2 = __fadd_rn(a2, dequant_code<SCHEME, BITS>(f, 2, m.x, m.y));
-                    a3 = __fadd_rn(a3, dequant_code<SCHEME, BITS>(f, 3, m.x, m.y));
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        a[c] = accumulate16<SCHEME, BITS>(a[c], f, c, m.x, m.y);
                     wst += G.worker_bytes;
                 }
-            } else {
+                float4 *o = reinterpret_cast<float4 *>(P.out + t0 + e);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float4 r = make_float4(a[4 * q4], a[4 * q4 + 1], a[4 * q4 + 2], a[4 * q4 + 3]);
+                    if (P.flags & 1)
+                        r = P.inv_m != 0.0f
+                                ? make_float4(__fmul_rn(r.x, P.inv_m), __fmul_rn(r.y, P.inv_m),
+                                              __fmul_rn(r.z, P.inv_m), __fmul_rn(r.w, P.inv_m))
+                                : make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf),
+                                              __fdiv_rn(r.z, Mf), __fdiv_rn(r.w, Mf));
+                    if (P.flags & 2) {
+                        const float4 prev = __ldcs(o + q4);
+                        r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
+                                        __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
+                    }
+                    __stcs(o + q4, r);
+                }
+            }
+        } else {
+            // Tail tile: 4 outputs per thread, bytes past the staged part read
+            // from global memory.
+            for (uint32_t e = static_cast<uint32_t>(ct) * 4u; e < tcnt; e += kConsumerWarps * 32 * 4) {
+                const uint32_t kb = G.bucket_shift >= 0 ? (e >> G.bucket_shift) : (e / P.bucket);
+                const float2 *meta = reinterpret_cast<const float2 *>(msc) + kb;
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
                 for (int w = 0; w < P.M; ++w) {
                     const uint32_t f = field4<BITS>(stage + static_cast<size_t>(w) * G.worker_bytes,
                                                     gcodes + w * P.codes_stride, e, wb);
                     const float2 m = meta[w * G.tb];
-                    a0 = __fadd_rn(a0, dequant_code<SCHEME, BITS>(f, 0, m.x, m.y));
-                    a1 = __fadd_rn(a1, dequant_code<SCHEME, BITS>(f, 1, m.x, m.y));
-                    a2 = __fadd_rn(a2, dequant_code<SCHEME, BITS>(f, 2, m.x, m.y));
-                    a3 = __fadd_rn(a3, dequant_code<SCHEME, BITS>(f, 3, m.x, m.y));
+                    a0 = accumulate_code<SCHEME, BITS>(a0, f, 0, m.x, m.y);
+                    a1 = accumulate_code<SCHEME, BITS>(a1, f, 1, m.x, m.y);
+                    a2 = accumulate_code<SCHEME, BITS>(a2, f, 2, m.x, m.y);
+                    a3 = accumulate_code<SCHEME, BITS>(a3, f, 3, m.x, m.y);
                 }
-            }
-            float4 r = make_float4(a0, a1, a2, a3);
-            if (P.flags & 1)
-                r = make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf), __fdiv_rn(r.z, Mf),
-                                __fdiv_rn(r.w, Mf));
-            const uint64_t i = t0 + e;
-            if (e + 4u <= tcnt) {
-                float4 *o = reinterpret_cast<float4 *>(P.out + i);
-                if (P.flags & 2) {
-                    const float4 prev = __ldcs(o);
-                    r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
-                                    __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
-                }
-                __stcs(o, r);
-            } else {
+                float4 r = make_float4(a0, a1, a2, a3);
+                if (P.flags & 1)
+                    r = P.inv_m != 0.0f
+                            ? make_float4(__fmul_rn(r.x, P.inv_m), __fmul_rn(r.y, P.inv_m),
+                                          __fmul_rn(r.z, P.inv_m), __fmul_rn(r.w, P.inv_m))
+                            : make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf), __fdiv_rn(r.z, Mf),
+                                          __fdiv_rn(r.w, Mf));
+                const uint64_t i = t0 + e;
+                if (e + 4u <= tcnt) {
+                    float4 *o = reinterpret_cast<float4 *>(P.out + i);
+                    if (P.flags & 2) {
+                        const float4 prev = __ldcs(o);
+                        r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
+                                        __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
+                    }
+                    __stcs(o, r);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (e + c < tcnt) {
-                        float v = get(r, c);
-                        if (P.flags & 2) v = __fadd_rn(P.out[i + c], v);
-                        P.out[i + c] = v;
+                    for (int c = 0; c < 4; ++c) {
+                        if (e + c < tcnt) {
+                            float v = get(r, c);
+                            if (P.flags & 2) v = __fadd_rn(P.out[i + c], v);
+                            P.out[i + c] = v;
+                        }
                     }
                 }
             }

@@ -82,6 +82,7 @@ struct DecodeParams {
     uint64_t nbuckets;
     float *out;
     int flags;
+    float inv_m;  // 1 / M when M is a power of two (an exact multiply), else 0
 };
 
 // Tiling of the pipelined decode: TB whole buckets (TE elements) per tile; a
