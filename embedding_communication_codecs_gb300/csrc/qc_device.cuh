@@ -50,6 +50,16 @@ __device__ __forceinline__ void uniform4(uint64_t i0, uint32_t step, const Philo
     u[3] = __fmul_rn(__uint2float_rn(r.w >> 8), 0x1p-24f);
 }
 
+// The single draw u for element i (the same value uniform4 gives it).
+__device__ __forceinline__ float uniform1(uint64_t i, uint32_t step, const PhiloxKeys &k) {
+    const uint64_t blk = i >> 2;
+    const uint4 r = philox4x32_10(
+        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), step, 0u), k);
+    const uint32_t c = static_cast<uint32_t>(i & 3u);
+    const uint32_t w = c == 0 ? r.x : c == 1 ? r.y : c == 2 ? r.z : r.w;
+    return __fmul_rn(__uint2float_rn(w >> 8), 0x1p-24f);
+}
+
 // ---------------------------------------------------------------------------
 // Integer helpers without conversion instructions.
 
