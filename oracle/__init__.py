@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY = 0, 1, 2
+SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY, SCHEME_QSGD = 0, 1, 2, 3
 ROUND_NEAREST, ROUND_STOCHASTIC = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OUT_SUM, OUT_MEAN, ACCUMULATE_INTO_OUT = 0, 1, 2
@@ -67,6 +67,7 @@ def _L():
         lib.oracle_encode_uniform.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P, P]
         lib.oracle_encode_sign.argtypes = [P, I, P, S, S, P, P]
         lib.oracle_encode_ternary.argtypes = [P, I, P, S, U64, S, I, U64, U32, P, P]
+        lib.oracle_encode_qsgd.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P]
         lib.oracle_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I]
         lib.oracle_sign_vote.argtypes = [P, S, I, S, P]
         lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
@@ -78,6 +79,7 @@ def _L():
         lib.oracle_rowwise_fp8.argtypes = [P, S, S, P, P]
         lib.oracle_rowwise_fp8_dequant.argtypes = [P, P, S, S, P]
         for name in ("oracle_encode_uniform", "oracle_encode_sign", "oracle_encode_ternary",
+                     "oracle_encode_qsgd",
                      "oracle_decode_accumulate", "oracle_sign_vote", "oracle_rowwise_fp8",
                      "oracle_rowwise_fp8_dequant"):
             getattr(lib, name).restype = I
@@ -162,6 +164,19 @@ def encode_ternary(grad, err=None, *, bucket, mode=ROUND_STOCHASTIC, seed=0, ste
                                     mode, seed, step, _ptr(codes), _ptr(scale))
     _check(rc, "encode_ternary")
     return codes[:code_words(n, 2)], scale[:num_buckets(n, bucket)]
+
+
+def encode_qsgd(grad, err=None, *, bits, bucket, mode=ROUND_STOCHASTIC, seed=0, step=0,
+                index_base=0):
+    """Returns (codes uint32[], unit f32[]); ``err`` is updated in place."""
+    g = np.ascontiguousarray(grad)
+    n = g.size
+    codes = np.zeros(max(code_words(n, bits), 1), dtype=np.uint32)
+    scale = np.zeros(max(num_buckets(n, bucket), 1), dtype=np.float32)
+    rc = _L().oracle_encode_qsgd(_ptr(g), _grad_dtype(g), _ptr(err), n, index_base, bits, bucket,
+                                 mode, seed, step, _ptr(codes), _ptr(scale))
+    _check(rc, "encode_qsgd")
+    return codes[:code_words(n, bits)], scale[:num_buckets(n, bucket)]
 
 
 def decode_accumulate(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM,

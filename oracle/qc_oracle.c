@@ -37,7 +37,7 @@
 
 #define ORC_API __attribute__((visibility("default")))
 
-enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2 };
+enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2, ORC_SCHEME_QSGD = 3 };
 enum { ORC_ROUND_NEAREST = 0, ORC_ROUND_STOCHASTIC = 1 };
 enum { ORC_DTYPE_F32 = 0, ORC_DTYPE_BF16 = 1 };
 enum { ORC_OUT_MEAN = 1, ORC_ACCUMULATE_INTO_OUT = 2 };
@@ -352,6 +352,83 @@ ORC_API int oracle_encode_ternary(const void *grad, int dtype, float *err, size_
 }
 
 /* ------------------------------------------------------------------------ */
+/* QSGD: s-level stochastic quantization scaled by the bucket's L2 norm.
+ *
+ * p3 "Quantized SGD Algorithms" (QSGD: stochastic quantization with an unbiased
+ * estimator, s levels, compression ratio 32/log2(s)); p4 "Why sparsification
+ * fights the all-reduce" (QSGD preserves unbiasedness).  The level rule is the
+ * named method's (Alistarh et al.): with l = floor(|v_i| / ||v|| * s), keep l
+ * with probability 1 - frac and l + 1 with probability frac.  Readings: the norm
+ * is taken per bucket; a b-bit code is one sign bit (top bit, set for p < 0)
+ * over b-1 level bits, s = 2^(b-1) - 1; the unit ||v|| / s is rounded once and
+ * the level is found like the uniform scheme's with min = 0:
+ *   p_i  = e_i + g_i
+ *   nrm  = sqrt(sum of p_i^2), fp64 sum in index order, rounded once to fp32
+ *   unit = nrm / s ;  unit == 0 -> every code 0
+ *   t_i  = |p_i| / unit
+ *   stochastic: lvl = min(floor(t_i) + [u_i < t_i - floor(t_i)], s)
+ *   nearest:    lvl = min(rint(t_i), s)
+ *   code = [p_i < 0] << (b-1) | lvl ;  deq_i = +-fl(lvl * unit)
+ *   e_i  = p_i - deq_i
+ * Outputs: packed codes, scale[k] = unit. */
+ORC_API int oracle_encode_qsgd(const void *grad, int dtype, float *err, size_t n,
+                               uint64_t index_base, int bits, size_t bucket, int mode,
+                               uint64_t seed, uint32_t step, uint32_t *codes, float *scale_out)
+{
+    if (!(bits == 2 || bits == 4 || bits == 8) || !orc_valid_bucket(bucket))
+        return -1;
+    const uint32_t s = (1u << (bits - 1)) - 1u;
+    const float sf = (float)s;
+    memset(codes, 0, oracle_code_words(n, bits) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    if (!p)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+        }
+        double ss = 0.0;
+        for (size_t j = 0; j < cnt; ++j)
+            ss += (double)p[j] * (double)p[j];
+        float nrm = (float)sqrt(ss);
+        float unit = nrm / sf;
+        for (size_t j = 0; j < cnt; ++j) {
+            uint32_t lvl = 0;
+            float a = fabsf(p[j]);
+            if (unit != 0.0f) {
+                float t = a / unit;
+                float level;
+                if (mode == ORC_ROUND_NEAREST) {
+                    level = rintf(t);
+                } else {
+                    float f = floorf(t);
+                    float frac = t - f;
+                    float u = oracle_uniform(seed, step, index_base + lo + j);
+                    level = (u < frac) ? f + 1.0f : f;
+                }
+                if (!(level >= 0.0f))
+                    level = 0.0f;
+                lvl = (level > sf) ? s : (uint32_t)level;
+            }
+            uint32_t neg = (p[j] < 0.0f) ? 1u : 0u;
+            orc_put_code(codes, lo + j, bits, (neg << (bits - 1)) | lvl);
+            if (err) {
+                float mag = (float)lvl * unit;
+                float deq = neg ? -mag : mag;
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = unit;
+    }
+    free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Receiver side: dequantize M workers' payloads and accumulate in fp32.
  *
  * p1 "Where Quantization Sits" (receive, dequantize, continue); p2 "How
@@ -380,6 +457,8 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
         return -1;
     if (scheme == ORC_SCHEME_TERNARY && bits != 2)
         return -1;
+    if (scheme == ORC_SCHEME_QSGD && !(bits == 2 || bits == 4 || bits == 8))
+        return -1;
     for (size_t i = 0; i < n; ++i) {
         size_t k = i / bucket;
         float acc = 0.0f;
@@ -392,8 +471,13 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
                 d = fmaf((float)q, s, offset[(size_t)w * meta_stride + k]);
             else if (scheme == ORC_SCHEME_SIGN)
                 d = q ? s : -s;
-            else
+            else if (scheme == ORC_SCHEME_TERNARY)
                 d = (float)((int)q - 1) * s;
+            else { /* QSGD: sign bit over the level */
+                uint32_t lvl = q & ((1u << (bits - 1)) - 1u);
+                float mag = (float)lvl * s;
+                d = (q >> (bits - 1)) ? -mag : mag;
+            }
             acc = acc + d;
         }
         float r = (flags & ORC_OUT_MEAN) ? acc / (float)M : acc;

@@ -564,3 +564,94 @@ def test_workload_distributions():
     assert abs(d.std() - math.sqrt(2) * 1e-3) < 5e-5
     b = wl.bf16_gradients(1 << 12, 2, seed=4)
     assert b.dtype == np.uint16 and b.shape == (2, 1 << 12)
+
+
+# -------------------------------------------------------------------------- QSGD
+
+def _exact_sqrt_f32(fr: Fraction) -> np.float32:
+    """binary32 rounding of sqrt of a nonnegative rational (bisection on floats)."""
+    x = np.float32(np.sqrt(float(fr)))
+    # adjust to the correctly rounded value by comparing squares of midpoints
+    for _ in range(4):
+        up = np.nextafter(x, np.float32(np.inf))
+        dn = np.nextafter(x, np.float32(0))
+        mid_up = (frac(x) + frac(up)) / 2
+        mid_dn = (frac(x) + frac(dn)) / 2
+        if mid_up * mid_up < fr:
+            x = up
+        elif mid_dn * mid_dn > fr:
+            x = dn
+        else:
+            break
+    return np.float32(x)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_qsgd_unit_levels_and_signs(bits):
+    s = (1 << (bits - 1)) - 1
+    bucket, n = 64, 64 * 3 + 20
+    g = _tiny_buckets(40 + bits, n)
+    g[5] = -0.0
+    codes, unit = orc.encode_qsgd(g, None, bits=bits, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                                  seed=3, step=1)
+    c = np.array(_unpack(codes, n, bits))
+    for k in range(orc.num_buckets(n, bucket)):
+        seg = g[k * bucket:(k + 1) * bucket]
+        sq = sum(frac(v) * frac(v) for v in seg)
+        nrm = _exact_sqrt_f32(sq)
+        # the oracle's fp64 sum may differ from the exact sum by far less than an ulp
+        want_unit = to_f32(frac(nrm) / s)
+        assert abs(frac(unit[k]) - frac(want_unit)) <= Fraction(ulp32(want_unit))
+        for j, v in enumerate(seg):
+            code = int(c[k * bucket + j])
+            assert (code >> (bits - 1)) == (1 if v < 0 else 0)
+            lvl = code & s
+            t = abs(frac(v)) / frac(unit[k])
+            fl = t.numerator // t.denominator
+            assert lvl in (min(fl, s), min(fl + 1, s))
+
+
+def test_qsgd_single_element_takes_top_level():
+    g = np.zeros(32, dtype=np.float32)
+    g[7] = np.float32(-0.37)
+    codes, unit = orc.encode_qsgd(g, None, bits=4, bucket=32, mode=orc.ROUND_NEAREST)
+    c = _unpack(codes, 32, 4)
+    assert c[7] == (1 << 3) | 7
+    assert all(v == 0 for i, v in enumerate(c) if i != 7)
+    z, u0 = orc.encode_qsgd(np.zeros(32, dtype=np.float32), None, bits=8, bucket=32)
+    assert u0[0] == 0.0 and not z.any()
+
+
+def test_qsgd_unbiased_and_variance_bound():
+    """E[Q(v)] = v, and E||Q(v) - v||^2 <= min(n / s^2, sqrt(n) / s) ||v||^2
+    (the QSGD variance bound), over many independent steps."""
+    bits, n = 4, 32
+    s = (1 << (bits - 1)) - 1
+    v = (np.random.default_rng(4).standard_normal(n)).astype(np.float32)
+    K = 4000
+    acc = np.zeros(n)
+    sqerr = 0.0
+    for step in range(K):
+        codes, unit = orc.encode_qsgd(v, None, bits=bits, bucket=n, seed=9, step=step)
+        c = np.array(_unpack(codes, n, bits))
+        deq = np.where(c >> (bits - 1), -1.0, 1.0) * (c & s) * float(unit[0])
+        acc += deq
+        sqerr += float(((deq - v) ** 2).sum())
+    mean = acc / K
+    nrm2 = float((v.astype(np.float64) ** 2).sum())
+    assert np.all(np.abs(mean - v) <= 6 * float(unit[0]) / math.sqrt(K))
+    bound = min(n / s ** 2, math.sqrt(n) / s) * nrm2
+    assert sqerr / K <= bound
+
+
+def test_qsgd_decode_closed_form():
+    n, bucket, bits = 64, 32, 4
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, 16, size=(2, n))
+    unit = np.array([[0.25, 2.0], [0.5, 0.125]], dtype=np.float32)
+    words = np.stack([_pack(q[w], bits) for w in range(2)])
+    out = orc.decode_accumulate(words, unit, None, M=2, n=n, bits=bits, bucket=bucket,
+                                scheme=orc.SCHEME_QSGD)
+    want = [sum((-1 if q[w, i] >> 3 else 1) * (q[w, i] & 7) * float(unit[w, i // bucket])
+                for w in range(2)) for i in range(n)]
+    assert out.tolist() == want
