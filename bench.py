@@ -139,15 +139,20 @@ class Fp8Rowwise(Component):
 
 
 class UniformEF(Component):
-    """Uniform encode with error feedback of one flat fp32 gradient, then decode M = 1."""
+    """Encode with error feedback of one flat fp32 gradient (uniform or QSGD
+    scheme), then decode M = 1."""
 
-    def __init__(self, name, n, bits, bucket, stochastic, seed, sigma_mode):
+    def __init__(self, name, n, bits, bucket, stochastic, seed, sigma_mode, scheme=0):
         self.name, self.n, self.bits, self.bucket = name, n, bits, bucket
         self.stochastic, self.seed, self.sigma_mode = stochastic, seed, sigma_mode
+        self.scheme = scheme
         words, nb = _words(n, bits), _nb(n, bucket)
-        enc = 12 * n + 4 * words + 8 * nb
-        dec = 4 * words + 8 * nb + 4 * n
-        self.kernels = {f"encode_u{bits}_ef": (1, enc), f"decode_u{bits}_m1": (1, dec)}
+        meta = 8 if scheme == 0 else 4
+        enc = 12 * n + 4 * words + meta * nb
+        dec = 4 * words + meta * nb + 4 * n
+        tag = f"u{bits}" if scheme == 0 else f"qsgd{bits}"
+        self.enc_name, self.dec_name = f"encode_{tag}_ef", f"decode_{tag}_m1"
+        self.kernels = {self.enc_name: (1, enc), self.dec_name: (1, dec)}
         self.units = 2 * n
         self.h2d = 4 * n
         self.d2h = 4 * n
@@ -163,17 +168,18 @@ class UniformEF(Component):
     def setup(self, q, torch):
         self.g = torch.from_numpy(self._grad(self.n)).cuda()
         self.err = torch.zeros(self.n, device="cuda")
-        self.codes, self.scale, self.offset = q.alloc_payload(self.n, self.bits, self.bucket, 0)
+        self.codes, self.scale, self.offset = q.alloc_payload(self.n, self.bits, self.bucket,
+                                                              self.scheme)
         self.out = torch.empty(self.n, device="cuda")
 
     def run(self, q, t, timer):
         mode = q.QC_ROUND_STOCHASTIC if self.stochastic else q.QC_ROUND_NEAREST
-        with timer(f"encode_u{self.bits}_ef"):
-            q.qc_encode_ef(self.g, self.err, self.n, self.bits, self.bucket, 0, mode, self.seed, t,
-                           self.codes, self.scale, self.offset)
-        with timer(f"decode_u{self.bits}_m1"):
+        with timer(self.enc_name):
+            q.qc_encode_ef(self.g, self.err, self.n, self.bits, self.bucket, self.scheme, mode,
+                           self.seed, t, self.codes, self.scale, self.offset)
+        with timer(self.dec_name):
             q.qc_decode_accumulate(self.codes, 0, self.scale, self.offset, 0, 1, self.n, self.bits,
-                                   self.bucket, 0, self.out, 0)
+                                   self.bucket, self.scheme, self.out, 0)
 
     def host_inputs(self):
         return [self.g]
@@ -192,10 +198,16 @@ class UniformEF(Component):
         mode = orc.ROUND_STOCHASTIC if self.stochastic else orc.ROUND_NEAREST
 
         def go(lo, hi):
-            c, s, o = orc.encode_uniform(g[lo:hi], err[lo:hi], bits=self.bits, bucket=self.bucket,
-                                         mode=mode, seed=self.seed, step=0, index_base=lo)
+            if self.scheme == 0:
+                c, s, o = orc.encode_uniform(g[lo:hi], err[lo:hi], bits=self.bits,
+                                             bucket=self.bucket, mode=mode, seed=self.seed,
+                                             step=0, index_base=lo)
+            else:
+                (c, s), o = orc.encode_qsgd(g[lo:hi], err[lo:hi], bits=self.bits,
+                                            bucket=self.bucket, mode=mode, seed=self.seed,
+                                            step=0, index_base=lo), None
             orc.decode_accumulate(c, s, o, M=1, n=hi - lo, bits=self.bits, bucket=self.bucket,
-                                  scheme=orc.SCHEME_UNIFORM)
+                                  scheme=self.scheme)
         return _split(go, n, self.bucket), 2 * n
 
 
@@ -356,10 +368,14 @@ def make_workload(name):
         "sign_ef_vote": lambda: [SignVote()],
         "rx_u8": lambda: [Receiver("rx_u8", 0, 8)],
         "rx_ternary": lambda: [Receiver("rx_ternary", 2, 2)],
+        "qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 250_000_000, 4, 512, True, 2, "bucket",
+                                       scheme=3)],
         "u8_ef_small": lambda: [UniformEF("u8_ef_small", 1 << 20, 8, 2048, False, 0, "outlier")],
         "u8_ef_large": lambda: [UniformEF("u8_ef_large", 1 << 28, 8, 2048, False, 0, "outlier")],
         # smaller single-kernel cases (inputs still larger than L2) for profiler captures
         "probe_sr4_ef": lambda: [UniformEF("sr4_ef", 1 << 26, 4, 512, True, 2, "bucket")],
+        "probe_qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 1 << 26, 4, 512, True, 2, "bucket",
+                                             scheme=3)],
         "probe_sign": lambda: [SignVote(n=1 << 24, M=2)],
         "probe_u8_bf16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 27, M=1)],
         "probe_ternary_bf16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 27, M=1)],

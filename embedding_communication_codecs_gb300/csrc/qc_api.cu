@@ -10,6 +10,10 @@
 #include "../../include/qcodec.h"
 #include "qc_internal.h"
 
+static_assert(int{QC_SCHEME_UNIFORM} == qc::kUniform && int{QC_SCHEME_SIGN} == qc::kSign &&
+                  int{QC_SCHEME_TERNARY} == qc::kTernary && int{QC_SCHEME_QSGD} == qc::kQsgd,
+              "the public scheme numbers are the kernels' template arguments");
+
 namespace {
 
 thread_local char g_last_error[512] = "";
@@ -244,6 +248,9 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
             return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme is deterministic; mode must be NEAREST");
     } else if (scheme == QC_SCHEME_TERNARY) {
         if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: ternary scheme needs bits == 2 (got %d)", bits);
+    } else if (scheme == QC_SCHEME_QSGD) {
+        if (bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: QSGD bits must be 2, 4 or 8 (got %d)", bits);
     } else {
         return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown scheme %d", scheme);
     }
@@ -316,6 +323,9 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
         if (bits != 1) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: sign scheme needs bits == 1");
     } else if (scheme == QC_SCHEME_TERNARY) {
         if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: ternary scheme needs bits == 2");
+    } else if (scheme == QC_SCHEME_QSGD) {
+        if (bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: QSGD bits must be 2, 4 or 8");
     } else {
         return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: unknown scheme %d", scheme);
     }

@@ -33,6 +33,12 @@ __device__ __forceinline__ float dequant_code(uint32_t f, int c, float sc, float
         return __fmaf_rn(code_value<BITS>(f, c), sc, of);
     } else if constexpr (SCHEME == kTernary) {
         return __fmaf_rn(code_value<BITS>(f, c), sc, -sc);
+    } else if constexpr (SCHEME == kQsgd) {
+        // sign bit over the level: +-fl(level * unit), the sign set by OR
+        const uint32_t code = (f >> (c * BITS)) & ((1u << BITS) - 1u);
+        const uint32_t lvl = code & ((1u << (BITS - 1)) - 1u);
+        const float mag = __fmul_rn(__fsub_rn(__uint_as_float(lvl | 0x4B000000u), 8388608.0f), sc);
+        return __uint_as_float(__float_as_uint(mag) | ((code << (32 - BITS)) & 0x80000000u));
     } else {
         return ((f >> c) & 1u) ? sc : -sc;
     }

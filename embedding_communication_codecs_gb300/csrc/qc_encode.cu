@@ -141,6 +141,11 @@ cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stoch
                           cudaStream_t stream) {
     if (scheme == kSign) return launch_dtype<kSign, 1, false>(p, bf16, stream);
     if (scheme == kTernary) return launch_round<kTernary, 2>(p, stochastic, bf16, stream);
+    if (scheme == kQsgd) {
+        if (bits == 2) return launch_round<kQsgd, 2>(p, stochastic, bf16, stream);
+        if (bits == 4) return launch_round<kQsgd, 4>(p, stochastic, bf16, stream);
+        return launch_round<kQsgd, 8>(p, stochastic, bf16, stream);
+    }
     switch (bits) {
         case 1: return launch_round<kUniform, 1>(p, stochastic, bf16, stream);
         case 2: return launch_round<kUniform, 2>(p, stochastic, bf16, stream);

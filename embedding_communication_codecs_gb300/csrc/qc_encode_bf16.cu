@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kBlock, SR ? 3 : 4) encode_bf16_kernel(const _
                 raw[sl] = make_uint4(0u, 0u, 0u, 0u);
                 if (j + kEps <= cnt && e + kEps <= staged) {
                     raw[sl] = *reinterpret_cast<const uint4 *>(stage + e * 2u);
-                    if constexpr (SCHEME == kSign) {
+                    if constexpr (SCHEME == kSign || SCHEME == kQsgd) {
                         float v[8];
                         unpack8(raw[sl], v);
 #pragma unroll
@@ -326,6 +326,11 @@ cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int 
                                int stochastic, cudaStream_t stream) {
     if (scheme == kSign) return launch_one<kSign, 1, false>(p, g, stream);
     if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, stream);
+    if (scheme == kQsgd) {
+        if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, stream);
+        if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, stream);
+        return launch_round<kQsgd, 8>(p, g, stochastic, stream);
+    }
     switch (bits) {
         case 1: return launch_round<kUniform, 1>(p, g, stochastic, stream);
         case 2: return launch_round<kUniform, 2>(p, g, stochastic, stream);

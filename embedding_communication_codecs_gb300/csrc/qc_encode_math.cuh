@@ -53,6 +53,18 @@ struct Stats<kSign> {  // sum of |p| as a double word
     __device__ void merge(const Stats &o) { sum = dw_add(sum, o.sum); }
 };
 
+template <>
+struct Stats<kQsgd> {  // sum of p^2 as a double word; each square is split exactly
+    DWord sum;
+    __device__ void init() { sum = DWord{0.0f, 0.0f}; }
+    __device__ void add(float x) {
+        const float hi = __fmul_rn(x, x);
+        sum = dw_add(sum, DWord{hi, __fmaf_rn(x, x, -hi)});
+    }
+    __device__ void warp_reduce() { sum = warp_sum(sum); }
+    __device__ void merge(const Stats &o) { sum = dw_add(sum, o.sum); }
+};
+
 // Per-bucket quantization parameters derived from the statistics.
 struct BucketParams {
     float a;      // UNIFORM: min (offset); SIGN / TERNARY: s
@@ -85,6 +97,26 @@ struct Finish<kSign, BITS> {
     }
 };
 
+// QSGD: unit = ||p|| / s with s = 2^(BITS-1) - 1.  The norm is the binary32
+// rounding of sqrt(hi + lo): r0 = sqrt(hi) correctly rounded, the remainder
+// hi - r0^2 is exact by fma, and (remainder + lo) / (2 r0) is the first-order
+// correction.
+template <int BITS>
+struct Finish<kQsgd, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kQsgd> &st, uint32_t) {
+        const float hi = st.sum.hi;
+        float nrm = 0.0f;
+        if (hi > 0.0f) {
+            const float r0 = __fsqrt_rn(hi);
+            const float rem = __fadd_rn(__fmaf_rn(-r0, r0, hi), st.sum.lo);
+            nrm = __fadd_rn(r0, __fdiv_rn(rem, __fmul_rn(2.0f, r0)));
+        }
+        constexpr float kS = static_cast<float>((1u << (BITS - 1)) - 1u);
+        const float unit = __fdiv_rn(nrm, kS);
+        return BucketParams{unit, unit};
+    }
+};
+
 // ------------------------------------------------------------- per element
 
 // Code and dequantized value of one element.
@@ -108,6 +140,25 @@ __device__ __forceinline__ uint32_t quantize(float p, float u, const BucketParam
         q = min(q, L);
         deq = __fmaf_rn(small_uint_to_float(q), bp.scale, bp.a);
         return q;
+    } else if constexpr (SCHEME == kQsgd) {
+        // the uniform level of |p| with min 0 and scale = unit, under a sign bit
+        constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
+        const uint32_t neg = p < 0.0f ? 1u : 0u;
+        const float unit = bp.a;
+        uint32_t q = 0u;
+        if (unit != 0.0f) {
+            const float t = __fdiv_rn(fabsf(p), unit);
+            q = rint_small(t);
+            if constexpr (SR) {
+                if (small_uint_to_float(q) > t) q -= 1u;
+                const float fr = __fsub_rn(t, small_uint_to_float(q));
+                q += (u < fr) ? 1u : 0u;
+            }
+            q = min(q, S);
+        }
+        const float mag = __fmul_rn(small_uint_to_float(q), unit);
+        deq = neg ? -mag : mag;
+        return (neg << (BITS - 1)) | q;
     } else if constexpr (SCHEME == kSign) {
         const bool pos = p >= 0.0f;
         deq = pos ? bp.a : -bp.a;
@@ -157,7 +208,9 @@ __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
     const bool normal = d >= 0x1p-125f && d <= 0x1p125f;
     f.usable = SCHEME == kSign || normal;  // the sign code needs no division
     f.rinv = (SCHEME != kSign && normal) ? __frcp_rn(d) : 0.0f;
-    f.delta2 = (SCHEME == kUniform) ? static_cast<float>(1u << BITS) * 0x1p-21f : 0x1p-21f;
+    f.delta2 = SCHEME == kUniform ? static_cast<float>(1u << BITS) * 0x1p-21f
+               : SCHEME == kQsgd     ? static_cast<float>(1u << (BITS - 1)) * 0x1p-21f
+                                     : 0x1p-21f;
     return f;
 }
 
@@ -193,6 +246,33 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
         q = min(q, L);
         deq = __fmaf_rn(fminf(qf, static_cast<float>(L)), bp.scale, bp.a);
         return q;
+    } else if constexpr (SCHEME == kQsgd) {
+        constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
+        constexpr float kMagic = 12582912.0f;
+        const uint32_t neg = p < 0.0f ? 1u : 0u;
+        const float ta = __fmul_rn(fabsf(p), fq.rinv);
+        float qf;
+        uint32_t q;
+        if constexpr (!SR) {
+            const float y = __fadd_rn(ta, kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            qf = __fsub_rn(y, kMagic);
+            redo = fabsf(__fsub_rn(ta, qf)) >= 0.5f - fq.delta2;
+        } else {
+            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            const float ff = __fsub_rn(y, kMagic);
+            const float fr = __fsub_rn(ta, ff);
+            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
+                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
+            const bool up = u < fr;
+            q += up ? 1u : 0u;
+            qf = up ? __fadd_rn(ff, 1.0f) : ff;
+        }
+        q = min(q, S);
+        const float mag = __fmul_rn(fminf(qf, static_cast<float>(S)), bp.a);
+        deq = neg ? -mag : mag;
+        return (neg << (BITS - 1)) | q;
     } else if constexpr (SCHEME == kTernary) {
         const float s = bp.a;
         const float pa = __fmul_rn(fabsf(p), fq.rinv);
@@ -254,6 +334,24 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
         }
         // keep ? (p > 0 ? 2 : 0) : 1; a kept element is never zero
         return keep ? ((__float_as_uint(p) >> 31) ? 0u : 2u) : 1u;
+    } else if constexpr (SCHEME == kQsgd) {
+        constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
+        constexpr float kMagic = 12582912.0f;
+        const float ta = __fmul_rn(fabsf(p), fq.rinv);
+        uint32_t q;
+        if constexpr (!SR) {
+            const float y = __fadd_rn(ta, kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            redo = fabsf(__fsub_rn(ta, __fsub_rn(y, kMagic))) >= 0.5f - fq.delta2;
+        } else {
+            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
+            q = __float_as_uint(y) - 0x4B400000u;
+            const float fr = __fsub_rn(ta, __fsub_rn(y, kMagic));
+            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
+                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
+            q += (u < fr) ? 1u : 0u;
+        }
+        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | min(q, S);
     } else {
         redo = false;
         return p >= 0.0f ? 1u : 0u;

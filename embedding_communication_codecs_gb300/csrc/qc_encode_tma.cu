@@ -214,6 +214,11 @@ cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int s
                               int stochastic, int bf16, cudaStream_t stream) {
     if (scheme == kSign) return launch_dtype<kSign, 1, false>(p, g, bf16, stream);
     if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, bf16, stream);
+    if (scheme == kQsgd) {
+        if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, bf16, stream);
+        if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, bf16, stream);
+        return launch_round<kQsgd, 8>(p, g, stochastic, bf16, stream);
+    }
     switch (bits) {
         case 1: return launch_round<kUniform, 1>(p, g, stochastic, bf16, stream);
         case 2: return launch_round<kUniform, 2>(p, g, stochastic, bf16, stream);

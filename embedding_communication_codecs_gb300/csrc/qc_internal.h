@@ -7,7 +7,7 @@
 
 namespace qc {
 
-enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2 };
+enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2, kQsgd = 3 };
 
 // Elements a team of W warps covers per window: 4 float4 slots per lane.
 constexpr int kSlots = 4;

@@ -64,7 +64,8 @@ typedef enum {
 typedef enum {
     QC_SCHEME_UNIFORM = 0,    /* per-bucket min/max, 2^bits levels, fp32 scale+offset */
     QC_SCHEME_SIGN = 1,       /* 1 bit: sign, per-bucket fp32 scale = mean |p|        */
-    QC_SCHEME_TERNARY = 2     /* 2 bits: {-1,0,+1} -> codes {0,1,2}, scale = max |p|  */
+    QC_SCHEME_TERNARY = 2,    /* 2 bits: {-1,0,+1} -> codes {0,1,2}, scale = max |p|  */
+    QC_SCHEME_QSGD = 3        /* sign bit over bits-1 level bits, scale = ||p||_2 / s */
 } qc_scheme;
 
 typedef enum {
@@ -115,6 +116,17 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *     s = max |p| (+0 for an all-zero bucket, then every code is 1).
  *       STOCHASTIC: keep_i = [u_i < fl(|p_i| / s)];  NEAREST: keep_i = [fl(|p_i|/s) > 0.5]
  *     code_i = keep_i ? (p_i > 0 ? 2 : 0) : 1; deq_i = (code_i - 1) * s; scale[k] = s.
+ *   QSGD ("Quantized SGD Algorithms", QSGD; bits 2, 4 or 8): s = 2^(bits-1) - 1,
+ *     nrm = ||p||_2 over the bucket rounded to binary32, unit = fl(nrm / s).
+ *     unit == 0: every code 0.  Else t_i = fl(|p_i| / unit) and the level is
+ *       NEAREST:    l_i = min(rint(t_i), s)
+ *       STOCHASTIC: l_i = min(floor(t_i) + [u_i < t_i - floor(t_i)], s)
+ *     code_i = [p_i < 0] << (bits-1) | l_i; deq_i = +-fl(l_i * unit); scale[k] = unit.
+ *     The norm is the square root of a double-word sum of exactly split squares:
+ *     it is the correctly rounded norm unless that lies within about 2^-40
+ *     (relative) of a rounding boundary.  Norms must stay below 2^63 (the
+ *     squares are summed in binary32 range); below 2^-40 the squares of the
+ *     smallest elements are no longer split exactly.
  * Then, with error feedback, err_i = fl(p_i - deq_i) is written in place.
  *
  * Stochastic draw for element i (global index within this call):
@@ -123,7 +135,7 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *
  * grad   : n elements of `dtype`; 16-byte aligned (f32) or 8-byte aligned (bf16).
  * err    : n fp32, in/out, 16-byte aligned, or NULL for no error feedback.
- * bits   : UNIFORM 1, 2, 4 or 8; SIGN 1; TERNARY 2.
+ * bits   : UNIFORM 1, 2, 4 or 8; SIGN 1; TERNARY 2; QSGD 2, 4 or 8.
  * bucket : elements per bucket, a multiple of 32, 32 <= bucket <= 2^24.
  * codes  : out, qc_code_words(n, bits) uint32 words, 4-byte aligned.
  * scale  : out, qc_num_buckets(n, bucket) fp32.
@@ -145,7 +157,8 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
  * average or sum).  For every element i (bucket k = i / bucket):
  *   acc = +0; for w = 0 .. M-1 in this order: acc = fl(acc + d_w,i) with
  *     UNIFORM d = fma(q, scale_w[k], offset_w[k]); SIGN d = bit ? s_w[k] : -s_w[k];
- *     TERNARY d = (code - 1) * s_w[k]
+ *     TERNARY d = (code - 1) * s_w[k]; QSGD d = +-fl(level * unit_w[k]) with the
+ *     sign from the code's top bit and the level from the rest
  *   r = (flags & QC_OUT_MEAN) ? fl(acc / M) : acc
  *   out_i = (flags & QC_ACCUMULATE_INTO_OUT) ? fl(out_i + r) : r
  *
