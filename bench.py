@@ -337,6 +337,75 @@ class Receiver(Component):
         return _split(go, n, self.bucket), 2 * self.M * n
 
 
+class Reencode(Receiver):
+    """M workers' bf16 gradients encoded without error feedback, then the
+    receiver's fused decode + MEAN + re-encode with its own residual (the
+    reduce-scatter owner's step of a two-phase quantized all-reduce)."""
+
+    def __init__(self, name, scheme, bits, n=1 << 26, M=16, bucket=1024, seed=4):
+        super().__init__(name, scheme, bits, n=n, M=M, bucket=bucket, seed=seed)
+        words, nb = _words(n, bits), _nb(n, bucket)
+        meta = 8 if scheme == 0 else 4
+        tag = "u8" if scheme == 0 else ("ternary" if scheme == 2 else f"s{scheme}b{bits}")
+        self.dec_name = f"reencode_{tag}_m{M}"
+        self.kernels = {self.enc_name: (M, 2 * n + 4 * words + meta * nb),
+                        self.dec_name: (1, M * (4 * words + meta * nb) + 8 * n + 4 * words +
+                                        meta * nb)}
+        self.units = 2 * M * n + n
+        self.d2h = 4 * words
+
+    def setup(self, q, torch):
+        super().setup(q, torch)
+        self.err = torch.zeros(self.n, device="cuda")
+        self.codes2, self.scale2, self.offset2 = q.alloc_payload(self.n, self.bits, self.bucket,
+                                                                 self.scheme)
+
+    def run(self, q, t, timer):
+        mode = q.QC_ROUND_NEAREST if self.scheme == 0 else q.QC_ROUND_STOCHASTIC
+        for w in range(self.M):
+            with timer(self.enc_name):
+                q.qc_encode_ef(self.g[w], None, self.n, self.bits, self.bucket, self.scheme, mode,
+                               self.seed | (w << 32), t, self.codes[w], self.scale[w],
+                               self.offset[w] if self.offset is not None else None,
+                               dtype=q.QC_DTYPE_BF16)
+        with timer(self.dec_name):
+            q.qc_reencode(self.codes, self.codes.stride(0), self.scale, self.offset,
+                          self.scale.stride(0), self.M, self.n, self.bits, self.bucket,
+                          self.scheme, q.QC_OUT_MEAN, self.err, mode, self.seed | (1 << 40), t,
+                          self.codes2, self.scale2, self.offset2, None)
+
+    def host_outputs(self):
+        return [self.codes2]
+
+    def kernel_units(self):
+        return {self.enc_name: self.n, self.dec_name: self.M * self.n}
+
+    def oracle_sample(self, frac):
+        import oracle as orc
+        n = max(self.bucket, int(self.n * frac) // self.bucket * self.bucket)
+        gb = wl.bf16_gradients(n, self.M, self.seed)
+        err = np.zeros(n, dtype=np.float32)
+        mode = orc.ROUND_NEAREST if self.scheme == 0 else orc.ROUND_STOCHASTIC
+
+        def go(lo, hi):
+            cs, ss, os_ = [], [], []
+            for w in range(self.M):
+                if self.scheme == 0:
+                    c, s, o = orc.encode_uniform(gb[w, lo:hi], None, bits=8, bucket=self.bucket,
+                                                 index_base=lo)
+                    os_.append(o)
+                else:
+                    c, s = orc.encode_ternary(gb[w, lo:hi], None, bucket=self.bucket,
+                                              mode=orc.ROUND_STOCHASTIC,
+                                              seed=self.seed | (w << 32), index_base=lo)
+                cs.append(c)
+                ss.append(s)
+            orc.reencode(np.stack(cs), np.stack(ss), np.stack(os_) if os_ else None, M=self.M,
+                         n=hi - lo, bits=self.bits, bucket=self.bucket, scheme=self.scheme,
+                         flags=orc.OUT_MEAN, err=err[lo:hi], mode=mode)
+        return _split(go, n, self.bucket), self.units * n // self.n
+
+
 def _split(fn, n, align):
     """A closure running fn over n elements in bucket-aligned parts on every core."""
     cores = _cores()
@@ -370,6 +439,8 @@ def make_workload(name):
         "rx_ternary": lambda: [Receiver("rx_ternary", 2, 2)],
         "qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 250_000_000, 4, 512, True, 2, "bucket",
                                        scheme=3)],
+        "rx_reencode_u8": lambda: [Reencode("rx_reencode_u8", 0, 8)],
+        "rx_reencode_ternary": lambda: [Reencode("rx_reencode_ternary", 2, 2)],
         "u8_ef_small": lambda: [UniformEF("u8_ef_small", 1 << 20, 8, 2048, False, 0, "outlier")],
         "u8_ef_large": lambda: [UniformEF("u8_ef_large", 1 << 28, 8, 2048, False, 0, "outlier")],
         # smaller single-kernel cases (inputs still larger than L2) for profiler captures
@@ -381,6 +452,7 @@ def make_workload(name):
         "probe_ternary_bf16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 27, M=1)],
         "probe_decode_u8_m16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 24, M=16)],
         "probe_decode_ternary_m16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 24, M=16)],
+        "probe_reencode_u8_m16": lambda: [Reencode("rx_reencode_u8", 0, 8, n=1 << 24, M=16)],
         "probe_fp8": lambda: [Fp8Rowwise(rows=1 << 19)],
     }
     return table[name]()

@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ER
 
 # Every symbol the C ABI exports, in header order.
 EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
-           "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
+           "qc_reencode", "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
            "qc_last_error", "qc_version")
 
 
@@ -54,10 +54,12 @@ def _load():
     lib.qc_num_buckets.argtypes, lib.qc_num_buckets.restype = [S, S], S
     lib.qc_encode_ef.argtypes = [P, I, P, S, I, S, I, I, U64, U32, P, P, P, P]
     lib.qc_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I, P]
+    lib.qc_reencode.argtypes = [P, S, P, P, S, I, S, I, S, I, I, P, I, U64, U32, P, P, P, P, P]
     lib.qc_sign_vote.argtypes = [P, S, I, S, P, P]
     lib.qc_rowwise_fp8.argtypes = [P, S, S, P, P, P]
     lib.qc_rowwise_fp8_dequant.argtypes = [P, P, S, S, P, P]
-    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8",
+    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_reencode", "qc_sign_vote",
+                 "qc_rowwise_fp8",
                  "qc_rowwise_fp8_dequant"):
         getattr(lib, name).restype = I
     lib.qc_take_device_errors.argtypes, lib.qc_take_device_errors.restype = [P], I
@@ -141,6 +143,19 @@ def qc_decode_accumulate(codes, codes_stride_words, scale, offset, meta_stride, 
     _check(lib.qc_decode_accumulate(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
                                     meta_stride, M, n, bits, bucket, scheme, _ptr(out), flags,
                                     _stream(stream)))
+
+
+def qc_reencode(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                scheme, flags, err, mode, seed, step, codes_out, scale_out, offset_out, out=None,
+                stream=None):
+    """Receiver re-encode: decode and accumulate M payloads (sum, or mean with
+    QC_OUT_MEAN), then encode the result with the residual ``err`` (fp32,
+    in/out, or None) in the same scheme, bits and bucket.  ``out`` (optional)
+    receives the decoded result itself."""
+    _check(lib.qc_reencode(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
+                           meta_stride, M, n, bits, bucket, scheme, flags, _ptr(err), mode, seed,
+                           step, _ptr(codes_out), _ptr(scale_out), _ptr(offset_out), _ptr(out),
+                           _stream(stream)))
 
 
 def qc_sign_vote(signs, stride_words, M, n, out, stream=None):

@@ -147,6 +147,66 @@ bool decode_tiles_for(const qc::DecodeParams &p, int bits, qc::DecodeTiles &t) {
     return true;
 }
 
+// Tiling for the fused re-encode: tiles of whole buckets whose element count is
+// a multiple of 128, 4096 elements where the bucket allows (one bucket when
+// buckets are larger), so that both phases keep every consumer thread busy (16
+// outputs per thread in the decode, a full set of teams in the encode); as many
+// workers per stage as fit in about 26 KB of codes and metadata, the rest in
+// further chunks, three stages.  Buckets above 8192 elements and payloads
+// without 16-byte aligned worker slices are not supported.
+bool reencode_tiles_for(const qc::ReencodeParams &p, int bits, qc::ReencodeTiles &t) {
+    if (!aligned(p.codes, 16) || p.codes_stride % 4 != 0) return false;
+    const uint64_t B = p.bucket;
+    const uint64_t unit = B / gcd_u64(B, 128) * 128;
+    if (unit > 8192) return false;
+    const uint64_t budget = 26 * 1024;
+    const uint64_t M = static_cast<uint64_t>(p.M);
+    const uint64_t te = unit > 4096 ? unit : 4096 / unit * unit;
+    const uint64_t worker_bytes = te * bits / 8;
+    const uint64_t tb = te / B;
+    const uint64_t per_worker = worker_bytes + 8 * tb;
+    uint64_t mc = budget / per_worker;
+    if (mc < 1) mc = 1;
+    if (mc > M) mc = M;
+    const uint64_t nchunks = (M + mc - 1) / mc;
+    mc = (M + nchunks - 1) / nchunks;
+    const uint64_t stage = (mc * per_worker + 127) / 128 * 128;
+    t.tb = static_cast<uint32_t>(tb);
+    t.te = static_cast<uint32_t>(te);
+    t.mc = static_cast<uint32_t>(mc);
+    t.nchunks = static_cast<uint32_t>(nchunks);
+    t.worker_bytes = static_cast<uint32_t>(worker_bytes);
+    t.meta_offset = static_cast<uint32_t>(mc * worker_bytes);
+    t.stage_bytes = static_cast<uint32_t>(stage);
+    t.stages = stage <= 28 * 1024 ? 3u : 2u;
+    int sh = -1;
+    if ((B & (B - 1)) == 0) {
+        sh = 0;
+        while ((1ull << sh) < B) ++sh;
+    }
+    t.bucket_shift = sh;
+    t.ntiles = (p.n + te - 1) / te;
+    return true;
+}
+
+// Bits and rounding mode allowed for a scheme; QC_OK or the failure status.
+qc_status check_scheme(const char *fn, qc_scheme scheme, int bits) {
+    if (scheme == QC_SCHEME_UNIFORM) {
+        if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "%s: uniform bits must be 1, 2, 4 or 8 (got %d)", fn, bits);
+    } else if (scheme == QC_SCHEME_SIGN) {
+        if (bits != 1) return fail(QC_ERR_INVALID_ARG, "%s: sign scheme needs bits == 1 (got %d)", fn, bits);
+    } else if (scheme == QC_SCHEME_TERNARY) {
+        if (bits != 2) return fail(QC_ERR_INVALID_ARG, "%s: ternary scheme needs bits == 2 (got %d)", fn, bits);
+    } else if (scheme == QC_SCHEME_QSGD) {
+        if (bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "%s: QSGD bits must be 2, 4 or 8 (got %d)", fn, bits);
+    } else {
+        return fail(QC_ERR_INVALID_ARG, "%s: unknown scheme %d", fn, scheme);
+    }
+    return QC_OK;
+}
+
 }  // namespace
 
 namespace qc {
@@ -229,7 +289,8 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = 0;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors() | qc::take_encode_bf16_errors() | qc::take_decode_errors();
+    *flags = qc::take_encode_errors() | qc::take_encode_bf16_errors() | qc::take_decode_errors() |
+             qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }
 
@@ -374,6 +435,87 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
                          "qc_decode_accumulate");
     return from_cuda(qc::launch_decode(p, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),
                      "qc_decode_accumulate");
+}
+
+qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const float *scale,
+                      const float *offset, size_t meta_stride, int M, size_t n, int bits,
+                      size_t bucket, qc_scheme scheme, int flags, float *err, qc_round mode,
+                      uint64_t seed, uint32_t step, uint32_t *codes_out, float *scale_out,
+                      float *offset_out, float *out, qc_stream_t stream) {
+    static const char *fn = "qc_reencode";
+    const qc_status sc = check_scheme(fn, scheme, bits);
+    if (sc != QC_OK) return sc;
+    if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
+        return fail(QC_ERR_INVALID_ARG, "%s: unknown rounding mode %d", fn, mode);
+    if (scheme == QC_SCHEME_SIGN && mode != QC_ROUND_NEAREST)
+        return fail(QC_ERR_INVALID_ARG, "%s: sign scheme is deterministic; mode must be NEAREST", fn);
+    if (M < 1 || M > QC_MAX_WORKERS)
+        return fail(QC_ERR_INVALID_ARG, "%s: M must be in [1, %d] (got %d)", fn, QC_MAX_WORKERS, M);
+    if (flags & ~QC_OUT_MEAN)
+        return fail(QC_ERR_INVALID_ARG, "%s: flags may hold only QC_OUT_MEAN (got 0x%x)", fn, flags);
+    if (!valid_bucket(bucket))
+        return fail(QC_ERR_INVALID_ARG, "%s: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", fn, bucket);
+    if (n == 0) return ok();
+    if (n > (static_cast<size_t>(1) << 40))
+        return fail(QC_ERR_UNSUPPORTED, "%s: n = %zu exceeds 2^40 elements", fn, n);
+    const size_t words = qc_code_words(n, bits), nb = qc_num_buckets(n, bucket);
+    if (M > 1 && (codes_stride_words < words || meta_stride < nb))
+        return fail(QC_ERR_INVALID_ARG, "%s: strides (%zu words, %zu buckets) are shorter than one payload (%zu, %zu)",
+                    fn, codes_stride_words, meta_stride, words, nb);
+    if (!codes || !scale || !codes_out || !scale_out)
+        return fail(QC_ERR_NULL, "%s: codes, scale, codes_out and scale_out must be non-NULL", fn);
+    const bool uni = scheme == QC_SCHEME_UNIFORM;
+    if (uni && (!offset || !offset_out))
+        return fail(QC_ERR_NULL, "%s: the uniform scheme needs offset and offset_out", fn);
+    if ((err && !aligned(err, 16)) || (out && !aligned(out, 16)))
+        return fail(QC_ERR_ALIGNMENT, "%s: err and out must be 16-byte aligned", fn);
+    if (!aligned(codes, 4) || !aligned(scale, 4) || (offset && !aligned(offset, 4)) ||
+        !aligned(codes_out, 4) || !aligned(scale_out, 4) || (offset_out && !aligned(offset_out, 4)))
+        return fail(QC_ERR_ALIGNMENT, "%s: code words and metadata must be 4-byte aligned", fn);
+    const size_t span_c = ((M - 1) * (M > 1 ? codes_stride_words : 0) + words) * 4;
+    const size_t span_m = ((M - 1) * (M > 1 ? meta_stride : 0) + nb) * 4;
+    const void *ins[3] = {codes, scale, uni ? offset : nullptr};
+    const size_t isz[3] = {span_c, span_m, span_m};
+    const void *outs[5] = {codes_out, scale_out, uni ? offset_out : nullptr, err, out};
+    const size_t osz[5] = {words * 4, nb * 4, nb * 4, n * 4, n * 4};
+    for (int a = 0; a < 5; ++a) {
+        for (int b = 0; b < 3; ++b)
+            if (overlaps(outs[a], osz[a], ins[b], isz[b]))
+                return fail(QC_ERR_INVALID_ARG, "%s: an output overlaps an input payload", fn);
+        for (int b = a + 1; b < 5; ++b)
+            if (overlaps(outs[a], osz[a], outs[b], osz[b]))
+                return fail(QC_ERR_INVALID_ARG, "%s: outputs overlap each other", fn);
+    }
+
+    qc::ReencodeParams p{};
+    p.codes = codes;
+    p.codes_stride = M > 1 ? codes_stride_words : 0;
+    p.scale = scale;
+    p.offset = offset;
+    p.meta_stride = M > 1 ? meta_stride : 0;
+    p.M = M;
+    p.n = n;
+    p.bucket = static_cast<uint32_t>(bucket);
+    p.nbuckets = nb;
+    p.flags = flags;
+    p.inv_m = (M & (M - 1)) == 0 ? 1.0f / static_cast<float>(M) : 0.0f;
+    p.out = out;
+    p.err = err;
+    p.step = step;
+    p.team_warps = team_warps_for(bucket);
+    p.keys = qc::philox_round_keys(seed);
+    p.codes_out = codes_out;
+    p.scale_out = scale_out;
+    p.offset_out = offset_out;
+    qc::ReencodeTiles tiles{};
+    if (!reencode_tiles_for(p, bits, tiles))
+        return fail(QC_ERR_UNSUPPORTED,
+                    "%s: needs 16-byte aligned codes, a worker stride that is a multiple of 4 words "
+                    "and a bucket whose tile (a multiple of 128 elements) is at most 8192; "
+                    "qc_decode_accumulate followed by qc_encode_ef computes the same result", fn);
+    return from_cuda(qc::launch_reencode(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
 }
 
 qc_status qc_sign_vote(const uint32_t *signs, size_t stride_words, int M, size_t n,

@@ -26,30 +26,6 @@ namespace {
 
 constexpr int kDecodeBlock = kProducerBlock;
 
-// The 4*BITS-bit field of the four codes of tile element e (e % 4 == 0) of one
-// worker: from the stage when staged, else from global memory (tile tail).
-template <int BITS>
-__device__ __forceinline__ uint32_t field4(const unsigned char *wstage, const uint32_t *wglob,
-                                           uint32_t e, uint32_t staged_bytes) {
-    const uint32_t byte = (e * BITS) / 8u;
-    if constexpr (BITS == 8) {
-        return byte + 4u <= staged_bytes ? *reinterpret_cast<const uint32_t *>(wstage + byte)
-                                         : __ldcs(wglob + e / 4u);
-    } else if constexpr (BITS == 4) {
-        return byte + 2u <= staged_bytes
-                   ? *reinterpret_cast<const unsigned short *>(wstage + byte)
-                   : __ldcs(reinterpret_cast<const unsigned short *>(wglob) + e / 4u);
-    } else if constexpr (BITS == 2) {
-        return byte < staged_bytes ? wstage[byte]
-                                   : __ldcs(reinterpret_cast<const unsigned char *>(wglob) + e / 4u);
-    } else {
-        const uint32_t b = byte < staged_bytes
-                               ? wstage[byte]
-                               : __ldcs(reinterpret_cast<const unsigned char *>(wglob) + e / 8u);
-        return (b >> ((e & 4u) ? 4u : 0u)) & 0xFu;
-    }
-}
-
 template <int SCHEME, int BITS>
 __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __grid_constant__ DecodeParams P,
                                                                   const __grid_constant__ DecodeTiles G) {

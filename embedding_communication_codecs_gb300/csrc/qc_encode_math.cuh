@@ -475,14 +475,19 @@ __device__ __forceinline__ void store_meta(float *scale, float *offset, uint64_t
 }
 
 // Team-wide reduction of the statistics: warp butterflies, then (W > 1) one
-// exchange through shared memory.  Every thread of the block must call it.
-template <int SCHEME>
+// exchange through shared memory.  Every thread of the block (with kNamed, every
+// thread of the kBlock consumer threads on named barrier 1) must call it.
+template <int SCHEME, bool kNamed = false>
 __device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
                                             int &buf, int W, int warp, int lane, int team) {
     st.warp_reduce();
     if (W > 1) {
         if (lane == 0) red[buf][warp] = st;
-        __syncthreads();
+        if constexpr (kNamed) {
+            asm volatile("bar.sync 1, %0;" ::"n"(kBlock) : "memory");
+        } else {
+            __syncthreads();
+        }
         st = red[buf][team * W];
         for (int w = 1; w < W; ++w) st.merge(red[buf][team * W + w]);
         buf ^= 1;

@@ -114,6 +114,53 @@ struct VoteParams {
     uint32_t *out;
 };
 
+// Receiver re-encode: the decode of M payloads (DecodeParams' fields) feeding an
+// encode of the result with its own residual buffer, same scheme, bits and bucket.
+struct ReencodeParams {
+    const uint32_t *codes;
+    uint64_t codes_stride;  // words
+    const float *scale;
+    const float *offset;
+    uint64_t meta_stride;   // floats
+    int M;
+    uint64_t n;
+    uint32_t bucket;
+    uint64_t nbuckets;
+    int flags;
+    float inv_m;
+    float *out;             // the decoded result r, or null
+    float *err;             // the receiver's residual (in/out), or null
+    uint32_t step;
+    int team_warps;
+    PhiloxKeys keys;
+    uint32_t *codes_out;
+    float *scale_out;
+    float *offset_out;
+};
+
+// Tiling of the re-encode: TB whole buckets (TE elements) per tile, the M
+// workers in chunks of MC per stage (nchunks stages per tile).  A stage holds MC
+// slices of worker_bytes code bytes, then MC x TB (scale, offset) pairs at
+// meta_offset.  Two TE-element fp32 buffers hold the running sums.
+struct ReencodeTiles {
+    uint32_t tb;
+    uint32_t te;
+    uint32_t mc;
+    uint32_t nchunks;
+    uint32_t stages;
+    uint32_t stage_bytes;
+    uint32_t worker_bytes;
+    uint32_t meta_offset;
+    int bucket_shift;
+    uint64_t ntiles;
+};
+
+// Stages, the two sum buffers, the full and empty barriers, the team-reduction buffer.
+inline size_t reencode_tiles_smem(const ReencodeTiles &g, size_t stats_bytes) {
+    return static_cast<size_t>(g.stages) * g.stage_bytes + 2u * 4u * g.te + 16u * g.stages +
+           2u * 8u * stats_bytes;
+}
+
 struct Fp8Params {
     const float *x;
     const uint8_t *codes_in;
@@ -137,6 +184,8 @@ cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int 
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
 cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int scheme, int bits,
                               cudaStream_t stream);
+cudaError_t launch_reencode(const ReencodeParams &p, const ReencodeTiles &g, int scheme, int bits,
+                            int stochastic, cudaStream_t stream);
 cudaError_t launch_vote(const VoteParams &p, bool vectorised, cudaStream_t stream);
 cudaError_t launch_fp8_quant(const Fp8Params &p, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const Fp8Params &p, cudaStream_t stream);
@@ -152,5 +201,6 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 uint32_t take_encode_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();
+uint32_t take_reencode_errors();
 
 }  // namespace qc

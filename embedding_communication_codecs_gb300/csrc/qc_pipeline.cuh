@@ -19,6 +19,28 @@
 namespace qc {
 
 constexpr uint32_t kWaitRounds = 1u << 22;
+
+// Named barrier 1 over the first `threads` threads of the block (the consumer
+// warps of a warp-specialised block; the producer warp never takes part).
+template <int THREADS>
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+}
+
+// The same barrier, returning whether `v` holds on every participating thread.
+template <int THREADS>
+__device__ __forceinline__ bool consumer_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(THREADS)
+        : "memory");
+    return r != 0u;
+}
 constexpr uint32_t kErrPipelineTimeout = 1u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

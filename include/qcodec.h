@@ -176,6 +176,41 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
                                float *out, int flags, qc_stream_t stream);
 
 /*
+ * qc_reencode -- receiver re-encode: the far side of a two-phase quantized
+ * all-reduce.  The owner of a shard decodes the M workers' payloads of that
+ * shard, accumulates them, and quantizes the result again, with its own
+ * error-feedback residual, for the all-gather phase ("Quantization for
+ * Communication", "Quantization-Aware All-Reduce": dequantize after the
+ * exchange, accumulate in higher precision; "Gradient Compression and
+ * Quantised Collectives": reduce-scatter then all-gather).  Per element:
+ *   r_i = qc_decode_accumulate's result with `flags` (QC_OUT_SUM or QC_OUT_MEAN;
+ *         QC_ACCUMULATE_INTO_OUT is not accepted)
+ *   then qc_encode_ef of r (as an F32 gradient) with residual `err`, the SAME
+ *   scheme, bits and bucket as the incoming payloads, `mode`, `seed`, `step`:
+ *   p_i = err ? fl(err_i + r_i) : r_i, the scheme's statistics, codes and,
+ *   with err, err_i = fl(p_i - deq_i).
+ * The result equals qc_decode_accumulate into a buffer followed by qc_encode_ef
+ * of that buffer, bit for bit; one kernel does both without the fp32 round trip.
+ *
+ * codes, scale, offset, meta_stride, codes_stride_words, M, bits, bucket,
+ * scheme : as for qc_decode_accumulate.  `codes` must be 16-byte aligned and,
+ *          for M > 1, codes_stride_words a multiple of 4, and the bucket at
+ *          most 8192 elements; otherwise QC_ERR_UNSUPPORTED (the two-call
+ *          composition above serves those layouts).
+ * err    : n fp32 residual of this receiver, in/out, 16-byte aligned, or NULL.
+ * mode, seed, step : as for qc_encode_ef (SIGN needs NEAREST).
+ * codes_out, scale_out, offset_out : the new payload, laid out as
+ *          qc_encode_ef's outputs (offset_out UNIFORM only, else may be NULL).
+ * out    : n fp32, 16-byte aligned, receives r; or NULL to skip it.
+ * No output may overlap an input or another output.
+ */
+qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const float *scale,
+                      const float *offset, size_t meta_stride, int M, size_t n, int bits,
+                      size_t bucket, qc_scheme scheme, int flags, float *err, qc_round mode,
+                      uint64_t seed, uint32_t step, uint32_t *codes_out, float *scale_out,
+                      float *offset_out, float *out, qc_stream_t stream);
+
+/*
  * qc_sign_vote -- signSGD aggregation by majority vote ("Quantization for
  * Communication", "Quantized SGD Algorithms"; "Gradient Compression and
  * Quantised Collectives", "Why sparsification fights the all-reduce").

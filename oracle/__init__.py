@@ -199,6 +199,28 @@ def decode_accumulate(codes, scale, offset, *, M, n, bits, bucket, scheme, flags
     return out
 
 
+def reencode(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM, err=None,
+             mode=ROUND_NEAREST, seed=0, step=0, codes_stride_words=None, meta_stride=None):
+    """Receiver re-encode ("Quantization-Aware All-Reduce": dequantize after the
+    exchange, accumulate, quantize again for the all-gather): the decode of M
+    payloads followed by the encode of the result, with the residual ``err``
+    (updated in place), in the same scheme, bits and bucket.  Returns
+    (r, codes, scale, offset-or-None)."""
+    r = decode_accumulate(codes, scale, offset, M=M, n=n, bits=bits, bucket=bucket,
+                          scheme=scheme, flags=flags, codes_stride_words=codes_stride_words,
+                          meta_stride=meta_stride)
+    if scheme == SCHEME_UNIFORM:
+        c, s, o = encode_uniform(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed, step=step)
+        return r, c, s, o
+    if scheme == SCHEME_SIGN:
+        c, s = encode_sign(r, err, bucket=bucket)
+    elif scheme == SCHEME_TERNARY:
+        c, s = encode_ternary(r, err, bucket=bucket, mode=mode, seed=seed, step=step)
+    else:
+        c, s = encode_qsgd(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed, step=step)
+    return r, c, s, None
+
+
 def sign_vote(signs, *, M, n, stride_words=None):
     s = np.ascontiguousarray(signs, dtype=np.uint32)
     if stride_words is None:

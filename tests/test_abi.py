@@ -139,3 +139,43 @@ def test_vote_and_fp8_reject(q):
     assert L.qc_rowwise_fp8(A, 0, 128, None, None, 0) == q.QC_OK
     assert L.qc_rowwise_fp8_dequant(C, D, 10, 128, A + 4, 0) == q.QC_ERR_ALIGNMENT
     assert L.qc_rowwise_fp8_dequant(C, D, 10, 128, C, 0) == q.QC_ERR_INVALID_ARG
+
+
+def test_qsgd_bits_rejected(q):
+    for bits in (1, 3, 16):
+        assert _enc(q, scheme=q.QC_SCHEME_QSGD, bits=bits) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scheme=q.QC_SCHEME_QSGD, bits=4, offset=None, n=0) == q.QC_OK
+
+
+def test_reencode_rejects(q):
+    E = 0x50000000
+    F = 0x60000000
+
+    def re_(**kw):
+        a = dict(codes=C, cs=1024, scale=D, offset=D + 0x100000, ms=2, M=2, n=4096, bits=8,
+                 bucket=2048, scheme=q.QC_SCHEME_UNIFORM, flags=q.QC_OUT_MEAN, err=B,
+                 mode=q.QC_ROUND_NEAREST, codes_out=E, scale_out=F, offset_out=F + 0x1000,
+                 out=A)
+        a.update(kw)
+        return q.lib.qc_reencode(a["codes"], a["cs"], a["scale"], a["offset"], a["ms"], a["M"],
+                                 a["n"], a["bits"], a["bucket"], a["scheme"], a["flags"],
+                                 a["err"], a["mode"], 0, 0, a["codes_out"], a["scale_out"],
+                                 a["offset_out"], a["out"], 0)
+    assert re_(M=0) == q.QC_ERR_INVALID_ARG
+    assert re_(flags=q.QC_ACCUMULATE_INTO_OUT) == q.QC_ERR_INVALID_ARG
+    assert re_(bits=3) == q.QC_ERR_INVALID_ARG
+    assert re_(scheme=q.QC_SCHEME_SIGN, bits=1, mode=q.QC_ROUND_STOCHASTIC) == q.QC_ERR_INVALID_ARG
+    assert re_(mode=4) == q.QC_ERR_INVALID_ARG
+    assert re_(cs=1023) == q.QC_ERR_INVALID_ARG
+    assert re_(codes_out=None) == q.QC_ERR_NULL
+    assert re_(offset_out=None) == q.QC_ERR_NULL
+    assert re_(err=B + 4) == q.QC_ERR_ALIGNMENT
+    assert re_(out=A + 8) == q.QC_ERR_ALIGNMENT
+    assert re_(codes_out=C + 64) == q.QC_ERR_INVALID_ARG     # output over the input payload
+    assert re_(out=B) == q.QC_ERR_INVALID_ARG                # output over another output
+    # layouts the fused kernel does not take
+    assert re_(cs=1026) == q.QC_ERR_UNSUPPORTED
+    assert re_(codes=C + 4) == q.QC_ERR_UNSUPPORTED
+    assert re_(bucket=16384, n=1 << 15, cs=1 << 13, ms=2) == q.QC_ERR_UNSUPPORTED
+    assert b"qc_decode_accumulate followed by qc_encode_ef" in q.lib.qc_last_error()
+    assert re_(n=0, codes=None, codes_out=None) == q.QC_OK

@@ -655,3 +655,93 @@ def test_qsgd_decode_closed_form():
     want = [sum((-1 if q[w, i] >> 3 else 1) * (q[w, i] & 7) * float(unit[w, i // bucket])
                 for w in range(2)) for i in range(n)]
     assert out.tolist() == want
+
+
+# ------------------------------------------------------------- re-encode
+
+def _payloads(scheme, bits, M, n, bucket, seed):
+    """M workers' payloads from the oracle's own encoder on seeded gradients."""
+    cs, ss, os_ = [], [], []
+    for w in range(M):
+        g = wl.std_normal(seed + w, 1, n) * np.float32(1e-2)
+        if scheme == orc.SCHEME_UNIFORM:
+            c, s, o = orc.encode_uniform(g, bits=bits, bucket=bucket)
+            os_.append(o)
+        elif scheme == orc.SCHEME_SIGN:
+            c, s = orc.encode_sign(g, bucket=bucket)
+        elif scheme == orc.SCHEME_TERNARY:
+            c, s = orc.encode_ternary(g, bucket=bucket, mode=orc.ROUND_NEAREST)
+        else:
+            c, s = orc.encode_qsgd(g, bits=bits, bucket=bucket, mode=orc.ROUND_NEAREST)
+        cs.append(c)
+        ss.append(s)
+    return np.stack(cs), np.stack(ss), (np.stack(os_) if os_ else None)
+
+
+def _unpack_codes(words, n, bits):
+    per = 32 // bits
+    sh = (np.arange(per, dtype=np.uint32) * bits).astype(np.uint32)
+    return ((words[..., :, None] >> sh) & np.uint32((1 << bits) - 1)).reshape(*words.shape[:-1], -1)[..., :n]
+
+
+def test_reencode_mean_and_quantizer_bound():
+    """The decoded mean agrees with an fp64 evaluation of the dequantized
+    payloads (so the sum runs over all M workers and divides by M once), and the
+    re-encoded payload decodes to within half a step of err + r (round to
+    nearest on the new bucket grid), with err' = (err + r) - deq' exactly."""
+    M, n, bits, bucket = 5, 3000 + 17, 8, 512
+    c, s, o = _payloads(orc.SCHEME_UNIFORM, bits, M, n, bucket, 40)
+    q = _unpack_codes(c, n, bits).astype(np.float64)
+    k = np.arange(n) // bucket
+    d64 = q * s[:, k].astype(np.float64) + o[:, k].astype(np.float64)
+    mean64 = d64.sum(axis=0) / M
+    err0 = (wl.std_normal(9, 1, n) * np.float32(1e-5)).astype(np.float32)
+    err = err0.copy()
+    r, c2, s2, o2 = orc.reencode(c, s, o, M=M, n=n, bits=bits, bucket=bucket,
+                                 scheme=orc.SCHEME_UNIFORM, flags=orc.OUT_MEAN, err=err)
+    assert np.all(np.abs(r - mean64) <= 8 * np.finfo(np.float32).eps * np.abs(d64).sum(axis=0) / M + 1e-30)
+    p = (err0 + r).astype(np.float32)
+    q2 = _unpack_codes(c2, n, bits).astype(np.float64)
+    deq2 = q2 * s2[k] + o2[k]
+    assert np.all(np.abs(deq2 - p) <= 0.5 * s2[k] * (1 + 1e-5) + 1e-12)
+    assert np.array_equal(err, (p - orc.decode_accumulate(c2, s2, o2, M=1, n=n, bits=bits,
+                                                          bucket=bucket, scheme=orc.SCHEME_UNIFORM))
+                          .astype(np.float32))
+
+
+@pytest.mark.parametrize("scheme,bits", [(orc.SCHEME_UNIFORM, 8), (orc.SCHEME_UNIFORM, 2),
+                                         (orc.SCHEME_SIGN, 1), (orc.SCHEME_TERNARY, 2)])
+@pytest.mark.parametrize("mode", [orc.ROUND_NEAREST, orc.ROUND_STOCHASTIC])
+def test_reencode_of_identical_payloads_is_idempotent(scheme, bits, mode):
+    """Two identical payloads averaged give back each dequantized value exactly
+    (x + x and the halving are exact), and those values already sit on the
+    quantizer's grid: re-encoding them returns the payload's own codes.  For the
+    uniform scheme every bucket holds code 0 and code L so that its min and max
+    are the grid's ends; stochastic rounding of a value on the grid has nothing
+    to round."""
+    if scheme == orc.SCHEME_SIGN and mode == orc.ROUND_STOCHASTIC:
+        pytest.skip("the sign scheme is deterministic")
+    n, bucket = 4096 + 64, 512
+    c, s, o = _payloads(scheme, bits, 1, n, bucket, 77)
+    if scheme == orc.SCHEME_UNIFORM:
+        codes = _unpack_codes(c[0], n, bits)
+        L = (1 << bits) - 1
+        codes[0::bucket] = 0
+        codes[1::bucket] = L
+        per = 32 // bits
+        padded = np.zeros(-(-n // per) * per, dtype=np.uint32)
+        padded[:n] = codes
+        words = np.zeros(padded.size // per, dtype=np.uint32)
+        for j in range(per):
+            words |= padded[j::per] << np.uint32(j * bits)
+        c = words[None, :]
+    c2 = np.concatenate([c, c])
+    s2 = np.concatenate([s, s])
+    o2 = None if o is None else np.concatenate([o, o])
+    r, cr, sr, orr = orc.reencode(c2, s2, o2, M=2, n=n, bits=bits, bucket=bucket, scheme=scheme,
+                                  flags=orc.OUT_MEAN, mode=mode, seed=5, step=1)
+    d1 = orc.decode_accumulate(c, s, o, M=1, n=n, bits=bits, bucket=bucket, scheme=scheme)
+    assert np.array_equal(r.view(np.uint32), d1.view(np.uint32))
+    assert np.array_equal(cr, c[0])
+    if scheme == orc.SCHEME_TERNARY or scheme == orc.SCHEME_SIGN:
+        assert np.array_equal(sr, s[0])
