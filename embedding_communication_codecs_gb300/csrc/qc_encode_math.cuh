@@ -374,14 +374,16 @@ __device__ __forceinline__ float deq_of(uint32_t field, int c, const BucketParam
 
 // ------------------------------------------------------------- slot level
 
-// Adds the valid elements of the lane's slots to the statistics.
-template <int SCHEME>
+// Adds the valid elements of the lane's slots to the statistics.  FULL: the
+// caller guarantees cnt == team_threads * kSlots * 4 (every slot valid), which
+// removes the per-slot bounds checks.
+template <int SCHEME, bool FULL = false>
 __device__ __forceinline__ void accumulate_slots(Stats<SCHEME> &st, const float4 (&p)[kSlots],
                                                  int tt, int team_threads, uint32_t cnt) {
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
         const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
-        if (j + 4u <= cnt) {
+        if (FULL || j + 4u <= cnt) {
             st.add(p[s].x);
             st.add(p[s].y);
             st.add(p[s].z);
@@ -396,8 +398,9 @@ __device__ __forceinline__ void accumulate_slots(Stats<SCHEME> &st, const float4
 
 // Quantizes the lane's slots of bucket [b0, b0 + cnt), packs and stores the code
 // words, and (with error feedback) stores the new residual.  All 32 lanes of the
-// warp must call this together (the packing uses shuffles).
-template <int SCHEME, int BITS, bool SR, bool EF>
+// warp must call this together (the packing uses shuffles).  FULL as for
+// accumulate_slots.
+template <int SCHEME, int BITS, bool SR, bool EF, bool FULL = false>
 __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err, uint64_t b0,
                                                      uint32_t cnt, int tt, int team_threads,
                                                      int lane, const float4 (&p)[kSlots],
@@ -410,11 +413,11 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
         const uint64_t i = b0 + j;
         float u[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (SR) {
-            if (j < cnt) uniform4(i, step, keys, u);
+            if (FULL || j < cnt) uniform4(i, step, keys, u);
         }
         uint32_t field = 0;
         float4 e;
-        if (j + 4u <= cnt && fq.usable) {
+        if ((FULL || j + 4u <= cnt) && fq.usable) {
             float d[4];
             bool redo[4];
             uint32_t q[4];
@@ -429,7 +432,7 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
             field = q[0] | (q[1] << BITS) | (q[2] << (2 * BITS)) | (q[3] << (3 * BITS));
             e = make_float4(__fsub_rn(p[s].x, d[0]), __fsub_rn(p[s].y, d[1]),
                             __fsub_rn(p[s].z, d[2]), __fsub_rn(p[s].w, d[3]));
-        } else if (j + 4u <= cnt) {
+        } else if (FULL || j + 4u <= cnt) {
             float d0, d1, d2, d3;
             field = quantize<SCHEME, BITS, SR>(p[s].x, u[0], bp, d0) |
                     (quantize<SCHEME, BITS, SR>(p[s].y, u[1], bp, d1) << BITS) |
@@ -450,9 +453,9 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
             }
         }
         const uint32_t word = gather_word<BITS>(field);
-        if (j < cnt && stores_word<BITS>(lane)) __stcs(codes + (i * BITS) / 32u, word);
+        if ((FULL || j < cnt) && stores_word<BITS>(lane)) __stcs(codes + (i * BITS) / 32u, word);
         if constexpr (EF) {
-            if (j + 4u <= cnt) {
+            if (FULL || j + 4u <= cnt) {
                 __stcs(reinterpret_cast<float4 *>(err + i), e);
             } else if (j < cnt) {
 #pragma unroll

@@ -60,8 +60,9 @@ __device__ __forceinline__ float smem_grad1(const unsigned char *stage, uint32_t
     }
 }
 
-// p = e + g for the lane's slots of the bucket at tile offset b_off.
-template <typename TIn, bool EF>
+// p = e + g for the lane's slots of the bucket at tile offset b_off.  FULL: every
+// slot is valid and staged.
+template <typename TIn, bool EF, bool FULL = false>
 __device__ __forceinline__ void load_slots_staged(const EncodeParams &P, const EncodeTiles &G,
                                                   const unsigned char *stage, uint64_t t0,
                                                   uint32_t b_off, uint32_t cnt, uint32_t staged,
@@ -73,7 +74,7 @@ __device__ __forceinline__ void load_slots_staged(const EncodeParams &P, const E
         const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
         const uint32_t e = b_off + j;
         float4 gv = make_float4(0.f, 0.f, 0.f, 0.f), ev = gv;
-        if (j + 4u <= cnt && e + 4u <= staged) {
+        if (FULL || (j + 4u <= cnt && e + 4u <= staged)) {
             gv = smem_grad4<TIn>(stage, e);
             if constexpr (EF) ev = *reinterpret_cast<const float4 *>(stage + G.e_offset + e * 4u);
         } else if (j < cnt) {
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
     const int team = warp / W;
     const int tt = (warp % W) * 32 + lane;
     const int team_threads = W * 32;
+    const uint32_t window = static_cast<uint32_t>(team_threads) * kSlots * 4u;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < G.stages; ++s) mbar_init(&full[s], 1);
@@ -145,15 +147,29 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
             const uint32_t kb = kb0 + team;
             const uint32_t b_off = kb * P.bucket;
             const uint32_t cnt = (kb < G.tb && b_off < tcnt) ? min(P.bucket, tcnt - b_off) : 0u;
+            // a bucket that fills the team's window and is wholly staged takes
+            // the path without per-slot bounds checks (uniform across the team)
+            const bool whole = cnt == window && b_off + cnt <= staged;
             float4 p[kSlots];
-            load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
             Stats<SCHEME> st;
             st.init();
-            accumulate_slots<SCHEME>(st, p, tt, team_threads, cnt);
+            if (whole) {
+                load_slots_staged<TIn, EF, true>(P, G, stage, t0, b_off, cnt, staged, tt,
+                                                 team_threads, p);
+                accumulate_slots<SCHEME, true>(st, p, tt, team_threads, cnt);
+            } else {
+                load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+                accumulate_slots<SCHEME>(st, p, tt, team_threads, cnt);
+            }
             team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
             const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
-            quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, t0 + b_off, cnt, tt,
-                                                       team_threads, lane, p, bp, P.step, keys);
+            if (whole)
+                quantize_store_slots<SCHEME, BITS, SR, EF, true>(P.codes, P.err, t0 + b_off, cnt, tt,
+                                                                 team_threads, lane, p, bp, P.step,
+                                                                 keys);
+            else
+                quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, t0 + b_off, cnt, tt,
+                                                           team_threads, lane, p, bp, P.step, keys);
             if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);
         }
         // Every thread is done with this stage (and agrees the wait succeeded)

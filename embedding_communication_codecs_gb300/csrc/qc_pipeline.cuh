@@ -80,6 +80,13 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned),
+// cached in L2 only; completion by cp_async_wait_all() of the issuing thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed (the
 // arrival is one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {

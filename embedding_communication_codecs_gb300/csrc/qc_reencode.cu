@@ -40,13 +40,14 @@ __device__ __forceinline__ float finish_r(float a, const ReencodeParams &P, floa
 }
 
 // The lane's slots of the bucket window [w0, w0 + cnt) at tile offset b_off,
-// read from the sum buffer (zeros past cnt).
+// read from the sum buffer (zeros past cnt).  FULL: every slot is valid.
+template <bool FULL = false>
 __device__ __forceinline__ void load_slots_sum(const float *pb, uint32_t b_off, uint32_t cnt,
                                                int tt, int team_threads, float4 (&p)[kSlots]) {
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
         const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
-        if (j + 4u <= cnt) {
+        if (FULL || j + 4u <= cnt) {
             p[s] = *reinterpret_cast<const float4 *>(pb + b_off + j);
         } else {
             p[s] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -147,6 +148,61 @@ __global__ void __launch_bounds__(kReBlock, 2) reencode_kernel(const __grid_cons
         bool ok = true;
 
         // ---- phase 1: decode and accumulate, chunk by chunk, into pb
+        if (G.te == 16u * kConsumers && tcnt == G.te) {
+            // One group of 16 consecutive outputs (all in one bucket) per
+            // thread: the sums stay in registers across the chunks and pb is
+            // written once.
+            const uint32_t e = static_cast<uint32_t>(ct) * 16u;
+            const uint32_t kb = G.bucket_shift >= 0 ? (e >> G.bucket_shift) : (e / P.bucket);
+            float a[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) a[k] = 0.0f;
+            float4 *ps = reinterpret_cast<float4 *>(pb + e);
+            for (uint32_t c = 0; c < G.nchunks; ++c, ++it) {
+                const uint32_t s = it % G.stages;
+                if constexpr (EF) {
+                    // the residual lands in this thread's own slots of pb (free
+                    // until the end of the phase) while the last chunk runs
+                    if (c + 1 == G.nchunks) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            cp_async16(ps + q4, reinterpret_cast<const float4 *>(P.err + t0 + e) + q4);
+                    }
+                }
+                if (ok) ok = mbar_wait(&full[s], (it / G.stages) & 1u);
+                if (ok) {
+                    const unsigned char *stage = smem + s * G.stage_bytes;
+                    const float2 *meta = reinterpret_cast<const float2 *>(stage + G.meta_offset) + kb;
+                    const int mc = static_cast<int>(min(G.mc, static_cast<uint32_t>(P.M) - c * G.mc));
+                    const unsigned char *wst = stage + (e * BITS) / 8u;
+#pragma unroll 4
+                    for (int w = 0; w < mc; ++w) {
+                        uint32_t f[4];
+                        load_codes16<BITS>(wst, f);
+                        const float2 m = meta[w * G.tb];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            a[k] = accumulate16<SCHEME, BITS>(a[k], f, k, m.x, m.y);
+                        wst += G.worker_bytes;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if constexpr (EF) cp_async_wait_all();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float4 v = make_float4(finish_r(a[4 * q4], P, Mf), finish_r(a[4 * q4 + 1], P, Mf),
+                                       finish_r(a[4 * q4 + 2], P, Mf), finish_r(a[4 * q4 + 3], P, Mf));
+                if (P.out) __stcs(reinterpret_cast<float4 *>(P.out + t0 + e) + q4, v);
+                if constexpr (EF) {
+                    const float4 ev = ps[q4];
+                    v = make_float4(__fadd_rn(ev.x, v.x), __fadd_rn(ev.y, v.y), __fadd_rn(ev.z, v.z),
+                                    __fadd_rn(ev.w, v.w));
+                }
+                ps[q4] = v;
+            }
+        } else
         for (uint32_t c = 0; c < G.nchunks; ++c, ++it) {
             const uint32_t s = it % G.stages;
             if (ok) ok = mbar_wait(&full[s], (it / G.stages) & 1u);
@@ -247,20 +303,34 @@ __global__ void __launch_bounds__(kReBlock, 2) reencode_kernel(const __grid_cons
             const uint32_t kb = kb0 + team;
             const uint32_t b_off = kb * P.bucket;
             const uint32_t cnt = (kb < G.tb && b_off < tcnt) ? min(P.bucket, tcnt - b_off) : 0u;
+            // a bucket exactly one team window long takes the path without
+            // per-slot bounds checks (uniform across the team)
+            const bool whole = cnt == window;
             float4 p[kSlots];
-            load_slots_sum(pb, b_off, min(cnt, window), tt, team_threads, p);
             Stats<SCHEME> st;
             st.init();
-            accumulate_slots<SCHEME>(st, p, tt, team_threads, min(cnt, window));
-            for (uint32_t w0 = window; w0 < cnt; w0 += window) {  // buckets above one window
-                float4 q[kSlots];
-                load_slots_sum(pb, b_off + w0, min(cnt - w0, window), tt, team_threads, q);
-                accumulate_slots<SCHEME>(st, q, tt, team_threads, min(cnt - w0, window));
+            if (whole) {
+                load_slots_sum<true>(pb, b_off, window, tt, team_threads, p);
+                accumulate_slots<SCHEME, true>(st, p, tt, team_threads, window);
+            } else {
+                load_slots_sum(pb, b_off, min(cnt, window), tt, team_threads, p);
+                accumulate_slots<SCHEME>(st, p, tt, team_threads, min(cnt, window));
+                for (uint32_t w0 = window; w0 < cnt; w0 += window) {  // buckets above one window
+                    float4 q[kSlots];
+                    load_slots_sum(pb, b_off + w0, min(cnt - w0, window), tt, team_threads, q);
+                    accumulate_slots<SCHEME>(st, q, tt, team_threads, min(cnt - w0, window));
+                }
             }
             team_reduce<SCHEME, true>(st, red, buf, W, warp, lane, team);
             const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
-            quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes_out, P.err, t0 + b_off, min(cnt, window),
-                                                       tt, team_threads, lane, p, bp, P.step, P.keys);
+            if (whole)
+                quantize_store_slots<SCHEME, BITS, SR, EF, true>(P.codes_out, P.err, t0 + b_off, window,
+                                                                 tt, team_threads, lane, p, bp, P.step,
+                                                                 P.keys);
+            else
+                quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes_out, P.err, t0 + b_off,
+                                                           min(cnt, window), tt, team_threads, lane,
+                                                           p, bp, P.step, P.keys);
             for (uint32_t w0 = window; w0 < cnt; w0 += window) {
                 load_slots_sum(pb, b_off + w0, min(cnt - w0, window), tt, team_threads, p);
                 quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes_out, P.err, t0 + b_off + w0,
