@@ -81,13 +81,16 @@ bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool gra
     return true;
 }
 
-// Tiling for the bf16 encode without error feedback: W = ceil(bucket / 1024)
-// warps per bucket (a power of two, at most 8), whole buckets per tile, about
-// 16 KB of bf16 per stage, three stages.
+// Tiling for the bf16 encode without error feedback: buckets of 1024, 2048,
+// 4096 or 8192 elements, W = bucket / 1024 warps per bucket, whole buckets per
+// tile, about 16 KB of bf16 per stage, three stages.
 bool bf16_tiles_for(const qc::EncodeParams &p, bool grad16, qc::EncodeTiles &t) {
     if (!grad16 || p.err != nullptr || p.bucket > 8192) return false;
     uint32_t w = 1;
     while (w < 8 && 1024u * w < p.bucket) w <<= 1;
+    // a team covers exactly one bucket (1024 elements per warp); other bucket
+    // sizes take the general pipelined kernel
+    if (p.bucket != 1024u * w) return false;
     const uint32_t teams = (qc::kBlock / 32) / w;
     uint32_t tb = static_cast<uint32_t>((16 * 1024) / (static_cast<size_t>(p.bucket) * 2));
     tb = tb / teams * teams;

@@ -36,6 +36,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys &k) {
     return c;
 }
 
+// The four raw Philox words of elements i0 .. i0+3 (i0 % 4 == 0): counter
+// (i0/4 low, i0/4 high, step, 0), key (seed low, seed high).
+__device__ __forceinline__ uint4 philox_words(uint64_t i0, uint32_t step, const PhiloxKeys &k) {
+    const uint64_t blk = i0 >> 2;
+    return philox4x32_10(
+        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), step, 0u), k);
+}
+
 // Four uniform draws u in [0, 1) for elements i0 .. i0+3 (i0 % 4 == 0):
 // counter (i0/4 low, i0/4 high, step, 0), key (seed low, seed high),
 // u = (word >> 8) * 2^-24, exact in binary32.

@@ -109,8 +109,38 @@ __device__ __forceinline__ void issue_tile(const EncodeParams &P, const EncodeTi
     if (gb) bulk_load(stage, static_cast<const uint16_t *>(P.grad) + t0, gb, bar);
 }
 
+// Stochastic ternary codes of the 8 elements of a slot, packed (element c in bits
+// 2c, 2c+1), without conversions or selects: most of the work moves from the
+// integer/logic pipe to the multiply-add pipe.
+//   pa1 = fl(|v| * (1/s) + 1)          one fma
+//   f   = 1 + (w >> 9) * 2^-23          the draw's top 23 bits as a mantissa
+//   d   = f - pa1                       exact (both in [1, 2])
+// d differs from u - fl(|v| / s) by less than 2^-22 (the reciprocal, the fma's
+// rounding, the dropped 24th bit of u), so keep = [d < 0] is the exact decision
+// whenever |d| > 2^-21; otherwise `near` is set and the caller recomputes the
+// slot exactly.  Code bits: b0 = !keep, b1 = keep & (v >= +0).
+__device__ __forceinline__ uint32_t ternary_sr_field8(const float (&v)[8], const uint4 &r0,
+                                                      const uint4 &r1, float rinv, float delta2,
+                                                      bool &near) {
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    uint32_t field = 0u, far = 0xFFFFFFFFu;
+#pragma unroll
+    for (int c = 7; c >= 0; --c) {
+        const float pa1 = __fmaf_rn(fabsf(v[c]), rinv, 1.0f);
+        const float f = __uint_as_float((w[c] >> 9) | 0x3F800000u);
+        const float d = __fsub_rn(f, pa1);
+        far &= __float_as_uint(__fsub_rn(delta2, fabsf(d)));  // sign set while |d| > delta2
+        const uint32_t D = __float_as_uint(d);
+        const uint32_t x = D & ~__float_as_uint(v[c]);
+        field = __funnelshift_l(x, field, 1);   // b1 = keep & !sign(v)
+        field = __funnelshift_l(D, field, 1);   // keep, inverted below
+    }
+    near = (far >> 31) == 0u;
+    return field ^ 0x5555u;
+}
+
 template <int SCHEME, int BITS, bool SR>
-__global__ void __launch_bounds__(kBlock, SR ? 3 : 4) encode_bf16_kernel(const __grid_constant__ EncodeParams P,
+__global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_constant__ EncodeParams P,
                                                              const __grid_constant__ EncodeTiles G) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
@@ -203,14 +233,35 @@ __global__ void __launch_bounds__(kBlock, SR ? 3 : 4) encode_bf16_kernel(const _
             // ---- quantize, pack and store, one slot at a time: a division-free
             // pass, an exact recompute of the slot in the rare case that one of its
             // elements lies near a decision boundary, then the store
-            const uint32_t jlast = static_cast<uint32_t>((kSlots - 1) * team_threads + tt) * kEps;
-            if (fq.usable && jlast + kEps <= cnt && b_off + jlast + kEps <= staged) {
+            // whole buckets take the fast path; the test is uniform across the
+            // team, so the packing shuffles always see the whole warp
+            const uint32_t window = static_cast<uint32_t>(team_threads) * kSlots * kEps;
+            if (fq.usable && cnt == window && b_off + window <= staged) {
 #pragma unroll 2
                 for (int sl = 0; sl < kSlots; ++sl) {
                     const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
                     const uint64_t i0 = b0 + j;
                     float v[8], u[8];
                     unpack8(*reinterpret_cast<const uint4 *>(stage + (b_off + j) * 2u), v);
+                    if constexpr (SCHEME == kTernary && SR) {
+                        bool near;
+                        const uint32_t f16 = ternary_sr_field8(v, philox_words(i0, P.step, keys),
+                                                               philox_words(i0 + 4, P.step, keys),
+                                                               fq.rinv, fq.delta2, near);
+                        uint32_t f0 = f16 & 0xFFu, f1 = f16 >> 8;
+                        if (near) {  // rare: recompute the slot with the division
+                            uniform4(i0, P.step, keys, u);
+                            uniform4(i0 + 4, P.step, keys, u + 4);
+                            f0 = f1 = 0;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                f0 |= code_exact<SCHEME, BITS, SR>(v[c], u[c], bp) << (c * BITS);
+                                f1 |= code_exact<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp) << (c * BITS);
+                            }
+                        }
+                        store_codes8<BITS>(P.codes, i0, true, lane, f0, f1);
+                        continue;
+                    }
 #pragma unroll
                     for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
                     if constexpr (SR) {

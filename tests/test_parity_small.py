@@ -430,3 +430,30 @@ def test_most_workers(q):
     vote = torch.empty(sw, dtype=torch.int32, device="cuda")
     q.qc_sign_vote(dev(signs), sw, M, n, vote)
     assert_bits_equal(u32(vote), orc.sign_vote(signs, M=M, n=n), "vote M=1024")
+
+
+def test_encode_ternary_bf16_near_draws(q):
+    """The bf16 ternary kernel decides keep = [u < |p| / s] division-free and
+    falls back to the exact path when u and |p| / s are within 2^-21.  Buckets
+    with s = 1 make |p| / s = |p|; every element whose draw u is below 2^-12 gets
+    |p| = u rounded to bf16 (or one bf16 step either side), which lands within
+    reach of the fallback and sometimes exactly on u."""
+    bucket, nb = 1024, 256
+    n = bucket * nb
+    g = (wl.std_normal(41, 1, n) * np.float32(0.2)).astype(np.float32)
+    g = np.clip(g, -0.9, 0.9)
+    g[::bucket] = 1.0                                   # s = max|p| = 1 in every bucket
+    u = np.array([orc.uniform(SEED, STEP, i) for i in range(n)], dtype=np.float32)
+    small = np.flatnonzero((u < 2.0 ** -12) & (np.arange(n) % bucket != 0))
+    assert small.size > 20
+    gb = wl.to_bf16_bits(g)
+    ub = wl.to_bf16_bits(u[small])
+    side = (np.arange(small.size) % 3).astype(np.int32) - 1   # -1, 0, +1 bf16 steps
+    gb[small] = (ub.astype(np.int32) + side).astype(np.uint16)
+    exact_hits = int((wl.bf16_bits_to_f32(gb[small]) == u[small]).sum())
+    codes, scale, _, _ = _run_encode(q, gb, None, n, 2, bucket, q.QC_SCHEME_TERNARY, 1)
+    c_or, s_or = orc.encode_ternary(gb, None, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                                    seed=SEED, step=STEP)
+    assert np.all(s_or == 1.0)
+    assert_bits_equal(codes, c_or, f"ternary bf16 near draws ({small.size} planted, "
+                                   f"{exact_hits} exactly on u)")
