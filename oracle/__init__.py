@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY, SCHEME_QSGD = 0, 1, 2, 3
+SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY, SCHEME_QSGD, SCHEME_UNIFORM_CLIP = 0, 1, 2, 3, 4
 ROUND_NEAREST, ROUND_STOCHASTIC = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OUT_SUM, OUT_MEAN, ACCUMULATE_INTO_OUT = 0, 1, 2
@@ -65,6 +65,7 @@ def _L():
         lib.oracle_num_buckets.argtypes = [S, S]
         lib.oracle_num_buckets.restype = S
         lib.oracle_encode_uniform.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P, P]
+        lib.oracle_encode_uniform_clip.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P, P]
         lib.oracle_encode_sign.argtypes = [P, I, P, S, S, P, P]
         lib.oracle_encode_ternary.argtypes = [P, I, P, S, U64, S, I, U64, U32, P, P]
         lib.oracle_encode_qsgd.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P]
@@ -78,7 +79,8 @@ def _L():
         lib.oracle_e4m3_from_f32_array.restype = None
         lib.oracle_rowwise_fp8.argtypes = [P, S, S, P, P]
         lib.oracle_rowwise_fp8_dequant.argtypes = [P, P, S, S, P]
-        for name in ("oracle_encode_uniform", "oracle_encode_sign", "oracle_encode_ternary",
+        for name in ("oracle_encode_uniform", "oracle_encode_uniform_clip", "oracle_encode_sign",
+                     "oracle_encode_ternary",
                      "oracle_encode_qsgd",
                      "oracle_decode_accumulate", "oracle_sign_vote", "oracle_rowwise_fp8",
                      "oracle_rowwise_fp8_dequant"):
@@ -141,6 +143,25 @@ def encode_uniform(grad, err=None, *, bits, bucket, mode=ROUND_NEAREST, seed=0, 
     _check(rc, "encode_uniform")
     nw = code_words(n, bits)
     return codes[:nw], scale[:num_buckets(n, bucket)], offset[:num_buckets(n, bucket)]
+
+
+def encode_uniform_clip(grad, err=None, *, bits, bucket, mode=ROUND_NEAREST, seed=0, step=0,
+                        index_base=0):
+    """Uniform quantization over the bucket's 1st..99th percentile range
+    (nearest rank); returns (codes, scale, offset) and updates ``err``."""
+    g = np.ascontiguousarray(grad)
+    n = g.size
+    if err is not None:
+        assert err.dtype == np.float32 and err.flags.c_contiguous and err.size == n
+    codes = np.zeros(max(code_words(n, bits), 1), dtype=np.uint32)
+    nb = max(num_buckets(n, bucket), 1)
+    scale = np.zeros(nb, dtype=np.float32)
+    offset = np.zeros(nb, dtype=np.float32)
+    rc = _L().oracle_encode_uniform_clip(_ptr(g), _grad_dtype(g), _ptr(err), n, index_base, bits,
+                                         bucket, mode, seed, step, _ptr(codes), _ptr(scale),
+                                         _ptr(offset))
+    _check(rc, "encode_uniform_clip")
+    return codes[:code_words(n, bits)], scale[:num_buckets(n, bucket)], offset[:num_buckets(n, bucket)]
 
 
 def encode_sign(grad, err=None, *, bucket):
@@ -211,6 +232,10 @@ def reencode(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM,
                           meta_stride=meta_stride)
     if scheme == SCHEME_UNIFORM:
         c, s, o = encode_uniform(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed, step=step)
+        return r, c, s, o
+    if scheme == SCHEME_UNIFORM_CLIP:
+        c, s, o = encode_uniform_clip(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed,
+                                      step=step)
         return r, c, s, o
     if scheme == SCHEME_SIGN:
         c, s = encode_sign(r, err, bucket=bucket)

@@ -37,7 +37,8 @@
 
 #define ORC_API __attribute__((visibility("default")))
 
-enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2, ORC_SCHEME_QSGD = 3 };
+enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2, ORC_SCHEME_QSGD = 3,
+       ORC_SCHEME_UNIFORM_CLIP = 4 };
 enum { ORC_ROUND_NEAREST = 0, ORC_ROUND_STOCHASTIC = 1 };
 enum { ORC_DTYPE_F32 = 0, ORC_DTYPE_BF16 = 1 };
 enum { ORC_OUT_MEAN = 1, ORC_ACCUMULATE_INTO_OUT = 2 };
@@ -239,6 +240,93 @@ ORC_API int oracle_encode_uniform(const void *grad, int dtype, float *err, size_
         offset_out[k] = mn;
     }
     free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Uniform quantization over a percentile-clipped range, with error feedback.
+ *
+ * p3 "Adaptive Quantization Strategies", Percentile Clipping: outliers are
+ * clipped before quantizing by setting min and max to the 1st and 99th
+ * percentiles instead of the absolute extremes.  Readings: the percentile is
+ * the nearest-rank one (the value of rank ceil(P * cnt / 100) in the sorted
+ * bucket, 1-based), so both bounds are elements of the bucket:
+ *   k_lo = ceil(cnt / 100) - 1,  k_hi = ceil(99 * cnt / 100) - 1   (0-based)
+ *   mn = sorted(p)[k_lo],  mx = sorted(p)[k_hi]     (zero taken as +0)
+ * Every element is clamped into [mn, mx] and then quantized exactly as in
+ * oracle_encode_uniform with these mn and mx; the dequantized value is that of
+ * the clamped element, so the error-feedback residual e = p - deq carries the
+ * clipped part.  Buckets of at most 99 elements have k_lo = 0, k_hi = cnt - 1:
+ * the absolute min and max.  Decoding is the uniform decode. */
+static int orc_cmp_float(const void *a, const void *b)
+{
+    float x = *(const float *)a, y = *(const float *)b;
+    return (x > y) - (x < y);
+}
+
+ORC_API int oracle_encode_uniform_clip(const void *grad, int dtype, float *err, size_t n,
+                                       uint64_t index_base, int bits, size_t bucket, int mode,
+                                       uint64_t seed, uint32_t step, uint32_t *codes,
+                                       float *scale_out, float *offset_out)
+{
+    if (!(bits == 1 || bits == 2 || bits == 4 || bits == 8) || !orc_valid_bucket(bucket))
+        return -1;
+    const uint32_t L = (1u << bits) - 1u;
+    const float Lf = (float)L;
+    memset(codes, 0, oracle_code_words(n, bits) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    float *sorted = (float *)malloc(bucket * sizeof(float));
+    if (!p || !sorted) {
+        free(p);
+        free(sorted);
+        return -2;
+    }
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+            sorted[j] = p[j];
+        }
+        qsort(sorted, cnt, sizeof(float), orc_cmp_float);
+        size_t k_lo = (cnt + 99) / 100 - 1;
+        size_t k_hi = (99 * cnt + 99) / 100 - 1;
+        float mn = orc_positive_zero(sorted[k_lo]);
+        float mx = orc_positive_zero(sorted[k_hi]);
+        float range = mx - mn;
+        float scale = range / Lf;
+        for (size_t j = 0; j < cnt; ++j) {
+            float pc = p[j] < mn ? mn : (p[j] > mx ? mx : p[j]);
+            uint32_t q = 0;
+            if (scale != 0.0f) {
+                float diff = pc - mn;
+                float t = diff / scale;
+                float level;
+                if (mode == ORC_ROUND_NEAREST) {
+                    level = rintf(t);
+                } else {
+                    float f = floorf(t);
+                    float frac = t - f;
+                    float u = oracle_uniform(seed, step, index_base + lo + j);
+                    level = (u < frac) ? f + 1.0f : f;
+                }
+                if (!(level >= 0.0f))
+                    level = 0.0f;
+                q = (level > Lf) ? L : (uint32_t)level;
+            }
+            orc_put_code(codes, lo + j, bits, q);
+            if (err) {
+                float deq = fmaf((float)q, scale, mn);
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = scale;
+        offset_out[k] = mn;
+    }
+    free(p);
+    free(sorted);
     return 0;
 }
 
@@ -451,6 +539,10 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
 {
     if (M < 1 || !orc_valid_bucket(bucket))
         return -1;
+    if (scheme < ORC_SCHEME_UNIFORM || scheme > ORC_SCHEME_UNIFORM_CLIP)
+        return -1;
+    if (scheme == ORC_SCHEME_UNIFORM_CLIP) /* a uniform payload over the clipped range */
+        scheme = ORC_SCHEME_UNIFORM;
     if (scheme == ORC_SCHEME_UNIFORM && !(bits == 1 || bits == 2 || bits == 4 || bits == 8))
         return -1;
     if (scheme == ORC_SCHEME_SIGN && bits != 1)

@@ -745,3 +745,82 @@ def test_reencode_of_identical_payloads_is_idempotent(scheme, bits, mode):
     assert np.array_equal(cr, c[0])
     if scheme == orc.SCHEME_TERNARY or scheme == orc.SCHEME_SIGN:
         assert np.array_equal(sr, s[0])
+
+
+# ------------------------------------------------------------- percentile clip
+
+def _nearest_rank_index(cnt, pct):
+    """0-based index of the nearest-rank percentile: rank ceil(pct/100 * cnt)."""
+    return math.ceil(Fraction(pct, 100) * cnt) - 1
+
+
+@pytest.mark.parametrize("cnt", [1, 2, 37, 99, 100, 101, 512, 1000, 2048, 4096])
+def test_clip_bounds_are_nearest_rank_percentiles(cnt):
+    """offset = the 1st-percentile element and scale = (p99 - p1) / L, with the
+    order statistics taken from numpy's sort and the ranks from the definition."""
+    rng = np.random.default_rng(cnt)
+    bits, L = 8, 255
+    p = (rng.standard_normal(cnt) * 1e-3).astype(np.float32)
+    p[rng.integers(0, cnt, size=max(1, cnt // 50))] *= np.float32(100.0)   # outliers
+    _, s, o = orc.encode_uniform_clip(p, bits=bits, bucket=max(32, -(-cnt // 32) * 32))
+    srt = np.sort(p)
+    lo, hi = srt[_nearest_rank_index(cnt, 1)], srt[_nearest_rank_index(cnt, 99)]
+    assert o[0] == lo
+    assert s[0] == np.float32(np.float32(hi - lo) / np.float32(L))
+
+
+def test_clip_small_buckets_are_the_min_max_scheme():
+    """Up to 99 elements the 1st and 99th percentiles are the extremes: the
+    clipped encoder reproduces the min/max encoder bit for bit."""
+    g = wl.outlier_gradient(99 * 7, seed=12)
+    for bucket in (32, 64, 96):
+        for mode in (orc.ROUND_NEAREST, orc.ROUND_STOCHASTIC):
+            e1 = np.zeros(g.size, np.float32)
+            e2 = np.zeros(g.size, np.float32)
+            a = orc.encode_uniform(g, e1, bits=4, bucket=bucket, mode=mode, seed=3, step=1)
+            b = orc.encode_uniform_clip(g, e2, bits=4, bucket=bucket, mode=mode, seed=3, step=1)
+            for x, y in zip(a, b):
+                assert np.array_equal(x, y)
+            assert np.array_equal(e1, e2)
+
+
+def test_clip_outliers_saturate_and_residual_keeps_them():
+    """Elements beyond the clipped range take code 0 or L (nearest rounding); the
+    residual is exactly p - deq, so an outlier's excess stays in the error
+    feedback; inner elements are within half a step of their level."""
+    bucket, bits, L = 2048, 8, 255
+    g = wl.outlier_gradient(bucket * 4, seed=13)
+    err = np.zeros(g.size, np.float32)
+    c, s, o = orc.encode_uniform_clip(g, err, bits=bits, bucket=bucket)
+    q = np.array([(int(c[i // 4]) >> (8 * (i % 4))) & 0xFF for i in range(g.size)])
+    for k in range(4):
+        sl = slice(k * bucket, (k + 1) * bucket)
+        pk, qk = g[sl], q[sl]
+        mx = np.sort(pk)[_nearest_rank_index(bucket, 99)]
+        assert np.all(qk[pk < o[k]] == 0) and np.all(qk[pk > mx] == L)
+        # one rounding of the exact q * scale + offset
+        deq = np.array([to_f32(Fraction(int(a)) * Fraction(float(s[k])) + Fraction(float(o[k])))
+                        for a in qk], dtype=np.float32)
+        assert np.array_equal(err[sl], (pk - deq).astype(np.float32))
+        inner = (pk >= o[k]) & (pk <= mx)
+        assert np.all(np.abs(pk[inner].astype(np.float64) - deq[inner]) <= 0.5001 * float(s[k]))
+
+
+def test_clip_shrinks_the_step_on_outlier_buckets():
+    """On the outlier workload the clipped range is far narrower than min..max,
+    so the quantization step of the inner elements shrinks accordingly."""
+    g = wl.outlier_gradient(1 << 16, seed=14)
+    _, s_mm, _ = orc.encode_uniform(g, bits=8, bucket=2048)
+    _, s_cl, _ = orc.encode_uniform_clip(g, bits=8, bucket=2048)
+    assert np.all(s_cl <= s_mm)
+    assert np.median(s_mm / s_cl) > 3.0
+
+
+def test_clip_payload_decodes_as_uniform():
+    g = wl.outlier_gradient(5000, seed=15)
+    c, s, o = orc.encode_uniform_clip(g, bits=4, bucket=512)
+    a = orc.decode_accumulate(c, s, o, M=1, n=g.size, bits=4, bucket=512,
+                              scheme=orc.SCHEME_UNIFORM_CLIP)
+    b = orc.decode_accumulate(c, s, o, M=1, n=g.size, bits=4, bucket=512,
+                              scheme=orc.SCHEME_UNIFORM)
+    assert np.array_equal(a, b)
