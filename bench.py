@@ -147,10 +147,10 @@ class UniformEF(Component):
         self.stochastic, self.seed, self.sigma_mode = stochastic, seed, sigma_mode
         self.scheme = scheme
         words, nb = _words(n, bits), _nb(n, bucket)
-        meta = 8 if scheme == 0 else 4
+        meta = 8 if scheme in (0, 4) else 4
         enc = 12 * n + 4 * words + meta * nb
         dec = 4 * words + meta * nb + 4 * n
-        tag = f"u{bits}" if scheme == 0 else f"qsgd{bits}"
+        tag = {0: f"u{bits}", 3: f"qsgd{bits}", 4: f"clip{bits}"}[scheme]
         self.enc_name, self.dec_name = f"encode_{tag}_ef", f"decode_{tag}_m1"
         self.kernels = {self.enc_name: (1, enc), self.dec_name: (1, dec)}
         self.units = 2 * n
@@ -198,10 +198,10 @@ class UniformEF(Component):
         mode = orc.ROUND_STOCHASTIC if self.stochastic else orc.ROUND_NEAREST
 
         def go(lo, hi):
-            if self.scheme == 0:
-                c, s, o = orc.encode_uniform(g[lo:hi], err[lo:hi], bits=self.bits,
-                                             bucket=self.bucket, mode=mode, seed=self.seed,
-                                             step=0, index_base=lo)
+            if self.scheme in (0, 4):
+                enc = orc.encode_uniform if self.scheme == 0 else orc.encode_uniform_clip
+                c, s, o = enc(g[lo:hi], err[lo:hi], bits=self.bits, bucket=self.bucket, mode=mode,
+                              seed=self.seed, step=0, index_base=lo)
             else:
                 (c, s), o = orc.encode_qsgd(g[lo:hi], err[lo:hi], bits=self.bits,
                                             bucket=self.bucket, mode=mode, seed=self.seed,
@@ -442,6 +442,10 @@ def make_workload(name):
         "rx_reencode_u8": lambda: [Reencode("rx_reencode_u8", 0, 8)],
         "rx_reencode_ternary": lambda: [Reencode("rx_reencode_ternary", 2, 2)],
         "u8_ef_small": lambda: [UniformEF("u8_ef_small", 1 << 20, 8, 2048, False, 0, "outlier")],
+        "clip8_ef_small": lambda: [UniformEF("clip8_ef_small", 1 << 20, 8, 2048, False, 0,
+                                             "outlier", scheme=4)],
+        "clip8_ef_large": lambda: [UniformEF("clip8_ef_large", 1 << 28, 8, 2048, False, 0,
+                                             "outlier", scheme=4)],
         "u8_ef_large": lambda: [UniformEF("u8_ef_large", 1 << 28, 8, 2048, False, 0, "outlier")],
         # smaller single-kernel cases (inputs still larger than L2) for profiler captures
         "probe_sr4_ef": lambda: [UniformEF("sr4_ef", 1 << 26, 4, 512, True, 2, "bucket")],

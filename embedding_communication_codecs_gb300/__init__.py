@@ -22,6 +22,7 @@ from .build import LIB_PATH
 
 QC_OK, QC_ERR_NULL, QC_ERR_INVALID_ARG, QC_ERR_ALIGNMENT, QC_ERR_UNSUPPORTED, QC_ERR_CUDA = range(6)
 QC_SCHEME_UNIFORM, QC_SCHEME_SIGN, QC_SCHEME_TERNARY, QC_SCHEME_QSGD = 0, 1, 2, 3
+QC_SCHEME_UNIFORM_CLIP = 4
 QC_ROUND_NEAREST, QC_ROUND_STOCHASTIC = 0, 1
 QC_DTYPE_F32, QC_DTYPE_BF16 = 0, 1
 QC_OUT_SUM, QC_OUT_MEAN, QC_ACCUMULATE_INTO_OUT = 0, 1, 2
@@ -187,7 +188,7 @@ def alloc_payload(n: int, bits: int, bucket: int, scheme: int, device="cuda", wo
     codes = torch.empty(lead + (words,), dtype=torch.int32, device=device)
     scale = torch.empty(lead + (nb,), dtype=torch.float32, device=device)
     offset = (torch.empty(lead + (nb,), dtype=torch.float32, device=device)
-              if scheme == QC_SCHEME_UNIFORM else None)
+              if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP) else None)
     return codes, scale, offset
 
 

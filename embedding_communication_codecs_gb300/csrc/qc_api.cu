@@ -11,7 +11,8 @@
 #include "qc_internal.h"
 
 static_assert(int{QC_SCHEME_UNIFORM} == qc::kUniform && int{QC_SCHEME_SIGN} == qc::kSign &&
-                  int{QC_SCHEME_TERNARY} == qc::kTernary && int{QC_SCHEME_QSGD} == qc::kQsgd,
+                  int{QC_SCHEME_TERNARY} == qc::kTernary && int{QC_SCHEME_QSGD} == qc::kQsgd &&
+                  int{QC_SCHEME_UNIFORM_CLIP} == qc::kClip,
               "the public scheme numbers are the kernels' template arguments");
 
 namespace {
@@ -194,7 +195,7 @@ bool reencode_tiles_for(const qc::ReencodeParams &p, int bits, qc::ReencodeTiles
 
 // Bits and rounding mode allowed for a scheme; QC_OK or the failure status.
 qc_status check_scheme(const char *fn, qc_scheme scheme, int bits) {
-    if (scheme == QC_SCHEME_UNIFORM) {
+    if (scheme == QC_SCHEME_UNIFORM || scheme == QC_SCHEME_UNIFORM_CLIP) {
         if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
             return fail(QC_ERR_INVALID_ARG, "%s: uniform bits must be 1, 2, 4 or 8 (got %d)", fn, bits);
     } else if (scheme == QC_SCHEME_SIGN) {
@@ -292,8 +293,8 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = 0;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors() | qc::take_encode_bf16_errors() | qc::take_decode_errors() |
-             qc::take_reencode_errors();
+    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
+             qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }
 
@@ -303,21 +304,10 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
                        qc_stream_t stream) {
     if (dtype != QC_DTYPE_F32 && dtype != QC_DTYPE_BF16)
         return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: dtype %d is not F32 or BF16", dtype);
-    if (scheme == QC_SCHEME_UNIFORM) {
-        if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
-            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: uniform bits must be 1, 2, 4 or 8 (got %d)", bits);
-    } else if (scheme == QC_SCHEME_SIGN) {
-        if (bits != 1) return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme needs bits == 1 (got %d)", bits);
-        if (mode != QC_ROUND_NEAREST)
-            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme is deterministic; mode must be NEAREST");
-    } else if (scheme == QC_SCHEME_TERNARY) {
-        if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: ternary scheme needs bits == 2 (got %d)", bits);
-    } else if (scheme == QC_SCHEME_QSGD) {
-        if (bits != 2 && bits != 4 && bits != 8)
-            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: QSGD bits must be 2, 4 or 8 (got %d)", bits);
-    } else {
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown scheme %d", scheme);
-    }
+    const qc_status sc = check_scheme("qc_encode_ef", scheme, bits);
+    if (sc != QC_OK) return sc;
+    if (scheme == QC_SCHEME_SIGN && mode != QC_ROUND_NEAREST)
+        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme is deterministic; mode must be NEAREST");
     if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
         return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown rounding mode %d", mode);
     if (!valid_bucket(bucket))
@@ -326,8 +316,9 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     if (n > (static_cast<size_t>(1) << 40))
         return fail(QC_ERR_UNSUPPORTED, "qc_encode_ef: n = %zu exceeds 2^40 elements", n);
     if (!grad || !codes || !scale) return fail(QC_ERR_NULL, "qc_encode_ef: grad, codes and scale must be non-NULL");
-    if (scheme == QC_SCHEME_UNIFORM && !offset)
-        return fail(QC_ERR_NULL, "qc_encode_ef: the uniform scheme needs an offset array");
+    const bool uni = scheme == QC_SCHEME_UNIFORM || scheme == QC_SCHEME_UNIFORM_CLIP;
+    if (uni && !offset)
+        return fail(QC_ERR_NULL, "qc_encode_ef: the uniform schemes need an offset array");
     const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
     if (!aligned(grad, dtype == QC_DTYPE_F32 ? 16 : 8))
         return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: grad must be %d-byte aligned", dtype == QC_DTYPE_F32 ? 16 : 8);
@@ -336,7 +327,7 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
         return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: codes, scale and offset must be 4-byte aligned");
     const size_t nb = qc_num_buckets(n, bucket);
     const size_t cbytes = qc_code_words(n, bits) * 4, mbytes = nb * 4;
-    const void *outs[3] = {codes, scale, scheme == QC_SCHEME_UNIFORM ? offset : nullptr};
+    const void *outs[3] = {codes, scale, uni ? offset : nullptr};
     const size_t osz[3] = {cbytes, mbytes, mbytes};
     for (int a = 0; a < 3; ++a) {
         if (overlaps(outs[a], osz[a], grad, n * esize) || overlaps(outs[a], osz[a], err, n * 4))
@@ -364,6 +355,16 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     p.offset = offset;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     qc::EncodeTiles tiles{};
+    if (scheme == QC_SCHEME_UNIFORM_CLIP) {
+        // the percentile selection runs over a bucket held in registers by one team
+        if (!encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))
+            return fail(QC_ERR_UNSUPPORTED,
+                        "qc_encode_ef: percentile clipping needs a bucket of at most 4096 elements "
+                        "and a 16-byte aligned gradient");
+        return from_cuda(qc::launch_encode_clip(p, tiles, bits, mode == QC_ROUND_STOCHASTIC,
+                                                dtype == QC_DTYPE_BF16, st),
+                         "qc_encode_ef");
+    }
     if (dtype == QC_DTYPE_BF16 && bf16_tiles_for(p, aligned(grad, 16), tiles))
         return from_cuda(qc::launch_encode_bf16(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC, st),
                          "qc_encode_ef");
@@ -380,19 +381,10 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
                                const float *scale, const float *offset, size_t meta_stride,
                                int M, size_t n, int bits, size_t bucket, qc_scheme scheme,
                                float *out, int flags, qc_stream_t stream) {
-    if (scheme == QC_SCHEME_UNIFORM) {
-        if (bits != 1 && bits != 2 && bits != 4 && bits != 8)
-            return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: uniform bits must be 1, 2, 4 or 8 (got %d)", bits);
-    } else if (scheme == QC_SCHEME_SIGN) {
-        if (bits != 1) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: sign scheme needs bits == 1");
-    } else if (scheme == QC_SCHEME_TERNARY) {
-        if (bits != 2) return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: ternary scheme needs bits == 2");
-    } else if (scheme == QC_SCHEME_QSGD) {
-        if (bits != 2 && bits != 4 && bits != 8)
-            return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: QSGD bits must be 2, 4 or 8");
-    } else {
-        return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: unknown scheme %d", scheme);
-    }
+    const qc_status sc = check_scheme("qc_decode_accumulate", scheme, bits);
+    if (sc != QC_OK) return sc;
+    // a percentile-clipped payload is a uniform payload over its clipped range
+    if (scheme == QC_SCHEME_UNIFORM_CLIP) scheme = QC_SCHEME_UNIFORM;
     if (M < 1 || M > QC_MAX_WORKERS)
         return fail(QC_ERR_INVALID_ARG, "qc_decode_accumulate: M must be in [1, %d] (got %d)", QC_MAX_WORKERS, M);
     if (flags & ~(QC_OUT_MEAN | QC_ACCUMULATE_INTO_OUT))
@@ -448,6 +440,9 @@ qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const fl
     static const char *fn = "qc_reencode";
     const qc_status sc = check_scheme(fn, scheme, bits);
     if (sc != QC_OK) return sc;
+    if (scheme == QC_SCHEME_UNIFORM_CLIP)
+        return fail(QC_ERR_UNSUPPORTED, "%s: percentile clipping is not fused into the re-encode; "
+                    "use qc_decode_accumulate followed by qc_encode_ef", fn);
     if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
         return fail(QC_ERR_INVALID_ARG, "%s: unknown rounding mode %d", fn, mode);
     if (scheme == QC_SCHEME_SIGN && mode != QC_ROUND_NEAREST)

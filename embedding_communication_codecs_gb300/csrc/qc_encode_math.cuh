@@ -67,8 +67,9 @@ struct Stats<kQsgd> {  // sum of p^2 as a double word; each square is split exac
 
 // Per-bucket quantization parameters derived from the statistics.
 struct BucketParams {
-    float a;      // UNIFORM: min (offset); SIGN / TERNARY: s
-    float scale;  // UNIFORM: (max - min) / L
+    float a;           // UNIFORM: min (offset); SIGN / TERNARY: s; QSGD: unit
+    float scale;       // UNIFORM: (max - min) / L
+    float hi = 0.0f;   // CLIP: the upper bound elements are clamped to
 };
 
 template <int SCHEME, int BITS>
@@ -117,13 +118,34 @@ struct Finish<kQsgd, BITS> {
     }
 };
 
+// CLIP: the bounds are order statistics found by team_percentiles(), not a
+// running reduction, so the add/merge operations are never used.
+template <>
+struct Stats<kClip> {
+    float mn, mx;
+    __device__ void init() { mn = mx = 0.0f; }
+    __device__ void add(float) {}
+    __device__ void warp_reduce() {}
+    __device__ void merge(const Stats &) {}
+};
+
+template <int BITS>
+struct Finish<kClip, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kClip> &st, uint32_t) {
+        constexpr float L = static_cast<float>((1u << BITS) - 1u);
+        const float mn = positive_zero(st.mn), mx = positive_zero(st.mx);
+        return BucketParams{mn, __fdiv_rn(__fsub_rn(mx, mn), L), mx};
+    }
+};
+
 // ------------------------------------------------------------- per element
 
 // Code and dequantized value of one element.
 template <int SCHEME, int BITS, bool SR>
 __device__ __forceinline__ uint32_t quantize(float p, float u, const BucketParams &bp,
                                              float &deq) {
-    if constexpr (SCHEME == kUniform) {
+    if constexpr (SCHEME == kUniform || SCHEME == kClip) {
+        if constexpr (SCHEME == kClip) p = fminf(fmaxf(p, bp.a), bp.hi);  // clamp into [mn, mx]
         constexpr uint32_t L = (1u << BITS) - 1u;
         if (bp.scale == 0.0f) {
             deq = bp.a;
@@ -203,12 +225,12 @@ struct FastQ {
 
 template <int SCHEME, int BITS>
 __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
-    const float d = (SCHEME == kUniform) ? bp.scale : bp.a;
+    const float d = (SCHEME == kUniform || SCHEME == kClip) ? bp.scale : bp.a;
     FastQ f;
     const bool normal = d >= 0x1p-125f && d <= 0x1p125f;
     f.usable = SCHEME == kSign || normal;  // the sign code needs no division
     f.rinv = (SCHEME != kSign && normal) ? __frcp_rn(d) : 0.0f;
-    f.delta2 = SCHEME == kUniform ? static_cast<float>(1u << BITS) * 0x1p-21f
+    f.delta2 = (SCHEME == kUniform || SCHEME == kClip) ? static_cast<float>(1u << BITS) * 0x1p-21f
                : SCHEME == kQsgd     ? static_cast<float>(1u << (BITS - 1)) * 0x1p-21f
                                      : 0x1p-21f;
     return f;
@@ -219,7 +241,8 @@ __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
 template <int SCHEME, int BITS, bool SR>
 __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const BucketParams &bp,
                                                   const FastQ &fq, float &deq, bool &redo) {
-    if constexpr (SCHEME == kUniform) {
+    if constexpr (SCHEME == kUniform || SCHEME == kClip) {
+        if constexpr (SCHEME == kClip) p = fminf(fmaxf(p, bp.a), bp.hi);
         constexpr uint32_t L = (1u << BITS) - 1u;
         constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
@@ -301,7 +324,8 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
 template <int SCHEME, int BITS, bool SR>
 __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketParams &bp,
                                               const FastQ &fq, bool &redo) {
-    if constexpr (SCHEME == kUniform) {
+    if constexpr (SCHEME == kUniform || SCHEME == kClip) {
+        if constexpr (SCHEME == kClip) p = fminf(fmaxf(p, bp.a), bp.hi);
         constexpr uint32_t L = (1u << BITS) - 1u;
         constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
@@ -368,7 +392,8 @@ __device__ __forceinline__ uint32_t code_exact(float p, float u, const BucketPar
 // Dequantized value of code c of a packed field, identical to the encoder's deq.
 template <int SCHEME, int BITS>
 __device__ __forceinline__ float deq_of(uint32_t field, int c, const BucketParams &bp) {
-    if constexpr (SCHEME == kUniform) return dequant_code<SCHEME, BITS>(field, c, bp.scale, bp.a);
+    if constexpr (SCHEME == kUniform || SCHEME == kClip)
+        return dequant_code<kUniform, BITS>(field, c, bp.scale, bp.a);
     else return dequant_code<SCHEME, BITS>(field, c, bp.a, bp.a);
 }
 
@@ -469,7 +494,7 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
 template <int SCHEME>
 __device__ __forceinline__ void store_meta(float *scale, float *offset, uint64_t k,
                                            const BucketParams &bp) {
-    if constexpr (SCHEME == kUniform) {
+    if constexpr (SCHEME == kUniform || SCHEME == kClip) {
         scale[k] = bp.scale;
         offset[k] = bp.a;
     } else {
@@ -495,6 +520,123 @@ __device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*r
         for (int w = 1; w < W; ++w) st.merge(red[buf][team * W + w]);
         buf ^= 1;
     }
+}
+
+
+// ------------------------------------------------------------- percentiles
+
+// Unsigned keys that order like the floats (-0 just below +0).
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// 256-bin histograms with 16-bit counters, two bins per word (a bucket holds at
+// most 4096 elements, so a count never carries into its neighbour).
+constexpr int kHistWords = 128;
+constexpr int kHistTeamWords = 3 * 2 * kHistWords;  // 3 rotating buffers x (low, high)
+
+__device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin) {
+    atomicAdd(h + (bin >> 1), 1u << ((bin & 1u) << 4));
+}
+
+// The bin of a 256-bin histogram that holds rank r (0-based); r becomes the rank
+// within that bin.  Every lane of the calling warp gets the same answer.
+__device__ __forceinline__ uint32_t hist_find(const uint32_t *h, uint32_t &r, int lane) {
+    uint32_t c[8], sum = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w = h[4 * lane + q];
+        c[2 * q] = w & 0xFFFFu;
+        c[2 * q + 1] = w >> 16;
+        sum += c[2 * q] + c[2 * q + 1];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t excl = incl - sum;
+    const bool mine = excl <= r && r < incl;
+    const int owner = __ffs(__ballot_sync(kFull, mine)) - 1;
+    uint32_t bin = 0u, before = 0u, acc = excl;
+    bool found = false;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (!found && r < acc + c[k]) {
+            bin = static_cast<uint32_t>(8 * lane + k);
+            before = acc;
+            found = true;
+        }
+        acc += c[k];
+    }
+    bin = __shfl_sync(kFull, bin, owner);
+    before = __shfl_sync(kFull, before, owner);
+    r -= before;
+    return bin;
+}
+
+// Barrier over one team: the warp itself, or named barrier 1 + team over its W
+// warps (teams never wait for one another).
+__device__ __forceinline__ void team_sync(int W, int team) {
+    if (W == 1) {
+        __syncwarp();
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(W * 32) : "memory");
+    }
+}
+
+// The nearest-rank 1st and 99th percentiles of the cnt valid elements in the
+// team's slots (ranks k_lo = ceil(cnt/100) - 1 and k_hi = ceil(99 cnt/100) - 1,
+// 0-based): four rounds of 8-bit radix selection over order keys, most
+// significant byte first.  Round 0 builds one histogram of every element's top
+// byte; later rounds count only the elements that share the bytes already
+// fixed for each rank.  `hist` is the team's kHistTeamWords words; `round`
+// counts rounds across calls so the three buffers rotate: a round fills one
+// buffer, and after the barrier clears the one filled two rounds earlier,
+// which every warp has finished reading.  cnt > 0; every thread of the team
+// calls this together.
+__device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint32_t cnt, int tt,
+                                                 int team_threads, int W, int team, int lane,
+                                                 uint32_t *hist, uint32_t &round, float &lo,
+                                                 float &hi) {
+    uint32_t r_lo = (cnt + 99u) / 100u - 1u, r_hi = (99u * cnt + 99u) / 100u - 1u;
+    uint32_t pre_lo = 0u, pre_hi = 0u;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass, ++round) {
+        const int shift = 24 - 8 * pass;
+        uint32_t *h = hist + (round % 3u) * (2 * kHistWords);
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
+                if (j < cnt) {
+                    const uint32_t key = order_key(get(p[s], c));
+                    const uint32_t d = (key >> shift) & 0xFFu;
+                    if (pass == 0) {
+                        hist_add(h, d);
+                    } else {
+                        const uint32_t top = key >> (shift + 8);
+                        if (top == (pre_lo >> (shift + 8))) hist_add(h, d);
+                        if (top == (pre_hi >> (shift + 8))) hist_add(h + kHistWords, d);
+                    }
+                }
+            }
+        }
+        team_sync(W, team);
+        pre_lo |= hist_find(h, r_lo, lane) << shift;
+        pre_hi |= hist_find(pass == 0 ? h : h + kHistWords, r_hi, lane) << shift;
+        uint32_t *old = hist + ((round + 2u) % 3u) * (2 * kHistWords);
+        for (int i = tt; i < 2 * kHistWords; i += team_threads) old[i] = 0u;
+    }
+    lo = key_value(pre_lo);
+    hi = key_value(pre_hi);
 }
 
 }  // namespace qc

@@ -7,7 +7,7 @@
 
 namespace qc {
 
-enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2, kQsgd = 3 };
+enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2, kQsgd = 3, kClip = 4 };
 
 // Elements a team of W warps covers per window: 4 float4 slots per lane.
 constexpr int kSlots = 4;
@@ -179,6 +179,9 @@ cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stoch
                           int bf16, cudaStream_t stream);
 cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                               int stochastic, int bf16, cudaStream_t stream);
+// The percentile-clipped uniform scheme (its own translation unit).
+cudaError_t launch_encode_clip(const EncodeParams &p, const EncodeTiles &g, int bits,
+                               int stochastic, int bf16, cudaStream_t stream);
 cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                                int stochastic, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
@@ -199,6 +202,7 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 
 // Device-side error flags of the pipelined kernels (read and cleared).
 uint32_t take_encode_errors();
+uint32_t take_encode_clip_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();
 uint32_t take_reencode_errors();

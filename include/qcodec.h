@@ -65,7 +65,8 @@ typedef enum {
     QC_SCHEME_UNIFORM = 0,    /* per-bucket min/max, 2^bits levels, fp32 scale+offset */
     QC_SCHEME_SIGN = 1,       /* 1 bit: sign, per-bucket fp32 scale = mean |p|        */
     QC_SCHEME_TERNARY = 2,    /* 2 bits: {-1,0,+1} -> codes {0,1,2}, scale = max |p|  */
-    QC_SCHEME_QSGD = 3        /* sign bit over bits-1 level bits, scale = ||p||_2 / s */
+    QC_SCHEME_QSGD = 3,       /* sign bit over bits-1 level bits, scale = ||p||_2 / s */
+    QC_SCHEME_UNIFORM_CLIP = 4 /* uniform over the 1st..99th percentile range          */
 } qc_scheme;
 
 typedef enum {
@@ -127,6 +128,15 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *     (relative) of a rounding boundary.  Norms must stay below 2^63 (the
  *     squares are summed in binary32 range); below 2^-40 the squares of the
  *     smallest elements are no longer split exactly.
+ *   UNIFORM_CLIP ("Adaptive Quantization Strategies", Percentile Clipping; bits
+ *     1, 2, 4 or 8): as UNIFORM, but mn and mx are the bucket's nearest-rank 1st
+ *     and 99th percentiles (the elements of 0-based rank ceil(cnt/100) - 1 and
+ *     ceil(99 cnt/100) - 1 in sorted order; zero taken as +0), and every p_i is
+ *     clamped into [mn, mx] before t_i is formed.  deq_i is that of the clamped
+ *     element, so with error feedback err_i = fl(p_i - deq_i) keeps the clipped
+ *     part.  Buckets of at most 99 elements reduce to UNIFORM.  Needs a bucket of
+ *     at most 4096 elements and a 16-byte aligned gradient (else
+ *     QC_ERR_UNSUPPORTED).  The payload decodes as UNIFORM.
  * Then, with error feedback, err_i = fl(p_i - deq_i) is written in place.
  *
  * Stochastic draw for element i (global index within this call):
@@ -135,12 +145,12 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *
  * grad   : n elements of `dtype`; 16-byte aligned (f32) or 8-byte aligned (bf16).
  * err    : n fp32, in/out, 16-byte aligned, or NULL for no error feedback.
- * bits   : UNIFORM 1, 2, 4 or 8; SIGN 1; TERNARY 2; QSGD 2, 4 or 8.
+ * bits   : UNIFORM and UNIFORM_CLIP 1, 2, 4 or 8; SIGN 1; TERNARY 2; QSGD 2, 4 or 8.
  * bucket : elements per bucket, a multiple of 32, 32 <= bucket <= 2^24.
  * codes  : out, qc_code_words(n, bits) uint32 words, 4-byte aligned.
  * scale  : out, qc_num_buckets(n, bucket) fp32.
- * offset : out, qc_num_buckets(n, bucket) fp32 for UNIFORM; ignored otherwise
- *          (may be NULL).
+ * offset : out, qc_num_buckets(n, bucket) fp32 for UNIFORM and UNIFORM_CLIP;
+ *          ignored otherwise (may be NULL).
  */
 qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
                        size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
@@ -166,8 +176,10 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
  *          (codes_stride_words >= qc_code_words(n, bits) when M > 1); 4-byte aligned.
  * scale  : worker w's per-bucket scales at scale + w * meta_stride
  *          (meta_stride >= qc_num_buckets(n, bucket) when M > 1).
- * offset : same layout as scale; UNIFORM only (ignored otherwise, may be NULL).
- * M      : 1 .. QC_MAX_WORKERS.   bits/scheme as for qc_encode_ef.
+ * offset : same layout as scale; UNIFORM and UNIFORM_CLIP only (ignored
+ *          otherwise, may be NULL).
+ * M      : 1 .. QC_MAX_WORKERS.   bits/scheme as for qc_encode_ef (an
+ *          UNIFORM_CLIP payload decodes exactly as a UNIFORM one).
  * out    : n fp32, 16-byte aligned; read only with QC_ACCUMULATE_INTO_OUT.
  */
 qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
@@ -193,7 +205,8 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
  * of that buffer, bit for bit; one kernel does both without the fp32 round trip.
  *
  * codes, scale, offset, meta_stride, codes_stride_words, M, bits, bucket,
- * scheme : as for qc_decode_accumulate.  `codes` must be 16-byte aligned and,
+ * scheme : as for qc_decode_accumulate (UNIFORM_CLIP: QC_ERR_UNSUPPORTED, the
+ *          clipped encode is not fused here).  `codes` must be 16-byte aligned and,
  *          for M > 1, codes_stride_words a multiple of 4, and the bucket at
  *          most 8192 elements; otherwise QC_ERR_UNSUPPORTED (the two-call
  *          composition above serves those layouts).

@@ -179,3 +179,14 @@ def test_reencode_rejects(q):
     assert re_(bucket=16384, n=1 << 15, cs=1 << 13, ms=2) == q.QC_ERR_UNSUPPORTED
     assert b"qc_decode_accumulate followed by qc_encode_ef" in q.lib.qc_last_error()
     assert re_(n=0, codes=None, codes_out=None) == q.QC_OK
+
+
+def test_clip_rejects(q):
+    C_ = q.QC_SCHEME_UNIFORM_CLIP
+    assert _enc(q, scheme=C_, bits=3) == q.QC_ERR_INVALID_ARG
+    assert _enc(q, scheme=C_, offset=None) == q.QC_ERR_NULL
+    assert _enc(q, scheme=C_, bucket=8192, n=1 << 15) == q.QC_ERR_UNSUPPORTED
+    assert b"percentile" in q.lib.qc_last_error()
+    assert _enc(q, scheme=C_, grad=A + 8, dtype=q.QC_DTYPE_BF16) == q.QC_ERR_UNSUPPORTED
+    assert q.lib.qc_reencode(C, 1024, D, D + 0x100000, 2, 2, 4096, 8, 2048, C_, 0, B, 0, 0, 0,
+                             0x50000000, 0x60000000, 0x60001000, A, 0) == q.QC_ERR_UNSUPPORTED
