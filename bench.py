@@ -451,6 +451,8 @@ def make_workload(name):
         "probe_sr4_ef": lambda: [UniformEF("sr4_ef", 1 << 26, 4, 512, True, 2, "bucket")],
         "probe_qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 1 << 26, 4, 512, True, 2, "bucket",
                                              scheme=3)],
+        "probe_clip8_ef": lambda: [UniformEF("clip8_ef", 1 << 26, 8, 2048, False, 0, "outlier",
+                                             scheme=4)],
         "probe_sign": lambda: [SignVote(n=1 << 24, M=2)],
         "probe_u8_bf16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 27, M=1)],
         "probe_ternary_bf16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 27, M=1)],

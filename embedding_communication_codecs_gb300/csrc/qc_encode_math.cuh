@@ -544,16 +544,16 @@ __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin) {
     atomicAdd(h + (bin >> 1), 1u << ((bin & 1u) << 4));
 }
 
-// The bin of a 256-bin histogram that holds rank r (0-based); r becomes the rank
-// within that bin.  Every lane of the calling warp gets the same answer.
+// The bin of a histogram of 64 * WPL bins (WPL packed words per lane) that
+// holds rank r (0-based); r becomes the rank within that bin.  Every lane of
+// the calling warp gets the same answer.
+template <int WPL>
 __device__ __forceinline__ uint32_t hist_find(const uint32_t *h, uint32_t &r, int lane) {
-    uint32_t c[8], sum = 0u;
+    uint32_t w[WPL], sum = 0u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t w = h[4 * lane + q];
-        c[2 * q] = w & 0xFFFFu;
-        c[2 * q + 1] = w >> 16;
-        sum += c[2 * q] + c[2 * q + 1];
+    for (int q = 0; q < WPL; ++q) {
+        w[q] = h[WPL * lane + q];
+        sum += (w[q] & 0xFFFFu) + (w[q] >> 16);
     }
     uint32_t incl = sum;
 #pragma unroll
@@ -567,13 +567,14 @@ __device__ __forceinline__ uint32_t hist_find(const uint32_t *h, uint32_t &r, in
     uint32_t bin = 0u, before = 0u, acc = excl;
     bool found = false;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (!found && r < acc + c[k]) {
-            bin = static_cast<uint32_t>(8 * lane + k);
+    for (int k = 0; k < 2 * WPL; ++k) {
+        const uint32_t c = (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
+        if (!found && r < acc + c) {
+            bin = static_cast<uint32_t>(2 * WPL * lane + k);
             before = acc;
             found = true;
         }
-        acc += c[k];
+        acc += c;
     }
     bin = __shfl_sync(kFull, bin, owner);
     before = __shfl_sync(kFull, before, owner);
@@ -591,26 +592,24 @@ __device__ __forceinline__ void team_sync(int W, int team) {
     }
 }
 
-// The nearest-rank 1st and 99th percentiles of the cnt valid elements in the
-// team's slots (ranks k_lo = ceil(cnt/100) - 1 and k_hi = ceil(99 cnt/100) - 1,
-// 0-based): four rounds of 8-bit radix selection over order keys, most
-// significant byte first.  Round 0 builds one histogram of every element's top
-// byte; later rounds count only the elements that share the bytes already
-// fixed for each rank.  `hist` is the team's kHistTeamWords words; `round`
-// counts rounds across calls so the three buffers rotate: a round fills one
-// buffer, and after the barrier clears the one filled two rounds earlier,
-// which every warp has finished reading.  cnt > 0; every thread of the team
-// calls this together.
-__device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint32_t cnt, int tt,
-                                                 int team_threads, int W, int team, int lane,
-                                                 uint32_t *hist, uint32_t &round, float &lo,
-                                                 float &hi) {
-    uint32_t r_lo = (cnt + 99u) / 100u - 1u, r_hi = (99u * cnt + 99u) / 100u - 1u;
+// Full radix selection: the nearest-rank 1st and 99th percentiles of the cnt
+// valid elements in the team's slots (ranks r_lo, r_hi, 0-based), by four
+// rounds of 8-bit selection over order keys, most significant byte first.
+// Round 0 builds one histogram of every element's top byte; later rounds
+// count only the elements sharing the bytes already fixed for each rank.  The
+// three buffers of `region` (3 x 2 x kHistWords words, all zero on entry)
+// rotate: a round fills one, and after the barrier clears the one filled two
+// rounds earlier, which every warp has finished reading.  Every thread of the
+// team calls this together; `region` is left with arbitrary contents.
+__device__ __forceinline__ void team_radix_select(const float4 (&p)[kSlots], uint32_t cnt, int tt,
+                                                  int team_threads, int W, int team, int lane,
+                                                  uint32_t *region, uint32_t r_lo, uint32_t r_hi,
+                                                  uint32_t &key_lo, uint32_t &key_hi) {
     uint32_t pre_lo = 0u, pre_hi = 0u;
 #pragma unroll
-    for (int pass = 0; pass < 4; ++pass, ++round) {
+    for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        uint32_t *h = hist + (round % 3u) * (2 * kHistWords);
+        uint32_t *h = region + (pass % 3) * (2 * kHistWords);
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
 #pragma unroll
@@ -630,13 +629,188 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
             }
         }
         team_sync(W, team);
-        pre_lo |= hist_find(h, r_lo, lane) << shift;
-        pre_hi |= hist_find(pass == 0 ? h : h + kHistWords, r_hi, lane) << shift;
-        uint32_t *old = hist + ((round + 2u) % 3u) * (2 * kHistWords);
+        pre_lo |= hist_find<kHistWords / 32>(h, r_lo, lane) << shift;
+        pre_hi |= hist_find<kHistWords / 32>(pass == 0 ? h : h + kHistWords, r_hi, lane) << shift;
+        uint32_t *old = region + ((pass + 2) % 3) * (2 * kHistWords);
         for (int i = tt; i < 2 * kHistWords; i += team_threads) old[i] = 0u;
     }
-    lo = key_value(pre_lo);
-    hi = key_value(pre_hi);
+    key_lo = pre_lo;
+    key_hi = pre_hi;
+}
+
+// The element of rank r (0-based, by key) among the m keys of `list`; every
+// lane of the calling warp gets it.  Each lane ranks its own candidates
+// against the whole list (broadcast reads), so a value with fewer than r + 1
+// keys below it and more than r keys at or below it is the answer.
+__device__ __forceinline__ uint32_t list_select(const uint32_t *list, uint32_t m, uint32_t r,
+                                                int lane) {
+    uint32_t ans = 0u;
+    bool found = false;
+    for (uint32_t i = static_cast<uint32_t>(lane); i < m; i += 32u) {
+        const uint32_t x = list[i];
+        uint32_t less = 0u, leq = 0u;
+        for (uint32_t j = 0; j < m; ++j) {
+            const uint32_t y = list[j];
+            less += y < x ? 1u : 0u;
+            leq += y <= x ? 1u : 0u;
+        }
+        if (less <= r && r < leq) {
+            ans = x;
+            found = true;
+        }
+    }
+    const uint32_t who = __ballot_sync(kFull, found);
+    return __shfl_sync(kFull, ans, __ffs(who) - 1);
+}
+
+// Layout of a team's selection region (words): two sets (alternating between
+// buckets) of three 256-bin histograms (top key byte; second byte for each
+// rank); the short lists of keys sharing both bytes; two sets of counters; the
+// results; the two candidate lists of bucket / 4 keys each.  The full radix
+// selection overlays the two histogram sets with its three rotating buffers.
+constexpr int kShortCap = 64;
+constexpr int kSelSet = 3 * kHistWords;
+static_assert(2 * kSelSet == kHistTeamWords, "the radix buffers overlay the histogram sets");
+constexpr int kSelShortLo = 2 * kSelSet, kSelShortHi = kSelShortLo + kShortCap;
+constexpr int kSelCount = kSelShortHi + kShortCap;  // 2 sets x (list lo, list hi, short lo, short hi)
+constexpr int kSelResult = kSelCount + 8;
+constexpr int kSelLists = kSelResult + 4;
+
+__host__ __device__ constexpr int sel_region_words(uint32_t bucket) {
+    return kSelLists + 2 * static_cast<int>(bucket / 4u);
+}
+
+// The element of rank r among the keys of `list` that have top 16 bits `pre`,
+// computed by one warp: the matching keys are gathered into `sub` (ballot
+// compaction), then each lane ranks its own against all of them.  Returns
+// false if more than kShortCap keys match (the caller falls back).
+__device__ __forceinline__ bool list_select16(const uint32_t *list, uint32_t m, uint32_t pre,
+                                              uint32_t r, uint32_t *sub, int lane,
+                                              uint32_t &out) {
+    uint32_t ms = 0u;
+    for (uint32_t i0 = 0; i0 < m; i0 += 32u) {
+        const uint32_t i = i0 + static_cast<uint32_t>(lane);
+        const uint32_t x = i < m ? list[i] : 0u;
+        const bool hit = i < m && (x >> 16) == pre;
+        const uint32_t mask = __ballot_sync(kFull, hit);
+        const uint32_t at = ms + __popc(mask & ((1u << lane) - 1u));
+        if (hit && at < kShortCap) sub[at] = x;
+        ms += __popc(mask);
+    }
+    if (ms > kShortCap) return false;
+    __syncwarp();
+    out = list_select(sub, ms, r, lane);
+    return true;
+}
+
+// The nearest-rank 1st and 99th percentiles of the cnt valid elements in the
+// team's slots: ranks k_lo = ceil(cnt/100) - 1 and k_hi = ceil(99 cnt/100) - 1
+// (0-based).  Round 0 histograms every element's top key byte; every warp finds
+// the bins holding the two ranks.  Round 1 histograms the second byte of the
+// elements in those bins, one histogram per rank, and appends their keys to a
+// list per rank.  After the barrier one warp per rank finds the second byte,
+// gathers the listed keys sharing both bytes (a handful for spread-out data)
+// and selects the exact element among them.  Buckets whose bin holds more than
+// a quarter of the bucket, or whose two-byte prefix is shared by more than
+// kShortCap keys (constant buckets, heavy ties), take the full radix
+// selection.  Histograms and counters alternate between two sets (`parity`,
+// flipped per call): a set is cleared after the third barrier of one bucket and
+// next used, already clear, by the bucket after, so the fast path needs three
+// barriers.  cnt > 0; every thread of the team calls this together.  FULL:
+// every slot is valid.
+template <bool FULL>
+__device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint32_t cnt, uint32_t bucket,
+                                                 int tt, int team_threads, int W, int team,
+                                                 int warp_in_team, int lane, uint32_t *region,
+                                                 uint32_t &parity, float &lo, float &hi) {
+    const uint32_t k_lo = (cnt + 99u) / 100u - 1u, k_hi = (99u * cnt + 99u) / 100u - 1u;
+    const uint32_t cap = bucket / 4u;
+    uint32_t *set = region + parity * kSelSet;
+    uint32_t *hist0 = set, *hist_lo = set + kHistWords, *hist_hi = set + 2 * kHistWords;
+    uint32_t *count = region + kSelCount + 4 * parity;
+    uint32_t *list_lo = region + kSelLists, *list_hi = list_lo + cap;
+    uint32_t key[kSlots][4];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            key[s][c] = order_key(get(p[s], c));
+            const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
+            if (FULL || j < cnt) hist_add(hist0, key[s][c] >> 24);
+        }
+    }
+    team_sync(W, team);  // (1)
+    uint32_t r_lo = k_lo, r_hi = k_hi;
+    const uint32_t b_lo = hist_find<kHistWords / 32>(hist0, r_lo, lane);
+    const uint32_t b_hi = hist_find<kHistWords / 32>(hist0, r_hi, lane);
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
+            const uint32_t top = key[s][c] >> 24, d = (key[s][c] >> 16) & 0xFFu;
+            if ((FULL || j < cnt) && top == b_lo) {
+                hist_add(hist_lo, d);
+                const uint32_t at = atomicAdd(count, 1u);
+                if (at < cap) list_lo[at] = key[s][c];
+            }
+            if ((FULL || j < cnt) && top == b_hi) {
+                hist_add(hist_hi, d);
+                const uint32_t at = atomicAdd(count + 1, 1u);
+                if (at < cap) list_hi[at] = key[s][c];
+            }
+        }
+    }
+    team_sync(W, team);  // (2)
+    const uint32_t m_lo = count[0], m_hi = count[1];
+    bool fast = m_lo <= cap && m_hi <= cap;
+    uint32_t key_lo = 0u, key_hi = 0u;
+    if (fast) {
+        // the selecting warps flag an overflowing short list in the counters
+        if (warp_in_team == 0) {
+            const uint32_t pre = (b_lo << 8) | hist_find<kHistWords / 32>(hist_lo, r_lo, lane);
+            uint32_t x = 0u;
+            const bool ok = list_select16(list_lo, m_lo, pre, r_lo, region + kSelShortLo, lane, x);
+            if (lane == 0) {
+                region[kSelResult] = x;
+                count[2] = ok ? 0u : 1u;
+            }
+        }
+        if (warp_in_team == (W > 1 ? 1 : 0)) {
+            const uint32_t pre = (b_hi << 8) | hist_find<kHistWords / 32>(hist_hi, r_hi, lane);
+            uint32_t x = 0u;
+            const bool ok = list_select16(list_hi, m_hi, pre, r_hi, region + kSelShortHi, lane, x);
+            if (lane == 0) {
+                region[kSelResult + 1] = x;
+                count[3] = ok ? 0u : 1u;
+            }
+        }
+        team_sync(W, team);  // (3)
+        fast = count[2] == 0u && count[3] == 0u;
+        key_lo = region[kSelResult];
+        key_hi = region[kSelResult + 1];
+    }
+    if (fast) {
+        // this set is next used two buckets from now; the other set and its
+        // counters were cleared during the previous bucket
+        for (int i = tt; i < kSelSet; i += team_threads) set[i] = 0u;
+        if (tt == 0) {
+            uint32_t *other = region + kSelCount + 4 * (parity ^ 1u);
+            other[0] = other[1] = other[2] = other[3] = 0u;
+        }
+    } else {
+        team_sync(W, team);  // every thread has read the counters
+        for (int i = tt; i < 2 * kSelSet; i += team_threads) region[i] = 0u;
+        team_sync(W, team);
+        team_radix_select(p, cnt, tt, team_threads, W, team, lane, region, k_lo, k_hi, key_lo, key_hi);
+        team_sync(W, team);  // every warp is done with the last round's buffer
+        for (int i = tt; i < 2 * kSelSet; i += team_threads) region[i] = 0u;
+        for (int i = tt; i < 8; i += team_threads) region[kSelCount + i] = 0u;
+        team_sync(W, team);  // all clear before the next bucket
+    }
+    parity ^= 1u;
+    lo = key_value(key_lo);
+    hi = key_value(key_hi);
 }
 
 }  // namespace qc

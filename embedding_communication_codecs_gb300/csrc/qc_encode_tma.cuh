@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
         fence_barrier_init();
     }
     if constexpr (SCHEME == kClip) {
-        for (int i = threadIdx.x; i < teams * kHistTeamWords; i += kBlock) hist[i] = 0u;
+        for (int i = threadIdx.x; i < teams * sel_region_words(P.bucket); i += kBlock) hist[i] = 0u;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
     const PhiloxKeys &keys = P.keys;
 
     int buf = 0;
-    uint32_t round = 0;  // CLIP: selection rounds so far (rotates the histogram buffers)
+    uint32_t sel_parity = 0;  // CLIP: which histogram set the team's next bucket uses
     uint32_t it = 0;
     bool failed = false;
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
@@ -171,9 +171,13 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                 if constexpr (SCHEME != kClip) accumulate_slots<SCHEME>(st, p, tt, team_threads, cnt);
             }
             if constexpr (SCHEME == kClip) {
-                if (cnt)
-                    team_percentiles(p, cnt, tt, team_threads, W, team, lane,
-                                     hist + team * kHistTeamWords, round, st.mn, st.mx);
+                uint32_t *region = hist + team * sel_region_words(P.bucket);
+                if (whole)
+                    team_percentiles<true>(p, cnt, P.bucket, tt, team_threads, W, team, warp % W,
+                                           lane, region, sel_parity, st.mn, st.mx);
+                else if (cnt)
+                    team_percentiles<false>(p, cnt, P.bucket, tt, team_threads, W, team, warp % W,
+                                            lane, region, sel_parity, st.mn, st.mx);
             } else {
                 team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
             }
@@ -215,7 +219,7 @@ cudaError_t launch_one(const EncodeParams &p, const EncodeTiles &g, cudaStream_t
     auto fn = &encode_tma_kernel<SCHEME, BITS, SR, TIn, EF>;
     size_t smem = encode_tiles_smem(g, sizeof(Stats<SCHEME>));
     if (SCHEME == kClip)
-        smem += static_cast<size_t>((kBlock / 32) / p.team_warps) * kHistTeamWords * 4u;
+        smem += static_cast<size_t>((kBlock / 32) / p.team_warps) * sel_region_words(p.bucket) * 4u;
     cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
     if (e != cudaSuccess) return e;
     const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kBlock, g.ntiles, smem);
