@@ -71,6 +71,8 @@ def _L():
         lib.oracle_encode_qsgd.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P]
         lib.oracle_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I]
         lib.oracle_sign_vote.argtypes = [P, S, I, S, P]
+        lib.oracle_topk_encode.argtypes = [P, I, P, S, U64, S, S, I, U64, U32, P, P, P, P]
+        lib.oracle_topk_decode.argtypes = [P, P, S, P, P, S, I, S, S, S, P, I]
         lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_f32.restype = ctypes.c_float
         lib.oracle_e4m3_from_f32.argtypes = [ctypes.c_float]
@@ -83,6 +85,7 @@ def _L():
                      "oracle_encode_ternary",
                      "oracle_encode_qsgd",
                      "oracle_decode_accumulate", "oracle_sign_vote", "oracle_rowwise_fp8",
+                     "oracle_topk_encode", "oracle_topk_decode",
                      "oracle_rowwise_fp8_dequant"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -244,6 +247,45 @@ def reencode(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM,
     else:
         c, s = encode_qsgd(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed, step=step)
     return r, c, s, None
+
+
+def topk_encode(grad, err=None, *, bucket, keep, mode=ROUND_NEAREST, seed=0, step=0,
+                index_base=0):
+    """Per-bucket top-k (largest |p|, ties to the lower index) with 8-bit codes of
+    the kept values; returns (idx uint32[nb*keep], codes uint8[nb*keep], scale,
+    offset) and updates ``err``."""
+    g = np.ascontiguousarray(grad)
+    n = g.size
+    if err is not None:
+        assert err.dtype == np.float32 and err.flags.c_contiguous and err.size == n
+    nb = num_buckets(n, bucket)
+    idx = np.zeros(max(nb * keep, 1), dtype=np.uint32)
+    codes = np.zeros(max(nb * keep, 1), dtype=np.uint8)
+    scale = np.zeros(max(nb, 1), dtype=np.float32)
+    offset = np.zeros(max(nb, 1), dtype=np.float32)
+    rc = _L().oracle_topk_encode(_ptr(g), _grad_dtype(g), _ptr(err), n, index_base, bucket, keep,
+                                 mode, seed, step, _ptr(idx), _ptr(codes), _ptr(scale),
+                                 _ptr(offset))
+    _check(rc, "topk_encode")
+    return idx[:nb * keep], codes[:nb * keep], scale[:nb], offset[:nb]
+
+
+def topk_decode(idx, codes, scale, offset, *, M, n, bucket, keep, flags=OUT_SUM,
+                pair_stride=None, meta_stride=None, out=None):
+    i = np.ascontiguousarray(idx, dtype=np.uint32)
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    o = np.ascontiguousarray(offset, dtype=np.float32)
+    if pair_stride is None:
+        pair_stride = i.shape[-1] if i.ndim == 2 else num_buckets(n, bucket) * keep
+    if meta_stride is None:
+        meta_stride = s.shape[-1] if s.ndim == 2 else num_buckets(n, bucket)
+    if out is None:
+        out = np.zeros(n, dtype=np.float32)
+    rc = _L().oracle_topk_decode(_ptr(i), _ptr(c), pair_stride, _ptr(s), _ptr(o), meta_stride, M,
+                                 n, bucket, keep, _ptr(out), flags)
+    _check(rc, "topk_decode")
+    return out
 
 
 def sign_vote(signs, *, M, n, stride_words=None):

@@ -579,6 +579,174 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
 }
 
 /* ------------------------------------------------------------------------ */
+/* Top-k sparsification with 8-bit quantization of the kept values and error
+ * feedback, per bucket.
+ *
+ * p2 "Quantization Schemes" (Top-K Sparsification: send only the largest K% of
+ * gradients, combined with quantization; Error Feedback: accumulate the errors
+ * locally); p3 "Combination with Other Techniques" (quantize the sparse
+ * gradients); p4 intro and "Why sparsification fights the all-reduce" (the
+ * largest-magnitude coordinates travel as index-value pairs).  Readings: the
+ * largest K are taken per bucket (like every other statistic here, and giving
+ * a fixed payload per bucket); order by |p| descending, ties to the lower
+ * index; the kept values are quantized with the uniform 8-bit formulas over
+ * their own min..max; an element not kept stays whole in the residual.
+ * Per bucket k (cnt elements, K = min(keep, cnt)):
+ *   p_i = e_i + g_i (or g_i)
+ *   kept = the first K of the bucket's elements ordered by (|p| desc, i asc)
+ *   mn, mx = min, max of p over kept (zero taken as +0); scale = (mx - mn)/255
+ *   q, deq: as oracle_encode_uniform (8 bits) for each kept element
+ *   e_i = kept ? p_i - deq_i : p_i
+ * Outputs: slot t < K of bucket k holds the t-th kept element in ascending
+ * index order: idx[k*keep + t] = its global index (index_base + i),
+ * codes[k*keep + t] = q; slots t >= K hold index 0xFFFFFFFF and code 0;
+ * scale[k], offset[k] = mn. */
+typedef struct {
+    float mag;
+    uint32_t j;
+} orc_mag_index;
+
+static int orc_cmp_topk(const void *a, const void *b)
+{
+    const orc_mag_index *x = (const orc_mag_index *)a, *y = (const orc_mag_index *)b;
+    if (x->mag != y->mag)
+        return x->mag > y->mag ? -1 : 1; /* larger magnitude first */
+    return (x->j > y->j) - (x->j < y->j); /* then the lower index */
+}
+
+ORC_API int oracle_topk_encode(const void *grad, int dtype, float *err, size_t n,
+                               uint64_t index_base, size_t bucket, size_t keep, int mode,
+                               uint64_t seed, uint32_t step, uint32_t *idx_out,
+                               uint8_t *codes_out, float *scale_out, float *offset_out)
+{
+    if (!orc_valid_bucket(bucket) || keep < 1 || keep > bucket)
+        return -1;
+    const float Lf = 255.0f;
+    float *p = (float *)malloc(bucket * sizeof(float));
+    orc_mag_index *order = (orc_mag_index *)malloc(bucket * sizeof(orc_mag_index));
+    unsigned char *kept = (unsigned char *)malloc(bucket);
+    if (!p || !order || !kept) {
+        free(p);
+        free(order);
+        free(kept);
+        return -2;
+    }
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        size_t K = keep < cnt ? keep : cnt;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+            order[j].mag = fabsf(p[j]);
+            order[j].j = (uint32_t)j;
+            kept[j] = 0;
+        }
+        qsort(order, cnt, sizeof(orc_mag_index), orc_cmp_topk);
+        for (size_t t = 0; t < K; ++t)
+            kept[order[t].j] = 1;
+        float mn = 0.0f, mx = 0.0f;
+        int first = 1;
+        for (size_t j = 0; j < cnt; ++j) {
+            if (!kept[j])
+                continue;
+            if (first || p[j] < mn)
+                mn = p[j];
+            if (first || p[j] > mx)
+                mx = p[j];
+            first = 0;
+        }
+        mn = orc_positive_zero(mn);
+        mx = orc_positive_zero(mx);
+        float scale = (mx - mn) / Lf;
+        size_t t = 0;
+        for (size_t j = 0; j < cnt; ++j) {
+            if (!kept[j]) {
+                if (err)
+                    err[lo + j] = p[j];
+                continue;
+            }
+            uint32_t q = 0;
+            if (scale != 0.0f) {
+                float t_ = (p[j] - mn) / scale;
+                float level;
+                if (mode == ORC_ROUND_NEAREST) {
+                    level = rintf(t_);
+                } else {
+                    float f = floorf(t_);
+                    float frac = t_ - f;
+                    float u = oracle_uniform(seed, step, index_base + lo + j);
+                    level = (u < frac) ? f + 1.0f : f;
+                }
+                if (!(level >= 0.0f))
+                    level = 0.0f;
+                q = (level > Lf) ? 255u : (uint32_t)level;
+            }
+            idx_out[k * keep + t] = (uint32_t)(index_base + lo + j);
+            codes_out[k * keep + t] = (uint8_t)q;
+            ++t;
+            if (err) {
+                float deq = fmaf((float)q, scale, mn);
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        for (; t < keep; ++t) {
+            idx_out[k * keep + t] = 0xFFFFFFFFu;
+            codes_out[k * keep + t] = 0;
+        }
+        scale_out[k] = scale;
+        offset_out[k] = mn;
+    }
+    free(p);
+    free(order);
+    free(kept);
+    return 0;
+}
+
+/* Receiver of top-k payloads: scatter and accumulate M workers' index-value
+ * pairs into a dense fp32 vector in fixed worker order ("Why sparsification
+ * fights the all-reduce": the exchange is an all-gather of index-value pairs).
+ *   acc_i = +0 for every i
+ *   for w = 0 .. M-1, for each bucket k, for each slot t:
+ *       i = idx_w[k*keep + t]; skipped unless k*bucket <= i < min((k+1)*bucket, n)
+ *       acc_i = acc_i + fma(code, scale_w[k], offset_w[k])
+ *   r = mean ? acc / M : acc ;  out_i = accumulate ? out_i + r : r
+ * Worker w's pairs start at w * pair_stride, its metadata at w * meta_stride. */
+ORC_API int oracle_topk_decode(const uint32_t *idx, const uint8_t *codes, size_t pair_stride,
+                               const float *scale, const float *offset, size_t meta_stride, int M,
+                               size_t n, size_t bucket, size_t keep, float *out, int flags)
+{
+    if (M < 1 || !orc_valid_bucket(bucket) || keep < 1 || keep > bucket)
+        return -1;
+    float *acc = (float *)calloc(n ? n : 1, sizeof(float));
+    if (!acc)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (int w = 0; w < M; ++w) {
+        for (size_t k = 0; k < nb; ++k) {
+            size_t lo = k * bucket;
+            size_t hi = (n - lo < bucket) ? n : lo + bucket;
+            float s = scale[(size_t)w * meta_stride + k];
+            float o = offset[(size_t)w * meta_stride + k];
+            for (size_t t = 0; t < keep; ++t) {
+                size_t at = (size_t)w * pair_stride + k * keep + t;
+                uint32_t i = idx[at];
+                if (i < lo || i >= hi)
+                    continue;
+                acc[i] = acc[i] + fmaf((float)codes[at], s, o);
+            }
+        }
+    }
+    for (size_t i = 0; i < n; ++i) {
+        float r = (flags & ORC_OUT_MEAN) ? acc[i] / (float)M : acc[i];
+        out[i] = (flags & ORC_ACCUMULATE_INTO_OUT) ? out[i] + r : r;
+    }
+    free(acc);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* signSGD majority vote (p3 "Quantized SGD Algorithms"; p4 "Why sparsification
  * fights the all-reduce"): out bit i = [2 * (number of workers with bit i set)
  * >= M].  A tie (even M) gives 1, matching sign(0) = +1 (a reading).  Bits past

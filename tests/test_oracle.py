@@ -824,3 +824,109 @@ def test_clip_payload_decodes_as_uniform():
     b = orc.decode_accumulate(c, s, o, M=1, n=g.size, bits=4, bucket=512,
                               scheme=orc.SCHEME_UNIFORM)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ top-k
+
+def _topk_expected(p, bucket, keep):
+    """Kept indices per bucket from numpy's lexsort: |p| descending, then index."""
+    out = []
+    for lo in range(0, p.size, bucket):
+        seg = p[lo:lo + bucket]
+        order = np.lexsort((np.arange(seg.size), -np.abs(seg.astype(np.float64))))
+        kept = np.sort(order[:min(keep, seg.size)]) + lo
+        out.append(np.concatenate([kept, np.full(keep - kept.size, 0xFFFFFFFF)]).astype(np.uint32))
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("bucket,keep,n", [(32, 1, 100), (512, 5, 3000), (1024, 10, 5000),
+                                           (2048, 100, 2048 * 3 + 7), (64, 64, 200)])
+def test_topk_kept_set_brute_force(bucket, keep, n):
+    g = wl.outlier_gradient(n, seed=bucket + keep)
+    idx, codes, s, o = orc.topk_encode(g, bucket=bucket, keep=keep)
+    assert np.array_equal(idx, _topk_expected(g, bucket, keep))
+    assert np.all(codes[idx == 0xFFFFFFFF] == 0)
+
+
+@pytest.mark.parametrize("mode", [orc.ROUND_NEAREST, orc.ROUND_STOCHASTIC])
+def test_topk_keep_all_is_the_uniform_8bit_scheme(mode):
+    """Keeping every element of every bucket reduces to the uniform 8-bit encoder:
+    same codes in index order, same scale, offset and residual."""
+    bucket = 256
+    g = wl.outlier_gradient(bucket * 5, seed=21)
+    e1, e2 = np.zeros(g.size, np.float32), np.zeros(g.size, np.float32)
+    idx, codes, s, o = orc.topk_encode(g, e1, bucket=bucket, keep=bucket, mode=mode, seed=4, step=2)
+    c_u, s_u, o_u = orc.encode_uniform(g, e2, bits=8, bucket=bucket, mode=mode, seed=4, step=2)
+    assert np.array_equal(idx, np.arange(g.size, dtype=np.uint32))
+    assert np.array_equal(codes, c_u.view(np.uint8))
+    assert np.array_equal(s, s_u) and np.array_equal(o, o_u) and np.array_equal(e1, e2)
+
+
+def test_topk_ties_go_to_the_lower_index():
+    bucket, keep = 128, 7
+    g = np.where(np.arange(bucket * 2) % 2, 1.0, -1.0).astype(np.float32)
+    g[bucket + 100] = 3.0
+    idx, _, _, _ = orc.topk_encode(g, bucket=bucket, keep=keep)
+    assert list(idx[:keep]) == list(range(keep))
+    assert list(idx[keep:]) == sorted([bucket + 100] + list(range(bucket, bucket + keep - 1)))
+
+
+def test_topk_residual_keeps_what_was_not_sent():
+    """Dropped elements stay whole in the residual; kept ones leave p - deq, with
+    deq the exact fma of code, scale and offset rounded once."""
+    bucket, keep = 512, 9
+    g = wl.outlier_gradient(bucket * 3, seed=22)
+    e0 = (wl.std_normal(5, 1, g.size) * np.float32(1e-3)).astype(np.float32)
+    err = e0.copy()
+    idx, codes, s, o = orc.topk_encode(g, err, bucket=bucket, keep=keep)
+    p = (e0 + g).astype(np.float32)
+    sent = np.zeros(g.size, bool)
+    sent[idx[idx != 0xFFFFFFFF]] = True
+    assert np.array_equal(err[~sent], p[~sent])
+    for t, i in enumerate(idx):
+        k = int(i) // bucket
+        deq = to_f32(Fraction(int(codes[t])) * Fraction(float(s[k])) + Fraction(float(o[k])))
+        assert err[i] == np.float32(p[i] - deq)
+
+
+def test_topk_error_feedback_delays_not_loses():
+    """Over steps, everything sent plus the final residual adds up to the sum of
+    the gradients (to fp32 rounding of the accumulations)."""
+    bucket, keep, n, steps = 256, 4, 1024, 30
+    err = np.zeros(n, np.float32)
+    sent = np.zeros(n, np.float64)
+    total = np.zeros(n, np.float64)
+    for t in range(steps):
+        g = wl.std_normal(100 + t, 1, n) * np.float32(1e-2)
+        total += g
+        idx, codes, s, o = orc.topk_encode(g, err, bucket=bucket, keep=keep)
+        sent += orc.topk_decode(idx, codes, s, o, M=1, n=n, bucket=bucket, keep=keep)
+    assert np.allclose(sent + err, total, atol=1e-5)
+
+
+def test_topk_decode_scatter_order_and_skips():
+    """Hand-built pairs: sentinel and out-of-bucket indices are skipped; two
+    workers adding to the same element accumulate in worker order."""
+    n, bucket, keep = 40, 32, 3
+    idx = np.array([[5, 31, 0xFFFFFFFF, 32, 39, 3],            # worker 0: 3 is outside bucket 1
+                    [5, 6, 40, 33, 0xFFFFFFFF, 0xFFFFFFFF]],   # worker 1: 40 is past n
+                   dtype=np.uint32)
+    codes = np.array([[2, 1, 9, 4, 1, 7], [1, 3, 5, 2, 0, 0]], dtype=np.uint8)
+    scale = np.array([[1.0, 2.0], [0.5, 0.25]], dtype=np.float32)
+    offset = np.array([[0.0, -1.0], [1.0, 0.0]], dtype=np.float32)
+    out = orc.topk_decode(idx, codes, scale, offset, M=2, n=n, bucket=bucket, keep=keep)
+    want = np.zeros(n, np.float32)
+    want[5] = 2.0 + 1.5
+    want[31] = 1.0
+    want[6] = 2.5
+    want[32] = 7.0
+    want[39] = 1.0
+    want[33] = 0.5
+    assert np.array_equal(out, want)
+    # fixed worker order: 1 + 2^-24 + 2^-24 rounds to 1 when added one by one
+    idx2 = np.array([[0], [0], [0]], dtype=np.uint32)
+    c2 = np.array([[1], [1], [1]], dtype=np.uint8)
+    s2 = np.array([[1.0], [2.0 ** -24], [2.0 ** -24]], dtype=np.float32)
+    o2 = np.zeros((3, 1), np.float32)
+    r = orc.topk_decode(idx2, c2, s2, o2, M=3, n=1, bucket=32, keep=1)
+    assert r[0] == np.float32(1.0)
