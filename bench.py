@@ -337,6 +337,67 @@ class Receiver(Component):
         return _split(go, n, self.bucket), 2 * self.M * n
 
 
+class TopkEF(Component):
+    """M workers' fp32 gradients sparsified to the largest 1 % per bucket with
+    8-bit codes and error feedback, then scattered and averaged by the receiver."""
+
+    def __init__(self, name="topk_ef", n=25_600_000, M=8, bucket=1024, keep=10, seed=3):
+        self.name, self.n, self.M, self.bucket, self.keep, self.seed = name, n, M, bucket, keep, seed
+        nb = _nb(n, bucket)
+        self.kernels = {"topk_encode_ef": (M, 12 * n + 5 * nb * keep + 8 * nb),
+                        f"topk_decode_m{M}": (1, M * (5 * nb * keep + 8 * nb) + 4 * n)}
+        self.units = 2 * M * n
+        self.h2d = 4 * M * n
+        self.d2h = 4 * n
+
+    def setup(self, q, torch):
+        self.g = torch.from_numpy(wl.shared_mean_gradients(self.n, self.M, self.seed)).cuda()
+        self.err = torch.zeros((self.M, self.n), device="cuda")
+        nb = _nb(self.n, self.bucket)
+        self.slots = nb * self.keep
+        self.idx = torch.empty((self.M, self.slots), dtype=torch.int32, device="cuda")
+        self.codes = torch.empty((self.M, self.slots), dtype=torch.uint8, device="cuda")
+        self.scale = torch.empty((self.M, nb), device="cuda")
+        self.offset = torch.empty((self.M, nb), device="cuda")
+        self.out = torch.empty(self.n, device="cuda")
+
+    def run(self, q, t, timer):
+        for w in range(self.M):
+            with timer("topk_encode_ef"):
+                q.qc_topk_encode_ef(self.g[w], self.err[w], self.n, self.bucket, self.keep,
+                                    q.QC_ROUND_NEAREST, 0, t, self.idx[w], self.codes[w],
+                                    self.scale[w], self.offset[w])
+        with timer(f"topk_decode_m{self.M}"):
+            q.qc_topk_decode_accumulate(self.idx, self.codes, self.slots, self.scale, self.offset,
+                                        self.scale.shape[1], self.M, self.n, self.bucket, self.keep,
+                                        self.out, q.QC_OUT_MEAN)
+
+    def host_inputs(self):
+        return [self.g]
+
+    def host_outputs(self):
+        return [self.out]
+
+    def kernel_units(self):
+        return {"topk_encode_ef": self.n, f"topk_decode_m{self.M}": self.M * self.n}
+
+    def oracle_sample(self, frac):
+        import oracle as orc
+        n = max(self.bucket, int(self.n * frac) // self.bucket * self.bucket)
+        gw = wl.shared_mean_gradients(n, self.M, self.seed)
+
+        def go(lo, hi):
+            parts = []
+            for w in range(self.M):
+                parts.append(orc.topk_encode(gw[w, lo:hi], np.zeros(hi - lo, np.float32),
+                                             bucket=self.bucket, keep=self.keep, index_base=0))
+            orc.topk_decode(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]),
+                            np.stack([p[2] for p in parts]), np.stack([p[3] for p in parts]),
+                            M=self.M, n=hi - lo, bucket=self.bucket, keep=self.keep,
+                            flags=orc.OUT_MEAN)
+        return _split(go, n, self.bucket), 2 * self.M * n
+
+
 class Reencode(Receiver):
     """M workers' bf16 gradients encoded without error feedback, then the
     receiver's fused decode + MEAN + re-encode with its own residual (the
@@ -441,6 +502,8 @@ def make_workload(name):
                                        scheme=3)],
         "rx_reencode_u8": lambda: [Reencode("rx_reencode_u8", 0, 8)],
         "rx_reencode_ternary": lambda: [Reencode("rx_reencode_ternary", 2, 2)],
+        "topk_ef": lambda: [TopkEF()],
+        "probe_topk_ef": lambda: [TopkEF(n=1 << 24, M=2)],
         "u8_ef_small": lambda: [UniformEF("u8_ef_small", 1 << 20, 8, 2048, False, 0, "outlier")],
         "clip8_ef_small": lambda: [UniformEF("clip8_ef_small", 1 << 20, 8, 2048, False, 0,
                                              "outlier", scheme=4)],

@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ER
 
 # Every symbol the C ABI exports, in header order.
 EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
-           "qc_reencode", "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
+           "qc_reencode", "qc_topk_encode_ef", "qc_topk_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
            "qc_last_error", "qc_version")
 
 
@@ -56,10 +56,13 @@ def _load():
     lib.qc_encode_ef.argtypes = [P, I, P, S, I, S, I, I, U64, U32, P, P, P, P]
     lib.qc_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I, P]
     lib.qc_reencode.argtypes = [P, S, P, P, S, I, S, I, S, I, I, P, I, U64, U32, P, P, P, P, P]
+    lib.qc_topk_encode_ef.argtypes = [P, I, P, S, S, U32, I, U64, U32, P, P, P, P, P]
+    lib.qc_topk_decode_accumulate.argtypes = [P, P, S, P, P, S, I, S, S, U32, P, I, P]
     lib.qc_sign_vote.argtypes = [P, S, I, S, P, P]
     lib.qc_rowwise_fp8.argtypes = [P, S, S, P, P, P]
     lib.qc_rowwise_fp8_dequant.argtypes = [P, P, S, S, P, P]
-    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_reencode", "qc_sign_vote",
+    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_reencode", "qc_topk_encode_ef",
+                 "qc_topk_decode_accumulate", "qc_sign_vote",
                  "qc_rowwise_fp8",
                  "qc_rowwise_fp8_dequant"):
         getattr(lib, name).restype = I
@@ -157,6 +160,23 @@ def qc_reencode(codes, codes_stride_words, scale, offset, meta_stride, M, n, bit
                            meta_stride, M, n, bits, bucket, scheme, flags, _ptr(err), mode, seed,
                            step, _ptr(codes_out), _ptr(scale_out), _ptr(offset_out), _ptr(out),
                            _stream(stream)))
+
+
+def qc_topk_encode_ef(grad, err, n, bucket, keep, mode, seed, step, idx, codes, scale, offset,
+                      stream=None, dtype=None):
+    """Top-k sparsification per bucket with 8-bit codes of the kept values and
+    error feedback (``err`` may be None); outputs keep slots per bucket."""
+    _check(lib.qc_topk_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bucket, keep,
+                                 mode, seed, step, _ptr(idx), _ptr(codes), _ptr(scale),
+                                 _ptr(offset), _stream(stream)))
+
+
+def qc_topk_decode_accumulate(idx, codes, pair_stride, scale, offset, meta_stride, M, n, bucket,
+                              keep, out, flags=QC_OUT_SUM, stream=None):
+    """Scatter M workers' top-k pairs into a dense fp32 vector in worker order."""
+    _check(lib.qc_topk_decode_accumulate(_ptr(idx), _ptr(codes), pair_stride, _ptr(scale),
+                                         _ptr(offset), meta_stride, M, n, bucket, keep, _ptr(out),
+                                         flags, _stream(stream)))
 
 
 def qc_sign_vote(signs, stride_words, M, n, out, stream=None):

@@ -293,7 +293,7 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = 0;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
+    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() | qc::take_topk_errors() |
              qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }
@@ -514,6 +514,118 @@ qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const fl
     return from_cuda(qc::launch_reencode(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                          reinterpret_cast<cudaStream_t>(stream)),
                      fn);
+}
+
+qc_status qc_topk_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, size_t bucket,
+                            uint32_t keep, qc_round mode, uint64_t seed, uint32_t step,
+                            uint32_t *idx, uint8_t *codes, float *scale, float *offset,
+                            qc_stream_t stream) {
+    static const char *fn = "qc_topk_encode_ef";
+    if (dtype != QC_DTYPE_F32 && dtype != QC_DTYPE_BF16)
+        return fail(QC_ERR_INVALID_ARG, "%s: dtype %d is not F32 or BF16", fn, dtype);
+    if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
+        return fail(QC_ERR_INVALID_ARG, "%s: unknown rounding mode %d", fn, mode);
+    if (!valid_bucket(bucket))
+        return fail(QC_ERR_INVALID_ARG, "%s: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", fn, bucket);
+    if (keep < 1 || keep > bucket)
+        return fail(QC_ERR_INVALID_ARG, "%s: keep must be in [1, bucket] (got %u)", fn, keep);
+    if (bucket > 4096)
+        return fail(QC_ERR_UNSUPPORTED, "%s: buckets above 4096 elements are not supported", fn);
+    if (n == 0) return ok();
+    if (n >= (static_cast<size_t>(1) << 32))
+        return fail(QC_ERR_UNSUPPORTED, "%s: indices are 32-bit; n = %zu is too large", fn, n);
+    if (!grad || !idx || !codes || !scale || !offset)
+        return fail(QC_ERR_NULL, "%s: grad, idx, codes, scale and offset must be non-NULL", fn);
+    const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
+    if (!aligned(grad, 16))
+        return fail(QC_ERR_UNSUPPORTED, "%s: the gradient must be 16-byte aligned", fn);
+    if (err && !aligned(err, 16)) return fail(QC_ERR_ALIGNMENT, "%s: err must be 16-byte aligned", fn);
+    if (!aligned(idx, 4) || !aligned(scale, 4) || !aligned(offset, 4))
+        return fail(QC_ERR_ALIGNMENT, "%s: idx, scale and offset must be 4-byte aligned", fn);
+    const size_t nb = qc_num_buckets(n, bucket), slots = nb * keep;
+    const void *outs[4] = {idx, codes, scale, offset};
+    const size_t osz[4] = {slots * 4, slots, nb * 4, nb * 4};
+    for (int x = 0; x < 4; ++x) {
+        if (overlaps(outs[x], osz[x], grad, n * esize) || overlaps(outs[x], osz[x], err, n * 4))
+            return fail(QC_ERR_INVALID_ARG, "%s: an output overlaps grad or err", fn);
+        for (int y = x + 1; y < 4; ++y)
+            if (overlaps(outs[x], osz[x], outs[y], osz[y]))
+                return fail(QC_ERR_INVALID_ARG, "%s: outputs overlap each other", fn);
+    }
+    if (overlaps(err, n * 4, grad, n * esize)) return fail(QC_ERR_INVALID_ARG, "%s: err overlaps grad", fn);
+
+    qc::TopkParams t{};
+    t.e.grad = grad;
+    t.e.err = err;
+    t.e.n = n;
+    t.e.bucket = static_cast<uint32_t>(bucket);
+    t.e.nbuckets = nb;
+    t.e.team_warps = team_warps_for(bucket);
+    t.e.two_pass = 0;
+    t.e.seed = seed;
+    t.e.step = step;
+    t.e.keys = qc::philox_round_keys(seed);
+    t.e.scale = scale;
+    t.e.offset = offset;
+    t.keep = keep;
+    t.idx = idx;
+    t.codes8 = codes;
+    qc::EncodeTiles tiles{};
+    if (!encode_tiles_for(t.e, esize, err != nullptr, true, tiles))
+        return fail(QC_ERR_UNSUPPORTED, "%s: no tiling for this bucket", fn);
+    return from_cuda(qc::launch_topk_encode(t, tiles, mode == QC_ROUND_STOCHASTIC,
+                                            dtype == QC_DTYPE_BF16,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+qc_status qc_topk_decode_accumulate(const uint32_t *idx, const uint8_t *codes, size_t pair_stride,
+                                    const float *scale, const float *offset, size_t meta_stride,
+                                    int M, size_t n, size_t bucket, uint32_t keep, float *out,
+                                    int flags, qc_stream_t stream) {
+    static const char *fn = "qc_topk_decode_accumulate";
+    if (M < 1 || M > QC_MAX_WORKERS)
+        return fail(QC_ERR_INVALID_ARG, "%s: M must be in [1, %d] (got %d)", fn, QC_MAX_WORKERS, M);
+    if (flags & ~(QC_OUT_MEAN | QC_ACCUMULATE_INTO_OUT))
+        return fail(QC_ERR_INVALID_ARG, "%s: unknown flag bits 0x%x", fn, flags);
+    if (!valid_bucket(bucket))
+        return fail(QC_ERR_INVALID_ARG, "%s: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", fn, bucket);
+    if (keep < 1 || keep > bucket)
+        return fail(QC_ERR_INVALID_ARG, "%s: keep must be in [1, bucket] (got %u)", fn, keep);
+    if (bucket > 16384)
+        return fail(QC_ERR_UNSUPPORTED, "%s: buckets above 16384 elements are not supported", fn);
+    if (n == 0) return ok();
+    if (n >= (static_cast<size_t>(1) << 32))
+        return fail(QC_ERR_UNSUPPORTED, "%s: indices are 32-bit; n = %zu is too large", fn, n);
+    const size_t nb = qc_num_buckets(n, bucket), slots = nb * keep;
+    if (M > 1 && (pair_stride < slots || meta_stride < nb))
+        return fail(QC_ERR_INVALID_ARG, "%s: strides (%zu slots, %zu buckets) are shorter than one payload (%zu, %zu)",
+                    fn, pair_stride, meta_stride, slots, nb);
+    if (!idx || !codes || !scale || !offset || !out)
+        return fail(QC_ERR_NULL, "%s: idx, codes, scale, offset and out must be non-NULL", fn);
+    if (!aligned(idx, 4) || !aligned(scale, 4) || !aligned(offset, 4) || !aligned(out, 4))
+        return fail(QC_ERR_ALIGNMENT, "%s: idx, scale, offset and out must be 4-byte aligned", fn);
+    const size_t ps = M > 1 ? pair_stride : 0, ms = M > 1 ? meta_stride : 0;
+    const size_t span_p = (M - 1) * ps + slots, span_m = ((M - 1) * ms + nb) * 4;
+    if (overlaps(out, n * 4, idx, span_p * 4) || overlaps(out, n * 4, codes, span_p) ||
+        overlaps(out, n * 4, scale, span_m) || overlaps(out, n * 4, offset, span_m))
+        return fail(QC_ERR_INVALID_ARG, "%s: out overlaps an input", fn);
+    qc::TopkDecodeParams d{};
+    d.idx = idx;
+    d.codes8 = codes;
+    d.pair_stride = ps;
+    d.scale = scale;
+    d.offset = offset;
+    d.meta_stride = ms;
+    d.M = M;
+    d.n = n;
+    d.bucket = static_cast<uint32_t>(bucket);
+    d.nbuckets = nb;
+    d.keep = keep;
+    d.out = out;
+    d.flags = flags;
+    d.inv_m = (M & (M - 1)) == 0 ? 1.0f / static_cast<float>(M) : 0.0f;
+    return from_cuda(qc::launch_topk_decode(d, reinterpret_cast<cudaStream_t>(stream)), fn);
 }
 
 qc_status qc_sign_vote(const uint32_t *signs, size_t stride_words, int M, size_t n,

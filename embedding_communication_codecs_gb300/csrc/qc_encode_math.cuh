@@ -592,19 +592,19 @@ __device__ __forceinline__ void team_sync(int W, int team) {
     }
 }
 
-// Full radix selection: the nearest-rank 1st and 99th percentiles of the cnt
-// valid elements in the team's slots (ranks r_lo, r_hi, 0-based), by four
-// rounds of 8-bit selection over order keys, most significant byte first.
+// Full radix selection: the keys of ranks r_lo and r_hi (0-based, ascending)
+// among the cnt valid keys of the team's slots, by four rounds of 8-bit
+// selection, most significant byte first.
 // Round 0 builds one histogram of every element's top byte; later rounds
 // count only the elements sharing the bytes already fixed for each rank.  The
 // three buffers of `region` (3 x 2 x kHistWords words, all zero on entry)
 // rotate: a round fills one, and after the barrier clears the one filled two
 // rounds earlier, which every warp has finished reading.  Every thread of the
 // team calls this together; `region` is left with arbitrary contents.
-__device__ __forceinline__ void team_radix_select(const float4 (&p)[kSlots], uint32_t cnt, int tt,
-                                                  int team_threads, int W, int team, int lane,
-                                                  uint32_t *region, uint32_t r_lo, uint32_t r_hi,
-                                                  uint32_t &key_lo, uint32_t &key_hi) {
+__device__ __forceinline__ void team_radix_select(const uint32_t (&keys)[kSlots][4], uint32_t cnt,
+                                                  int tt, int team_threads, int W, int team,
+                                                  int lane, uint32_t *region, uint32_t r_lo,
+                                                  uint32_t r_hi, uint32_t &key_lo, uint32_t &key_hi) {
     uint32_t pre_lo = 0u, pre_hi = 0u;
 #pragma unroll
     for (int pass = 0; pass < 4; ++pass) {
@@ -616,7 +616,7 @@ __device__ __forceinline__ void team_radix_select(const float4 (&p)[kSlots], uin
             for (int c = 0; c < 4; ++c) {
                 const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
                 if (j < cnt) {
-                    const uint32_t key = order_key(get(p[s], c));
+                    const uint32_t key = keys[s][c];
                     const uint32_t d = (key >> shift) & 0xFFu;
                     if (pass == 0) {
                         hist_add(h, d);
@@ -703,38 +703,35 @@ __device__ __forceinline__ bool list_select16(const uint32_t *list, uint32_t m, 
     return true;
 }
 
-// The nearest-rank 1st and 99th percentiles of the cnt valid elements in the
-// team's slots: ranks k_lo = ceil(cnt/100) - 1 and k_hi = ceil(99 cnt/100) - 1
-// (0-based).  Round 0 histograms every element's top key byte; every warp finds
-// the bins holding the two ranks.  Round 1 histograms the second byte of the
-// elements in those bins, one histogram per rank, and appends their keys to a
-// list per rank.  After the barrier one warp per rank finds the second byte,
-// gathers the listed keys sharing both bytes (a handful for spread-out data)
-// and selects the exact element among them.  Buckets whose bin holds more than
-// a quarter of the bucket, or whose two-byte prefix is shared by more than
-// kShortCap keys (constant buckets, heavy ties), take the full radix
-// selection.  Histograms and counters alternate between two sets (`parity`,
-// flipped per call): a set is cleared after the third barrier of one bucket and
-// next used, already clear, by the bucket after, so the fast path needs three
-// barriers.  cnt > 0; every thread of the team calls this together.  FULL:
-// every slot is valid.
-template <bool FULL>
-__device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint32_t cnt, uint32_t bucket,
-                                                 int tt, int team_threads, int W, int team,
-                                                 int warp_in_team, int lane, uint32_t *region,
-                                                 uint32_t &parity, float &lo, float &hi) {
-    const uint32_t k_lo = (cnt + 99u) / 100u - 1u, k_hi = (99u * cnt + 99u) / 100u - 1u;
+// The keys of ranks r_lo and r_hi (0-based, ascending; NR = 1: r_lo only)
+// among the cnt valid keys of the team's slots.  Round 0 histograms every key's
+// top byte; every warp finds the bins holding the ranks.  Round 1 histograms
+// the second byte of the keys in those bins, one histogram per rank, and
+// appends them to a list per rank.  After the barrier one warp per rank finds
+// the second byte, gathers the listed keys sharing both bytes (a handful for
+// spread-out data) and selects the exact key among them.  Buckets whose bin
+// holds more than a quarter of the bucket, or whose two-byte prefix is shared
+// by more than kShortCap keys (constant buckets, heavy ties), take the full
+// radix selection.  Histograms and counters alternate between two sets
+// (`parity`, flipped per call): a set is cleared after the third barrier of
+// one bucket and next used, already clear, by the bucket after, so the fast
+// path needs three barriers.  cnt > 0; every thread of the team calls this
+// together.  FULL: every slot is valid.
+template <int NR, bool FULL>
+__device__ __forceinline__ void team_select(const uint32_t (&key)[kSlots][4], uint32_t cnt,
+                                            uint32_t bucket, uint32_t k_lo, uint32_t k_hi, int tt,
+                                            int team_threads, int W, int team, int warp_in_team,
+                                            int lane, uint32_t *region, uint32_t &parity,
+                                            uint32_t &key_lo, uint32_t &key_hi) {
     const uint32_t cap = bucket / 4u;
     uint32_t *set = region + parity * kSelSet;
     uint32_t *hist0 = set, *hist_lo = set + kHistWords, *hist_hi = set + 2 * kHistWords;
     uint32_t *count = region + kSelCount + 4 * parity;
     uint32_t *list_lo = region + kSelLists, *list_hi = list_lo + cap;
-    uint32_t key[kSlots][4];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            key[s][c] = order_key(get(p[s], c));
             const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
             if (FULL || j < cnt) hist_add(hist0, key[s][c] >> 24);
         }
@@ -742,7 +739,7 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
     team_sync(W, team);  // (1)
     uint32_t r_lo = k_lo, r_hi = k_hi;
     const uint32_t b_lo = hist_find<kHistWords / 32>(hist0, r_lo, lane);
-    const uint32_t b_hi = hist_find<kHistWords / 32>(hist0, r_hi, lane);
+    const uint32_t b_hi = NR > 1 ? hist_find<kHistWords / 32>(hist0, r_hi, lane) : 0u;
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
 #pragma unroll
@@ -754,7 +751,7 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
                 const uint32_t at = atomicAdd(count, 1u);
                 if (at < cap) list_lo[at] = key[s][c];
             }
-            if ((FULL || j < cnt) && top == b_hi) {
+            if (NR > 1 && (FULL || j < cnt) && top == b_hi) {
                 hist_add(hist_hi, d);
                 const uint32_t at = atomicAdd(count + 1, 1u);
                 if (at < cap) list_hi[at] = key[s][c];
@@ -764,7 +761,7 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
     team_sync(W, team);  // (2)
     const uint32_t m_lo = count[0], m_hi = count[1];
     bool fast = m_lo <= cap && m_hi <= cap;
-    uint32_t key_lo = 0u, key_hi = 0u;
+    key_lo = key_hi = 0u;
     if (fast) {
         // the selecting warps flag an overflowing short list in the counters
         if (warp_in_team == 0) {
@@ -776,7 +773,7 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
                 count[2] = ok ? 0u : 1u;
             }
         }
-        if (warp_in_team == (W > 1 ? 1 : 0)) {
+        if (NR > 1 && warp_in_team == (W > 1 ? 1 : 0)) {
             const uint32_t pre = (b_hi << 8) | hist_find<kHistWords / 32>(hist_hi, r_hi, lane);
             uint32_t x = 0u;
             const bool ok = list_select16(list_hi, m_hi, pre, r_hi, region + kSelShortHi, lane, x);
@@ -802,13 +799,33 @@ __device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint
         team_sync(W, team);  // every thread has read the counters
         for (int i = tt; i < 2 * kSelSet; i += team_threads) region[i] = 0u;
         team_sync(W, team);
-        team_radix_select(p, cnt, tt, team_threads, W, team, lane, region, k_lo, k_hi, key_lo, key_hi);
+        team_radix_select(key, cnt, tt, team_threads, W, team, lane, region, k_lo,
+                          NR > 1 ? k_hi : k_lo, key_lo, key_hi);
         team_sync(W, team);  // every warp is done with the last round's buffer
         for (int i = tt; i < 2 * kSelSet; i += team_threads) region[i] = 0u;
         for (int i = tt; i < 8; i += team_threads) region[kSelCount + i] = 0u;
         team_sync(W, team);  // all clear before the next bucket
     }
     parity ^= 1u;
+}
+
+// The nearest-rank 1st and 99th percentiles of the cnt valid elements in the
+// team's slots: the order keys of ranks ceil(cnt/100) - 1 and
+// ceil(99 cnt/100) - 1 (0-based), by team_select.
+template <bool FULL>
+__device__ __forceinline__ void team_percentiles(const float4 (&p)[kSlots], uint32_t cnt, uint32_t bucket,
+                                                 int tt, int team_threads, int W, int team,
+                                                 int warp_in_team, int lane, uint32_t *region,
+                                                 uint32_t &parity, float &lo, float &hi) {
+    uint32_t key[kSlots][4];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) key[s][c] = order_key(get(p[s], c));
+    uint32_t key_lo, key_hi;
+    team_select<2, FULL>(key, cnt, bucket, (cnt + 99u) / 100u - 1u, (99u * cnt + 99u) / 100u - 1u,
+                         tt, team_threads, W, team, warp_in_team, lane, region, parity, key_lo,
+                         key_hi);
     lo = key_value(key_lo);
     hi = key_value(key_hi);
 }

@@ -114,6 +114,34 @@ struct VoteParams {
     uint32_t *out;
 };
 
+// Top-k sparsification: the encode parameters plus the kept count per bucket
+// and the index / 8-bit code outputs (keep slots per bucket).
+struct TopkParams {
+    EncodeParams e;
+    uint32_t keep;
+    uint32_t *idx;
+    uint8_t *codes8;
+};
+
+// Receiver of top-k payloads: M workers' (index, code) slots at pair_stride,
+// metadata at meta_stride; a dense fp32 output.
+struct TopkDecodeParams {
+    const uint32_t *idx;
+    const uint8_t *codes8;
+    uint64_t pair_stride;
+    const float *scale;
+    const float *offset;
+    uint64_t meta_stride;
+    int M;
+    uint64_t n;
+    uint32_t bucket;
+    uint64_t nbuckets;
+    uint32_t keep;
+    float *out;
+    int flags;
+    float inv_m;
+};
+
 // Receiver re-encode: the decode of M payloads (DecodeParams' fields) feeding an
 // encode of the result with its own residual buffer, same scheme, bits and bucket.
 struct ReencodeParams {
@@ -189,6 +217,9 @@ cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int s
                               cudaStream_t stream);
 cudaError_t launch_reencode(const ReencodeParams &p, const ReencodeTiles &g, int scheme, int bits,
                             int stochastic, cudaStream_t stream);
+cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int stochastic, int bf16,
+                               cudaStream_t stream);
+cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream);
 cudaError_t launch_vote(const VoteParams &p, bool vectorised, cudaStream_t stream);
 cudaError_t launch_fp8_quant(const Fp8Params &p, cudaStream_t stream);
 cudaError_t launch_fp8_dequant(const Fp8Params &p, cudaStream_t stream);
@@ -203,6 +234,7 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 // Device-side error flags of the pipelined kernels (read and cleared).
 uint32_t take_encode_errors();
 uint32_t take_encode_clip_errors();
+uint32_t take_topk_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();
 uint32_t take_reencode_errors();

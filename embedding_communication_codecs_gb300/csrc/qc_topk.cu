@@ -1,0 +1,338 @@
+// qc_topk.cu -- top-k sparsification with 8-bit quantization of the kept
+// values and error feedback, and its receiver.
+//
+// "Gradient quantization for communication", "Quantization Schemes" (Top-K
+// Sparsification: send only the largest K% of gradients, combined with
+// quantization; Error Feedback); "Quantization for Communication",
+// "Combination with Other Techniques" (quantize the sparse gradients);
+// "Gradient Compression and Quantised Collectives", "Why sparsification fights
+// the all-reduce" (the kept coordinates travel as index-value pairs, and the
+// receiver sums an all-gather of them).
+//
+// Encode, per bucket of B <= 4096 elements (K = min(keep, cnt)):
+//   p = e + g; the K elements of largest |p| (ties to the lower index) are
+//   kept, in ascending index order, as (global index, 8-bit code) slots; the
+//   codes are the uniform 8-bit quantization over the kept values' own min and
+//   max; e = p - deq for kept elements, e = p for the others; unused slots of a
+//   short last bucket hold index 0xFFFFFFFF and code 0.
+// The kernel is the pipelined encode's (qc_encode_tma.cuh) tile and team
+// layout.  The K-th largest |p| comes from team_select (qc_encode_math.cuh) on
+// the keys |p| (non-negative floats order like their bit patterns).  One team
+// scan in index order of two packed counters (keys >= T, keys == T) then gives
+// every element whether it is kept (all keys > T, and the first `need` ties)
+// and its output slot.
+//
+// Decode: a block per bucket accumulates the workers' pairs into a
+// shared-memory copy of the bucket's output, worker by worker with a barrier in
+// between (a worker's indices within a bucket are distinct, so each step is
+// race-free and the fixed worker order holds), then writes the dense result.
+#include "qc_encode_tma.cuh"
+
+namespace qc {
+
+static __device__ unsigned int g_topk_errors;
+
+namespace {
+
+constexpr uint32_t kNoIndex = 0xFFFFFFFFu;
+constexpr int kScanWords = kSlots * (kBlock / 32);  // per team: one total per slot and warp
+
+// Exclusive prefix, in index order, of the lane's per-slot values a[s] over the
+// team (slot-major, then lane order), and the team total.  Values are packed
+// counters that never carry between halves.
+__device__ __forceinline__ void team_scan(const uint32_t (&a)[kSlots], int W, int team,
+                                          int warp_in_team, int lane, uint32_t *tot,
+                                          uint32_t (&excl)[kSlots], uint32_t &total) {
+    uint32_t incl[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        incl[s] = a[s];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl[s], o);
+            if (lane >= o) incl[s] += t;
+        }
+        if (lane == 31) tot[s * 8 + warp_in_team] = incl[s];
+    }
+    team_sync(W, team);
+    uint32_t running = 0u;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        uint32_t slot_total = 0u, before = 0u;
+        for (int w = 0; w < W; ++w) {
+            const uint32_t v = tot[s * 8 + w];
+            slot_total += v;
+            before += w < warp_in_team ? v : 0u;
+        }
+        excl[s] = running + before + (incl[s] - a[s]);
+        running += slot_total;
+    }
+    total = running;
+}
+
+template <typename TIn, bool EF, bool SR>
+__global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ TopkParams T,
+                                                      const __grid_constant__ EncodeTiles G) {
+    const EncodeParams &P = T.e;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
+    auto red = reinterpret_cast<Stats<kUniform>(*)[kBlock / 32]>(full + G.stages);
+    uint32_t *teamwords = reinterpret_cast<uint32_t *>(red + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = P.team_warps;
+    const int teams = (kBlock / 32) / W;
+    const int team = warp / W;
+    const int tt = (warp % W) * 32 + lane;
+    const int team_threads = W * 32;
+    const uint32_t window = static_cast<uint32_t>(team_threads) * kSlots * 4u;
+    const int region_words = sel_region_words(P.bucket) + kScanWords;
+    uint32_t *region = teamwords + team * region_words;
+    uint32_t *tot = region + sel_region_words(P.bucket);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < G.stages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    for (int i = threadIdx.x; i < teams * region_words; i += kBlock) teamwords[i] = 0u;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < G.stages; ++s) {
+            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
+            if (tile < G.ntiles) issue_tile<TIn, EF>(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+        }
+    }
+
+    int buf = 0;
+    uint32_t parity = 0, it = 0;
+    bool failed = false;
+    for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
+        const uint32_t s = it % G.stages;
+        const unsigned char *stage = smem + s * G.stage_bytes;
+        const bool ok = mbar_wait(&full[s], (it / G.stages) & 1u);
+        const uint64_t t0 = tile * G.te;
+        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
+        const uint32_t staged = staged_elems<TIn, EF>(tcnt);
+        for (uint32_t kb0 = 0; kb0 < G.tb; kb0 += teams) {
+            const uint32_t kb = kb0 + team;
+            const uint32_t b_off = kb * P.bucket;
+            const uint32_t cnt = (kb < G.tb && b_off < tcnt) ? min(P.bucket, tcnt - b_off) : 0u;
+            const uint64_t b0 = t0 + b_off;
+            const uint64_t k = tile * G.tb + kb;
+            const bool whole = cnt == window && b_off + cnt <= staged;
+            float4 p[kSlots];
+            if (whole)
+                load_slots_staged<TIn, EF, true>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+            else
+                load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+
+            Stats<kUniform> st;
+            st.init();
+            uint32_t K = 0u, need = 0u, thr = 0u;
+            uint32_t key[kSlots][4], excl[kSlots];
+#pragma unroll
+            for (int sl = 0; sl < kSlots; ++sl)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) key[sl][c] = __float_as_uint(get(p[sl], c)) & 0x7FFFFFFFu;
+            if (cnt) {
+                K = min(T.keep, cnt);
+                uint32_t unused;
+                if (whole)
+                    team_select<1, true>(key, cnt, P.bucket, cnt - K, cnt - K, tt, team_threads, W,
+                                         team, warp % W, lane, region, parity, thr, unused);
+                else
+                    team_select<1, false>(key, cnt, P.bucket, cnt - K, cnt - K, tt, team_threads, W,
+                                          team, warp % W, lane, region, parity, thr, unused);
+                // counters in index order: keys >= thr (low half), keys == thr (high half)
+                uint32_t a[kSlots];
+#pragma unroll
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    a[sl] = 0u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+                        if (j < cnt)
+                            a[sl] += (key[sl][c] >= thr ? 1u : 0u) + (key[sl][c] == thr ? 0x10000u : 0u);
+                    }
+                }
+                uint32_t total;
+                team_scan(a, W, team, warp % W, lane, tot, excl, total);
+                need = K - ((total & 0xFFFFu) - (total >> 16));  // ties to keep, >= 1
+                // statistics of the kept values
+#pragma unroll
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    uint32_t run = excl[sl];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+                        if (j < cnt) {
+                            const bool kept = key[sl][c] > thr || (key[sl][c] == thr && (run >> 16) < need);
+                            if (kept) st.add(get(p[sl], c));
+                            run += (key[sl][c] >= thr ? 1u : 0u) + (key[sl][c] == thr ? 0x10000u : 0u);
+                        }
+                    }
+                }
+            }
+            team_reduce<kUniform>(st, red, buf, W, warp, lane, team);
+            if (cnt) {
+                const BucketParams bp = Finish<kUniform, 8>::run(st, K);
+#pragma unroll
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    uint32_t run = excl[sl];
+                    float4 e = p[sl];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+                        if (j < cnt) {
+                            const uint32_t kk = key[sl][c];
+                            const uint32_t ge_before = run & 0xFFFFu, tie_before = run >> 16;
+                            const bool kept = kk > thr || (kk == thr && tie_before < need);
+                            if (kept) {
+                                const uint64_t i = b0 + j;
+                                float u = 0.0f;
+                                if constexpr (SR) u = uniform1(i, P.step, P.keys);
+                                float deq;
+                                const uint32_t q = quantize<kUniform, 8, SR>(get(p[sl], c), u, bp, deq);
+                                const uint32_t pos = (ge_before - tie_before) + min(tie_before, need);
+                                T.idx[k * T.keep + pos] = static_cast<uint32_t>(i);
+                                T.codes8[k * T.keep + pos] = static_cast<uint8_t>(q);
+                                set(e, c, __fsub_rn(get(p[sl], c), deq));
+                            }
+                            run += (kk >= thr ? 1u : 0u) + (kk == thr ? 0x10000u : 0u);
+                        }
+                    }
+                    if constexpr (EF) {
+                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u;
+                        if (j + 4u <= cnt) {
+                            __stcs(reinterpret_cast<float4 *>(P.err + b0 + j), e);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (j + c < cnt) P.err[b0 + j + c] = get(e, c);
+                        }
+                    }
+                }
+                for (uint32_t t = K + static_cast<uint32_t>(tt); t < T.keep; t += team_threads) {
+                    T.idx[k * T.keep + t] = kNoIndex;
+                    T.codes8[k * T.keep + t] = 0;
+                }
+                if (tt == 0) store_meta<kUniform>(P.scale, P.offset, k, bp);
+            }
+        }
+        if (!__syncthreads_and(ok)) {
+            failed = true;
+            break;
+        }
+        if (threadIdx.x == 0) {
+            const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
+            if (next < G.ntiles) issue_tile<TIn, EF>(P, G, next, smem + s * G.stage_bytes, &full[s]);
+        }
+    }
+    if (failed && threadIdx.x == 0) {
+        atomicOr(&g_topk_errors, kErrPipelineTimeout);
+        for (uint32_t d = 0; d < G.stages; ++d) {
+            const uint32_t j = it + d;
+            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
+            if (tile < G.ntiles) mbar_wait(&full[j % G.stages], (j / G.stages) & 1u);
+        }
+    }
+}
+
+constexpr int kDecodeThreads = 256;
+
+// One bucket per block iteration: zero the bucket's accumulators in shared
+// memory, add each worker's pairs in worker order (the next worker's first
+// slots already loaded while the current one is applied), then write the
+// dense result with the MEAN / accumulate flags.
+__global__ void __launch_bounds__(kDecodeThreads) topk_decode_kernel(const __grid_constant__ TopkDecodeParams D) {
+    extern __shared__ float acc[];
+    const float Mf = static_cast<float>(D.M);
+    for (uint64_t k = blockIdx.x; k < D.nbuckets; k += gridDim.x) {
+        const uint64_t lo = k * D.bucket;
+        const uint32_t cnt = static_cast<uint32_t>(min(static_cast<uint64_t>(D.bucket), D.n - lo));
+        for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) acc[j] = 0.0f;
+        // prefetch of slot threadIdx.x of the next worker
+        uint32_t nidx = kNoIndex, ncode = 0u;
+        if (threadIdx.x < D.keep) {
+            nidx = __ldg(D.idx + k * D.keep + threadIdx.x);
+            ncode = __ldg(D.codes8 + k * D.keep + threadIdx.x);
+        }
+        __syncthreads();
+        for (int w = 0; w < D.M; ++w) {
+            const uint64_t base = static_cast<uint64_t>(w) * D.pair_stride + k * D.keep;
+            const float s = __ldg(D.scale + static_cast<uint64_t>(w) * D.meta_stride + k);
+            const float o = __ldg(D.offset + static_cast<uint64_t>(w) * D.meta_stride + k);
+            const uint32_t cidx = nidx, ccode = ncode;
+            if (w + 1 < D.M && threadIdx.x < D.keep) {
+                const uint64_t nb = base + D.pair_stride;
+                nidx = __ldg(D.idx + nb + threadIdx.x);
+                ncode = __ldg(D.codes8 + nb + threadIdx.x);
+            }
+            for (uint32_t t = threadIdx.x; t < D.keep; t += kDecodeThreads) {
+                uint32_t i = cidx, q = ccode;
+                if (t >= kDecodeThreads) {  // slots past the prefetched one
+                    i = __ldg(D.idx + base + t);
+                    q = __ldg(D.codes8 + base + t);
+                }
+                if (i >= lo && i < lo + cnt) {
+                    const float d = __fmaf_rn(__fsub_rn(__uint_as_float(q | 0x4B000000u), 8388608.0f), s, o);
+                    acc[i - lo] = __fadd_rn(acc[i - lo], d);
+                }
+            }
+            __syncthreads();
+        }
+        for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) {
+            float r = acc[j];
+            if (D.flags & 1) r = D.inv_m != 0.0f ? __fmul_rn(r, D.inv_m) : __fdiv_rn(r, Mf);
+            if (D.flags & 2) r = __fadd_rn(D.out[lo + j], r);
+            D.out[lo + j] = r;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename TIn, bool EF, bool SR>
+cudaError_t launch_one(const TopkParams &p, const EncodeTiles &g, cudaStream_t stream) {
+    auto fn = &topk_kernel<TIn, EF, SR>;
+    const int teams = (kBlock / 32) / p.e.team_warps;
+    const size_t smem = encode_tiles_smem(g, sizeof(Stats<kUniform>)) +
+                        static_cast<size_t>(teams) * (sel_region_words(p.e.bucket) + kScanWords) * 4u;
+    cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kBlock, g.ntiles, smem);
+    fn<<<grid, kBlock, smem, stream>>>(p, g);
+    return cudaGetLastError();
+}
+
+template <bool SR>
+cudaError_t launch_dtype(const TopkParams &p, const EncodeTiles &g, int bf16, cudaStream_t stream) {
+    const bool ef = p.e.err != nullptr;
+    if (bf16) return ef ? launch_one<uint16_t, true, SR>(p, g, stream) : launch_one<uint16_t, false, SR>(p, g, stream);
+    return ef ? launch_one<float, true, SR>(p, g, stream) : launch_one<float, false, SR>(p, g, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int stochastic, int bf16,
+                               cudaStream_t stream) {
+    return stochastic ? launch_dtype<true>(p, g, bf16, stream) : launch_dtype<false>(p, g, bf16, stream);
+}
+
+cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(p.bucket) * 4u;
+    auto fn = &topk_decode_kernel;
+    cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kDecodeThreads, p.nbuckets, smem);
+    fn<<<grid, kDecodeThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+uint32_t take_topk_errors() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_topk_errors, sizeof v);
+    cudaMemcpyToSymbol(g_topk_errors, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace qc

@@ -224,6 +224,60 @@ qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const fl
                       float *offset_out, float *out, qc_stream_t stream);
 
 /*
+ * qc_topk_encode_ef -- top-k sparsification with 8-bit codes and error feedback
+ * ("Gradient quantization for communication", "Quantization Schemes": send only
+ * the largest K% of gradients, combined with quantization, with error
+ * feedback; "Quantization for Communication", "Combination with Other
+ * Techniques"; "Gradient Compression and Quantised Collectives", "Why
+ * sparsification fights the all-reduce": the exchange is index-value pairs).
+ * Per bucket k of cnt elements, K = min(keep, cnt):
+ *   p_i = err ? fl(err_i + grad_i) : grad_i
+ *   kept = the K elements of largest |p_i|, ties to the lower index
+ *   mn, mx = min and max of p over kept (zero taken as +0); scale = fl(fl(mx-mn)/255)
+ *   each kept element: q_i and deq_i exactly as qc_encode_ef's UNIFORM 8-bit
+ *     (NEAREST or STOCHASTIC, the draw of element i)
+ *   err_i = kept ? fl(p_i - deq_i) : p_i
+ * Slot t (0 <= t < keep) of bucket k, at k*keep + t: the t-th kept element in
+ * ascending index order, idx = its index (0-based in this call), codes = q;
+ * slots t >= K (a short last bucket) hold idx 0xFFFFFFFF and code 0.
+ * scale[k] = scale, offset[k] = mn.
+ *
+ * grad   : n elements of `dtype`, 16-byte aligned (else QC_ERR_UNSUPPORTED).
+ * err    : n fp32, in/out, 16-byte aligned, or NULL for no error feedback.
+ * bucket : a multiple of 32, at most 4096 (else QC_ERR_UNSUPPORTED).
+ * keep   : kept elements per bucket, 1 .. bucket.
+ * idx    : out, qc_num_buckets(n, bucket) * keep uint32.
+ * codes  : out, qc_num_buckets(n, bucket) * keep bytes.
+ * scale, offset : out, qc_num_buckets(n, bucket) fp32 each.
+ * n must be below 2^32 (32-bit indices).
+ */
+qc_status qc_topk_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, size_t bucket,
+                            uint32_t keep, qc_round mode, uint64_t seed, uint32_t step,
+                            uint32_t *idx, uint8_t *codes, float *scale, float *offset,
+                            qc_stream_t stream);
+
+/*
+ * qc_topk_decode_accumulate -- receiver of top-k payloads: the M workers' pairs
+ * scattered into a dense fp32 vector and accumulated in fixed worker order.
+ *   acc_i = +0; for w = 0 .. M-1, for every bucket k and slot t:
+ *     i = idx_w[k*keep + t]; skipped unless k*bucket <= i < min((k+1)*bucket, n)
+ *     acc_i = fl(acc_i + fma(code, scale_w[k], offset_w[k]))
+ *   r = (flags & QC_OUT_MEAN) ? fl(acc / M) : acc
+ *   out_i = (flags & QC_ACCUMULATE_INTO_OUT) ? fl(out_i + r) : r
+ * A worker's indices within one bucket must be distinct (as the encoder writes
+ * them); duplicates leave that element's sum unspecified (never out of bounds).
+ *
+ * idx, codes : worker w's slots start at w * pair_stride
+ *              (pair_stride >= qc_num_buckets(n, bucket) * keep when M > 1).
+ * scale, offset : worker w's at w * meta_stride (>= qc_num_buckets when M > 1).
+ * M      : 1 .. QC_MAX_WORKERS.  bucket <= 16384.  out : n fp32, 4-byte aligned.
+ */
+qc_status qc_topk_decode_accumulate(const uint32_t *idx, const uint8_t *codes, size_t pair_stride,
+                                    const float *scale, const float *offset, size_t meta_stride,
+                                    int M, size_t n, size_t bucket, uint32_t keep, float *out,
+                                    int flags, qc_stream_t stream);
+
+/*
  * qc_sign_vote -- signSGD aggregation by majority vote ("Quantization for
  * Communication", "Quantized SGD Algorithms"; "Gradient Compression and
  * Quantised Collectives", "Why sparsification fights the all-reduce").

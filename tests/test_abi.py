@@ -190,3 +190,40 @@ def test_clip_rejects(q):
     assert _enc(q, scheme=C_, grad=A + 8, dtype=q.QC_DTYPE_BF16) == q.QC_ERR_UNSUPPORTED
     assert q.lib.qc_reencode(C, 1024, D, D + 0x100000, 2, 2, 4096, 8, 2048, C_, 0, B, 0, 0, 0,
                              0x50000000, 0x60000000, 0x60001000, A, 0) == q.QC_ERR_UNSUPPORTED
+
+
+def test_topk_rejects(q):
+    L = q.lib
+    E = 0x50000000
+
+    def enc(**kw):
+        a = dict(grad=A, dtype=q.QC_DTYPE_F32, err=B, n=4096, bucket=1024, keep=10,
+                 mode=q.QC_ROUND_NEAREST, idx=C, codes=E, scale=D, offset=D + 0x100000)
+        a.update(kw)
+        return L.qc_topk_encode_ef(a["grad"], a["dtype"], a["err"], a["n"], a["bucket"], a["keep"],
+                                   a["mode"], 0, 0, a["idx"], a["codes"], a["scale"], a["offset"], 0)
+    assert enc(keep=0) == q.QC_ERR_INVALID_ARG
+    assert enc(keep=1025) == q.QC_ERR_INVALID_ARG
+    assert enc(bucket=48) == q.QC_ERR_INVALID_ARG
+    assert enc(bucket=8192, n=1 << 15) == q.QC_ERR_UNSUPPORTED
+    assert enc(n=1 << 32) == q.QC_ERR_UNSUPPORTED
+    assert enc(idx=None) == q.QC_ERR_NULL
+    assert enc(grad=A + 4) == q.QC_ERR_UNSUPPORTED
+    assert enc(err=B + 4) == q.QC_ERR_ALIGNMENT
+    assert enc(idx=A + 64) == q.QC_ERR_INVALID_ARG
+    assert enc(n=0, grad=None, idx=None) == q.QC_OK
+
+    def dec(**kw):
+        a = dict(idx=C, codes=E, ps=40, scale=D, offset=D + 0x100000, ms=4, M=2, n=4096,
+                 bucket=1024, keep=10, out=A, flags=1)
+        a.update(kw)
+        return L.qc_topk_decode_accumulate(a["idx"], a["codes"], a["ps"], a["scale"], a["offset"],
+                                           a["ms"], a["M"], a["n"], a["bucket"], a["keep"], a["out"],
+                                           a["flags"], 0)
+    assert dec(M=0) == q.QC_ERR_INVALID_ARG
+    assert dec(ps=39) == q.QC_ERR_INVALID_ARG
+    assert dec(flags=8) == q.QC_ERR_INVALID_ARG
+    assert dec(out=None) == q.QC_ERR_NULL
+    assert dec(out=C) == q.QC_ERR_INVALID_ARG
+    assert dec(bucket=32768, n=1 << 16, ps=20, ms=2, keep=10) == q.QC_ERR_UNSUPPORTED
+    assert dec(n=0, idx=None, out=None) == q.QC_OK
