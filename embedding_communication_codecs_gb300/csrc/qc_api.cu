@@ -62,7 +62,7 @@ int team_warps_for(size_t elems) {
 // stages (two above 32 KB), so small stages leave room for 4 blocks per SM.  Buckets larger than one team window (4096) and
 // gradients whose base is not 16-byte aligned take the direct kernel.
 bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool grad16,
-                      qc::EncodeTiles &t) {
+                      qc::EncodeTiles &t, size_t extra_smem = 0) {
     if (!grad16 || p.two_pass) return false;
     const size_t per_elem = esize + (ef ? 4 : 0);
     const uint32_t teams = (qc::kBlock / 32) / p.team_warps;
@@ -72,7 +72,9 @@ bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool gra
     if (tb < teams) tb = teams;
     const size_t stage = static_cast<size_t>(tb) * p.bucket * per_elem;
     if (stage > 64 * 1024) return false;
-    const uint32_t stages = stage <= 32 * 1024 ? 3u : 2u;
+    uint32_t stages = stage <= 32 * 1024 ? 3u : 2u;
+    // kernels with per-team selection buffers keep two blocks per SM
+    if (stages == 3 && 3 * stage + extra_smem > 110 * 1024) stages = 2;
     t.tb = tb;
     t.te = tb * p.bucket;
     t.stages = stages;
@@ -357,7 +359,9 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
     qc::EncodeTiles tiles{};
     if (scheme == QC_SCHEME_UNIFORM_CLIP) {
         // the percentile selection runs over a bucket held in registers by one team
-        if (!encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))
+        const size_t teams = (qc::kBlock / 32) / p.team_warps;
+        if (!encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles,
+                              teams * qc::sel_region_words(p.bucket) * 4))
             return fail(QC_ERR_UNSUPPORTED,
                         "qc_encode_ef: percentile clipping needs a bucket of at most 4096 elements "
                         "and a 16-byte aligned gradient");
@@ -571,7 +575,9 @@ qc_status qc_topk_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t
     t.idx = idx;
     t.codes8 = codes;
     qc::EncodeTiles tiles{};
-    if (!encode_tiles_for(t.e, esize, err != nullptr, true, tiles))
+    const size_t teams = (qc::kBlock / 32) / t.e.team_warps;
+    if (!encode_tiles_for(t.e, esize, err != nullptr, true, tiles,
+                          teams * (qc::sel_region_words(t.e.bucket) + qc::kTopkScanWords) * 4))
         return fail(QC_ERR_UNSUPPORTED, "%s: no tiling for this bucket", fn);
     return from_cuda(qc::launch_topk_encode(t, tiles, mode == QC_ROUND_STOCHASTIC,
                                             dtype == QC_DTYPE_BF16,
@@ -592,8 +598,8 @@ qc_status qc_topk_decode_accumulate(const uint32_t *idx, const uint8_t *codes, s
         return fail(QC_ERR_INVALID_ARG, "%s: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", fn, bucket);
     if (keep < 1 || keep > bucket)
         return fail(QC_ERR_INVALID_ARG, "%s: keep must be in [1, bucket] (got %u)", fn, keep);
-    if (bucket > 16384)
-        return fail(QC_ERR_UNSUPPORTED, "%s: buckets above 16384 elements are not supported", fn);
+    if (bucket > 16384 || keep > 1024)
+        return fail(QC_ERR_UNSUPPORTED, "%s: buckets above 16384 elements or keep above 1024 are not supported", fn);
     if (n == 0) return ok();
     if (n >= (static_cast<size_t>(1) << 32))
         return fail(QC_ERR_UNSUPPORTED, "%s: indices are 32-bit; n = %zu is too large", fn, n);

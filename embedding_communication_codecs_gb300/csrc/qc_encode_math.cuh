@@ -675,10 +675,7 @@ constexpr int kSelShortLo = 2 * kSelSet, kSelShortHi = kSelShortLo + kShortCap;
 constexpr int kSelCount = kSelShortHi + kShortCap;  // 2 sets x (list lo, list hi, short lo, short hi)
 constexpr int kSelResult = kSelCount + 8;
 constexpr int kSelLists = kSelResult + 4;
-
-__host__ __device__ constexpr int sel_region_words(uint32_t bucket) {
-    return kSelLists + 2 * static_cast<int>(bucket / 4u);
-}
+static_assert(kSelLists == kSelFixedWords, "sel_region_words() in qc_internal.h");
 
 // The element of rank r among the keys of `list` that have top 16 bits `pre`,
 // computed by one warp: the matching keys are gathered into `sub` (ballot

@@ -114,6 +114,16 @@ struct VoteParams {
     uint32_t *out;
 };
 
+// Shared-memory words of one team's order-statistic selection (percentile
+// clipping, top-k): histogram sets, short lists, counters, results, then two
+// candidate lists of bucket / 4 keys each (layout in qc_encode_math.cuh).
+constexpr int kSelFixedWords = 908;
+__host__ __device__ constexpr int sel_region_words(uint32_t bucket) {
+    return kSelFixedWords + 2 * static_cast<int>(bucket / 4u);
+}
+// Words of one team's scan totals in the top-k kernel (one per slot and warp).
+constexpr int kTopkScanWords = 4 * 8;
+
 // Top-k sparsification: the encode parameters plus the kept count per bucket
 // and the index / 8-bit code outputs (keep slots per bucket).
 struct TopkParams {

@@ -17,15 +17,18 @@
 //   short last bucket hold index 0xFFFFFFFF and code 0.
 // The kernel is the pipelined encode's (qc_encode_tma.cuh) tile and team
 // layout.  The K-th largest |p| comes from team_select (qc_encode_math.cuh) on
-// the keys |p| (non-negative floats order like their bit patterns).  One team
+// the keys bits(p) << 1: |p|'s bit pattern without its sign, moved up one bit
+// so that the top byte is the exponent (one binade per histogram bin;
+// non-negative floats order like their bit patterns).  One team
 // scan in index order of two packed counters (keys >= T, keys == T) then gives
 // every element whether it is kept (all keys > T, and the first `need` ties)
 // and its output slot.
 //
-// Decode: a block per bucket accumulates the workers' pairs into a
-// shared-memory copy of the bucket's output, worker by worker with a barrier in
-// between (a worker's indices within a bucket are distinct, so each step is
-// race-free and the fixed worker order holds), then writes the dense result.
+// Decode: a block per bucket stages the workers' pairs for the bucket in shared
+// memory, accumulates them into a shared-memory copy of the bucket's output,
+// worker by worker with a barrier in between (a worker's indices within a
+// bucket are distinct, so each step is race-free and the fixed worker order
+// holds), then writes the dense result.
 #include "qc_encode_tma.cuh"
 
 namespace qc {
@@ -35,7 +38,8 @@ static __device__ unsigned int g_topk_errors;
 namespace {
 
 constexpr uint32_t kNoIndex = 0xFFFFFFFFu;
-constexpr int kScanWords = kSlots * (kBlock / 32);  // per team: one total per slot and warp
+constexpr int kScanWords = kTopkScanWords;  // per team: one total per slot and warp
+static_assert(kScanWords == kSlots * (kBlock / 32), "scan totals");
 
 // Exclusive prefix, in index order, of the lane's per-slot values a[s] over the
 // team (slot-major, then lane order), and the team total.  Values are packed
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
 #pragma unroll
             for (int sl = 0; sl < kSlots; ++sl)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) key[sl][c] = __float_as_uint(get(p[sl], c)) & 0x7FFFFFFFu;
+                for (int c = 0; c < 4; ++c) key[sl][c] = __float_as_uint(get(p[sl], c)) << 1;
             if (cnt) {
                 K = min(T.keep, cnt);
                 uint32_t unused;
@@ -238,48 +242,51 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
     }
 }
 
-constexpr int kDecodeThreads = 256;
+constexpr int kDecodeThreads = 128;
+constexpr int kDecodePairs = 1024;  // pairs of one bucket staged in shared memory at a time
 
 // One bucket per block iteration: zero the bucket's accumulators in shared
-// memory, add each worker's pairs in worker order (the next worker's first
-// slots already loaded while the current one is applied), then write the
-// dense result with the MEAN / accumulate flags.
+// memory and stage the workers' pairs for the bucket (all of them when they fit,
+// so their loads overlap), then add them worker by worker with a barrier in
+// between, and write the dense result with the MEAN / accumulate flags.
 __global__ void __launch_bounds__(kDecodeThreads) topk_decode_kernel(const __grid_constant__ TopkDecodeParams D) {
     extern __shared__ float acc[];
+    uint32_t *pidx = reinterpret_cast<uint32_t *>(acc + D.bucket);
+    uint32_t *pcode = pidx + kDecodePairs;
+    float *pmeta = reinterpret_cast<float *>(pcode + kDecodePairs);  // (scale, offset) per worker
     const float Mf = static_cast<float>(D.M);
+    const int per = static_cast<int>(kDecodePairs / D.keep);     // workers per staging round (>= 1)
     for (uint64_t k = blockIdx.x; k < D.nbuckets; k += gridDim.x) {
         const uint64_t lo = k * D.bucket;
         const uint32_t cnt = static_cast<uint32_t>(min(static_cast<uint64_t>(D.bucket), D.n - lo));
         for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) acc[j] = 0.0f;
-        // prefetch of slot threadIdx.x of the next worker
-        uint32_t nidx = kNoIndex, ncode = 0u;
-        if (threadIdx.x < D.keep) {
-            nidx = __ldg(D.idx + k * D.keep + threadIdx.x);
-            ncode = __ldg(D.codes8 + k * D.keep + threadIdx.x);
-        }
-        __syncthreads();
-        for (int w = 0; w < D.M; ++w) {
-            const uint64_t base = static_cast<uint64_t>(w) * D.pair_stride + k * D.keep;
-            const float s = __ldg(D.scale + static_cast<uint64_t>(w) * D.meta_stride + k);
-            const float o = __ldg(D.offset + static_cast<uint64_t>(w) * D.meta_stride + k);
-            const uint32_t cidx = nidx, ccode = ncode;
-            if (w + 1 < D.M && threadIdx.x < D.keep) {
-                const uint64_t nb = base + D.pair_stride;
-                nidx = __ldg(D.idx + nb + threadIdx.x);
-                ncode = __ldg(D.codes8 + nb + threadIdx.x);
+        for (int w0 = 0; w0 < D.M; w0 += per) {
+            const int nw = min(per, D.M - w0);
+            const uint32_t np = static_cast<uint32_t>(nw) * D.keep;
+            for (uint32_t t = threadIdx.x; t < np; t += kDecodeThreads) {
+                const uint32_t w = t / D.keep, s = t - w * D.keep;
+                const uint64_t at = static_cast<uint64_t>(w0 + w) * D.pair_stride + k * D.keep + s;
+                pidx[t] = __ldg(D.idx + at);
+                pcode[t] = __ldg(D.codes8 + at);
             }
-            for (uint32_t t = threadIdx.x; t < D.keep; t += kDecodeThreads) {
-                uint32_t i = cidx, q = ccode;
-                if (t >= kDecodeThreads) {  // slots past the prefetched one
-                    i = __ldg(D.idx + base + t);
-                    q = __ldg(D.codes8 + base + t);
-                }
-                if (i >= lo && i < lo + cnt) {
-                    const float d = __fmaf_rn(__fsub_rn(__uint_as_float(q | 0x4B000000u), 8388608.0f), s, o);
-                    acc[i - lo] = __fadd_rn(acc[i - lo], d);
-                }
+            for (int w = threadIdx.x; w < nw; w += kDecodeThreads) {
+                const uint64_t at = static_cast<uint64_t>(w0 + w) * D.meta_stride + k;
+                pmeta[2 * w] = __ldg(D.scale + at);
+                pmeta[2 * w + 1] = __ldg(D.offset + at);
             }
             __syncthreads();
+            for (int w = 0; w < nw; ++w) {
+                const float s = pmeta[2 * w], o = pmeta[2 * w + 1];
+                for (uint32_t t = threadIdx.x; t < D.keep; t += kDecodeThreads) {
+                    const uint32_t i = pidx[w * D.keep + t];
+                    if (i >= lo && i < lo + cnt) {
+                        const uint32_t q = pcode[w * D.keep + t];
+                        const float d = __fmaf_rn(__fsub_rn(__uint_as_float(q | 0x4B000000u), 8388608.0f), s, o);
+                        acc[i - lo] = __fadd_rn(acc[i - lo], d);
+                    }
+                }
+                __syncthreads();
+            }
         }
         for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) {
             float r = acc[j];
@@ -319,7 +326,8 @@ cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int st
 }
 
 cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(p.bucket) * 4u;
+    const size_t smem = static_cast<size_t>(p.bucket) * 4u + 2u * kDecodePairs * 4u +
+                        2u * (kDecodePairs / p.keep) * 4u;
     auto fn = &topk_decode_kernel;
     cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
     if (e != cudaSuccess) return e;

@@ -270,7 +270,8 @@ qc_status qc_topk_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t
  * idx, codes : worker w's slots start at w * pair_stride
  *              (pair_stride >= qc_num_buckets(n, bucket) * keep when M > 1).
  * scale, offset : worker w's at w * meta_stride (>= qc_num_buckets when M > 1).
- * M      : 1 .. QC_MAX_WORKERS.  bucket <= 16384.  out : n fp32, 4-byte aligned.
+ * M      : 1 .. QC_MAX_WORKERS.  bucket <= 16384, keep <= 1024 (else
+ *          QC_ERR_UNSUPPORTED).  out : n fp32, 4-byte aligned.
  */
 qc_status qc_topk_decode_accumulate(const uint32_t *idx, const uint8_t *codes, size_t pair_stride,
                                     const float *scale, const float *offset, size_t meta_stride,

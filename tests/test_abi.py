@@ -226,4 +226,5 @@ def test_topk_rejects(q):
     assert dec(out=None) == q.QC_ERR_NULL
     assert dec(out=C) == q.QC_ERR_INVALID_ARG
     assert dec(bucket=32768, n=1 << 16, ps=20, ms=2, keep=10) == q.QC_ERR_UNSUPPORTED
+    assert dec(bucket=4096, keep=2000, ps=2000) == q.QC_ERR_UNSUPPORTED
     assert dec(n=0, idx=None, out=None) == q.QC_OK
