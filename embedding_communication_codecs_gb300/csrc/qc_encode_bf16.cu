@@ -267,37 +267,34 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                             uniform4(i0, P.step, keys, u);
                             uniform4(i0 + 4, P.step, keys, u + 4);
                         }
-                        uint32_t f0 = 0, f1 = 0, redo = 0;
+                        uint32_t f0 = 0, f1 = 0;
+                        bool any = false;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             bool r0, r1;
                             f0 |= code_fast<SCHEME, BITS, SR>(v[c], u[c], bp, fq, r0) << (c * BITS);
                             f1 |= code_fast<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp, fq, r1) << (c * BITS);
-                            if constexpr (SCHEME == kUniform) {  // which elements
-                                redo |= (r0 ? 1u : 0u) << c;
-                                redo |= (r1 ? 1u : 0u) << (c + 4);
-                            } else {  // whether any
-                                redo |= (r0 | r1) ? 1u : 0u;
-                            }
+                            any |= r0 | r1;
                         }
                         if constexpr (SCHEME == kUniform) {
-                            // bf16 gradients are coarse, so (p - min) / scale often lands
-                            // exactly on a tie: recompute only the flagged elements, each
-                            // re-read from the stage and redrawn on its own.
-                            while (redo) {
-                                const int c = __ffs(redo) - 1;
-                                redo &= redo - 1;
-                                const float vc = bf16_bits_to_float(
-                                    *reinterpret_cast<const unsigned short *>(stage + (b_off + j + c) * 2u));
-                                float uc = 0.0f;
-                                if constexpr (SR) uc = uniform1(i0 + c, P.step, keys);
-                                const uint32_t q = code_exact<SCHEME, BITS, SR>(vc, uc, bp);
+                            // rare (bf16 gradients land exactly on a tie a few times in
+                            // a thousand): find the flagged elements again and recompute
+                            // only those with the division
+                            if (any) {
                                 constexpr uint32_t kMask = (1u << BITS) - 1u;
-                                const int sh = (c & 3) * BITS;
-                                if (c < 4) f0 = (f0 & ~(kMask << sh)) | (q << sh);
-                                else f1 = (f1 & ~(kMask << sh)) | (q << sh);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    bool r;
+                                    (void)code_fast<SCHEME, BITS, SR>(v[c], u[c], bp, fq, r);
+                                    if (r) {
+                                        const uint32_t q = code_exact<SCHEME, BITS, SR>(v[c], u[c], bp);
+                                        const int sh = (c & 3) * BITS;
+                                        if (c < 4) f0 = (f0 & ~(kMask << sh)) | (q << sh);
+                                        else f1 = (f1 & ~(kMask << sh)) | (q << sh);
+                                    }
+                                }
                             }
-                        } else if (redo) {  // rare: recompute the whole slot
+                        } else if (any) {  // rare: recompute the whole slot
                             f0 = f1 = 0;
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {

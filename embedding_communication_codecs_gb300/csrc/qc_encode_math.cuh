@@ -266,8 +266,9 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             q += up ? 1u : 0u;
             qf = up ? __fadd_rn(ff, 1.0f) : ff;
         }
-        q = min(q, L);
-        deq = __fmaf_rn(fminf(qf, static_cast<float>(L)), bp.scale, bp.a);
+        // no clamp: 0 <= ta <= L (1 + 2^-22), so a level above L needs ta within
+        // reach of L + 1/2 (impossible) or of the integer L (flagged by redo)
+        deq = __fmaf_rn(qf, bp.scale, bp.a);
         return q;
     } else if constexpr (SCHEME == kQsgd) {
         constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
@@ -292,8 +293,8 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             q += up ? 1u : 0u;
             qf = up ? __fadd_rn(ff, 1.0f) : ff;
         }
-        q = min(q, S);
-        const float mag = __fmul_rn(fminf(qf, static_cast<float>(S)), bp.a);
+        // no clamp: t <= S (1 + 2^-22); a level above S would be flagged by redo
+        const float mag = __fmul_rn(qf, bp.a);
         deq = neg ? -mag : mag;
         return (neg << (BITS - 1)) | q;
     } else if constexpr (SCHEME == kTernary) {
@@ -344,7 +345,7 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
                    (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
             q += (u < fr) ? 1u : 0u;
         }
-        return min(q, L);
+        return q;  // no clamp needed outside redo (see quantize_fast)
     } else if constexpr (SCHEME == kTernary) {
         const float pa = __fmul_rn(fabsf(p), fq.rinv);
         bool keep;
@@ -375,7 +376,7 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
                    (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
             q += (u < fr) ? 1u : 0u;
         }
-        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | min(q, S);
+        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | q;  // no clamp outside redo
     } else {
         redo = false;
         return p >= 0.0f ? 1u : 0u;
