@@ -123,18 +123,21 @@ __device__ __forceinline__ uint32_t ternary_sr_field8(const float (&v)[8], const
                                                       const uint4 &r1, float rinv, float delta2,
                                                       bool &near) {
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-    uint32_t field = 0u, far = 0xFFFFFFFFu;
+    uint32_t field = 0u, far = 0xFFFFFFFFu, m[8];
 #pragma unroll
     for (int c = 7; c >= 0; --c) {
         const float pa1 = __fmaf_rn(fabsf(v[c]), rinv, 1.0f);
-        const float f = __uint_as_float((w[c] >> 9) | 0x3F800000u);
+        // (0x7F : w) >> 9 = 0x3F800000 | (w >> 9): one funnel shift
+        const float f = __uint_as_float(__funnelshift_r(w[c], 0x7Fu, 9));
         const float d = __fsub_rn(f, pa1);
-        far &= __float_as_uint(__fsub_rn(delta2, fabsf(d)));  // sign set while |d| > delta2
+        m[c] = __float_as_uint(__fsub_rn(delta2, fabsf(d)));  // sign set while |d| > delta2
         const uint32_t D = __float_as_uint(d);
         const uint32_t x = D & ~__float_as_uint(v[c]);
         field = __funnelshift_l(x, field, 1);   // b1 = keep & !sign(v)
         field = __funnelshift_l(D, field, 1);   // keep, inverted below
     }
+#pragma unroll
+    for (int c = 0; c < 8; c += 2) far &= m[c] & m[c + 1];
     near = (far >> 31) == 0u;
     return field ^ 0x5555u;
 }
