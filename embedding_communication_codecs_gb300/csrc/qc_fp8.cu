@@ -61,26 +61,34 @@ __global__ void __launch_bounds__(kBlock) fp8_quant_narrow(const Fp8Params P) {
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kBlock / 32);
     const uint64_t groups = (P.rows + kRowsPerWarp - 1) / kRowsPerWarp;
     const bool col_ok = static_cast<uint32_t>(lane) * 4u < P.dim;
-    for (uint64_t g = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
-         g < groups; g += warps) {
-        float4 v[kRowsPerWarp];
-        bool ok[kRowsPerWarp];
+    // the rows of the warp's next group are loaded before the current group is
+    // reduced and converted, so loads stay in flight during the arithmetic
+    auto load = [&](uint64_t g, float4 (&v)[kRowsPerWarp]) {
 #pragma unroll
         for (int s = 0; s < kRowsPerWarp; ++s) {
             const uint64_t r = g * kRowsPerWarp + s;
-            ok[s] = col_ok && r < P.rows;
-            v[s] = ok[s] ? __ldcs(reinterpret_cast<const float4 *>(P.x + r * P.dim) + lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[s] = (g < groups && col_ok && r < P.rows)
+                       ? __ldcs(reinterpret_cast<const float4 *>(P.x + r * P.dim) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    uint64_t g = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
+    float4 cur[kRowsPerWarp];
+    load(g, cur);
+    for (; g < groups; g += warps) {
+        float4 nxt[kRowsPerWarp];
+        load(g + warps, nxt);
 #pragma unroll
         for (int s = 0; s < kRowsPerWarp; ++s) {
             const uint64_t r = g * kRowsPerWarp + s;
-            const float sc = __fdiv_rn(positive_zero(warp_max(absmax4(v[s]))), 448.0f);
-            if (ok[s]) {
-                __stcs(reinterpret_cast<uint32_t *>(P.codes + r * P.dim) + lane, encode4(v[s], sc));
+            const float sc = __fdiv_rn(positive_zero(warp_max(absmax4(cur[s]))), 448.0f);
+            if (col_ok && r < P.rows) {
+                __stcs(reinterpret_cast<uint32_t *>(P.codes + r * P.dim) + lane, encode4(cur[s], sc));
                 if (lane == 0) P.row_scale[r] = sc;
             }
         }
+#pragma unroll
+        for (int s = 0; s < kRowsPerWarp; ++s) cur[s] = nxt[s];
     }
 }
 
