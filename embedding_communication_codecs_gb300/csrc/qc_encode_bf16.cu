@@ -142,6 +142,30 @@ __device__ __forceinline__ uint32_t ternary_sr_field8(const float (&v)[8], const
     return field ^ 0x5555u;
 }
 
+// 8-bit nearest codes of the 8 elements of a slot, four per word.  y = ta +
+// 1.5 * 2^23 holds rint(ta) in its low mantissa bits and ta <= 255 (1 + 2^-22),
+// so the low byte of y's bit pattern is the code itself: three byte permutes
+// pack four codes.  `near` is set when some ta lies within reach of a
+// half-integer (the caller recomputes those elements with the division).
+__device__ __forceinline__ void uniform8_rn_fields(const float (&v)[8], const BucketParams &bp,
+                                                   const FastQ &fq, uint32_t &f0, uint32_t &f1,
+                                                   bool &near) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const float thr = 0.5f - fq.delta2;
+    uint32_t y[8];
+    bool any = false;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float ta = __fmul_rn(__fsub_rn(v[c], bp.a), fq.rinv);
+        const float yf = __fadd_rn(ta, kMagic);
+        y[c] = __float_as_uint(yf);
+        any |= fabsf(__fsub_rn(ta, __fsub_rn(yf, kMagic))) >= thr;
+    }
+    f0 = __byte_perm(__byte_perm(y[0], y[1], 0x0040), __byte_perm(y[2], y[3], 0x0040), 0x5410);
+    f1 = __byte_perm(__byte_perm(y[4], y[5], 0x0040), __byte_perm(y[6], y[7], 0x0040), 0x5410);
+    near = any;
+}
+
 template <int SCHEME, int BITS, bool SR>
 __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_constant__ EncodeParams P,
                                                              const __grid_constant__ EncodeTiles G) {
@@ -246,7 +270,25 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                     const uint64_t i0 = b0 + j;
                     float v[8], u[8];
                     unpack8(*reinterpret_cast<const uint4 *>(stage + (b_off + j) * 2u), v);
-                    if constexpr (SCHEME == kTernary && SR) {
+                    if constexpr (SCHEME == kUniform && BITS == 8 && !SR) {
+                        uint32_t f0, f1;
+                        bool near;
+                        uniform8_rn_fields(v, bp, fq, f0, f1, near);
+                        if (near) {  // rare: recompute the flagged elements with the division
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                bool r;
+                                (void)code_fast<SCHEME, BITS, SR>(v[c], 0.0f, bp, fq, r);
+                                if (r) {
+                                    const uint32_t q = code_exact<SCHEME, BITS, SR>(v[c], 0.0f, bp);
+                                    const int sh = (c & 3) * 8;
+                                    if (c < 4) f0 = (f0 & ~(0xFFu << sh)) | (q << sh);
+                                    else f1 = (f1 & ~(0xFFu << sh)) | (q << sh);
+                                }
+                            }
+                        }
+                        store_codes8<BITS>(P.codes, i0, true, lane, f0, f1);
+                    } else if constexpr (SCHEME == kTernary && SR) {
                         bool near;
                         const uint32_t f16 = ternary_sr_field8(v, philox_words(i0, P.step, keys),
                                                                philox_words(i0 + 4, P.step, keys),
