@@ -295,7 +295,9 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = 0;
     const cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() | qc::take_topk_errors() |
+    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
+             qc::take_encode_clip_bf16_errors() | qc::take_reencode_other_errors() |
+             qc::take_topk_errors() |
              qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }

@@ -243,7 +243,6 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
                                                   const FastQ &fq, float &deq, bool &redo) {
     if constexpr (SCHEME == kUniform || SCHEME == kClip) {
         if constexpr (SCHEME == kClip) p = fminf(fmaxf(p, bp.a), bp.hi);
-        constexpr uint32_t L = (1u << BITS) - 1u;
         constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
         float qf;
@@ -271,7 +270,6 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
         deq = __fmaf_rn(qf, bp.scale, bp.a);
         return q;
     } else if constexpr (SCHEME == kQsgd) {
-        constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
         constexpr float kMagic = 12582912.0f;
         const uint32_t neg = p < 0.0f ? 1u : 0u;
         const float ta = __fmul_rn(fabsf(p), fq.rinv);
@@ -327,7 +325,6 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
                                               const FastQ &fq, bool &redo) {
     if constexpr (SCHEME == kUniform || SCHEME == kClip) {
         if constexpr (SCHEME == kClip) p = fminf(fmaxf(p, bp.a), bp.hi);
-        constexpr uint32_t L = (1u << BITS) - 1u;
         constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float ta = __fmul_rn(__fsub_rn(p, bp.a), fq.rinv);
         uint32_t q;
@@ -360,7 +357,6 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
         // keep ? (p > 0 ? 2 : 0) : 1; a kept element is never zero
         return keep ? ((__float_as_uint(p) >> 31) ? 0u : 2u) : 1u;
     } else if constexpr (SCHEME == kQsgd) {
-        constexpr uint32_t S = (1u << (BITS - 1)) - 1u;
         constexpr float kMagic = 12582912.0f;
         const float ta = __fmul_rn(fabsf(p), fq.rinv);
         uint32_t q;

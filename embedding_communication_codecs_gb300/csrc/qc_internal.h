@@ -220,6 +220,8 @@ cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int s
 // The percentile-clipped uniform scheme (its own translation unit).
 cudaError_t launch_encode_clip(const EncodeParams &p, const EncodeTiles &g, int bits,
                                int stochastic, int bf16, cudaStream_t stream);
+cudaError_t launch_encode_clip_bf16(const EncodeParams &p, const EncodeTiles &g, int bits,
+                                    int stochastic, cudaStream_t stream);
 cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                                int stochastic, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
@@ -227,6 +229,8 @@ cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int s
                               cudaStream_t stream);
 cudaError_t launch_reencode(const ReencodeParams &p, const ReencodeTiles &g, int scheme, int bits,
                             int stochastic, cudaStream_t stream);
+cudaError_t launch_reencode_other(const ReencodeParams &p, const ReencodeTiles &g, int scheme,
+                                  int bits, int stochastic, cudaStream_t stream);
 cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int stochastic, int bf16,
                                cudaStream_t stream);
 cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream);
@@ -244,6 +248,8 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 // Device-side error flags of the pipelined kernels (read and cleared).
 uint32_t take_encode_errors();
 uint32_t take_encode_clip_errors();
+uint32_t take_encode_clip_bf16_errors();
+uint32_t take_reencode_other_errors();
 uint32_t take_topk_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();

@@ -1,0 +1,24 @@
+// qc_reencode_other.cu -- the sign, ternary and QSGD instances of the fused
+// receiver re-encode (qc_reencode.cu has the method's description and the
+// uniform instances; both instantiate the kernel template of qc_reencode.cuh).
+#include "qc_reencode.cuh"
+
+namespace qc {
+
+cudaError_t launch_reencode_other(const ReencodeParams &p, const ReencodeTiles &g, int scheme,
+                                  int bits, int stochastic, cudaStream_t stream) {
+    if (scheme == kSign) return launch_ef<kSign, 1, false>(p, g, stream);
+    if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, stream);
+    if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, stream);
+    if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, stream);
+    return launch_round<kQsgd, 8>(p, g, stochastic, stream);
+}
+
+uint32_t take_reencode_other_errors() {
+    unsigned int v = 0, zero = 0;
+    cudaMemcpyFromSymbol(&v, g_reencode_errors, sizeof v);
+    cudaMemcpyToSymbol(g_reencode_errors, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace qc
