@@ -84,6 +84,22 @@ class Component:
         """Elements each launch of each kernel processes (for scaling counters)."""
         return {}
 
+    def quality(self, q, torch):
+        """Compression ratio and the error of one more step's result against the
+        exact value (torch, outside the timed region); None if not defined."""
+        return None
+
+
+def _rel_rms(torch, got, want):
+    d = (got.double() - want.double()).pow(2).mean().sqrt()
+    w = want.double().pow(2).mean().sqrt()
+    return float(d / w) if float(w) > 0 else 0.0
+
+
+def _rms_ratio(torch, a, b):
+    w = b.double().pow(2).mean().sqrt()
+    return float(a.double().pow(2).mean().sqrt() / w) if float(w) > 0 else 0.0
+
 
 def _words(n, bits):
     return (n * bits + 31) // 32
@@ -126,6 +142,11 @@ class Fp8Rowwise(Component):
 
     def kernel_units(self):
         return {"fp8_quant": self.rows * self.dim, "fp8_dequant": self.rows * self.dim}
+
+    def quality(self, q, torch):
+        self.run(q, 0, KernelTimer(torch, enabled=False))
+        return {"compression": round(4 * self.dim / (self.dim + 4), 3),
+                "rel_rms_error": _rel_rms(torch, self.out, self.x)}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -190,6 +211,15 @@ class UniformEF(Component):
     def kernel_units(self):
         return {k: self.n for k in self.kernels}
 
+    def quality(self, q, torch):
+        e_old = self.err.clone()
+        self.run(q, 10_000, KernelTimer(torch, enabled=False))
+        meta = 8 if self.scheme in (0, 4) else 4
+        p = self.g + e_old
+        return {"compression": round(32 / (self.bits + 8 * meta / self.bucket), 3),
+                "rel_rms_error_of_step": _rel_rms(torch, self.out, p),
+                "residual_rms_over_gradient_rms": _rms_ratio(torch, self.err, self.g)}
+
     def oracle_sample(self, frac):
         import oracle as orc
         n = max(self.bucket, int(self.n * frac) // self.bucket * self.bucket)
@@ -248,6 +278,15 @@ class SignVote(Component):
 
     def kernel_units(self):
         return {"encode_sign_ef": self.n, "sign_vote": self.M * self.n}
+
+    def quality(self, q, torch):
+        self.run(q, 10_000, KernelTimer(torch, enabled=False))
+        mean = self.g.mean(dim=0)
+        bits = ((self.vote.view(torch.int32).unsqueeze(1) >>
+                 torch.arange(32, device="cuda", dtype=torch.int32)) & 1).reshape(-1)[:self.n]
+        agree = float(((mean >= 0).to(torch.int32) == bits).float().mean())
+        return {"compression": round(32 * self.bucket / (self.bucket + 32), 3),
+                "vote_agrees_with_sign_of_mean": round(agree, 5)}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -312,6 +351,13 @@ class Receiver(Component):
 
     def host_outputs(self):
         return [self.out]
+
+    def quality(self, q, torch):
+        self.run(q, 10_000, KernelTimer(torch, enabled=False))
+        g = self.g.view(torch.bfloat16).float()
+        meta = 8 if self.scheme == 0 else 4
+        return {"compression_vs_bf16": round(16 / (self.bits + 8 * meta / self.bucket), 3),
+                "rel_rms_error_of_mean": _rel_rms(torch, self.out, g.mean(dim=0))}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -381,6 +427,12 @@ class TopkEF(Component):
     def kernel_units(self):
         return {"topk_encode_ef": self.n, f"topk_decode_m{self.M}": self.M * self.n}
 
+    def quality(self, q, torch):
+        self.run(q, 10_000, KernelTimer(torch, enabled=False))
+        return {"compression": round(4 * self.bucket / (5 * self.keep + 8), 3),
+                "kept_fraction": round(self.keep / self.bucket, 5),
+                "rel_rms_error_of_mean": _rel_rms(torch, self.out, self.g.mean(dim=0))}
+
     def oracle_sample(self, frac):
         import oracle as orc
         n = max(self.bucket, int(self.n * frac) // self.bucket * self.bucket)
@@ -437,6 +489,10 @@ class Reencode(Receiver):
 
     def host_outputs(self):
         return [self.codes2]
+
+    def quality(self, q, torch):
+        meta = 8 if self.scheme == 0 else 4
+        return {"compression_vs_fp32": round(32 / (self.bits + 8 * meta / self.bucket), 3)}
 
     def kernel_units(self):
         return {self.enc_name: self.n, self.dec_name: self.M * self.n}
@@ -757,6 +813,13 @@ def run_ours(args, world, rank, local):
     for k in kinfo:
         kinfo[k]["frac_of_peak"] = round(kinfo[k]["gbs"] / peak, 4)
 
+    quality = {}
+    for c in comps:
+        qc = c.quality(q, torch)
+        if qc is not None:
+            quality[c.name] = {k: (round(v, 6) if isinstance(v, float) else v) for k, v in qc.items()}
+    torch.cuda.synchronize()
+
     e2e = run_e2e(args, comps, q, torch, world, units)
 
     line = {
@@ -777,6 +840,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": timer.launches,
         "clocks": clocks,
+        "quality": quality,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(comps, args.cpu_seconds)

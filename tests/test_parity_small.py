@@ -457,3 +457,23 @@ def test_encode_ternary_bf16_near_draws(q):
     assert np.all(s_or == 1.0)
     assert_bits_equal(codes, c_or, f"ternary bf16 near draws ({small.size} planted, "
                                    f"{exact_hits} exactly on u)")
+
+
+def test_decode_after_a_worker_drops_out(q):
+    """A worker that fails before sending: the receiver decodes the M - 1
+    payloads that arrived (gathered contiguously on the host), and the result is
+    the oracle's over the same M - 1 workers in their order."""
+    M, n, bits, bucket = 6, 20_000 + 9, 8, 1024
+    payloads = [orc.encode_uniform(wl.outlier_gradient(n, seed=300 + w), bits=bits, bucket=bucket)
+                for w in range(M)]
+    dropped = 2
+    kept = [payloads[w] for w in range(M) if w != dropped]
+    codes = np.stack([c for c, _, _ in kept])
+    scale = np.stack([s for _, s, _ in kept])
+    offset = np.stack([o for _, _, o in kept])
+    out = torch.empty(n, device="cuda")
+    q.qc_decode_accumulate(dev(codes), codes.shape[1], dev(scale), dev(offset), scale.shape[1],
+                           M - 1, n, bits, bucket, 0, out, q.QC_OUT_MEAN)
+    want = orc.decode_accumulate(codes, scale, offset, M=M - 1, n=n, bits=bits, bucket=bucket,
+                                 scheme=0, flags=orc.OUT_MEAN)
+    assert_bits_equal(host(out), want, "decode without worker 2")
