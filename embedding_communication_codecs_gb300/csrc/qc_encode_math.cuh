@@ -520,6 +520,13 @@ __device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*r
 }
 
 
+// Team-wide reduction like team_reduce, synchronised only within the team
+// (team_sync), so teams proceed independently.  Every thread of the team calls
+// it together.
+template <int SCHEME>
+__device__ __forceinline__ void team_reduce_local(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
+                                                  int &buf, int W, int warp, int lane, int team);
+
 // ------------------------------------------------------------- percentiles
 
 // Unsigned keys that order like the floats (-0 just below +0).
@@ -695,6 +702,19 @@ __device__ __forceinline__ bool list_select16(const uint32_t *list, uint32_t m, 
     __syncwarp();
     out = list_select(sub, ms, r, lane);
     return true;
+}
+
+template <int SCHEME>
+__device__ __forceinline__ void team_reduce_local(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
+                                                  int &buf, int W, int warp, int lane, int team) {
+    st.warp_reduce();
+    if (W > 1) {
+        if (lane == 0) red[buf][warp] = st;
+        team_sync(W, team);
+        st = red[buf][team * W];
+        for (int w = 1; w < W; ++w) st.merge(red[buf][team * W + w]);
+        buf ^= 1;
+    }
 }
 
 // The keys of ranks r_lo and r_hi (0-based, ascending; NR = 1: r_lo only)

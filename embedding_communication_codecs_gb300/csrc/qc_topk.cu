@@ -74,6 +74,113 @@ __device__ __forceinline__ void team_scan(const uint32_t (&a)[kSlots], int W, in
     total = running;
 }
 
+// One bucket of the team (cnt > 0): selection, the counter scan, the kept
+// values' statistics, codes, slots, residuals and metadata.  FULL: every slot
+// of the team's window is valid.
+template <bool EF, bool SR, bool FULL>
+__device__ __forceinline__ void topk_bucket(const TopkParams &T, const float4 (&p)[kSlots],
+                                            uint32_t cnt, uint64_t b0, uint64_t k, int tt,
+                                            int team_threads, int W, int team, int warp, int lane,
+                                            uint32_t *region, uint32_t *tot,
+                                            Stats<kUniform> (*red)[kBlock / 32], int &buf,
+                                            uint32_t &parity) {
+    const EncodeParams &P = T.e;
+    const uint32_t K = min(T.keep, cnt);
+    uint32_t key[kSlots][4];
+#pragma unroll
+    for (int sl = 0; sl < kSlots; ++sl)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) key[sl][c] = __float_as_uint(get(p[sl], c)) << 1;
+    uint32_t thr, unused;
+    team_select<1, FULL>(key, cnt, P.bucket, cnt - K, cnt - K, tt, team_threads, W, team, warp % W,
+                         lane, region, parity, thr, unused);
+    // counters in index order: keys >= thr (low half), keys == thr (high half);
+    // and the statistics of the values with keys >= thr and with keys > thr
+    uint32_t a[kSlots];
+    Stats<kUniform> st_ge, st_gt;
+    st_ge.init();
+    st_gt.init();
+#pragma unroll
+    for (int sl = 0; sl < kSlots; ++sl) {
+        a[sl] = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+            if (FULL || j < cnt) {
+                const uint32_t kk = key[sl][c];
+                a[sl] += (kk >= thr ? 1u : 0u) + (kk == thr ? 0x10000u : 0u);
+                if (kk >= thr) st_ge.add(get(p[sl], c));
+                if (kk > thr) st_gt.add(get(p[sl], c));
+            }
+        }
+    }
+    uint32_t excl[kSlots], total;
+    team_scan(a, W, team, warp % W, lane, tot, excl, total);
+    const uint32_t ties = total >> 16;
+    const uint32_t need = K - ((total & 0xFFFFu) - ties);  // ties to keep, >= 1
+    Stats<kUniform> st;
+    if (need == ties) {
+        st = st_ge;  // every tie is kept
+    } else {         // rare: the first `need` ties in index order
+        st = st_gt;
+#pragma unroll
+        for (int sl = 0; sl < kSlots; ++sl) {
+            uint32_t run = excl[sl];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+                if (FULL || j < cnt) {
+                    const uint32_t kk = key[sl][c];
+                    if (kk == thr && (run >> 16) < need) st.add(get(p[sl], c));
+                    run += (kk >= thr ? 1u : 0u) + (kk == thr ? 0x10000u : 0u);
+                }
+            }
+        }
+    }
+    team_reduce_local<kUniform>(st, red, buf, W, warp, lane, team);
+    const BucketParams bp = Finish<kUniform, 8>::run(st, K);
+#pragma unroll
+    for (int sl = 0; sl < kSlots; ++sl) {
+        uint32_t run = excl[sl];
+        float4 e = p[sl];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
+            if (FULL || j < cnt) {
+                const uint32_t kk = key[sl][c];
+                const uint32_t ge_before = run & 0xFFFFu, tie_before = run >> 16;
+                if (kk > thr || (kk == thr && tie_before < need)) {
+                    const uint64_t i = b0 + j;
+                    float u = 0.0f;
+                    if constexpr (SR) u = uniform1(i, P.step, P.keys);
+                    float deq;
+                    const uint32_t q = quantize<kUniform, 8, SR>(get(p[sl], c), u, bp, deq);
+                    const uint32_t pos = (ge_before - tie_before) + min(tie_before, need);
+                    T.idx[k * T.keep + pos] = static_cast<uint32_t>(i);
+                    T.codes8[k * T.keep + pos] = static_cast<uint8_t>(q);
+                    set(e, c, __fsub_rn(get(p[sl], c), deq));
+                }
+                run += (kk >= thr ? 1u : 0u) + (kk == thr ? 0x10000u : 0u);
+            }
+        }
+        if constexpr (EF) {
+            const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u;
+            if (FULL || j + 4u <= cnt) {
+                __stcs(reinterpret_cast<float4 *>(P.err + b0 + j), e);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (j + c < cnt) P.err[b0 + j + c] = get(e, c);
+            }
+        }
+    }
+    for (uint32_t t = K + static_cast<uint32_t>(tt); t < T.keep; t += team_threads) {
+        T.idx[k * T.keep + t] = kNoIndex;
+        T.codes8[k * T.keep + t] = 0;
+    }
+    if (tt == 0) store_meta<kUniform>(P.scale, P.offset, k, bp);
+}
+
 template <typename TIn, bool EF, bool SR>
 __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ TopkParams T,
                                                       const __grid_constant__ EncodeTiles G) {
@@ -123,104 +230,15 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
             const uint32_t cnt = (kb < G.tb && b_off < tcnt) ? min(P.bucket, tcnt - b_off) : 0u;
             const uint64_t b0 = t0 + b_off;
             const uint64_t k = tile * G.tb + kb;
-            const bool whole = cnt == window && b_off + cnt <= staged;
             float4 p[kSlots];
-            if (whole)
+            if (cnt == window && b_off + cnt <= staged) {
                 load_slots_staged<TIn, EF, true>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
-            else
+                topk_bucket<EF, SR, true>(T, p, cnt, b0, k, tt, team_threads, W, team, warp, lane,
+                                          region, tot, red, buf, parity);
+            } else if (cnt) {
                 load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
-
-            Stats<kUniform> st;
-            st.init();
-            uint32_t K = 0u, need = 0u, thr = 0u;
-            uint32_t key[kSlots][4], excl[kSlots];
-#pragma unroll
-            for (int sl = 0; sl < kSlots; ++sl)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) key[sl][c] = __float_as_uint(get(p[sl], c)) << 1;
-            if (cnt) {
-                K = min(T.keep, cnt);
-                uint32_t unused;
-                if (whole)
-                    team_select<1, true>(key, cnt, P.bucket, cnt - K, cnt - K, tt, team_threads, W,
-                                         team, warp % W, lane, region, parity, thr, unused);
-                else
-                    team_select<1, false>(key, cnt, P.bucket, cnt - K, cnt - K, tt, team_threads, W,
-                                          team, warp % W, lane, region, parity, thr, unused);
-                // counters in index order: keys >= thr (low half), keys == thr (high half)
-                uint32_t a[kSlots];
-#pragma unroll
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    a[sl] = 0u;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
-                        if (j < cnt)
-                            a[sl] += (key[sl][c] >= thr ? 1u : 0u) + (key[sl][c] == thr ? 0x10000u : 0u);
-                    }
-                }
-                uint32_t total;
-                team_scan(a, W, team, warp % W, lane, tot, excl, total);
-                need = K - ((total & 0xFFFFu) - (total >> 16));  // ties to keep, >= 1
-                // statistics of the kept values
-#pragma unroll
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    uint32_t run = excl[sl];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
-                        if (j < cnt) {
-                            const bool kept = key[sl][c] > thr || (key[sl][c] == thr && (run >> 16) < need);
-                            if (kept) st.add(get(p[sl], c));
-                            run += (key[sl][c] >= thr ? 1u : 0u) + (key[sl][c] == thr ? 0x10000u : 0u);
-                        }
-                    }
-                }
-            }
-            team_reduce<kUniform>(st, red, buf, W, warp, lane, team);
-            if (cnt) {
-                const BucketParams bp = Finish<kUniform, 8>::run(st, K);
-#pragma unroll
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    uint32_t run = excl[sl];
-                    float4 e = p[sl];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u + c;
-                        if (j < cnt) {
-                            const uint32_t kk = key[sl][c];
-                            const uint32_t ge_before = run & 0xFFFFu, tie_before = run >> 16;
-                            const bool kept = kk > thr || (kk == thr && tie_before < need);
-                            if (kept) {
-                                const uint64_t i = b0 + j;
-                                float u = 0.0f;
-                                if constexpr (SR) u = uniform1(i, P.step, P.keys);
-                                float deq;
-                                const uint32_t q = quantize<kUniform, 8, SR>(get(p[sl], c), u, bp, deq);
-                                const uint32_t pos = (ge_before - tie_before) + min(tie_before, need);
-                                T.idx[k * T.keep + pos] = static_cast<uint32_t>(i);
-                                T.codes8[k * T.keep + pos] = static_cast<uint8_t>(q);
-                                set(e, c, __fsub_rn(get(p[sl], c), deq));
-                            }
-                            run += (kk >= thr ? 1u : 0u) + (kk == thr ? 0x10000u : 0u);
-                        }
-                    }
-                    if constexpr (EF) {
-                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * 4u;
-                        if (j + 4u <= cnt) {
-                            __stcs(reinterpret_cast<float4 *>(P.err + b0 + j), e);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                if (j + c < cnt) P.err[b0 + j + c] = get(e, c);
-                        }
-                    }
-                }
-                for (uint32_t t = K + static_cast<uint32_t>(tt); t < T.keep; t += team_threads) {
-                    T.idx[k * T.keep + t] = kNoIndex;
-                    T.codes8[k * T.keep + t] = 0;
-                }
-                if (tt == 0) store_meta<kUniform>(P.scale, P.offset, k, bp);
+                topk_bucket<EF, SR, false>(T, p, cnt, b0, k, tt, team_threads, W, team, warp, lane,
+                                           region, tot, red, buf, parity);
             }
         }
         if (!__syncthreads_and(ok)) {
