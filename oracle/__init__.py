@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY, SCHEME_QSGD, SCHEME_UNIFORM_CLIP = 0, 1, 2, 3, 4
+SCHEME_UNIFORM, SCHEME_SIGN, SCHEME_TERNARY, SCHEME_QSGD, SCHEME_UNIFORM_CLIP, SCHEME_LOG = 0, 1, 2, 3, 4, 5
 ROUND_NEAREST, ROUND_STOCHASTIC = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OUT_SUM, OUT_MEAN, ACCUMULATE_INTO_OUT = 0, 1, 2
@@ -69,6 +69,7 @@ def _L():
         lib.oracle_encode_sign.argtypes = [P, I, P, S, S, P, P]
         lib.oracle_encode_ternary.argtypes = [P, I, P, S, U64, S, I, U64, U32, P, P]
         lib.oracle_encode_qsgd.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P]
+        lib.oracle_encode_log.argtypes = [P, I, P, S, U64, I, S, I, U64, U32, P, P]
         lib.oracle_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I]
         lib.oracle_sign_vote.argtypes = [P, S, I, S, P]
         lib.oracle_topk_encode.argtypes = [P, I, P, S, U64, S, S, I, U64, U32, P, P, P, P]
@@ -83,7 +84,7 @@ def _L():
         lib.oracle_rowwise_fp8_dequant.argtypes = [P, P, S, S, P]
         for name in ("oracle_encode_uniform", "oracle_encode_uniform_clip", "oracle_encode_sign",
                      "oracle_encode_ternary",
-                     "oracle_encode_qsgd",
+                     "oracle_encode_qsgd", "oracle_encode_log",
                      "oracle_decode_accumulate", "oracle_sign_vote", "oracle_rowwise_fp8",
                      "oracle_topk_encode", "oracle_topk_decode",
                      "oracle_rowwise_fp8_dequant"):
@@ -203,6 +204,19 @@ def encode_qsgd(grad, err=None, *, bits, bucket, mode=ROUND_STOCHASTIC, seed=0, 
     return codes[:code_words(n, bits)], scale[:num_buckets(n, bucket)]
 
 
+def encode_log(grad, err=None, *, bits, bucket, mode=ROUND_NEAREST, seed=0, step=0, index_base=0):
+    """Logarithmic levels s * 2^(j - J) under a sign bit; returns (codes, s) and
+    updates ``err``."""
+    g = np.ascontiguousarray(grad)
+    n = g.size
+    codes = np.zeros(max(code_words(n, bits), 1), dtype=np.uint32)
+    scale = np.zeros(max(num_buckets(n, bucket), 1), dtype=np.float32)
+    rc = _L().oracle_encode_log(_ptr(g), _grad_dtype(g), _ptr(err), n, index_base, bits, bucket,
+                                mode, seed, step, _ptr(codes), _ptr(scale))
+    _check(rc, "encode_log")
+    return codes[:code_words(n, bits)], scale[:num_buckets(n, bucket)]
+
+
 def decode_accumulate(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM,
                       codes_stride_words=None, meta_stride=None, out=None):
     """``codes`` is uint32 of shape [M, stride] (or flat with explicit strides)."""
@@ -242,6 +256,8 @@ def reencode(codes, scale, offset, *, M, n, bits, bucket, scheme, flags=OUT_SUM,
         return r, c, s, o
     if scheme == SCHEME_SIGN:
         c, s = encode_sign(r, err, bucket=bucket)
+    elif scheme == SCHEME_LOG:
+        c, s = encode_log(r, err, bits=bits, bucket=bucket, mode=mode, seed=seed, step=step)
     elif scheme == SCHEME_TERNARY:
         c, s = encode_ternary(r, err, bucket=bucket, mode=mode, seed=seed, step=step)
     else:

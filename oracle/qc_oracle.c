@@ -38,7 +38,7 @@
 #define ORC_API __attribute__((visibility("default")))
 
 enum { ORC_SCHEME_UNIFORM = 0, ORC_SCHEME_SIGN = 1, ORC_SCHEME_TERNARY = 2, ORC_SCHEME_QSGD = 3,
-       ORC_SCHEME_UNIFORM_CLIP = 4 };
+       ORC_SCHEME_UNIFORM_CLIP = 4, ORC_SCHEME_LOG = 5 };
 enum { ORC_ROUND_NEAREST = 0, ORC_ROUND_STOCHASTIC = 1 };
 enum { ORC_DTYPE_F32 = 0, ORC_DTYPE_BF16 = 1 };
 enum { ORC_OUT_MEAN = 1, ORC_ACCUMULATE_INTO_OUT = 2 };
@@ -517,6 +517,87 @@ ORC_API int oracle_encode_qsgd(const void *grad, int dtype, float *err, size_t n
 }
 
 /* ------------------------------------------------------------------------ */
+/* Logarithmic (non-uniform) quantization with error feedback.
+ *
+ * p3 "Quantization Schemes" (Non-Uniform Quantization: logarithmic levels, more
+ * levels near zero, dequantization through a lookup table).  Readings: a b-bit
+ * code is one sign bit (top, set for p < 0) over b-1 level bits j; with
+ * J = 2^(b-1) - 1 the level magnitudes are 0 (j = 0) and s * 2^(j - J)
+ * (j = 1 .. J), s = max |p| over the bucket (zero taken as +0), so each level
+ * below the top is half the next; x = fl(|p| / s) is placed between its two
+ * adjacent levels and rounded to the nearer (ties to the even level index) or,
+ * stochastically, up with probability equal to its position between them (the
+ * rule the pages give for stochastic rounding, unbiased):
+ *   x >= 1:               j = J
+ *   2^(1-J) <= x < 1:     lower level 2^e (e = floor(log2 x)), m = (x - 2^e) / 2^e,
+ *                         j = e + J + [m > 1/2, or m = 1/2 and e + J odd]   (nearest)
+ *                         j = e + J + [u < m]                              (stochastic)
+ *   x < 2^(1-J):          f = x / 2^(1-J);  j = [f > 1/2] or [u < f]
+ *   s == 0:               j = 0
+ *   deq = +-(j ? fl(s * 2^(j - J)) : 0) with the code's sign;  e = p - deq
+ * Outputs: packed codes, scale[k] = s. */
+ORC_API int oracle_encode_log(const void *grad, int dtype, float *err, size_t n,
+                              uint64_t index_base, int bits, size_t bucket, int mode,
+                              uint64_t seed, uint32_t step, uint32_t *codes, float *scale_out)
+{
+    if (!(bits == 2 || bits == 4 || bits == 8) || !orc_valid_bucket(bucket))
+        return -1;
+    const int J = (1 << (bits - 1)) - 1;
+    const float lo1 = ldexpf(1.0f, 1 - J); /* the smallest non-zero level, in units of s */
+    memset(codes, 0, oracle_code_words(n, bits) * sizeof(uint32_t));
+    float *p = (float *)malloc(bucket * sizeof(float));
+    if (!p)
+        return -2;
+    size_t nb = oracle_num_buckets(n, bucket);
+    for (size_t k = 0; k < nb; ++k) {
+        size_t lo = k * bucket;
+        size_t cnt = (n - lo < bucket) ? (n - lo) : bucket;
+        float s = 0.0f;
+        for (size_t j = 0; j < cnt; ++j) {
+            float g = orc_load_grad(grad, dtype, lo + j);
+            p[j] = err ? err[lo + j] + g : g;
+            if (fabsf(p[j]) > s)
+                s = fabsf(p[j]);
+        }
+        s = orc_positive_zero(s);
+        for (size_t j = 0; j < cnt; ++j) {
+            uint32_t neg = (p[j] < 0.0f) ? 1u : 0u;
+            int lvl = 0;
+            if (s != 0.0f) {
+                float x = fabsf(p[j]) / s;
+                float u = (mode == ORC_ROUND_STOCHASTIC)
+                              ? oracle_uniform(seed, step, index_base + lo + j) : 0.0f;
+                if (x >= 1.0f) {
+                    lvl = J;
+                } else if (x >= lo1) {
+                    int ex;
+                    (void)frexpf(x, &ex); /* x = fr * 2^ex, fr in [1/2, 1) */
+                    float lower = ldexpf(1.0f, ex - 1);
+                    float m = (x - lower) / lower;
+                    int j0 = (ex - 1) + J;
+                    int up = (mode == ORC_ROUND_NEAREST)
+                                 ? (m > 0.5f || (m == 0.5f && (j0 & 1)))
+                                 : (u < m);
+                    lvl = j0 + up;
+                } else {
+                    float f = x / lo1;
+                    lvl = (mode == ORC_ROUND_NEAREST) ? (f > 0.5f) : (u < f);
+                }
+            }
+            orc_put_code(codes, lo + j, bits, (neg << (bits - 1)) | (uint32_t)lvl);
+            if (err) {
+                float mag = lvl ? s * ldexpf(1.0f, lvl - J) : 0.0f;
+                float deq = neg ? -mag : mag;
+                err[lo + j] = p[j] - deq;
+            }
+        }
+        scale_out[k] = s;
+    }
+    free(p);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Receiver side: dequantize M workers' payloads and accumulate in fp32.
  *
  * p1 "Where Quantization Sits" (receive, dequantize, continue); p2 "How
@@ -539,7 +620,7 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
 {
     if (M < 1 || !orc_valid_bucket(bucket))
         return -1;
-    if (scheme < ORC_SCHEME_UNIFORM || scheme > ORC_SCHEME_UNIFORM_CLIP)
+    if (scheme < ORC_SCHEME_UNIFORM || scheme > ORC_SCHEME_LOG)
         return -1;
     if (scheme == ORC_SCHEME_UNIFORM_CLIP) /* a uniform payload over the clipped range */
         scheme = ORC_SCHEME_UNIFORM;
@@ -549,7 +630,7 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
         return -1;
     if (scheme == ORC_SCHEME_TERNARY && bits != 2)
         return -1;
-    if (scheme == ORC_SCHEME_QSGD && !(bits == 2 || bits == 4 || bits == 8))
+    if ((scheme == ORC_SCHEME_QSGD || scheme == ORC_SCHEME_LOG) && !(bits == 2 || bits == 4 || bits == 8))
         return -1;
     for (size_t i = 0; i < n; ++i) {
         size_t k = i / bucket;
@@ -565,9 +646,14 @@ ORC_API int oracle_decode_accumulate(const uint32_t *codes, size_t codes_stride_
                 d = q ? s : -s;
             else if (scheme == ORC_SCHEME_TERNARY)
                 d = (float)((int)q - 1) * s;
-            else { /* QSGD: sign bit over the level */
+            else if (scheme == ORC_SCHEME_QSGD) { /* sign bit over the level */
                 uint32_t lvl = q & ((1u << (bits - 1)) - 1u);
                 float mag = (float)lvl * s;
+                d = (q >> (bits - 1)) ? -mag : mag;
+            } else { /* LOG: sign bit over the level; the level's power of two */
+                int J = (1 << (bits - 1)) - 1;
+                int lvl = (int)(q & ((1u << (bits - 1)) - 1u));
+                float mag = lvl ? s * ldexpf(1.0f, lvl - J) : 0.0f;
                 d = (q >> (bits - 1)) ? -mag : mag;
             }
             acc = acc + d;

@@ -930,3 +930,71 @@ def test_topk_decode_scatter_order_and_skips():
     o2 = np.zeros((3, 1), np.float32)
     r = orc.topk_decode(idx2, c2, s2, o2, M=3, n=1, bucket=32, keep=1)
     assert r[0] == np.float32(1.0)
+
+
+# ------------------------------------------------------------------ log levels
+
+def _unpack4(c, n, bits):
+    per = 32 // bits
+    return np.array([(int(c[i // per]) >> (bits * (i % per))) & ((1 << bits) - 1) for i in range(n)])
+
+
+def test_log_levels_hand_worked():
+    """4-bit codes (J = 7, levels 2^(j-7) of s = 1): exact levels, the midpoints
+    (ties to the even level index), the region below the smallest level, signs."""
+    g = np.array([1.0, 0.5, 0.25, 0.75, 0.375, 0.7, 0.8, -0.5, 0.0, 2.0 ** -6, 2.0 ** -7,
+                  0.012, -0.3, 3 * 2.0 ** -8], np.float32)
+    want = [7, 6, 5, 6, 6, 6, 7, 8 | 6, 0, 1, 0, 1, 8 | 5, 1]
+    c, s = orc.encode_log(g, bits=4, bucket=32)
+    assert s[0] == 1.0
+    assert list(_unpack4(c, g.size, 4)) == want
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_log_nearest_is_the_nearest_level(bits):
+    """Nearest rounding picks a level at least as close as either neighbour,
+    measured exactly (fractions), on a random bucket of every width."""
+    J = (1 << (bits - 1)) - 1
+    g = (wl.std_normal(30 + bits, 1, 512) * np.float32(1e-2)).astype(np.float32)
+    c, s = orc.encode_log(g, bits=bits, bucket=512)
+    codes = _unpack4(c, g.size, bits)
+    sv = Fraction(float(s[0]))
+    levels = [Fraction(0)] + [sv * Fraction(2) ** (j - J) for j in range(1, J + 1)]
+    for v, code in zip(g, codes):
+        j = int(code) & ((1 << (bits - 1)) - 1)
+        assert (int(code) >> (bits - 1)) == (1 if v < 0 else 0)
+        x = abs(Fraction(float(v)))
+        best = min(abs(x - L) for L in levels)
+        # the oracle decides on fl(|p| / s), one rounding away from the exact ratio
+        assert abs(x - levels[j]) <= best + sv * Fraction(2) ** -23
+
+
+def test_log_stochastic_is_unbiased():
+    bits, n, steps = 4, 64, 4000
+    g = (wl.std_normal(33, 1, n) * np.float32(0.1)).astype(np.float32)
+    acc = np.zeros(n)
+    for t in range(steps):
+        c, s = orc.encode_log(g, bits=bits, bucket=64, mode=orc.ROUND_STOCHASTIC, seed=9, step=t)
+        acc += orc.decode_accumulate(c, s, None, M=1, n=n, bits=bits, bucket=64, scheme=orc.SCHEME_LOG)
+    mean = acc / steps
+    # the two levels around |p| are at most max(|p|, s * 2^(1-J)) apart (above the
+    # smallest level the gap is the lower level, below it the smallest level):
+    # one draw's sd is at most half the gap
+    gap = np.maximum(np.abs(g), s[0] * 2.0 ** (1 - ((1 << (bits - 1)) - 1)))
+    assert np.all(np.abs(mean - g) <= 6 * gap / 2 / np.sqrt(steps) + 1e-9)
+
+
+def test_log_decode_closed_form_and_zero_bucket():
+    bits, J = 8, 127
+    g = np.zeros(64, np.float32)
+    g[:32] = (wl.std_normal(34, 1, 32) * np.float32(1e-3)).astype(np.float32)
+    err = np.zeros(64, np.float32)
+    c, s = orc.encode_log(g, err, bits=bits, bucket=32)
+    assert s[1] == 0.0 and np.all(_unpack4(c, 64, bits)[32:] == 0)
+    d = orc.decode_accumulate(c, s, None, M=1, n=64, bits=bits, bucket=32, scheme=orc.SCHEME_LOG)
+    codes = _unpack4(c, 64, bits)
+    for i in range(32):
+        j = int(codes[i]) & 0x7F
+        mag = np.float32(0.0) if j == 0 else np.float32(s[0]) * np.float32(2.0 ** (j - J))
+        want = -mag if codes[i] >> 7 else mag
+        assert d[i] == want and err[i] == np.float32(g[i] - want)
