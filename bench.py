@@ -160,8 +160,8 @@ class Fp8Rowwise(Component):
 
 
 class UniformEF(Component):
-    """Encode with error feedback of one flat fp32 gradient (uniform or QSGD
-    scheme), then decode M = 1."""
+    """Encode with error feedback of one flat fp32 gradient (uniform, QSGD,
+    clipped uniform or logarithmic-level scheme), then decode M = 1."""
 
     def __init__(self, name, n, bits, bucket, stochastic, seed, sigma_mode, scheme=0):
         self.name, self.n, self.bits, self.bucket = name, n, bits, bucket
@@ -171,7 +171,7 @@ class UniformEF(Component):
         meta = 8 if scheme in (0, 4) else 4
         enc = 12 * n + 4 * words + meta * nb
         dec = 4 * words + meta * nb + 4 * n
-        tag = {0: f"u{bits}", 3: f"qsgd{bits}", 4: f"clip{bits}"}[scheme]
+        tag = {0: f"u{bits}", 3: f"qsgd{bits}", 4: f"clip{bits}", 5: f"log{bits}"}[scheme]
         self.enc_name, self.dec_name = f"encode_{tag}_ef", f"decode_{tag}_m1"
         self.kernels = {self.enc_name: (1, enc), self.dec_name: (1, dec)}
         self.units = 2 * n
@@ -233,9 +233,9 @@ class UniformEF(Component):
                 c, s, o = enc(g[lo:hi], err[lo:hi], bits=self.bits, bucket=self.bucket, mode=mode,
                               seed=self.seed, step=0, index_base=lo)
             else:
-                (c, s), o = orc.encode_qsgd(g[lo:hi], err[lo:hi], bits=self.bits,
-                                            bucket=self.bucket, mode=mode, seed=self.seed,
-                                            step=0, index_base=lo), None
+                enc = orc.encode_qsgd if self.scheme == 3 else orc.encode_log
+                (c, s), o = enc(g[lo:hi], err[lo:hi], bits=self.bits, bucket=self.bucket,
+                                mode=mode, seed=self.seed, step=0, index_base=lo), None
             orc.decode_accumulate(c, s, o, M=1, n=hi - lo, bits=self.bits, bucket=self.bucket,
                                   scheme=self.scheme)
         return _split(go, n, self.bucket), 2 * n
@@ -556,6 +556,8 @@ def make_workload(name):
         "rx_ternary": lambda: [Receiver("rx_ternary", 2, 2)],
         "qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 250_000_000, 4, 512, True, 2, "bucket",
                                        scheme=3)],
+        "log4_ef": lambda: [UniformEF("log4_ef", 250_000_000, 4, 512, True, 2, "bucket",
+                                      scheme=5)],
         "rx_reencode_u8": lambda: [Reencode("rx_reencode_u8", 0, 8)],
         "rx_reencode_ternary": lambda: [Reencode("rx_reencode_ternary", 2, 2)],
         "topk_ef": lambda: [TopkEF()],
@@ -570,6 +572,8 @@ def make_workload(name):
         "probe_sr4_ef": lambda: [UniformEF("sr4_ef", 1 << 26, 4, 512, True, 2, "bucket")],
         "probe_qsgd4_ef": lambda: [UniformEF("qsgd4_ef", 1 << 26, 4, 512, True, 2, "bucket",
                                              scheme=3)],
+        "probe_log4_ef": lambda: [UniformEF("log4_ef", 1 << 26, 4, 512, True, 2, "bucket",
+                                            scheme=5)],
         "probe_clip8_ef": lambda: [UniformEF("clip8_ef", 1 << 26, 8, 2048, False, 0, "outlier",
                                              scheme=4)],
         "probe_sign": lambda: [SignVote(n=1 << 24, M=2)],

@@ -23,6 +23,7 @@ from .build import LIB_PATH
 QC_OK, QC_ERR_NULL, QC_ERR_INVALID_ARG, QC_ERR_ALIGNMENT, QC_ERR_UNSUPPORTED, QC_ERR_CUDA = range(6)
 QC_SCHEME_UNIFORM, QC_SCHEME_SIGN, QC_SCHEME_TERNARY, QC_SCHEME_QSGD = 0, 1, 2, 3
 QC_SCHEME_UNIFORM_CLIP = 4
+QC_SCHEME_LOG = 5
 QC_ROUND_NEAREST, QC_ROUND_STOCHASTIC = 0, 1
 QC_DTYPE_F32, QC_DTYPE_BF16 = 0, 1
 QC_OUT_SUM, QC_OUT_MEAN, QC_ACCUMULATE_INTO_OUT = 0, 1, 2

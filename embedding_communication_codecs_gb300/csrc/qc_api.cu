@@ -12,7 +12,7 @@
 
 static_assert(int{QC_SCHEME_UNIFORM} == qc::kUniform && int{QC_SCHEME_SIGN} == qc::kSign &&
                   int{QC_SCHEME_TERNARY} == qc::kTernary && int{QC_SCHEME_QSGD} == qc::kQsgd &&
-                  int{QC_SCHEME_UNIFORM_CLIP} == qc::kClip,
+                  int{QC_SCHEME_UNIFORM_CLIP} == qc::kClip && int{QC_SCHEME_LOG} == qc::kLog,
               "the public scheme numbers are the kernels' template arguments");
 
 namespace {
@@ -207,6 +207,9 @@ qc_status check_scheme(const char *fn, qc_scheme scheme, int bits) {
     } else if (scheme == QC_SCHEME_QSGD) {
         if (bits != 2 && bits != 4 && bits != 8)
             return fail(QC_ERR_INVALID_ARG, "%s: QSGD bits must be 2, 4 or 8 (got %d)", fn, bits);
+    } else if (scheme == QC_SCHEME_LOG) {
+        if (bits != 2 && bits != 4 && bits != 8)
+            return fail(QC_ERR_INVALID_ARG, "%s: logarithmic-level bits must be 2, 4 or 8 (got %d)", fn, bits);
     } else {
         return fail(QC_ERR_INVALID_ARG, "%s: unknown scheme %d", fn, scheme);
     }
@@ -297,6 +300,7 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
     *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
              qc::take_encode_clip_bf16_errors() | qc::take_reencode_other_errors() |
+             qc::take_encode_log_errors() | qc::take_reencode_log_errors() |
              qc::take_topk_errors() |
              qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
@@ -378,6 +382,11 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
         return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                                dtype == QC_DTYPE_BF16, st),
                          "qc_encode_ef");
+    if (scheme == QC_SCHEME_LOG)
+        return fail(QC_ERR_UNSUPPORTED,
+                    "qc_encode_ef: logarithmic levels need a 16-byte aligned gradient and a bucket of "
+                    "at most %u elements (or 1024, 2048, 4096 or 8192 for bf16 without error feedback)",
+                    qc::kWindowPerWarp * (qc::kBlock / 32));
     return from_cuda(qc::launch_encode(p, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                        dtype == QC_DTYPE_BF16, st),
                      "qc_encode_ef");

@@ -219,6 +219,11 @@ cudaError_t launch_vote_np(const VoteParams &p, bool vec, cudaStream_t stream) {
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream) {
     if (scheme == kSign) return launch_decode_one<kSign, 1>(p, stream);
     if (scheme == kTernary) return launch_decode_one<kTernary, 2>(p, stream);
+    if (scheme == kLog) {
+        if (bits == 2) return launch_decode_one<kLog, 2>(p, stream);
+        if (bits == 4) return launch_decode_one<kLog, 4>(p, stream);
+        return launch_decode_one<kLog, 8>(p, stream);
+    }
     if (scheme == kQsgd) {
         if (bits == 2) return launch_decode_one<kQsgd, 2>(p, stream);
         if (bits == 4) return launch_decode_one<kQsgd, 4>(p, stream);

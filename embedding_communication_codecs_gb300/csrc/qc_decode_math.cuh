@@ -33,6 +33,14 @@ __device__ __forceinline__ float dequant_code(uint32_t f, int c, float sc, float
         return __fmaf_rn(code_value<BITS>(f, c), sc, of);
     } else if constexpr (SCHEME == kTernary) {
         return __fmaf_rn(code_value<BITS>(f, c), sc, -sc);
+    } else if constexpr (SCHEME == kLog) {
+        // sign bit over the level index j: +-fl(s * 2^(j - J)), the power of two
+        // built from its exponent bits (the level table), 0 for j = 0
+        constexpr uint32_t J = (1u << (BITS - 1)) - 1u;
+        const uint32_t code = (f >> (c * BITS)) & ((1u << BITS) - 1u);
+        const uint32_t lvl = code & J;
+        const float mag = lvl ? __fmul_rn(sc, __uint_as_float((lvl + 127u - J) << 23)) : 0.0f;
+        return __uint_as_float(__float_as_uint(mag) | ((code << (32 - BITS)) & 0x80000000u));
     } else if constexpr (SCHEME == kQsgd) {
         // sign bit over the level: +-fl(level * unit), the sign set by OR
         const uint32_t code = (f >> (c * BITS)) & ((1u << BITS) - 1u);

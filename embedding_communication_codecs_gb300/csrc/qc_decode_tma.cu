@@ -214,6 +214,11 @@ cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int s
                               cudaStream_t stream) {
     if (scheme == kSign) return launch_one<kSign, 1>(p, g, stream);
     if (scheme == kTernary) return launch_one<kTernary, 2>(p, g, stream);
+    if (scheme == kLog) {
+        if (bits == 2) return launch_one<kLog, 2>(p, g, stream);
+        if (bits == 4) return launch_one<kLog, 4>(p, g, stream);
+        return launch_one<kLog, 8>(p, g, stream);
+    }
     if (scheme == kQsgd) {
         if (bits == 2) return launch_one<kQsgd, 2>(p, g, stream);
         if (bits == 4) return launch_one<kQsgd, 4>(p, g, stream);

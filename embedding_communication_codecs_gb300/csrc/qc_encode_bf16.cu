@@ -72,7 +72,7 @@ struct PackedStats {
         if constexpr (SCHEME == kUniform) {
             st.mn = fminf(st.mn, fminf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u)));
             st.mx = fmaxf(st.mx, fmaxf(__uint_as_float(b << 16), __uint_as_float(b & 0xFFFF0000u)));
-        } else if constexpr (SCHEME == kTernary) {
+        } else if constexpr (SCHEME == kTernary || SCHEME == kLog) {  // max |p|
             st.add(__uint_as_float(a << 16));
             st.add(__uint_as_float(a & 0xFFFF0000u));
         }
@@ -423,6 +423,11 @@ cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int 
         if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, stream);
         if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, stream);
         return launch_round<kQsgd, 8>(p, g, stochastic, stream);
+    }
+    if (scheme == kLog) {
+        if (bits == 2) return launch_round<kLog, 2>(p, g, stochastic, stream);
+        if (bits == 4) return launch_round<kLog, 4>(p, g, stochastic, stream);
+        return launch_round<kLog, 8>(p, g, stochastic, stream);
     }
     switch (bits) {
         case 1: return launch_round<kUniform, 1>(p, g, stochastic, stream);

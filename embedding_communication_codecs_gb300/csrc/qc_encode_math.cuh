@@ -118,6 +118,16 @@ struct Finish<kQsgd, BITS> {
     }
 };
 
+template <>
+struct Stats<kLog> : Stats<kTernary> {};  // max |p|
+
+template <int BITS>
+struct Finish<kLog, BITS> {
+    static __device__ __forceinline__ BucketParams run(const Stats<kLog> &st, uint32_t) {
+        return BucketParams{positive_zero(st.amax), 0.0f};
+    }
+};
+
 // CLIP: the bounds are order statistics found by team_percentiles(), not a
 // running reduction, so the add/merge operations are never used.
 template <>
@@ -181,6 +191,38 @@ __device__ __forceinline__ uint32_t quantize(float p, float u, const BucketParam
         const float mag = __fmul_rn(small_uint_to_float(q), unit);
         deq = neg ? -mag : mag;
         return (neg << (BITS - 1)) | q;
+    } else if constexpr (SCHEME == kLog) {
+        // levels 0 and s * 2^(j - J): x = |p| / s sits between two levels; its
+        // exponent gives the lower one and its mantissa the position between
+        constexpr int J = (1 << (BITS - 1)) - 1;
+        const uint32_t neg = p < 0.0f ? 1u : 0u;
+        const float s = bp.a;
+        uint32_t lvl = 0u;
+        if (s != 0.0f) {
+            const float x = __fdiv_rn(fabsf(p), s);
+            const uint32_t xb = __float_as_uint(x);
+            const int e = static_cast<int>(xb >> 23) - 127;  // x is normal here when e >= 1 - J
+            if (x >= 1.0f) {
+                lvl = J;
+            } else if (e >= 1 - J) {
+                const uint32_t j0 = static_cast<uint32_t>(e + J);
+                const float m = __fsub_rn(__uint_as_float((xb & 0x7FFFFFu) | 0x3F800000u), 1.0f);
+                bool up;
+                if constexpr (SR) up = u < m;
+                else up = m > 0.5f || (m == 0.5f && (j0 & 1u));
+                lvl = j0 + (up ? 1u : 0u);
+            } else {
+                // below the smallest level 2^(1-J): the position x / 2^(1-J), exact
+                const float f = __fmul_rn(x, __uint_as_float(static_cast<uint32_t>(127 + J - 1) << 23));
+                bool up;
+                if constexpr (SR) up = u < f;
+                else up = f > 0.5f;
+                lvl = up ? 1u : 0u;
+            }
+        }
+        const float mag = lvl ? __fmul_rn(s, __uint_as_float((lvl + 127u - J) << 23)) : 0.0f;
+        deq = neg ? -mag : mag;
+        return (neg << (BITS - 1)) | lvl;
     } else if constexpr (SCHEME == kSign) {
         const bool pos = p >= 0.0f;
         deq = pos ? bp.a : -bp.a;
@@ -228,7 +270,7 @@ __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
     const float d = (SCHEME == kUniform || SCHEME == kClip) ? bp.scale : bp.a;
     FastQ f;
     const bool normal = d >= 0x1p-125f && d <= 0x1p125f;
-    f.usable = SCHEME == kSign || normal;  // the sign code needs no division
+    f.usable = SCHEME == kSign || (SCHEME != kLog && normal);  // sign: no division; LOG: exact only
     f.rinv = (SCHEME != kSign && normal) ? __frcp_rn(d) : 0.0f;
     f.delta2 = (SCHEME == kUniform || SCHEME == kClip) ? static_cast<float>(1u << BITS) * 0x1p-21f
                : SCHEME == kQsgd     ? static_cast<float>(1u << (BITS - 1)) * 0x1p-21f

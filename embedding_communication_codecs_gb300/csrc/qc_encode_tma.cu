@@ -20,6 +20,7 @@ namespace qc {
 
 cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                               int stochastic, int bf16, cudaStream_t stream) {
+    if (scheme == kLog) return launch_encode_log(p, g, bits, stochastic, bf16, stream);
     if (scheme == kSign) return launch_dtype<kSign, 1, false>(p, g, bf16, stream);
     if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, bf16, stream);
     if (scheme == kQsgd) {

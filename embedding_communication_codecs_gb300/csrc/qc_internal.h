@@ -7,7 +7,7 @@
 
 namespace qc {
 
-enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2, kQsgd = 3, kClip = 4 };
+enum Scheme : int { kUniform = 0, kSign = 1, kTernary = 2, kQsgd = 3, kClip = 4, kLog = 5 };
 
 // Elements a team of W warps covers per window: 4 float4 slots per lane.
 constexpr int kSlots = 4;
@@ -222,6 +222,9 @@ cudaError_t launch_encode_clip(const EncodeParams &p, const EncodeTiles &g, int 
                                int stochastic, int bf16, cudaStream_t stream);
 cudaError_t launch_encode_clip_bf16(const EncodeParams &p, const EncodeTiles &g, int bits,
                                     int stochastic, cudaStream_t stream);
+// The logarithmic-level scheme in the pipelined kernel (its own translation unit).
+cudaError_t launch_encode_log(const EncodeParams &p, const EncodeTiles &g, int bits,
+                              int stochastic, int bf16, cudaStream_t stream);
 cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                                int stochastic, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
@@ -231,6 +234,8 @@ cudaError_t launch_reencode(const ReencodeParams &p, const ReencodeTiles &g, int
                             int stochastic, cudaStream_t stream);
 cudaError_t launch_reencode_other(const ReencodeParams &p, const ReencodeTiles &g, int scheme,
                                   int bits, int stochastic, cudaStream_t stream);
+cudaError_t launch_reencode_log(const ReencodeParams &p, const ReencodeTiles &g, int bits,
+                                int stochastic, cudaStream_t stream);
 cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int stochastic, int bf16,
                                cudaStream_t stream);
 cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream);
@@ -249,7 +254,9 @@ cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 uint32_t take_encode_errors();
 uint32_t take_encode_clip_errors();
 uint32_t take_encode_clip_bf16_errors();
+uint32_t take_encode_log_errors();
 uint32_t take_reencode_other_errors();
+uint32_t take_reencode_log_errors();
 uint32_t take_topk_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();

@@ -7,6 +7,7 @@ namespace qc {
 
 cudaError_t launch_reencode_other(const ReencodeParams &p, const ReencodeTiles &g, int scheme,
                                   int bits, int stochastic, cudaStream_t stream) {
+    if (scheme == kLog) return launch_reencode_log(p, g, bits, stochastic, stream);
     if (scheme == kSign) return launch_ef<kSign, 1, false>(p, g, stream);
     if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, stream);
     if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, stream);

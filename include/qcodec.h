@@ -66,7 +66,8 @@ typedef enum {
     QC_SCHEME_SIGN = 1,       /* 1 bit: sign, per-bucket fp32 scale = mean |p|        */
     QC_SCHEME_TERNARY = 2,    /* 2 bits: {-1,0,+1} -> codes {0,1,2}, scale = max |p|  */
     QC_SCHEME_QSGD = 3,       /* sign bit over bits-1 level bits, scale = ||p||_2 / s */
-    QC_SCHEME_UNIFORM_CLIP = 4 /* uniform over the 1st..99th percentile range          */
+    QC_SCHEME_UNIFORM_CLIP = 4, /* uniform over the 1st..99th percentile range         */
+    QC_SCHEME_LOG = 5         /* sign bit over a power-of-two level index, s = max |p| */
 } qc_scheme;
 
 typedef enum {
@@ -137,6 +138,19 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *     part.  Buckets of at most 99 elements reduce to UNIFORM.  Needs a bucket of
  *     at most 4096 elements and a 16-byte aligned gradient (else
  *     QC_ERR_UNSUPPORTED).  The payload decodes as UNIFORM.
+ *   LOG ("Quantization Schemes", Non-Uniform Quantization: logarithmic levels,
+ *     finer near zero; bits 2, 4 or 8): J = 2^(bits-1) - 1, s = max |p| (zero
+ *     taken as +0), level magnitudes 0 (j = 0) and fl(s * 2^(j - J)) (j = 1..J).
+ *     s == 0: every code 0.  Else x = fl(|p_i| / s) and
+ *       x >= 1: j = J
+ *       2^(1-J) <= x < 1: x = 2^e (1 + m), 0 <= m < 1 (exact), and
+ *         NEAREST:    j = e + J + [m > 1/2, or m = 1/2 and e + J odd]
+ *         STOCHASTIC: j = e + J + [u_i < m]
+ *       x < 2^(1-J): f = x * 2^(J-1) (exact) and j = NEAREST ? [f > 1/2] : [u_i < f]
+ *     code_i = [p_i < 0] << (bits-1) | j; deq_i = +-(j ? fl(s * 2^(j - J)) : 0);
+ *     scale[k] = s.  Needs a 16-byte aligned gradient and a bucket of at most
+ *     4096 elements (bf16 without error feedback: 1024, 2048, 4096 or 8192),
+ *     else QC_ERR_UNSUPPORTED.
  * Then, with error feedback, err_i = fl(p_i - deq_i) is written in place.
  *
  * Stochastic draw for element i (global index within this call):
@@ -145,7 +159,8 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *
  * grad   : n elements of `dtype`; 16-byte aligned (f32) or 8-byte aligned (bf16).
  * err    : n fp32, in/out, 16-byte aligned, or NULL for no error feedback.
- * bits   : UNIFORM and UNIFORM_CLIP 1, 2, 4 or 8; SIGN 1; TERNARY 2; QSGD 2, 4 or 8.
+ * bits   : UNIFORM and UNIFORM_CLIP 1, 2, 4 or 8; SIGN 1; TERNARY 2; QSGD and LOG
+ *          2, 4 or 8.
  * bucket : elements per bucket, a multiple of 32, 32 <= bucket <= 2^24.
  * codes  : out, qc_code_words(n, bits) uint32 words, 4-byte aligned.
  * scale  : out, qc_num_buckets(n, bucket) fp32.
@@ -168,7 +183,9 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
  *   acc = +0; for w = 0 .. M-1 in this order: acc = fl(acc + d_w,i) with
  *     UNIFORM d = fma(q, scale_w[k], offset_w[k]); SIGN d = bit ? s_w[k] : -s_w[k];
  *     TERNARY d = (code - 1) * s_w[k]; QSGD d = +-fl(level * unit_w[k]) with the
- *     sign from the code's top bit and the level from the rest
+ *     sign from the code's top bit and the level from the rest; LOG
+ *     d = +-(j ? fl(s_w[k] * 2^(j - J)) : 0), the sign (a zero level keeps it,
+ *     giving -0) from the top bit and j from the rest
  *   r = (flags & QC_OUT_MEAN) ? fl(acc / M) : acc
  *   out_i = (flags & QC_ACCUMULATE_INTO_OUT) ? fl(out_i + r) : r
  *
