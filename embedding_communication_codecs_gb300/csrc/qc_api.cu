@@ -58,9 +58,13 @@ int team_warps_for(size_t elems) {
 }
 
 // Tiling for the TMA-pipelined encode: whole buckets per tile, the bucket count
-// a multiple of the block's teams, at least 16 KB of input per stage and three
-// stages (two above 32 KB), so small stages leave room for 4 blocks per SM.  Buckets larger than one team window (4096) and
-// gradients whose base is not 16-byte aligned take the direct kernel.
+// a multiple of the block's teams, at least 16 KB of input per stage.  Stages
+// under 32 KB come three to a block (room for 4 blocks per SM); from 32 KB on
+// two, so that three blocks share an SM (measured 2-16 % faster for the fp32
+// encodes with error feedback), except that a block of one team (4096-element
+// buckets) keeps three 32 KB stages, which measured faster there.  Buckets
+// larger than one team window (4096) and gradients whose base is not 16-byte
+// aligned take the direct kernel.
 bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool grad16,
                       qc::EncodeTiles &t, size_t extra_smem = 0) {
     if (!grad16 || p.two_pass) return false;
@@ -72,7 +76,7 @@ bool encode_tiles_for(const qc::EncodeParams &p, size_t esize, bool ef, bool gra
     if (tb < teams) tb = teams;
     const size_t stage = static_cast<size_t>(tb) * p.bucket * per_elem;
     if (stage > 64 * 1024) return false;
-    uint32_t stages = stage <= 32 * 1024 ? 3u : 2u;
+    uint32_t stages = (stage < 32 * 1024 || (stage == 32 * 1024 && teams == 1)) ? 3u : 2u;
     // kernels with per-team selection buffers keep two blocks per SM
     if (stages == 3 && 3 * stage + extra_smem > 110 * 1024) stages = 2;
     t.tb = tb;

@@ -13,6 +13,11 @@
 // team thread tt holds elements (s * 32 W + tt) * 8 .. +7 as one 16-byte
 // shared-memory read; a team of W = ceil(bucket / 1024) warps owns a bucket, so
 // the common bucket of 1024 needs no block barrier at all.
+//
+// Nor does the pipeline: each warp counts itself off a stage when it is done
+// with it (a shared-memory counter), and the warp that completes the count
+// refills the stage with the block's next tile but `stages`.  Warps therefore
+// run up to two tiles apart instead of meeting at a barrier every tile.
 #include "qc_encode_math.cuh"
 #include "qc_pipeline.cuh"
 
@@ -172,6 +177,9 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
     auto red = reinterpret_cast<Stats<SCHEME>(*)[kBlock / 32]>(full + G.stages);
+    // per stage: warps done with its current tile (cumulative), and tiles issued into it
+    uint32_t *done = reinterpret_cast<uint32_t *>(red + 2);
+    uint32_t *issued = done + G.stages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int W = G.warps;
@@ -182,14 +190,21 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
     const uint16_t *gsrc = static_cast<const uint16_t *>(P.grad);
 
     if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < G.stages; ++s) mbar_init(&full[s], 1);
+        for (uint32_t s = 0; s < G.stages; ++s) {
+            mbar_init(&full[s], 1);
+            done[s] = 0u;
+            issued[s] = 0u;
+        }
         fence_barrier_init();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < G.stages; ++s) {
             const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
-            if (tile < G.ntiles) issue_tile(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+            if (tile < G.ntiles) {
+                issue_tile(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+                issued[s] = 1u;
+            }
         }
     }
     const PhiloxKeys &keys = P.keys;
@@ -201,7 +216,11 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
         const uint32_t s = it % G.stages;
         const uint32_t parity = (it / G.stages) & 1u;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        const bool ok = mbar_wait(&full[s], parity);
+        // the team agrees on the wait's outcome, so its shuffles and barriers stay whole
+        if (!team_all(mbar_wait(&full[s], parity), W, team)) {
+            failed = true;
+            break;
+        }
 
         const uint64_t t0 = tile * G.te;
         const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
@@ -253,7 +272,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                 }
             }
             ps.fold_into(st);
-            team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
+            team_reduce_local<SCHEME>(st, red, buf, W, warp, lane, team);
             const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
             const FastQ fq = fast_params<SCHEME, BITS>(bp);
 
@@ -376,22 +395,31 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
             }
             if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);
         }
-        if (!__syncthreads_and(ok)) {
-            failed = true;
-            break;
-        }
-        if (threadIdx.x == 0) {
-            const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
-            if (next < G.ntiles) issue_tile(P, G, next, smem + s * G.stage_bytes, &full[s]);
+        // this warp is done with the stage (its reads have returned: their values
+        // are used above); the warp that completes the count refills the stage
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const uint32_t before = atomicAdd(&done[s], 1u);
+            if (before % (kBlock / 32) == (kBlock / 32) - 1) {
+                __threadfence_block();
+                fence_proxy_async_shared();  // generic reads before the bulk copy's writes
+                const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
+                if (next < G.ntiles) {
+                    issue_tile(P, G, next, smem + s * G.stage_bytes, &full[s]);
+                    issued[s] += 1u;
+                }
+            }
         }
     }
-    if (failed && threadIdx.x == 0) {
-        atomicOr(&g_encode_bf16_errors, kErrPipelineTimeout);
-        for (uint32_t d = 0; d < G.stages; ++d) {
-            const uint32_t j = it + d;
-            const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
-            if (tile < G.ntiles) mbar_wait(&full[j % G.stages], (j / G.stages) & 1u);
-        }
+    if (failed && lane == 0) atomicOr(&g_encode_bf16_errors, kErrPipelineTimeout);
+    // A team that gave up leaves its stages unrefilled, so the other teams' waits
+    // run out too; every warp gets here.  Copies still in flight (only after a
+    // failure) must land before the block's shared memory goes away.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (uint32_t d = 0; d < G.stages; ++d)
+            if (issued[d]) mbar_wait(&full[d], (issued[d] - 1u) & 1u);
     }
 }
 

@@ -270,12 +270,64 @@ __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
     const float d = (SCHEME == kUniform || SCHEME == kClip) ? bp.scale : bp.a;
     FastQ f;
     const bool normal = d >= 0x1p-125f && d <= 0x1p125f;
-    f.usable = SCHEME == kSign || (SCHEME != kLog && normal);  // sign: no division; LOG: exact only
+    f.usable = SCHEME == kSign || normal;  // the sign code needs no division
     f.rinv = (SCHEME != kSign && normal) ? __frcp_rn(d) : 0.0f;
     f.delta2 = (SCHEME == kUniform || SCHEME == kClip) ? static_cast<float>(1u << BITS) * 0x1p-21f
                : SCHEME == kQsgd     ? static_cast<float>(1u << (BITS - 1)) * 0x1p-21f
+               : SCHEME == kLog      ? 0x1p-20f
                                      : 0x1p-21f;
     return f;
+}
+
+// Logarithmic level index from xa = fl(|p| * rinv) instead of x = fl(|p| / s).
+// |xa - x| < 1.5 * 2^-23 * x, so the position between two levels (the mantissa
+// fraction m of x, or f = x * 2^(J-1) below the smallest level; an absolute
+// error under 2^-22 + 2^-24 there, subnormal quotients included) moves by less
+// than 2^-21.  The decision taken on xa is the decision on x unless the
+// position lies within delta2 = 2^-20 of a decision boundary -- 1/2 for nearest
+// rounding, u for stochastic rounding -- or, for stochastic rounding, of the
+// edge of its binade, where x and xa may sit in neighbouring binades and the
+// position jumps from 1 to 0 (for nearest rounding both sides of that jump give
+// the same level).  Those elements set redo.  |p| == s is the top level exactly;
+// any other |p| has x < 1.
+template <int BITS, bool SR>
+__device__ __forceinline__ uint32_t log_level_fast(float ap, float s, float u, const FastQ &fq,
+                                                   bool &redo) {
+    constexpr int J = (1 << (BITS - 1)) - 1;
+    if (ap == s) {
+        redo = false;
+        return J;
+    }
+    const float xa = __fmul_rn(ap, fq.rinv);
+    const uint32_t xb = __float_as_uint(xa);
+    const int e = static_cast<int>(xb >> 23) - 127;
+    if (xa >= 1.0f) {  // x < 1 here: leave it to the division
+        redo = true;
+        return J;
+    }
+    if (e >= 1 - J) {
+        const uint32_t j0 = static_cast<uint32_t>(e + J);
+        const float m = __fsub_rn(__uint_as_float((xb & 0x7FFFFFu) | 0x3F800000u), 1.0f);
+        bool up;
+        if constexpr (SR) {
+            up = u < m;
+            redo = (fabsf(__fsub_rn(u, m)) <= fq.delta2) | (fminf(m, __fsub_rn(1.0f, m)) <= fq.delta2);
+        } else {
+            up = m > 0.5f;  // a tie is within delta2 and recomputed
+            redo = fabsf(__fsub_rn(m, 0.5f)) <= fq.delta2;
+        }
+        return j0 + (up ? 1u : 0u);
+    }
+    const float f = __fmul_rn(xa, __uint_as_float(static_cast<uint32_t>(127 + J - 1) << 23));
+    bool up;
+    if constexpr (SR) {
+        up = u < f;
+        redo = (fabsf(__fsub_rn(u, f)) <= fq.delta2) | (f >= __fsub_rn(1.0f, fq.delta2));
+    } else {
+        up = f > 0.5f;
+        redo = fabsf(__fsub_rn(f, 0.5f)) <= fq.delta2;
+    }
+    return up ? 1u : 0u;
 }
 
 // Code and dequantized value of one element from ta; sets redo when the
@@ -354,6 +406,13 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
         }
         deq = p > 0.0f ? s : -s;
         return p > 0.0f ? 2u : 0u;
+    } else if constexpr (SCHEME == kLog) {
+        constexpr uint32_t J = (1u << (BITS - 1)) - 1u;
+        const uint32_t neg = p < 0.0f ? 1u : 0u;
+        const uint32_t lvl = log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo);
+        const float mag = lvl ? __fmul_rn(bp.a, __uint_as_float((lvl + 127u - J) << 23)) : 0.0f;
+        deq = neg ? -mag : mag;
+        return (neg << (BITS - 1)) | lvl;
     } else {
         redo = false;
         return quantize<SCHEME, BITS, SR>(p, u, bp, deq);
@@ -415,7 +474,10 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
             q += (u < fr) ? 1u : 0u;
         }
         return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | q;  // no clamp outside redo
+    } else if constexpr (SCHEME == kLog) {
+        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo);
     } else {
+        static_assert(SCHEME == kSign, "code_fast: every other scheme has its own branch");
         redo = false;
         return p >= 0.0f ? 1u : 0u;
     }
@@ -636,6 +698,21 @@ __device__ __forceinline__ void team_sync(int W, int team) {
     } else {
         asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(W * 32) : "memory");
     }
+}
+
+// Whether v holds on every thread of the team (the team's named barrier).
+__device__ __forceinline__ bool team_all(bool v, int W, int team) {
+    if (W == 1) return __all_sync(kFull, v);
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(1 + team), "r"(W * 32)
+        : "memory");
+    return r != 0u;
 }
 
 // Full radix selection: the keys of ranks r_lo and r_hi (0-based, ascending)
