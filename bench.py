@@ -69,8 +69,13 @@ class Component:
         raise NotImplementedError
 
     def host_inputs(self):
-        """(device tensor, pinned host tensor) pairs copied in per end-to-end step."""
+        """Device tensors refilled from pinned host memory every end-to-end step."""
         return []
+
+    def reads(self):
+        """Device tensors the step reads that come from the host (its own inputs
+        and any it shares with another component)."""
+        return self.host_inputs()
 
     def host_outputs(self):
         return []
@@ -345,6 +350,9 @@ class Receiver(Component):
 
     def host_inputs(self):
         return [self.g] if self.h2d else []
+
+    def reads(self):
+        return [self.g]
 
     def kernel_units(self):
         return {self.enc_name: self.n, self.dec_name: self.M * self.n}
@@ -852,37 +860,76 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, comps, q, torch, world, units):
+def run_e2e(args, comps, q, torch, world, units, results=None):
     """The same steps through the public API with host buffers: each step copies
-    its inputs in from pinned host memory and reads its results back."""
-    pairs_in, pairs_out = [], []
-    for c in comps:
-        for d in c.host_inputs():
-            pairs_in.append((d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True).copy_(d)))
-        for d in c.host_outputs():
-            pairs_out.append((d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)))
-    bi = sum(h.numel() * h.element_size() for _, h in pairs_in)
-    bo = sum(h.numel() * h.element_size() for _, h in pairs_out)
+    its inputs in from pinned host memory and reads its results back.  As a user
+    of the stream-ordered API would, the run keeps three streams busy at once:
+    component k's inputs go in on the copy-in stream while earlier components
+    run on the compute stream and their results come back on the copy-out
+    stream.  Events keep every buffer safe: an input is refilled only after the
+    previous step's last reader of it has run, and a component writes its
+    outputs only after the previous step's copy of them has left.  `results`, if
+    given, receives the pinned host copies of the last step's outputs."""
+    ins = [[(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True).copy_(d))
+            for d in c.host_inputs()] for c in comps]
+    outs = [[(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)) for d in c.host_outputs()]
+            for c in comps]
+    bi = sum(h.numel() * h.element_size() for pairs in ins for _, h in pairs)
+    bo = sum(h.numel() * h.element_size() for pairs in outs for _, h in pairs)
+    # the last component of the step that reads each component's inputs
+    last_reader = []
+    for k, c in enumerate(comps):
+        ptrs = {d.data_ptr() for d in c.host_inputs()}
+        last_reader.append(max([j for j, o in enumerate(comps)
+                                if ptrs & {d.data_ptr() for d in o.reads()}], default=k))
     steps = max(1, min(args.steps, args.e2e_steps))
     timer = KernelTimer(torch, enabled=False)
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
     torch.cuda.synchronize()
     barrier(world)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record()
+    s.record(cur)
+    for st in (s_in, s_cmp, s_out):
+        st.wait_event(s)
+    prev_c, prev_o = None, None
     for t in range(steps):
-        for d, h in pairs_in:
-            d.copy_(h, non_blocking=True)
-        for c in comps:
-            c.run(q, 1000 + t, timer)
-        for d, h in pairs_out:
-            h.copy_(d, non_blocking=True)
-    e.record()
+        done_c, done_o = [], []
+        for k, c in enumerate(comps):
+            with torch.cuda.stream(s_in):
+                if prev_c is not None:
+                    s_in.wait_event(prev_c[last_reader[k]])
+                for d, h in ins[k]:
+                    d.copy_(h, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_cmp.wait_event(ev_in)
+            if prev_o is not None:
+                s_cmp.wait_event(prev_o[k])
+            with torch.cuda.stream(s_cmp):
+                c.run(q, 1000 + t, timer)
+                ev_c = torch.cuda.Event()
+                ev_c.record(s_cmp)
+            done_c.append(ev_c)
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
+                for d, h in outs[k]:
+                    h.copy_(d, non_blocking=True)
+                ev_o = torch.cuda.Event()
+                ev_o.record(s_out)
+            done_o.append(ev_o)
+        prev_c, prev_o = done_c, done_o
+    for st in (s_in, s_cmp, s_out):
+        cur.wait_stream(st)
+    e.record(cur)
     torch.cuda.synchronize()
+    if results is not None:
+        results.extend(h for pairs in outs for _, h in pairs)
     ms = max_over_ranks(s.elapsed_time(e), world)
     value = world * units * 4 * steps / (ms * 1e-3) / 1e9
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "steps": steps}
+            "d2h_bytes_per_step": bo, "steps": steps, "streams": 3}
 
 
 def oracle_rate(comps, budget_s):
