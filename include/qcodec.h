@@ -57,7 +57,7 @@ typedef enum {
     QC_ERR_NULL = 1,          /* a required pointer is NULL                        */
     QC_ERR_INVALID_ARG = 2,   /* bad size, bits, bucket, scheme, flag or overlap    */
     QC_ERR_ALIGNMENT = 3,     /* a pointer or stride breaks the stated alignment    */
-    QC_ERR_UNSUPPORTED = 4,   /* valid in principle, outside this build's limits    */
+    QC_ERR_UNSUPPORTED = 4,   /* valid in principle, outside the library's limits  */
     QC_ERR_CUDA = 5           /* the CUDA runtime reported an error at launch       */
 } qc_status;
 
