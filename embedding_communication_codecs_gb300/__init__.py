@@ -36,6 +36,7 @@ STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ER
 # Every symbol the C ABI exports, in header order.
 EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
            "qc_reencode", "qc_topk_encode_ef", "qc_topk_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
+           "qc_selftest_wait_timeout",
            "qc_last_error", "qc_version")
 
 
@@ -68,6 +69,7 @@ def _load():
                  "qc_rowwise_fp8_dequant"):
         getattr(lib, name).restype = I
     lib.qc_take_device_errors.argtypes, lib.qc_take_device_errors.restype = [P], I
+    lib.qc_selftest_wait_timeout.argtypes, lib.qc_selftest_wait_timeout.restype = [U32, P], I
     lib.qc_last_error.argtypes, lib.qc_last_error.restype = [], ctypes.c_char_p
     lib.qc_version.argtypes, lib.qc_version.restype = [], ctypes.c_char_p
     return lib
@@ -98,6 +100,10 @@ def _stream(stream):
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def qc_selftest_wait_timeout(rounds, stream=None):
+    _check(lib.qc_selftest_wait_timeout(rounds, _stream(stream)))
 
 
 def qc_take_device_errors() -> int:

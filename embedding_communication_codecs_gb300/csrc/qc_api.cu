@@ -297,6 +297,13 @@ const char *qc_last_error(void) { return g_last_error; }
 
 const char *qc_version(void) { return "libqcodec 0.2.0 (sm_103a)"; }
 
+qc_status qc_selftest_wait_timeout(uint32_t rounds, qc_stream_t stream) {
+    if (rounds < 1 || rounds > (1u << 20))
+        return fail(QC_ERR_INVALID_ARG, "qc_selftest_wait_timeout: rounds must be in [1, 2^20] (got %u)", rounds);
+    return from_cuda(qc::launch_wait_timeout_selftest(rounds, reinterpret_cast<cudaStream_t>(stream)),
+                     "qc_selftest_wait_timeout");
+}
+
 qc_status qc_take_device_errors(uint32_t *flags) {
     if (!flags) return fail(QC_ERR_NULL, "qc_take_device_errors: flags must be non-NULL");
     *flags = 0;
@@ -305,6 +312,7 @@ qc_status qc_take_device_errors(uint32_t *flags) {
     *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
              qc::take_encode_clip_bf16_errors() | qc::take_reencode_other_errors() |
              qc::take_encode_log_errors() | qc::take_reencode_log_errors() |
+             qc::take_selftest_errors() |
              qc::take_topk_errors() |
              qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");

@@ -257,6 +257,11 @@ uint32_t take_encode_clip_bf16_errors();
 uint32_t take_encode_log_errors();
 uint32_t take_reencode_other_errors();
 uint32_t take_reencode_log_errors();
+uint32_t take_selftest_errors();
+
+// One block waits on a barrier nothing completes, `rounds` tries, and records
+// the pipeline-timeout flag (qc_selftest.cu).
+cudaError_t launch_wait_timeout_selftest(uint32_t rounds, cudaStream_t stream);
 uint32_t take_topk_errors();
 uint32_t take_encode_bf16_errors();
 uint32_t take_decode_errors();

@@ -18,7 +18,9 @@
 
 namespace qc {
 
-constexpr uint32_t kWaitRounds = 1u << 22;
+// An unsuccessful try_wait returns after about 6 us on GB300 (measured through
+// qc_selftest_wait_timeout), so a stalled pipeline gives up after about 1.5 s.
+constexpr uint32_t kWaitRounds = 1u << 18;
 
 // Named barrier 1 over the first `threads` threads of the block (the consumer
 // warps of a warp-specialised block; the producer warp never takes part).
@@ -112,11 +114,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait for the phase with the given parity; false if it never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t r = 0; r < kWaitRounds; ++r)
+// Wait for the phase with the given parity, at most `rounds` tries; false if it
+// never completed.
+__device__ __forceinline__ bool mbar_wait_rounds(uint64_t *bar, uint32_t parity, uint32_t rounds) {
+    for (uint32_t r = 0; r < rounds; ++r)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// The pipelines' bounded wait.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_rounds(bar, parity, kWaitRounds);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {

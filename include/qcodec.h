@@ -348,6 +348,16 @@ qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, s
  */
 qc_status qc_take_device_errors(uint32_t *flags);
 
+/*
+ * qc_selftest_wait_timeout -- exercises the failure path that
+ * qc_take_device_errors() reports, without a fault: one block waits on a
+ * shared-memory barrier that nothing completes, with the pipelines' bounded
+ * wait limited to `rounds` tries (1 .. 2^20, else QC_ERR_INVALID_ARG).  The wait
+ * runs out, the block sets the pipeline-timeout flag (bit 0) and returns; the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+qc_status qc_selftest_wait_timeout(uint32_t rounds, qc_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if none). */
 const char *qc_last_error(void);
 

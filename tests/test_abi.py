@@ -192,6 +192,12 @@ def test_clip_rejects(q):
                              0x50000000, 0x60000000, 0x60001000, A, 0) == q.QC_ERR_UNSUPPORTED
 
 
+def test_selftest_rejects(q):
+    for rounds in (0, (1 << 20) + 1):
+        assert q.lib.qc_selftest_wait_timeout(rounds, 0) == q.QC_ERR_INVALID_ARG
+    assert b"rounds" in q.lib.qc_last_error()
+
+
 def test_log_rejects(q):
     L_ = q.QC_SCHEME_LOG
     for bits in (1, 3, 16):
