@@ -394,11 +394,6 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
         return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                                dtype == QC_DTYPE_BF16, st),
                          "qc_encode_ef");
-    if (scheme == QC_SCHEME_LOG)
-        return fail(QC_ERR_UNSUPPORTED,
-                    "qc_encode_ef: logarithmic levels need a 16-byte aligned gradient and a bucket of "
-                    "at most %u elements (or 1024, 2048, 4096 or 8192 for bf16 without error feedback)",
-                    qc::kWindowPerWarp * (qc::kBlock / 32));
     return from_cuda(qc::launch_encode(p, scheme, bits, mode == QC_ROUND_STOCHASTIC,
                                        dtype == QC_DTYPE_BF16, st),
                      "qc_encode_ef");

@@ -148,9 +148,7 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *         STOCHASTIC: j = e + J + [u_i < m]
  *       x < 2^(1-J): f = x * 2^(J-1) (exact) and j = NEAREST ? [f > 1/2] : [u_i < f]
  *     code_i = [p_i < 0] << (bits-1) | j; deq_i = +-(j ? fl(s * 2^(j - J)) : 0);
- *     scale[k] = s.  Needs a 16-byte aligned gradient and a bucket of at most
- *     4096 elements (bf16 without error feedback: 1024, 2048, 4096 or 8192),
- *     else QC_ERR_UNSUPPORTED.
+ *     scale[k] = s.
  * Then, with error feedback, err_i = fl(p_i - deq_i) is written in place.
  *
  * Stochastic draw for element i (global index within this call):

@@ -150,6 +150,35 @@ def test_encode_log_degenerate(q, bits):
         assert np.all(codes[3 * bucket:4 * bucket] == J)
 
 
+@pytest.mark.parametrize("mode", [0, 1], ids=["nearest", "stochastic"])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_encode_log_direct_kernel(q, bits, mode):
+    """The direct kernel: buckets above the pipelined team window (two passes,
+    f32 with and without error feedback) and a bf16 gradient whose base is 8- but
+    not 16-byte aligned."""
+    for bucket in (8192, 16384):
+        n = 3 * bucket + 77
+        g = wl.outlier_gradient(n, seed=bucket + bits)
+        for ef in (False, True):
+            err0 = (wl.std_normal(98, 1, n) * np.float32(1e-4)) if ef else None
+            _check(q, g, err0, n, bits, bucket, mode, f"log direct b={bits} m={mode} B={bucket} ef={ef}")
+    bucket, n = 1024, 1024 * 9 + 20
+    gb = wl.to_bf16_bits(wl.outlier_gradient(n + 4, seed=bits))
+    base = torch.from_numpy(gb.view(np.int16).copy()).cuda()
+    g_dev = base[4:]                       # 8 bytes past a 16-byte aligned allocation
+    assert g_dev.data_ptr() % 16 == 8
+    words, nb = q.qc_code_words(n, bits), q.qc_num_buckets(n, bucket)
+    codes = torch.full((words,), -7, dtype=torch.int32, device="cuda")
+    scale = torch.full((nb,), -7.0, device="cuda")
+    q.qc_encode_ef(g_dev, None, n, bits, bucket, q.QC_SCHEME_LOG, mode, SEED, STEP, codes, scale,
+                   None, dtype=q.QC_DTYPE_BF16)
+    torch.cuda.synchronize()
+    c_or, s_or = orc.encode_log(gb[4:], None, bits=bits, bucket=bucket, mode=mode, seed=SEED,
+                                step=STEP)
+    assert_bits_equal(host(scale), s_or, "log bf16 unaligned scale")
+    assert_bits_equal(u32(codes), c_or, "log bf16 unaligned codes")
+
+
 def test_encode_log_large(q):
     """n = 2^22 + 3 f32 elements, 4 bits, stochastic rounding, error feedback,
     B = 512, compared whole."""
