@@ -747,6 +747,32 @@ def test_reencode_of_identical_payloads_is_idempotent(scheme, bits, mode):
         assert np.array_equal(sr, s[0])
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("mode", [orc.ROUND_NEAREST, orc.ROUND_STOCHASTIC])
+def test_reencode_of_identical_log_payloads_is_idempotent(bits, mode):
+    """The logarithmic levels s * 2^(j - J) are exact products at these widths
+    (no underflow), two identical payloads average back to them exactly, and
+    every bucket keeps its top level, so the re-encode sees the same s and each
+    value sits exactly on a level: the payload's own codes come back.  The one
+    exception is a negative element rounded to level 0: the accumulation starts
+    from +0, so it decodes to +0, which encodes with the sign bit clear."""
+    n, bucket = 4096 + 64, 512
+    J = (1 << (bits - 1)) - 1
+    g = wl.std_normal(78, 1, n) * np.float32(1e-2)
+    c, sc = orc.encode_log(g, bits=bits, bucket=bucket)
+    r, cr, sr, _ = orc.reencode(np.stack([c, c]), np.stack([sc, sc]), None, M=2, n=n, bits=bits,
+                                bucket=bucket, scheme=orc.SCHEME_LOG, flags=orc.OUT_MEAN,
+                                mode=mode, seed=5, step=1)
+    d1 = orc.decode_accumulate(c, sc, None, M=1, n=n, bits=bits, bucket=bucket,
+                               scheme=orc.SCHEME_LOG)
+    assert np.array_equal(r.view(np.uint32), d1.view(np.uint32))
+    assert np.array_equal(sr, sc)
+    codes = _unpack_codes(c, n, bits)
+    want = np.where((codes & np.uint32(J)) == 0, np.uint32(0), codes)
+    assert np.array_equal(_unpack_codes(cr, n, bits), want)
+    assert np.any(codes != want)          # the -0 case does occur in this draw
+
+
 # ------------------------------------------------------------- percentile clip
 
 def _nearest_rank_index(cnt, pct):
