@@ -24,7 +24,8 @@
  *
  * Arithmetic: IEEE-754 binary32, round-to-nearest-even, one rounding per
  * operation as written (build with -ffp-contract=off, never -ffast-math); fp64
- * only for the sign scheme's mean, as stated there.  Each function takes the
+ * only for the sign scheme's mean and exact integer arithmetic for the QSGD norm,
+ * as stated there.  Each function takes the
  * steps of the method in the order the pages give them, element by element in
  * index order.  Readings taken where the pages are silent are stated at each
  * step.
@@ -440,6 +441,155 @@ ORC_API int oracle_encode_ternary(const void *grad, int dtype, float *err, size_
 }
 
 /* ------------------------------------------------------------------------ */
+/* The L2 norm of a bucket, exactly rounded.
+ *
+ * The pages and the named method (Alistarh et al.) define QSGD's scale as the
+ * norm ||v||_2 and leave its arithmetic open.  Reading: nrm is the binary32
+ * value nearest (ties to even) to the square root of the EXACT sum of the
+ * squares, so it depends neither on the order of the sum nor on a working
+ * precision.
+ *
+ * Every binary32 x is m * 2^e with an integer m < 2^24 and e >= -149, so its
+ * square m^2 * 2^(2e) is an integer multiple of 2^-298.  The sum is therefore
+ * held exactly as an unsigned integer A in units of 2^-298, in 32-bit limbs
+ * (least significant first).  The largest finite square is below 2^256, so a
+ * bucket of up to 2^24 elements keeps A below 2^578. */
+#define ORC_WIDE_LIMBS 24 /* 768 bits: room for A * 2^60 below */
+
+/* w += x * 2^pos for a 32-bit x. */
+static void orc_wide_add32(uint32_t *w, uint32_t x, unsigned pos)
+{
+    unsigned k = pos / 32;
+    uint64_t t = (uint64_t)x << (pos % 32); /* spans limbs k and k + 1 */
+    uint64_t s = (uint64_t)w[k] + (uint32_t)t;
+    w[k] = (uint32_t)s;
+    s = (uint64_t)w[k + 1] + (t >> 32) + (s >> 32);
+    w[k + 1] = (uint32_t)s;
+    uint64_t carry = s >> 32;
+    for (unsigned j = k + 2; carry && j < ORC_WIDE_LIMBS; ++j) {
+        s = (uint64_t)w[j] + carry;
+        w[j] = (uint32_t)s;
+        carry = s >> 32;
+    }
+}
+
+/* A += x^2 / 2^-298 (exact).  Non-finite x is skipped (unspecified, never UB). */
+static void orc_wide_add_square(uint32_t *A, float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, sizeof b);
+    uint32_t ex = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
+    if (ex == 0xFFu)
+        return;
+    int e; /* |x| = m * 2^e */
+    if (ex == 0) {
+        e = -149;
+    } else {
+        m |= 0x800000u;
+        e = (int)ex - 150;
+    }
+    uint64_t sq = (uint64_t)m * m; /* < 2^48 */
+    unsigned pos = (unsigned)(2 * e + 298);
+    orc_wide_add32(A, (uint32_t)sq, pos);
+    orc_wide_add32(A, (uint32_t)(sq >> 32), pos + 32);
+}
+
+static int orc_wide_bit(const uint32_t *w, unsigned i)
+{
+    return (int)((w[i / 32] >> (i % 32)) & 1u);
+}
+
+/* a = (a << 2) | two, for a number of `nl` limbs. */
+static void orc_wide_shl2_in(uint32_t *a, int nl, uint32_t two)
+{
+    for (int j = nl - 1; j > 0; --j)
+        a[j] = (a[j] << 2) | (a[j - 1] >> 30);
+    a[0] = (a[0] << 2) | two;
+}
+
+/* a = (a << 1) | one. */
+static void orc_wide_shl1_in(uint32_t *a, int nl, uint32_t one)
+{
+    for (int j = nl - 1; j > 0; --j)
+        a[j] = (a[j] << 1) | (a[j - 1] >> 31);
+    a[0] = (a[0] << 1) | one;
+}
+
+static int orc_wide_geq(const uint32_t *a, const uint32_t *b, int nl)
+{
+    for (int j = nl - 1; j >= 0; --j)
+        if (a[j] != b[j])
+            return a[j] > b[j];
+    return 1;
+}
+
+static void orc_wide_sub(uint32_t *a, const uint32_t *b, int nl)
+{
+    uint64_t borrow = 0;
+    for (int j = 0; j < nl; ++j) {
+        uint64_t d = (uint64_t)a[j] - b[j] - borrow;
+        a[j] = (uint32_t)d;
+        borrow = (d >> 63) & 1u;
+    }
+}
+
+/* The binary32 value nearest (ties to even) to sqrt(A * 2^-298).
+ *
+ * N = A * 2^60 and R = floor(sqrt(N)) by the schoolbook digit-by-digit method
+ * (two bits of N per bit of the root, remainder kept exactly), so that
+ * sqrt(A * 2^-298) = (R + f) * 2^-179 with 0 <= f < 1 and f > 0 exactly when the
+ * remainder is not zero.  R >= 2^30 whenever A > 0.  The result keeps the top
+ * 24 bits of R (fewer below the normal range, where the quantum is 2^-149,
+ * i.e. 2^30 units of R) and rounds on the next bit and the bits below it. */
+static float orc_wide_sqrt_f32(const uint32_t *A)
+{
+    enum { NL = ORC_WIDE_LIMBS, RL = ORC_WIDE_LIMBS / 2 + 1 };
+    uint32_t N[NL] = {0};
+    for (int j = NL - 1; j >= 0; --j) { /* N = A << 60 */
+        uint32_t v = 0;
+        int src = j - 1;                 /* 60 = 32 + 28 */
+        if (src >= 0)
+            v |= A[src] << 28;
+        if (src - 1 >= 0)
+            v |= A[src - 1] >> 4;
+        N[j] = v;
+    }
+    int top = 32 * NL - 1;
+    while (top >= 0 && !orc_wide_bit(N, (unsigned)top))
+        --top;
+    if (top < 0)
+        return 0.0f;
+    uint32_t R[RL] = {0}, rem[RL] = {0}, t[RL];
+    for (int i = top / 2; i >= 0; --i) {
+        uint32_t two = (uint32_t)(orc_wide_bit(N, 2u * i + 1) << 1 | orc_wide_bit(N, 2u * i));
+        orc_wide_shl2_in(rem, RL, two);
+        memcpy(t, R, sizeof t); /* t = 4 R + 1 (R before this step) */
+        orc_wide_shl2_in(t, RL, 1u);
+        orc_wide_shl1_in(R, RL, 0u);
+        if (orc_wide_geq(rem, t, RL)) {
+            orc_wide_sub(rem, t, RL);
+            R[0] |= 1u;
+        }
+    }
+    int rbits = 32 * RL - 1;
+    while (!orc_wide_bit(R, (unsigned)rbits))
+        --rbits;
+    rbits += 1;                                  /* bit length of R */
+    int shift = rbits - 24 > 30 ? rbits - 24 : 30;
+    uint32_t m = 0;
+    for (int i = rbits - 1; i >= shift; --i)     /* the kept bits, at most 24 */
+        m = (m << 1) | (uint32_t)orc_wide_bit(R, (unsigned)i);
+    int guard = orc_wide_bit(R, (unsigned)(shift - 1));
+    int sticky = 0;
+    for (int i = 0; i < shift - 1; ++i)
+        sticky |= orc_wide_bit(R, (unsigned)i);
+    for (int j = 0; j < RL; ++j)
+        sticky |= rem[j] != 0;
+    if (guard && (sticky || (m & 1u)))
+        m += 1; /* may carry to 2^24: still exact */
+    return ldexpf((float)m, shift - 179);
+}
+
 /* QSGD: s-level stochastic quantization scaled by the bucket's L2 norm.
  *
  * p3 "Quantized SGD Algorithms" (QSGD: stochastic quantization with an unbiased
@@ -451,7 +601,8 @@ ORC_API int oracle_encode_ternary(const void *grad, int dtype, float *err, size_
  * over b-1 level bits, s = 2^(b-1) - 1; the unit ||v|| / s is rounded once and
  * the level is found like the uniform scheme's with min = 0:
  *   p_i  = e_i + g_i
- *   nrm  = sqrt(sum of p_i^2), fp64 sum in index order, rounded once to fp32
+ *   nrm  = sqrt(sum of p_i^2) with the sum exact and the root rounded once to
+ *          binary32 (orc_wide_sqrt_f32 above)
  *   unit = nrm / s ;  unit == 0 -> every code 0
  *   t_i  = |p_i| / unit
  *   stochastic: lvl = min(floor(t_i) + [u_i < t_i - floor(t_i)], s)
@@ -479,10 +630,10 @@ ORC_API int oracle_encode_qsgd(const void *grad, int dtype, float *err, size_t n
             float g = orc_load_grad(grad, dtype, lo + j);
             p[j] = err ? err[lo + j] + g : g;
         }
-        double ss = 0.0;
+        uint32_t A[ORC_WIDE_LIMBS] = {0};
         for (size_t j = 0; j < cnt; ++j)
-            ss += (double)p[j] * (double)p[j];
-        float nrm = (float)sqrt(ss);
+            orc_wide_add_square(A, p[j]);
+        float nrm = orc_wide_sqrt_f32(A);
         float unit = nrm / sf;
         for (size_t j = 0; j < cnt; ++j) {
             uint32_t lvl = 0;

@@ -6,6 +6,7 @@ even); they share nothing with the oracle or with the CUDA library.
 """
 from __future__ import annotations
 
+import math
 from fractions import Fraction
 
 import numpy as np
@@ -52,3 +53,27 @@ def ulp32(x) -> float:
 def dist_to_half_integer(fr: Fraction) -> Fraction:
     fl = fr.numerator // fr.denominator
     return abs(fr - fl - Fraction(1, 2))
+
+
+def sqrt_to_f32(s: Fraction) -> np.float32:
+    """The binary32 value nearest (ties to even) to the square root of a
+    nonnegative rational whose denominator is a power of two no larger than
+    2^600: the integer square root of s * 2^600 brackets the root within
+    2^-300, far below half the smallest binary32 quantum (2^-150), so the
+    rounding of the bracket's midpoint equals the rounding of the root unless
+    the root is exact, which the remainder tells."""
+    j = 300
+    x = s * Fraction(4) ** j
+    assert x.denominator == 1 and x >= 0
+    r = math.isqrt(x.numerator)
+    if r * r == x.numerator:
+        return to_f32(Fraction(r, 2 ** j))
+    return to_f32(Fraction(2 * r + 1, 2 ** (j + 1)))
+
+
+def sqrt_down_f32(s: Fraction) -> np.float32:
+    """The largest binary32 value whose square does not exceed s (s >= 0)."""
+    x = sqrt_to_f32(s)
+    while frac(x) * frac(x) > s:
+        x = np.nextafter(x, np.float32(0))
+    return np.float32(x)

@@ -17,6 +17,7 @@ import pytest
 import oracle as orc
 import workloads as wl
 from tests._exact import dist_to_half_integer, frac, round_half_even, to_f32, ulp32
+from tests._norm_cases import exact_norm_f32, midpoint_bucket
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -405,6 +406,56 @@ def test_decode_hand_built_exact():
         assert out4.tolist() == want4
 
 
+def _one_vs_two_roundings(q, s, o):
+    """(one rounding of q*s + o, two roundings) as binary32, from exact rationals."""
+    one = to_f32(q * frac(s) + frac(o))
+    two = to_f32(frac(to_f32(q * frac(s))) + frac(o))
+    return one, two
+
+
+def test_decode_dequantization_rounds_once():
+    """'x ~ q * scale + min' is read as one rounding (fma).  With scales and
+    offsets that are not powers of two, fl(q * s + o) and fl(fl(q * s) + o)
+    differ on many codes; the decode (M = 1) must give the first on every one."""
+    n, bucket, bits = 512, 256, 8
+    q = np.arange(n) % 256
+    words = _pack(q, bits)
+    scale = np.array([np.float32(0.1), np.float32(1.0) / np.float32(3.0)], dtype=np.float32)
+    off = np.array([np.float32(-12.7), np.float32(5.0e-3)], dtype=np.float32)
+    out = orc.decode_accumulate(words[None], scale[None], off[None], M=1, n=n, bits=bits,
+                                bucket=bucket, scheme=orc.SCHEME_UNIFORM)
+    differ = 0
+    for i in range(n):
+        one, two = _one_vs_two_roundings(int(q[i]), scale[i // bucket], off[i // bucket])
+        assert out[i] == one, i
+        differ += one != two
+    assert differ >= 20          # the pin tells the two readings apart
+
+
+@pytest.mark.parametrize("mode", [orc.ROUND_NEAREST, orc.ROUND_STOCHASTIC])
+def test_uniform_ef_residual_rounds_dequantization_once(mode):
+    """The encode's residual e = fl(p - deq) with deq = fl(q * scale + min) (one
+    rounding), checked bit for bit from exact rationals on every element, on
+    buckets whose scale and min are not powers of two; the two-rounding deq
+    differs on a good share of them."""
+    n, bucket, bits = 1024, 256, 4
+    rng = np.random.default_rng(31)
+    g = (rng.standard_normal(n) * 0.37 + 0.011).astype(np.float32)
+    e0 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    err = e0.copy()
+    codes, scale, off = orc.encode_uniform(g, err, bits=bits, bucket=bucket, mode=mode,
+                                           seed=5, step=2)
+    q = _unpack(codes, n, bits)
+    differ = 0
+    for i in range(n):
+        k = i // bucket
+        p = to_f32(frac(e0[i]) + frac(g[i]))
+        one, two = _one_vs_two_roundings(q[i], scale[k], off[k])
+        assert err[i] == to_f32(frac(p) - frac(one)), i
+        differ += to_f32(frac(p) - frac(one)) != to_f32(frac(p) - frac(two))
+    assert differ >= 20
+
+
 def test_decode_sign_ternary_closed_form():
     n, bucket = 96, 32
     rng = np.random.default_rng(1)
@@ -568,24 +619,6 @@ def test_workload_distributions():
 
 # -------------------------------------------------------------------------- QSGD
 
-def _exact_sqrt_f32(fr: Fraction) -> np.float32:
-    """binary32 rounding of sqrt of a nonnegative rational (bisection on floats)."""
-    x = np.float32(np.sqrt(float(fr)))
-    # adjust to the correctly rounded value by comparing squares of midpoints
-    for _ in range(4):
-        up = np.nextafter(x, np.float32(np.inf))
-        dn = np.nextafter(x, np.float32(0))
-        mid_up = (frac(x) + frac(up)) / 2
-        mid_dn = (frac(x) + frac(dn)) / 2
-        if mid_up * mid_up < fr:
-            x = up
-        elif mid_dn * mid_dn > fr:
-            x = dn
-        else:
-            break
-    return np.float32(x)
-
-
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_qsgd_unit_levels_and_signs(bits):
     s = (1 << (bits - 1)) - 1
@@ -597,11 +630,8 @@ def test_qsgd_unit_levels_and_signs(bits):
     c = np.array(_unpack(codes, n, bits))
     for k in range(orc.num_buckets(n, bucket)):
         seg = g[k * bucket:(k + 1) * bucket]
-        sq = sum(frac(v) * frac(v) for v in seg)
-        nrm = _exact_sqrt_f32(sq)
-        # the oracle's fp64 sum may differ from the exact sum by far less than an ulp
-        want_unit = to_f32(frac(nrm) / s)
-        assert abs(frac(unit[k]) - frac(want_unit)) <= Fraction(ulp32(want_unit))
+        want_unit = to_f32(frac(exact_norm_f32(seg)) / s)
+        assert unit[k] == want_unit
         for j, v in enumerate(seg):
             code = int(c[k * bucket + j])
             assert (code >> (bits - 1)) == (1 if v < 0 else 0)
@@ -609,6 +639,55 @@ def test_qsgd_unit_levels_and_signs(bits):
             t = abs(frac(v)) / frac(unit[k])
             fl = t.numerator // t.denominator
             assert lvl in (min(fl, s), min(fl + 1, s))
+
+
+def test_qsgd_norm_tie_and_tiny_tail():
+    """sqrt(1 + 2^-23 + 2^-48) = 1 + 2^-24 exactly: the midpoint between 1 and
+    its upper neighbour, so the norm rounds to even (1.0).  One element of 2^-100
+    more puts the exact root just above the midpoint (1 + 2^-23); a sum of the
+    squares in binary64 loses that element and would still give 1.0."""
+    g = np.zeros(32, dtype=np.float32)
+    g[:4] = [1.0, 2.0 ** -12, 2.0 ** -12, 2.0 ** -24]
+    _, u = orc.encode_qsgd(g, None, bits=2, bucket=32)      # s = 1: unit = norm
+    assert u[0] == np.float32(1.0)
+    g[9] = np.float32(2.0 ** -100)
+    _, u = orc.encode_qsgd(g, None, bits=2, bucket=32)
+    assert u[0] == np.float32(1.0 + 2.0 ** -23)
+    s64 = sum(float(v) * float(v) for v in g)
+    assert np.float32(math.sqrt(s64)) == np.float32(1.0)    # the binary64 sum cannot see it
+
+
+@pytest.mark.parametrize("f", [1.0, 3.7, 1e-20, 2.5e15, 0.1, 7.0e-30, 6.0e18])
+@pytest.mark.parametrize("side", ["below", "above"])
+def test_qsgd_norm_next_to_a_rounding_boundary(f, side):
+    """Buckets whose exact sum of squares lies within 2^-90 (relative) of the
+    square of a midpoint between two binary32 values: the unit is the exactly
+    rounded norm divided by s (compared with Python's integer square root on
+    the exact rational sum)."""
+    vals, want = midpoint_bucket(f, side=side)
+    bucket = 32
+    g = np.zeros(bucket, dtype=np.float32)
+    rng = np.random.default_rng(int(f * 1000) % 1000 + len(side))
+    pos = rng.permutation(bucket)[:len(vals)]
+    g[pos] = vals * np.where(rng.random(len(vals)) < 0.5, -1, 1).astype(np.float32)
+    assert exact_norm_f32(g) == want
+    for bits in (2, 4, 8):
+        s = (1 << (bits - 1)) - 1
+        _, u = orc.encode_qsgd(g, None, bits=bits, bucket=bucket, mode=orc.ROUND_NEAREST)
+        assert u[0] == to_f32(frac(want) / s)
+
+
+def test_qsgd_norm_random_buckets_every_magnitude():
+    """Units of random buckets from 2^-140 to 2^60 in magnitude, with subnormal
+    and zero elements mixed in, against the exact rational norm."""
+    rng = np.random.default_rng(12)
+    bucket = 64
+    for t in range(60):
+        g = (rng.standard_normal(bucket) * 2.0 ** rng.uniform(-140, 60)).astype(np.float32)
+        g[rng.integers(0, bucket, 4)] = np.float32(2.0 ** -149) * rng.integers(1, 9)
+        g[rng.integers(0, bucket, 2)] = 0.0
+        _, u = orc.encode_qsgd(g, None, bits=8, bucket=bucket)
+        assert u[0] == to_f32(frac(exact_norm_f32(g)) / 127), t
 
 
 def test_qsgd_single_element_takes_top_level():
