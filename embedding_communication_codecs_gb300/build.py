@@ -18,12 +18,12 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libqcodec.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["qc_api.cu", "qc_encode.cu", "qc_encode_tma.cu", "qc_encode_clip.cu",
-           "qc_encode_clip_bf16.cu", "qc_encode_bf16.cu", "qc_decode.cu", "qc_decode_tma.cu",
+           "qc_encode_clip_bf16.cu", "qc_encode_bf16.cu", "qc_encode_bf16_fast.cu", "qc_decode.cu", "qc_decode_tma.cu",
            "qc_reencode.cu", "qc_reencode_other.cu", "qc_topk.cu", "qc_fp8.cu",
            "qc_encode_log.cu", "qc_reencode_log.cu", "qc_selftest.cu", "qc_encode_direct_log.cu"]
 HEADERS = ["qc_device.cuh", "qc_internal.h", "qc_encode_math.cuh", "qc_encode_tma.cuh",
            "qc_encode_direct.cuh",
-           "qc_reencode.cuh", "qc_pipeline.cuh", "qc_decode_math.cuh"]
+           "qc_reencode.cuh", "qc_pipeline.cuh", "qc_decode_math.cuh", "qc_exact_norm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction; every fused op is an explicit

@@ -314,7 +314,7 @@ qc_status qc_take_device_errors(uint32_t *flags) {
              qc::take_encode_log_errors() | qc::take_reencode_log_errors() |
              qc::take_selftest_errors() |
              qc::take_topk_errors() |
-             qc::take_encode_bf16_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
+             qc::take_encode_bf16_errors() | qc::take_encode_bf16_fast_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
     return from_cuda(cudaGetLastError(), "qc_take_device_errors");
 }
 
@@ -387,7 +387,13 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
                                                 dtype == QC_DTYPE_BF16, st),
                          "qc_encode_ef");
     }
-    if (dtype == QC_DTYPE_BF16 && bf16_tiles_for(p, aligned(grad, 16), tiles))
+    if (dtype == QC_DTYPE_BF16 &&
+        qc::encode_bf16_fast_applies(p, scheme, bits, mode == QC_ROUND_STOCHASTIC, aligned(grad, 16),
+                                     aligned(codes, 8)))
+        return from_cuda(qc::launch_encode_bf16_fast(p, scheme, st), "qc_encode_ef");
+    // the bf16 kernel stores 8-bit codes eight bytes at a time
+    if (dtype == QC_DTYPE_BF16 && (bits != 8 || aligned(codes, 8)) &&
+        bf16_tiles_for(p, aligned(grad, 16), tiles))
         return from_cuda(qc::launch_encode_bf16(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC, st),
                          "qc_encode_ef");
     if (encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))

@@ -86,11 +86,14 @@ struct PackedStats {
 
 // Packs the 8 codes of a lane slot (c0 lowest) and stores them; every lane of
 // the warp calls this together.
+// `second`: the slot's last four elements exist (8-bit codes: their word is
+// written only then; the other widths never start a word past the end).
 template <int BITS>
 __device__ __forceinline__ void store_codes8(uint32_t *codes, uint64_t i0, bool valid, int lane,
-                                             uint32_t lo, uint32_t hi) {
+                                             uint32_t lo, uint32_t hi, bool second = true) {
     if constexpr (BITS == 8) {
-        if (valid) __stcs(reinterpret_cast<uint2 *>(codes + i0 / 4u), make_uint2(lo, hi));
+        if (valid && second) __stcs(reinterpret_cast<uint2 *>(codes + i0 / 4u), make_uint2(lo, hi));
+        else if (valid) __stcs(codes + i0 / 4u, lo);
     } else if constexpr (BITS == 4) {
         if (valid) __stcs(codes + i0 / 8u, lo | (hi << 16));
     } else if constexpr (BITS == 2) {
@@ -237,6 +240,11 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
             st.init();
             PackedStats<SCHEME> ps;
             ps.init();
+            // QSGD: each pair of slots (16 elements) is summed into a fresh double
+            // word and merged (the bound in Stats<kQsgd> counts 16 per window)
+            Stats<SCHEME> part;
+            part.init();
+            Stats<SCHEME> &acc = (SCHEME == kQsgd) ? part : st;
 #pragma unroll
             for (int sl = 0; sl < kSlots; ++sl) {
                 const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                         float v[8];
                         unpack8(raw[sl], v);
 #pragma unroll
-                        for (int c = 0; c < kEps; ++c) st.add(v[c]);
+                        for (int c = 0; c < kEps; ++c) acc.add(v[c]);
                     } else {
                         ps.add(raw[sl].x);
                         ps.add(raw[sl].y);
@@ -264,16 +272,38 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                             h[c] = (e + c < staged)
                                        ? *reinterpret_cast<const unsigned short *>(stage + (e + c) * 2u)
                                        : __ldcs(reinterpret_cast<const unsigned short *>(gsrc + t0 + e + c));
-                            st.add(bf16_bits_to_float(h[c]));
+                            acc.add(bf16_bits_to_float(h[c]));
                         }
                     }
                     raw[sl] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
                                          h[4] | (h[5] << 16), h[6] | (h[7] << 16));
                 }
+                if constexpr (SCHEME == kQsgd) {
+                    if (sl & 1) {
+                        st.merge(part);
+                        part.init();
+                    }
+                }
             }
             ps.fold_into(st);
             team_reduce_local<SCHEME>(st, red, buf, W, warp, lane, team);
-            const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            if constexpr (SCHEME == kQsgd) {
+                if (bp.exact) {  // rare: the norm next to a rounding boundary (uniform per team)
+                    WideSum wacc;
+                    wide_zero(wacc);
+#pragma unroll
+                    for (int sl = 0; sl < kSlots; ++sl) {
+                        const uint32_t j = static_cast<uint32_t>(sl * team_threads + tt) * kEps;
+                        const uint32_t w8[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+#pragma unroll
+                        for (int c = 0; c < kEps; ++c)
+                            if (j + c < cnt)
+                                wide_add_square(wacc, bf16_bits_to_float((w8[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu));
+                    }
+                    bp = qsgd_params<BITS>(team_exact_norm<SCHEME, 1>(wacc, red, W, warp, lane, team));
+                }
+            }
             const FastQ fq = fast_params<SCHEME, BITS>(bp);
 
             // ---- quantize, pack and store, one slot at a time: a division-free
@@ -390,7 +420,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                         if (j + c + 4 < cnt)
                             f1 |= code_exact<SCHEME, BITS, SR>(v[c + 4], u[c + 4], bp) << (c * BITS);
                     }
-                    store_codes8<BITS>(P.codes, b0 + j, j < cnt, lane, f0, f1);
+                    store_codes8<BITS>(P.codes, b0 + j, j < cnt, lane, f0, f1, j + 4 < cnt);
                 }
             }
             if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);

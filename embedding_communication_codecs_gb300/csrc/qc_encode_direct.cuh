@@ -96,7 +96,22 @@ __global__ void __launch_bounds__(kBlock) encode_kernel(const __grid_constant__ 
             }
         }
         team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
-        const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+        BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+        if constexpr (SCHEME == kQsgd) {
+            if (bp.exact) {  // rare: the norm next to a rounding boundary (uniform per team)
+                WideSum acc;
+                wide_zero(acc);
+                if (!P.two_pass) {
+                    wide_add_slots(acc, p, tt, team_threads, cnt);
+                } else {
+                    for (uint32_t w0 = 0; w0 < cnt; w0 += window) {
+                        load_slots<TIn, EF>(P, b0 + w0, cnt - w0, tt, team_threads, p);
+                        wide_add_slots(acc, p, tt, team_threads, cnt - w0);
+                    }
+                }
+                bp = qsgd_params<BITS>(team_exact_norm<SCHEME, 1>(acc, red, W, warp, lane, team));
+            }
+        }
 
         if (!P.two_pass) {
             quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, b0, cnt, tt, team_threads,

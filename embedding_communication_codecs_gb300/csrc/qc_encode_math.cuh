@@ -17,6 +17,7 @@
 
 #include "qc_decode_math.cuh"
 #include "qc_device.cuh"
+#include "qc_exact_norm.cuh"
 #include "qc_internal.h"
 
 namespace qc {
@@ -53,16 +54,38 @@ struct Stats<kSign> {  // sum of |p| as a double word
     __device__ void merge(const Stats &o) { sum = dw_add(sum, o.sum); }
 };
 
+// QSGD: the sum of p^2 as a double word.  Each square is split exactly
+// (x * x = hi + lo with lo = fma(x, x, -hi)) and added with an exact TwoSum on
+// the high words; the low words are summed in binary32.  A lane sums the
+// elements of one window (at most 16) into a fresh double word and merges it
+// into its running total; every merge (window, butterfly level, warp) is
+// followed by an exact renormalisation so that |lo| <= 2^-24 hi.  With u = 2^-24
+// the error of the total is then at most u^2 S (4 * 16^2 + 3 (windows + 12)):
+// the 32 low-word roundings of a window of 16 elements err by at most
+// 2 * 16 u^2 of its sum each, a renormalised merge by 3 u^2 of the merged sum
+// (Finish<kQsgd> uses this bound).
+__device__ __forceinline__ DWord dw_renorm(DWord a) {
+    const float s = __fadd_rn(a.hi, a.lo);  // |lo| <= hi: Fast2Sum is exact
+    return DWord{s, __fsub_rn(a.lo, __fsub_rn(s, a.hi))};
+}
+
 template <>
-struct Stats<kQsgd> {  // sum of p^2 as a double word; each square is split exactly
+struct Stats<kQsgd> {
     DWord sum;
     __device__ void init() { sum = DWord{0.0f, 0.0f}; }
     __device__ void add(float x) {
         const float hi = __fmul_rn(x, x);
         sum = dw_add(sum, DWord{hi, __fmaf_rn(x, x, -hi)});
     }
-    __device__ void warp_reduce() { sum = warp_sum(sum); }
-    __device__ void merge(const Stats &o) { sum = dw_add(sum, o.sum); }
+    __device__ void warp_reduce() {
+        sum = dw_renorm(sum);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            DWord p{__shfl_xor_sync(kFull, sum.hi, o), __shfl_xor_sync(kFull, sum.lo, o)};
+            sum = dw_renorm(dw_add(sum, p));
+        }
+    }
+    __device__ void merge(const Stats &o) { sum = dw_renorm(dw_add(sum, o.sum)); }
 };
 
 // Per-bucket quantization parameters derived from the statistics.
@@ -70,6 +93,7 @@ struct BucketParams {
     float a;           // UNIFORM: min (offset); SIGN / TERNARY: s; QSGD: unit
     float scale;       // UNIFORM: (max - min) / L
     float hi = 0.0f;   // CLIP: the upper bound elements are clamped to
+    bool exact = false;  // QSGD: the norm needs the exact path (qc_exact_norm.cuh)
 };
 
 template <int SCHEME, int BITS>
@@ -98,23 +122,53 @@ struct Finish<kSign, BITS> {
     }
 };
 
-// QSGD: unit = ||p|| / s with s = 2^(BITS-1) - 1.  The norm is the binary32
-// rounding of sqrt(hi + lo): r0 = sqrt(hi) correctly rounded, the remainder
+// QSGD: unit = nrm / s with s = 2^(BITS-1) - 1, where nrm is the binary32
+// rounding of sqrt(S), S the exact sum of squares.  From the renormalised
+// double word (hi, lo) ~ S: r0 = sqrt(hi) correctly rounded, the remainder
 // hi - r0^2 is exact by fma, and (remainder + lo) / (2 r0) is the first-order
-// correction.
+// correction, so N = r0 + corr is sqrt(S) within a relative
+//   half the sum's bound + 4.2 u^2     (u = 2^-24; the remainder, the two
+// roundings and the second-order term of the square root).  nrm = fl(N), and
+// `exact` is set when N lies within twice that bound (plus the 2^-46 that the
+// evaluation of its distance may err) of a midpoint between nrm and a
+// neighbour, or when hi lies outside [2^-60, 2^124] (squares whose low words
+// are not exact, or sums near overflow): such buckets take the exact path.
+template <int BITS>
+__device__ __forceinline__ BucketParams qsgd_params(float nrm) {
+    constexpr float kS = static_cast<float>((1u << (BITS - 1)) - 1u);
+    const float unit = __fdiv_rn(nrm, kS);
+    return BucketParams{unit, unit};
+}
+
 template <int BITS>
 struct Finish<kQsgd, BITS> {
-    static __device__ __forceinline__ BucketParams run(const Stats<kQsgd> &st, uint32_t) {
+    static __device__ __forceinline__ BucketParams run(const Stats<kQsgd> &st, uint32_t cnt) {
         const float hi = st.sum.hi;
-        float nrm = 0.0f;
-        if (hi > 0.0f) {
-            const float r0 = __fsqrt_rn(hi);
-            const float rem = __fadd_rn(__fmaf_rn(-r0, r0, hi), st.sum.lo);
-            nrm = __fadd_rn(r0, __fdiv_rn(rem, __fmul_rn(2.0f, r0)));
+        // hi == 0 (a zero bucket, or squares below the binary32 range) goes the exact way too
+        if (!(hi >= 0x1p-60f && hi <= 0x1p124f)) {
+            BucketParams bp = qsgd_params<BITS>(0.0f);
+            bp.exact = true;
+            return bp;
         }
-        constexpr float kS = static_cast<float>((1u << (BITS - 1)) - 1u);
-        const float unit = __fdiv_rn(nrm, kS);
-        return BucketParams{unit, unit};
+        const float r0 = __fsqrt_rn(hi);
+        const float rem = __fadd_rn(__fmaf_rn(-r0, r0, hi), st.sum.lo);
+        const float corr = __fdiv_rn(rem, __fmul_rn(2.0f, r0));
+        const float nrm = __fadd_rn(r0, corr);
+        // N - nrm, to within 2^-47 nrm (r0 - nrm is exact: they are within a few ulps)
+        const float d = __fadd_rn(__fsub_rn(r0, nrm), corr);
+        const uint32_t nb = __float_as_uint(nrm);
+        const float half_ulp = __uint_as_float((nb & 0x7F800000u) - (24u << 23));  // nrm >= 2^-30: normal
+        const bool pow2 = (nb & 0x7FFFFFu) == 0u;
+        const float windows = static_cast<float>((cnt + 511u) / 512u);
+        // twice the bound on |N - sqrt(S)| / nrm, plus the evaluation slack
+        const float rel = __fmaf_rn(3.0f * 0x1p-48f, windows, (1024.0f + 36.0f + 8.4f) * 0x1p-48f) +
+                          0x1p-46f;
+        const float slack = __fmul_rn(rel, nrm);
+        const bool near_up = d >= __fsub_rn(half_ulp, slack);
+        const bool near_dn = -d >= __fsub_rn(pow2 ? __fmul_rn(half_ulp, 0.5f) : half_ulp, slack);
+        BucketParams bp = qsgd_params<BITS>(nrm);
+        bp.exact = near_up || near_dn;
+        return bp;
     }
 };
 
@@ -210,7 +264,7 @@ __device__ __forceinline__ uint32_t quantize(float p, float u, const BucketParam
                 bool up;
                 if constexpr (SR) up = u < m;
                 else up = m > 0.5f || (m == 0.5f && (j0 & 1u));
-                lvl = j0 + (up ? 1u : 0u);
+                lvl = (j0 + (up ? 1u : 0u)) & static_cast<uint32_t>(J);  // a non-finite x stays in its field
             } else {
                 // below the smallest level 2^(1-J): the position x / 2^(1-J), exact
                 const float f = __fmul_rn(x, __uint_as_float(static_cast<uint32_t>(127 + J - 1) << 23));
@@ -360,9 +414,10 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             qf = up ? __fadd_rn(ff, 1.0f) : ff;
         }
         // no clamp: 0 <= ta <= L (1 + 2^-22), so a level above L needs ta within
-        // reach of L + 1/2 (impossible) or of the integer L (flagged by redo)
+        // reach of L + 1/2 (impossible) or of the integer L (flagged by redo).
+        // The mask keeps a non-finite element's code inside its own field.
         deq = __fmaf_rn(qf, bp.scale, bp.a);
-        return q;
+        return q & ((1u << BITS) - 1u);
     } else if constexpr (SCHEME == kQsgd) {
         constexpr float kMagic = 12582912.0f;
         const uint32_t neg = p < 0.0f ? 1u : 0u;
@@ -386,9 +441,10 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             qf = up ? __fadd_rn(ff, 1.0f) : ff;
         }
         // no clamp: t <= S (1 + 2^-22); a level above S would be flagged by redo
+        // (the mask keeps a non-finite element's code inside its own field)
         const float mag = __fmul_rn(qf, bp.a);
         deq = neg ? -mag : mag;
-        return (neg << (BITS - 1)) | q;
+        return (neg << (BITS - 1)) | (q & ((1u << (BITS - 1)) - 1u));
     } else if constexpr (SCHEME == kTernary) {
         const float s = bp.a;
         const float pa = __fmul_rn(fabsf(p), fq.rinv);
@@ -409,7 +465,7 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
     } else if constexpr (SCHEME == kLog) {
         constexpr uint32_t J = (1u << (BITS - 1)) - 1u;
         const uint32_t neg = p < 0.0f ? 1u : 0u;
-        const uint32_t lvl = log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo);
+        const uint32_t lvl = log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo) & J;
         const float mag = lvl ? __fmul_rn(bp.a, __uint_as_float((lvl + 127u - J) << 23)) : 0.0f;
         deq = neg ? -mag : mag;
         return (neg << (BITS - 1)) | lvl;
@@ -443,7 +499,7 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
                    (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
             q += (u < fr) ? 1u : 0u;
         }
-        return q;  // no clamp needed outside redo (see quantize_fast)
+        return q & ((1u << BITS) - 1u);  // no clamp needed outside redo (see quantize_fast)
     } else if constexpr (SCHEME == kTernary) {
         const float pa = __fmul_rn(fabsf(p), fq.rinv);
         bool keep;
@@ -473,9 +529,10 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
                    (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
             q += (u < fr) ? 1u : 0u;
         }
-        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | q;  // no clamp outside redo
+        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | (q & ((1u << (BITS - 1)) - 1u));  // no clamp outside redo
     } else if constexpr (SCHEME == kLog) {
-        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo);
+        return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) |
+               (log_level_fast<BITS, SR>(fabsf(p), bp.a, u, fq, redo) & ((1u << (BITS - 1)) - 1u));
     } else {
         static_assert(SCHEME == kSign, "code_fast: every other scheme has its own branch");
         redo = false;
@@ -506,20 +563,88 @@ __device__ __forceinline__ float deq_of(uint32_t field, int c, const BucketParam
 template <int SCHEME, bool FULL = false>
 __device__ __forceinline__ void accumulate_slots(Stats<SCHEME> &st, const float4 (&p)[kSlots],
                                                  int tt, int team_threads, uint32_t cnt) {
+    // QSGD sums a window into a fresh double word and merges it (see Stats<kQsgd>)
+    Stats<SCHEME> part;
+    if constexpr (SCHEME == kQsgd) part.init();
+    Stats<SCHEME> &acc = (SCHEME == kQsgd) ? part : st;
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
         const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u;
         if (FULL || j + 4u <= cnt) {
-            st.add(p[s].x);
-            st.add(p[s].y);
-            st.add(p[s].z);
-            st.add(p[s].w);
+            acc.add(p[s].x);
+            acc.add(p[s].y);
+            acc.add(p[s].z);
+            acc.add(p[s].w);
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                if (j + c < cnt) st.add(get(p[s], c));
+                if (j + c < cnt) acc.add(get(p[s], c));
         }
     }
+    if constexpr (SCHEME == kQsgd) st.merge(part);
+}
+
+// The exact sum of the squares of the lane's valid elements (the QSGD norm's
+// exact path).
+__device__ __forceinline__ void wide_add_slots(WideSum &acc, const float4 (&p)[kSlots], int tt,
+                                               int team_threads, uint32_t cnt) {
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t j = static_cast<uint32_t>(s * team_threads + tt) * 4u + c;
+            if (j < cnt) wide_add_square(acc, get(p[s], c));
+        }
+    }
+}
+
+// Barrier over one team on named barrier BAR0 + team (the warp itself for W = 1).
+template <int BAR0>
+__device__ __forceinline__ void team_bar(int W, int team) {
+    if (W == 1) {
+        __syncwarp();
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"r"(BAR0 + team), "r"(W * 32) : "memory");
+    }
+}
+
+// The exactly rounded norm from every team thread's exact partial sum: a warp
+// butterfly, then (W > 1) the warps' sums two limbs at a time through the
+// team's slots of the statistics buffer (alternating between its two halves),
+// one team barrier per round.  Every thread of the team calls this together
+// (the caller's decision is uniform across the team) and gets the same value.
+template <int SCHEME, int BAR0>
+__device__ __forceinline__ float team_exact_norm(WideSum &acc, Stats<SCHEME> (*red)[kBlock / 32],
+                                              int W, int warp, int lane, int team) {
+    static_assert(sizeof(Stats<SCHEME>) >= 8, "two limbs per warp slot");
+    wide_warp_sum(acc);
+    if (W > 1) {
+        uint64_t tot[kWideLimbs];
+#pragma unroll
+        for (int i = 0; i < kWideLimbs; ++i) tot[i] = 0u;
+        team_bar<BAR0>(W, team);  // every warp is done with the statistics buffer
+        for (int r = 0; r < kWideLimbs; r += 2) {
+            uint32_t *mine = reinterpret_cast<uint32_t *>(&red[(r >> 1) & 1][warp]);
+            if (lane == 0) {
+                mine[0] = acc.w[r];
+                mine[1] = acc.w[r + 1];
+            }
+            team_bar<BAR0>(W, team);
+            for (int w = 0; w < W; ++w) {
+                const uint32_t *o = reinterpret_cast<const uint32_t *>(&red[(r >> 1) & 1][team * W + w]);
+                tot[r] += o[0];
+                tot[r + 1] += o[1];
+            }
+        }
+        team_bar<BAR0>(W, team);  // every warp has read the last round
+        uint64_t carry = 0;
+        for (int i = 0; i < kWideLimbs; ++i) {
+            const uint64_t t = tot[i] + carry;
+            acc.w[i] = static_cast<uint32_t>(t);
+            carry = t >> 32;
+        }
+    }
+    return wide_sqrt_f32(acc);
 }
 
 // Quantizes the lane's slots of bucket [b0, b0 + cnt), packs and stores the code
@@ -630,6 +755,21 @@ __device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*r
 template <int SCHEME>
 __device__ __forceinline__ void team_reduce_local(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
                                                   int &buf, int W, int warp, int lane, int team);
+
+// The exact norm of a bucket whose elements the team holds in its slots (one
+// window).  Inlined like the rest of the exact path: a call would make the
+// kernel keep its live registers in the call convention's registers, costing
+// the main loop occupancy, while the inlined path keeps its limbs on the stack.
+template <int SCHEME, int BAR0>
+__device__ __forceinline__ float team_exact_norm_slots(const float4 (&p)[kSlots], int tt,
+                                                    int team_threads, uint32_t cnt,
+                                                    Stats<SCHEME> (*red)[kBlock / 32], int W,
+                                                    int warp, int lane, int team) {
+    WideSum acc;
+    wide_zero(acc);
+    wide_add_slots(acc, p, tt, team_threads, cnt);
+    return team_exact_norm<SCHEME, BAR0>(acc, red, W, warp, lane, team);
+}
 
 // ------------------------------------------------------------- percentiles
 

@@ -181,7 +181,13 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
             } else {
                 team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
             }
-            const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            if constexpr (SCHEME == kQsgd) {
+                if (bp.exact) {  // rare: the norm next to a rounding boundary (uniform per team)
+                    bp = qsgd_params<BITS>(team_exact_norm_slots<SCHEME, 1>(p, tt, team_threads, cnt,
+                                                                            red, W, warp, lane, team));
+                }
+            }
             if (whole)
                 quantize_store_slots<SCHEME, BITS, SR, EF, true>(P.codes, P.err, t0 + b_off, cnt, tt,
                                                                  team_threads, lane, p, bp, P.step,

@@ -227,6 +227,11 @@ cudaError_t launch_encode_log(const EncodeParams &p, const EncodeTiles &g, int b
                               int stochastic, int bf16, cudaStream_t stream);
 cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                                int stochastic, cudaStream_t stream);
+// The receiver's bf16 encodes without error feedback for buckets of 1024
+// (8-bit nearest, ternary stochastic): whether they apply, and the launch.
+bool encode_bf16_fast_applies(const EncodeParams &p, int scheme, int bits, int stochastic,
+                              bool grad16, bool codes8);
+cudaError_t launch_encode_bf16_fast(const EncodeParams &p, int scheme, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
 cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int scheme, int bits,
                               cudaStream_t stream);
@@ -264,6 +269,7 @@ uint32_t take_selftest_errors();
 cudaError_t launch_wait_timeout_selftest(uint32_t rounds, cudaStream_t stream);
 uint32_t take_topk_errors();
 uint32_t take_encode_bf16_errors();
+uint32_t take_encode_bf16_fast_errors();
 uint32_t take_decode_errors();
 uint32_t take_reencode_errors();
 

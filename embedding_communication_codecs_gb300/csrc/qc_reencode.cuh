@@ -305,7 +305,21 @@ __global__ void __launch_bounds__(kReBlock, 2) reencode_kernel(const __grid_cons
                 }
             }
             team_reduce<SCHEME, true>(st, red, buf, W, warp, lane, team);
-            const BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
+            if constexpr (SCHEME == kQsgd) {
+                if (bp.exact) {  // rare: the norm next to a rounding boundary (uniform per team)
+                    WideSum acc;
+                    wide_zero(acc);
+                    wide_add_slots(acc, p, tt, team_threads, min(cnt, window));
+                    for (uint32_t w0 = window; w0 < cnt; w0 += window) {
+                        float4 q[kSlots];
+                        load_slots_sum(pb, b_off + w0, min(cnt - w0, window), tt, team_threads, q);
+                        wide_add_slots(acc, q, tt, team_threads, min(cnt - w0, window));
+                    }
+                    // named barriers 8.. (barrier 1 belongs to the consumer group)
+                    bp = qsgd_params<BITS>(team_exact_norm<SCHEME, 8>(acc, red, W, warp, lane, team));
+                }
+            }
             if (whole)
                 quantize_store_slots<SCHEME, BITS, SR, EF, true>(P.codes_out, P.err, t0 + b_off, window,
                                                                  tt, team_threads, lane, p, bp, P.step,

@@ -17,29 +17,43 @@ import numpy as np
 from tests._exact import frac, sqrt_down_f32, sqrt_to_f32
 
 
-def midpoint_bucket(f: float, steps: int = 4, side: str = "below"):
-    """Elements (binary32) whose exact sum of squares lies within about
-    2^(-24 * steps) (relative) below the midpoint between f and its upper
-    neighbour ('below'), just above it ('above'), and the value the norm must
-    round to."""
+def _bf16_down(x: np.float32) -> np.float32:
+    """The bf16 value (as binary32) nearest to x towards zero."""
+    return np.array([x], dtype=np.float32).view(np.uint32)[0] & np.uint32(0xFFFF0000)
+
+
+def _to_f32_bits(b) -> np.float32:
+    return np.array([b], dtype=np.uint32).view(np.float32)[0]
+
+
+def midpoint_bucket(f: float, steps: int = 4, side: str = "below", bf16: bool = False):
+    """Elements (binary32, or bf16 values held as binary32 with bf16=True) whose
+    exact sum of squares lies within about 2^(-24 * steps) (2^(-8 * steps) for
+    bf16) relative below the midpoint between f and its upper neighbour
+    ('below'), just above it ('above'), and the value the norm must round to."""
     f = np.float32(f)
     fu = np.nextafter(f, np.float32(np.inf))
     m = (frac(f) + frac(fu)) / 2
     rem = m * m
     out = []
     for _ in range(steps):
-        if rem <= Fraction(1, 2 ** 290):
+        if rem <= Fraction(1, 2 ** 250):
             break
         x = sqrt_down_f32(rem)
+        if bf16:
+            x = _to_f32_bits(_bf16_down(x))
         if x == 0:
             break
         out.append(x)
         rem -= frac(x) * frac(x)
     if side == "above":
-        # the smallest binary32 whose square exceeds the remainder
+        # the smallest element whose square exceeds the remainder
         x = sqrt_to_f32(rem) if rem > 0 else np.float32(0)
         while frac(x) * frac(x) <= rem:
             x = np.nextafter(x, np.float32(np.inf))
+        if bf16:
+            b = int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+            x = _to_f32_bits(((b + 0xFFFF) & 0xFFFF0000) if b & 0xFFFF else b)
         out.append(x)
     want = f if side == "below" else fu
     return np.array(out, dtype=np.float32), want

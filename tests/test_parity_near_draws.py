@@ -193,3 +193,70 @@ def test_qsgd_near_draws(q, bits):
            lambda gg, e: orc.encode_qsgd(gg, e, bits=bits, bucket=BUCKET,
                                          mode=orc.ROUND_STOCHASTIC, seed=SEED, step=STEP),
            f"qsgd b={bits}")
+
+
+def _encode_bf16(q, g16, bits, scheme, mode, bucket):
+    n = g16.size
+    words, nb = q.qc_code_words(n, bits), q.qc_num_buckets(n, bucket)
+    codes = torch.full((words,), -7, dtype=torch.int32, device="cuda")
+    scale = torch.full((nb,), -7.0, device="cuda")
+    offset = torch.full((nb,), -7.0, device="cuda") if scheme == orc.SCHEME_UNIFORM else None
+    q.qc_encode_ef(dev(g16), None, n, bits, bucket, scheme, mode, SEED, STEP, codes, scale, offset,
+                   dtype=q.QC_DTYPE_BF16)
+    torch.cuda.synchronize()
+    return u32(codes), host(scale), host(offset) if offset is not None else None
+
+
+def test_ternary_bf16_draws_on_the_quotient(q):
+    """bf16 gradients in buckets of 1024 with max |p| = 1, so |p| / s = |p|
+    exactly: wherever an element's draw u has at most 8 significant bits it is
+    a bf16 value, and the element is planted at u itself (u < |p| / s is false),
+    one bf16 step above (true) or below (false), with random signs.  Every code
+    and scale matches the oracle bit for bit."""
+    bucket, n = 1024, 1 << 20
+    u = _draws(n)
+    k = np.round(u * 2.0 ** 24).astype(np.int64)
+    nz = k > 0
+    sig = np.zeros(n, dtype=np.int64)
+    sig[nz] = np.floor(np.log2(k[nz])).astype(np.int64) - (
+        np.log2(k[nz] & -k[nz]).astype(np.int64))          # span of significant bits - 1
+    hits = np.flatnonzero(nz & (sig <= 7))
+    assert hits.size >= 40, hits.size
+    rng = np.random.default_rng(8)
+    g = (rng.random(n) * 0.5).astype(np.float32) * np.where(rng.random(n) < 0.5, -1, 1).astype(np.float32)
+    g16 = wl.to_bf16_bits(g)
+    which = np.arange(hits.size) % 3
+    vals = wl.to_bf16_bits(u[hits].astype(np.float32))
+    vals = np.where(which == 1, vals + 1, np.where(which == 2, vals - 1, vals)).astype(np.uint16)
+    sign = np.where(rng.random(hits.size) < 0.5, 0x8000, 0).astype(np.uint16)
+    g16[hits] = vals | sign
+    g16[::bucket] = wl.to_bf16_bits(np.array([1.0], dtype=np.float32))[0]
+    assert np.array_equal(wl.bf16_bits_to_f32(g16[hits] & 0x7FFF)[which == 0], u[hits][which == 0])
+    c, s, _ = _encode_bf16(q, g16, 2, orc.SCHEME_TERNARY, q.QC_ROUND_STOCHASTIC, bucket)
+    c_or, s_or = orc.encode_ternary(g16, None, bucket=bucket, mode=orc.ROUND_STOCHASTIC,
+                                    seed=SEED, step=STEP)
+    assert_bits_equal(s, s_or, "ternary bf16 scale")
+    assert_bits_equal(c, c_or, "ternary bf16 codes")
+
+
+def test_uniform8_bf16_ties(q):
+    """bf16 buckets of 1024 with min 0 and max 255 * 2^-10, so scale = 2^-10 and
+    (p - min) / scale = p * 2^10 exactly: elements at k + 1/2 steps for every k
+    are ties, rounded to the even level; one bf16 step either side is not."""
+    bucket, nb = 1024, 64
+    n = bucket * nb
+    rng = np.random.default_rng(21)
+    t = rng.integers(0, 127, size=n) + 0.5
+    t = np.where(rng.random(n) < 0.2, rng.integers(0, 256, size=n), t)
+    g16 = wl.to_bf16_bits((t * 2.0 ** -10).astype(np.float32))
+    nudge = rng.integers(-1, 2, size=n)
+    g16 = (g16.astype(np.int32) + np.where(g16 > 0, nudge, 0)).astype(np.uint16)
+    g16[::bucket] = 0
+    g16[1::bucket] = wl.to_bf16_bits(np.array([255 * 2.0 ** -10], dtype=np.float32))[0]
+    g16 = np.minimum(g16, g16[1])                     # keep every bucket's max at 255 * 2^-10
+    c, s, o = _encode_bf16(q, g16, 8, orc.SCHEME_UNIFORM, q.QC_ROUND_NEAREST, bucket)
+    c_or, s_or, o_or = orc.encode_uniform(g16, None, bits=8, bucket=bucket)
+    assert np.all(s_or == np.float32(2.0 ** -10))
+    assert_bits_equal(s, s_or, "u8 bf16 scale")
+    assert_bits_equal(o, o_or, "u8 bf16 offset")
+    assert_bits_equal(c, c_or, "u8 bf16 codes")

@@ -4,8 +4,8 @@ payloads, then encode the result with the receiver's own residual).
 The decoded result r must match the oracle bit for bit.  The new payload and
 residual must match bit for bit for the uniform and ternary schemes; the sign
 scheme's mean |p| is compared within 1e-6 * max|p| of its bucket (its only
-freedom is the order of the sum) and QSGD's unit within one ulp (the norm's
-sum order), with codes and residuals bit-identical wherever the unit is.
+freedom is the order of the sum); QSGD's unit, codes and residuals are
+bit-identical (its norm is the exactly rounded one on both sides).
 Worker counts cover one chunk per stage and several; buckets cover one warp,
 teams and the largest supported bucket; every n leaves a ragged tail.
 """

@@ -477,3 +477,97 @@ def test_decode_after_a_worker_drops_out(q):
     want = orc.decode_accumulate(codes, scale, offset, M=M - 1, n=n, bits=bits, bucket=bucket,
                                  scheme=0, flags=orc.OUT_MEAN)
     assert_bits_equal(host(out), want, "decode without worker 2")
+
+
+def _unpack_codes(words, n, bits):
+    per = 32 // bits
+    sh = (np.arange(per, dtype=np.uint32) * bits).astype(np.uint32)
+    return ((words[:, None] >> sh[None, :]) & np.uint32((1 << bits) - 1)).reshape(-1)[:n]
+
+
+_NAN_CASES = [("uniform", 1), ("uniform", 2), ("uniform", 4), ("uniform", 8), ("ternary", 2),
+              ("qsgd", 2), ("qsgd", 4), ("qsgd", 8), ("log", 2), ("log", 4), ("log", 8)]
+
+
+@pytest.mark.parametrize("scheme,bits", _NAN_CASES)
+@pytest.mark.parametrize("dtype,ef,bucket", [("f32", True, 512), ("f32", False, 4096),
+                                             ("bf16", False, 1024), ("f32", True, 8192)])
+@pytest.mark.parametrize("mode", [0, 1], ids=["nearest", "stochastic"])
+def test_nan_element_keeps_to_its_own_field(q, scheme, bits, dtype, ef, bucket, mode):
+    """A NaN inside a packed word (never a bucket's first element, whose value the
+    oracle's running min/max starts from) gives an unspecified code for that
+    element only: every other element's code, every bucket's metadata and every
+    other residual match the oracle bit for bit, in the pipelined fp32 kernel,
+    the bf16 kernel and the two-pass direct kernel."""
+    sch = {"uniform": q.QC_SCHEME_UNIFORM, "ternary": q.QC_SCHEME_TERNARY,
+           "qsgd": q.QC_SCHEME_QSGD, "log": q.QC_SCHEME_LOG}[scheme]
+    n = 3 * bucket + 100
+    gf = wl.outlier_gradient(n, seed=4242 + bits)
+    nan_at = np.array([5, bucket + 33, 2 * bucket + bucket // 2 + 1])
+    gf[nan_at] = np.float32(np.nan)
+    g = wl.to_bf16_bits(gf) if dtype == "bf16" else gf
+    err0 = (wl.std_normal(17, 1, n) * np.float32(1e-4)) if ef else None
+    codes, scale, offset, err = _run_encode(q, g, err0, n, bits, bucket, sch, mode)
+    e_or = err0.copy() if ef else None
+    kw = dict(bucket=bucket, mode=mode, seed=SEED, step=STEP)
+    if scheme == "uniform":
+        c_or, s_or, o_or = orc.encode_uniform(g, e_or, bits=bits, **kw)
+        assert_bits_equal(offset, o_or, "offset")
+    elif scheme == "ternary":
+        c_or, s_or = orc.encode_ternary(g, e_or, **kw)
+    elif scheme == "qsgd":
+        c_or, s_or = orc.encode_qsgd(g, e_or, bits=bits, **kw)
+    else:
+        c_or, s_or = orc.encode_log(g, e_or, bits=bits, **kw)
+    assert_bits_equal(scale, s_or, "scale")
+    keep = np.ones(n, dtype=bool)
+    keep[nan_at] = False
+    cg, co = _unpack_codes(codes, n, bits), _unpack_codes(c_or, n, bits)
+    bad = np.flatnonzero(keep & (cg != co))
+    assert bad.size == 0, [(int(i), int(cg[i]), int(co[i])) for i in bad[:8]]
+    if ef:
+        assert_bits_equal(err[keep], e_or[keep], "residual")
+
+
+@pytest.mark.parametrize("scheme,bits,mode", [("uniform", 8, 0), ("uniform", 4, 1), ("ternary", 2, 1),
+                                              ("uniform", 2, 0), ("uniform", 1, 0)])
+@pytest.mark.parametrize("bucket", [1024, 2048])
+def test_bf16_tails_of_every_length(q, scheme, bits, mode, bucket):
+    """bf16 gradients whose last bucket holds 1 .. 9 elements past a multiple of
+    8 (and a word offset of the code buffer that is 4- but not 8-byte aligned):
+    codes, metadata and the canaries after the last code word match the
+    oracle, in the receiver kernels for buckets of 1024 and the general bf16
+    kernel for 2048."""
+    sch = q.QC_SCHEME_UNIFORM if scheme == "uniform" else q.QC_SCHEME_TERNARY
+    for r in range(1, 10):
+        n = 2 * bucket + 8 * 5 + r
+        g = wl.to_bf16_bits(wl.outlier_gradient(n, seed=300 + r))
+        codes, scale, offset, _ = _run_encode(q, g, None, n, bits, bucket, sch, mode)
+        if scheme == "uniform":
+            c_or, s_or, o_or = orc.encode_uniform(g, None, bits=bits, bucket=bucket, mode=mode,
+                                                  seed=SEED, step=STEP)
+            assert_bits_equal(offset, o_or, f"offset r={r}")
+        else:
+            c_or, s_or = orc.encode_ternary(g, None, bucket=bucket, mode=mode, seed=SEED, step=STEP)
+        assert_bits_equal(codes, c_or, f"codes r={r}")
+        assert_bits_equal(scale, s_or, f"scale r={r}")
+    # a code buffer one word into an 8-byte aligned allocation
+    n = 3 * bucket + 13
+    g = wl.to_bf16_bits(wl.outlier_gradient(n, seed=399))
+    words, nb = q.qc_code_words(n, bits), q.qc_num_buckets(n, bucket)
+    base = torch.full((words + 2,), -7, dtype=torch.int32, device="cuda")
+    codes = base[1:1 + words]
+    assert codes.data_ptr() % 8 == 4
+    scale = torch.empty(nb, device="cuda")
+    offset = torch.empty(nb, device="cuda") if scheme == "uniform" else None
+    q.qc_encode_ef(dev(g), None, n, bits, bucket, sch, mode, SEED, STEP, codes, scale, offset,
+                   dtype=q.QC_DTYPE_BF16)
+    torch.cuda.synchronize()
+    if scheme == "uniform":
+        c_or, _, _ = orc.encode_uniform(g, None, bits=bits, bucket=bucket, mode=mode, seed=SEED,
+                                        step=STEP)
+    else:
+        c_or, _ = orc.encode_ternary(g, None, bucket=bucket, mode=mode, seed=SEED, step=STEP)
+    assert_bits_equal(u32(codes), c_or, "codes at a 4-byte offset")
+    b = host(base)
+    assert b[0] == -7 and b[-1] == -7
