@@ -93,6 +93,73 @@ def _ptr(t):
     return t.data_ptr()
 
 
+# ------------------------------------------------------- argument validation
+#
+# The C ABI takes raw addresses and sizes, so it cannot see a tensor's dtype,
+# device, layout or length.  Before any call the wrappers check every torch
+# tensor they are given against what the call will read or write: its dtype,
+# that its rows are dense (flat buffers: contiguous), that it holds at least the
+# bytes the call touches; and, only after every argument has passed those,
+# that each lives on a CUDA device (so the other checks can be exercised
+# without a GPU).  A mismatch raises ValueError and
+# nothing is launched.  Raw integer addresses are passed through unchecked.
+
+def _torch():
+    import torch
+    return torch
+
+
+def _extent_bytes(t) -> int:
+    """Bytes from t's first element to one past its last (non-negative strides)."""
+    if t.numel() == 0:
+        return 0
+    return (sum((n - 1) * st for n, st in zip(t.shape, t.stride())) + 1) * t.element_size()
+
+
+def _need(t, name, nbytes, dtypes=None, flat=True):
+    """Check a tensor argument; `flat` asks for a contiguous buffer, otherwise
+    only the innermost dimension must be dense (stacked payload rows)."""
+    if t is None or isinstance(t, int):
+        return
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor or an integer address")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected one of {tuple(dtypes)}")
+    if any(st < 0 for st in t.stride()):
+        raise ValueError(f"{name} has a negative stride")
+    if flat and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not flat and t.dim() > 0 and t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must be dense along its last dimension")
+    if _extent_bytes(t) < nbytes:
+        raise ValueError(f"{name} spans {_extent_bytes(t)} bytes; the call needs {nbytes}")
+
+
+def _on_device(**tensors):
+    """The last check of every call: each tensor argument lives on a CUDA device."""
+    for name, t in tensors.items():
+        if t is not None and not isinstance(t, int) and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _row_stride(t, name, stride_elems, M):
+    """With M > 1 a 2-D payload tensor's row stride must be the stride passed."""
+    if M > 1 and t is not None and not isinstance(t, int) and t.dim() == 2:
+        if t.stride(0) * t.element_size() != stride_elems * 4:
+            raise ValueError(f"{name}'s row stride ({t.stride(0)} elements) differs from the "
+                             f"stride passed ({stride_elems} 4-byte units)")
+
+
+def _words32():
+    torch = _torch()
+    return (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+
+
+def _f32():
+    return (_torch().float32,)
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -143,14 +210,45 @@ def qc_encode_ef(grad, err, n, bits, bucket, scheme, mode, seed, step, codes, sc
 
     ``err`` (fp32, in/out) may be None for no error feedback; ``offset`` may be
     None unless ``scheme`` is uniform.  Raises QCodecError on a non-OK status."""
+    if not isinstance(grad, int):
+        dt = _dtype_code(grad, dtype)
+        torch = _torch()
+        want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
+        _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
+    nb = qc_num_buckets(n, bucket) if bucket else 0
+    _need(err, "err", 4 * n, _f32())
+    _need(codes, "codes", 4 * qc_code_words(n, bits), _words32())
+    _need(scale, "scale", 4 * nb, _f32())
+    if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP):
+        _need(offset, "offset", 4 * nb, _f32())
+    _on_device(grad=grad, err=err, codes=codes, scale=scale, offset=offset)
     _check(lib.qc_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bits, bucket,
                             scheme, mode, seed, step, _ptr(codes), _ptr(scale), _ptr(offset),
                             _stream(stream)))
 
 
+def _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                    scheme):
+    """The M stacked payloads a decode or re-encode reads."""
+    words = qc_code_words(n, bits)
+    nb = qc_num_buckets(n, bucket) if bucket else 0
+    cs, ms = (codes_stride_words, meta_stride) if M > 1 else (0, 0)
+    _need(codes, "codes", 4 * ((M - 1) * cs + words), _words32(), flat=False)
+    _need(scale, "scale", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+    _row_stride(codes, "codes", codes_stride_words, M)
+    _row_stride(scale, "scale", meta_stride, M)
+    if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP):
+        _need(offset, "offset", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+        _row_stride(offset, "offset", meta_stride, M)
+
+
 def qc_decode_accumulate(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits,
                          bucket, scheme, out, flags=QC_OUT_SUM, stream=None):
     """Receiver half: ``out`` = fixed-order fp32 sum (or mean) of M decoded payloads."""
+    _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                    scheme)
+    _need(out, "out", 4 * n, _f32())
+    _on_device(codes=codes, scale=scale, offset=offset, out=out)
     _check(lib.qc_decode_accumulate(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
                                     meta_stride, M, n, bits, bucket, scheme, _ptr(out), flags,
                                     _stream(stream)))
@@ -163,6 +261,17 @@ def qc_reencode(codes, codes_stride_words, scale, offset, meta_stride, M, n, bit
     QC_OUT_MEAN), then encode the result with the residual ``err`` (fp32,
     in/out, or None) in the same scheme, bits and bucket.  ``out`` (optional)
     receives the decoded result itself."""
+    _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                    scheme)
+    nb = qc_num_buckets(n, bucket) if bucket else 0
+    _need(err, "err", 4 * n, _f32())
+    _need(out, "out", 4 * n, _f32())
+    _need(codes_out, "codes_out", 4 * qc_code_words(n, bits), _words32())
+    _need(scale_out, "scale_out", 4 * nb, _f32())
+    if scheme == QC_SCHEME_UNIFORM:
+        _need(offset_out, "offset_out", 4 * nb, _f32())
+    _on_device(codes=codes, scale=scale, offset=offset, err=err, out=out, codes_out=codes_out,
+               scale_out=scale_out, offset_out=offset_out)
     _check(lib.qc_reencode(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
                            meta_stride, M, n, bits, bucket, scheme, flags, _ptr(err), mode, seed,
                            step, _ptr(codes_out), _ptr(scale_out), _ptr(offset_out), _ptr(out),
@@ -173,6 +282,18 @@ def qc_topk_encode_ef(grad, err, n, bucket, keep, mode, seed, step, idx, codes, 
                       stream=None, dtype=None):
     """Top-k sparsification per bucket with 8-bit codes of the kept values and
     error feedback (``err`` may be None); outputs keep slots per bucket."""
+    torch = _torch()
+    if not isinstance(grad, int):
+        dt = _dtype_code(grad, dtype)
+        want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
+        _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
+    nb = qc_num_buckets(n, bucket) if bucket else 0
+    _need(err, "err", 4 * n, _f32())
+    _need(idx, "idx", 4 * nb * keep, _words32())
+    _need(codes, "codes", nb * keep, (torch.uint8, torch.int8))
+    _need(scale, "scale", 4 * nb, _f32())
+    _need(offset, "offset", 4 * nb, _f32())
+    _on_device(grad=grad, err=err, idx=idx, codes=codes, scale=scale, offset=offset)
     _check(lib.qc_topk_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bucket, keep,
                                  mode, seed, step, _ptr(idx), _ptr(codes), _ptr(scale),
                                  _ptr(offset), _stream(stream)))
@@ -181,6 +302,15 @@ def qc_topk_encode_ef(grad, err, n, bucket, keep, mode, seed, step, idx, codes, 
 def qc_topk_decode_accumulate(idx, codes, pair_stride, scale, offset, meta_stride, M, n, bucket,
                               keep, out, flags=QC_OUT_SUM, stream=None):
     """Scatter M workers' top-k pairs into a dense fp32 vector in worker order."""
+    torch = _torch()
+    nb = qc_num_buckets(n, bucket) if bucket else 0
+    ps, ms = (pair_stride, meta_stride) if M > 1 else (0, 0)
+    _need(idx, "idx", 4 * ((M - 1) * ps + nb * keep), _words32(), flat=False)
+    _need(codes, "codes", (M - 1) * ps + nb * keep, (torch.uint8, torch.int8), flat=False)
+    _need(scale, "scale", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+    _need(offset, "offset", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+    _need(out, "out", 4 * n, _f32())
+    _on_device(idx=idx, codes=codes, scale=scale, offset=offset, out=out)
     _check(lib.qc_topk_decode_accumulate(_ptr(idx), _ptr(codes), pair_stride, _ptr(scale),
                                          _ptr(offset), meta_stride, M, n, bucket, keep, _ptr(out),
                                          flags, _stream(stream)))
@@ -188,16 +318,32 @@ def qc_topk_decode_accumulate(idx, codes, pair_stride, scale, offset, meta_strid
 
 def qc_sign_vote(signs, stride_words, M, n, out, stream=None):
     """Majority vote over M packed sign vectors."""
+    words = qc_code_words(n, 1)
+    _need(signs, "signs", 4 * ((M - 1) * (stride_words if M > 1 else 0) + words), _words32(),
+          flat=False)
+    _row_stride(signs, "signs", stride_words, M)
+    _need(out, "out", 4 * words, _words32())
+    _on_device(signs=signs, out=out)
     _check(lib.qc_sign_vote(_ptr(signs), stride_words, M, n, _ptr(out), _stream(stream)))
 
 
 def qc_rowwise_fp8(x, rows, dim, codes, row_scale, stream=None):
     """FP32 rows -> E4M3 codes + per-row fp32 scale."""
+    torch = _torch()
+    _need(x, "x", 4 * rows * dim, _f32())
+    _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
+    _need(row_scale, "row_scale", 4 * rows, _f32())
+    _on_device(x=x, codes=codes, row_scale=row_scale)
     _check(lib.qc_rowwise_fp8(_ptr(x), rows, dim, _ptr(codes), _ptr(row_scale), _stream(stream)))
 
 
 def qc_rowwise_fp8_dequant(codes, row_scale, rows, dim, out, stream=None):
     """E4M3 codes + per-row scale -> fp32 rows."""
+    torch = _torch()
+    _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
+    _need(row_scale, "row_scale", 4 * rows, _f32())
+    _need(out, "out", 4 * rows * dim, _f32())
+    _on_device(codes=codes, row_scale=row_scale, out=out)
     _check(lib.qc_rowwise_fp8_dequant(_ptr(codes), _ptr(row_scale), rows, dim, _ptr(out),
                                       _stream(stream)))
 
