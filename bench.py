@@ -183,16 +183,28 @@ class UniformEF(Component):
         self.h2d = 4 * n
         self.d2h = 4 * n
 
-    def _grad(self, n):
-        """The first n elements of the workload's step-0 gradient."""
+    def _grad(self, n, step=0):
+        """The first n elements of the workload's gradient of `step` (the
+        per-bucket-sigma recipe draws a fresh gradient every step)."""
         if self.sigma_mode == "bucket":
             sig = wl.bucket_sigmas(self.n, self.bucket, self.seed)
-            return wl.bucket_sigma_gradient(n, self.bucket, 0, self.seed,
+            return wl.bucket_sigma_gradient(n, self.bucket, step, self.seed,
                                             sigmas=sig[:(n + self.bucket - 1) // self.bucket])
         return wl.outlier_gradient(n, seed=self.seed)
 
-    def setup(self, q, torch):
-        self.g = torch.from_numpy(self._grad(self.n)).cuda()
+    def setup(self, q, torch, shared=None):
+        """`shared`: another component of the same recipe whose device gradients
+        this one reads instead of drawing its own."""
+        if shared is not None:
+            self.gs = shared.gs
+        else:
+            self.gs = [torch.from_numpy(self._grad(self.n, 0)).cuda()]
+            if self.sigma_mode == "bucket":
+                # two independent step draws, alternated step by step, so the
+                # residual evolves as under fresh gradients
+                self.gs.append(torch.from_numpy(self._grad(self.n, 1)).cuda())
+        self.g = self.gs[0]
+        self.fixed_input = False
         self.err = torch.zeros(self.n, device="cuda")
         self.codes, self.scale, self.offset = q.alloc_payload(self.n, self.bits, self.bucket,
                                                               self.scheme)
@@ -200,8 +212,9 @@ class UniformEF(Component):
 
     def run(self, q, t, timer):
         mode = q.QC_ROUND_STOCHASTIC if self.stochastic else q.QC_ROUND_NEAREST
+        g = self.g if self.fixed_input else self.gs[t % len(self.gs)]
         with timer(self.enc_name):
-            q.qc_encode_ef(self.g, self.err, self.n, self.bits, self.bucket, self.scheme, mode,
+            q.qc_encode_ef(g, self.err, self.n, self.bits, self.bucket, self.scheme, mode,
                            self.seed, t, self.codes, self.scale, self.offset)
         with timer(self.dec_name):
             q.qc_decode_accumulate(self.codes, 0, self.scale, self.offset, 0, 1, self.n, self.bits,
@@ -220,7 +233,7 @@ class UniformEF(Component):
         e_old = self.err.clone()
         self.run(q, 10_000, KernelTimer(torch, enabled=False))
         meta = 8 if self.scheme in (0, 4) else 4
-        p = self.g + e_old
+        p = self.gs[10_000 % len(self.gs)] + e_old
         return {"compression": round(32 / (self.bits + 8 * meta / self.bucket), 3),
                 "rel_rms_error_of_step": _rel_rms(torch, self.out, p),
                 "residual_rms_over_gradient_rms": _rms_ratio(torch, self.err, self.g)}
@@ -824,6 +837,10 @@ def run_ours(args, world, rank, local):
                 "bytes_per_launch": kinfo[dom]["bytes_per_launch"]}
     for k in kinfo:
         kinfo[k]["frac_of_peak"] = round(kinfo[k]["gbs"] / peak, 4)
+        u = units_per_launch.get(k)
+        if u:
+            kinfo[k]["units_per_launch"] = u
+            kinfo[k]["elements_per_s"] = float(f"{u / (kinfo[k]['avg_us'] * 1e-6):.4g}")
 
     quality = {}
     for c in comps:
@@ -884,6 +901,9 @@ def run_e2e(args, comps, q, torch, world, units, results=None):
                                 if ptrs & {d.data_ptr() for d in o.reads()}], default=k))
     steps = max(1, min(args.steps, args.e2e_steps))
     timer = KernelTimer(torch, enabled=False)
+    for c in comps:   # each step's gradient comes in from the host into the one buffer
+        if hasattr(c, "fixed_input"):
+            c.fixed_input = True
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     cur = torch.cuda.current_stream()
     torch.cuda.synchronize()
@@ -924,6 +944,9 @@ def run_e2e(args, comps, q, torch, world, units, results=None):
         cur.wait_stream(st)
     e.record(cur)
     torch.cuda.synchronize()
+    for c in comps:
+        if hasattr(c, "fixed_input"):
+            c.fixed_input = False
     if results is not None:
         results.extend(h for pairs in outs for _, h in pairs)
     ms = max_over_ranks(s.elapsed_time(e), world)
