@@ -332,7 +332,7 @@ class Receiver(Component):
         meta = 8 if scheme == 0 else 4
         tag = "u8" if scheme == 0 else "ternary"
         self.enc_name, self.dec_name = f"encode_{tag}_bf16", f"decode_{tag}_m{M}"
-        self.kernels = {self.enc_name: (M, 2 * n + 4 * words + meta * nb),
+        self.kernels = {self.enc_name: (1, M * (2 * n + 4 * words + meta * nb)),
                         self.dec_name: (1, M * (4 * words + meta * nb) + 4 * n)}
         self.units = 2 * M * n
         self.h2d = 2 * M * n if shared is None else 0
@@ -348,14 +348,19 @@ class Receiver(Component):
                                                               self.scheme, workers=self.M)
         self.out = torch.empty(self.n, device="cuda")
 
-    def run(self, q, t, timer):
+    def encode_all(self, q, t):
+        """The M workers' encodes as one multi-segment call (one launch): worker
+        w's draws are indexed w * n + i, the workers' gradients laid end to end
+        under the one seed."""
         mode = q.QC_ROUND_NEAREST if self.scheme == 0 else q.QC_ROUND_STOCHASTIC
-        for w in range(self.M):
-            with timer(self.enc_name):
-                q.qc_encode_ef(self.g[w], None, self.n, self.bits, self.bucket, self.scheme, mode,
-                               self.seed | (w << 32), t, self.codes[w], self.scale[w],
-                               self.offset[w] if self.offset is not None else None,
-                               dtype=q.QC_DTYPE_BF16)
+        segs = [(self.g[w], None, self.n, self.codes[w], self.scale[w],
+                 self.offset[w] if self.offset is not None else None) for w in range(self.M)]
+        q.qc_encode_ef_segments(segs, q.QC_DTYPE_BF16, self.bits, self.bucket, self.scheme, mode,
+                                self.seed, t)
+
+    def run(self, q, t, timer):
+        with timer(self.enc_name):
+            self.encode_all(q, t)
         with timer(self.dec_name):
             q.qc_decode_accumulate(self.codes, self.codes.stride(0), self.scale,
                                    self.offset, self.scale.stride(0), self.M, self.n, self.bits,
@@ -368,7 +373,7 @@ class Receiver(Component):
         return [self.g]
 
     def kernel_units(self):
-        return {self.enc_name: self.n, self.dec_name: self.M * self.n}
+        return {self.enc_name: self.M * self.n, self.dec_name: self.M * self.n}
 
     def host_outputs(self):
         return [self.out]
@@ -390,12 +395,12 @@ class Receiver(Component):
             for w in range(self.M):
                 if self.scheme == 0:
                     c, s, o = orc.encode_uniform(gb[w, lo:hi], None, bits=8, bucket=self.bucket,
-                                                 index_base=lo)
+                                                 index_base=w * self.n + lo)
                     os_.append(o)
                 else:
                     c, s = orc.encode_ternary(gb[w, lo:hi], None, bucket=self.bucket,
-                                              mode=orc.ROUND_STOCHASTIC,
-                                              seed=self.seed | (w << 32), index_base=lo)
+                                              mode=orc.ROUND_STOCHASTIC, seed=self.seed,
+                                              index_base=w * self.n + lo)
                 cs.append(c)
                 ss.append(s)
             orc.decode_accumulate(np.stack(cs), np.stack(ss), np.stack(os_) if os_ else None,
@@ -417,8 +422,13 @@ class TopkEF(Component):
         self.h2d = 4 * M * n
         self.d2h = 4 * n
 
-    def setup(self, q, torch):
-        self.g = torch.from_numpy(wl.shared_mean_gradients(self.n, self.M, self.seed)).cuda()
+    def setup(self, q, torch, shared=None):
+        """`shared`: the sign workload, whose device gradients (the same recipe)
+        this component reads instead of drawing its own."""
+        if shared is not None:
+            self.g = shared.g
+        else:
+            self.g = torch.from_numpy(wl.shared_mean_gradients(self.n, self.M, self.seed)).cuda()
         self.err = torch.zeros((self.M, self.n), device="cuda")
         nb = _nb(self.n, self.bucket)
         self.slots = nb * self.keep
@@ -482,7 +492,7 @@ class Reencode(Receiver):
         meta = 8 if scheme == 0 else 4
         tag = "u8" if scheme == 0 else ("ternary" if scheme == 2 else f"s{scheme}b{bits}")
         self.dec_name = f"reencode_{tag}_m{M}"
-        self.kernels = {self.enc_name: (M, 2 * n + 4 * words + meta * nb),
+        self.kernels = {self.enc_name: (1, M * (2 * n + 4 * words + meta * nb)),
                         self.dec_name: (1, M * (4 * words + meta * nb) + 8 * n + 4 * words +
                                         meta * nb)}
         self.units = 2 * M * n + n
@@ -496,12 +506,8 @@ class Reencode(Receiver):
 
     def run(self, q, t, timer):
         mode = q.QC_ROUND_NEAREST if self.scheme == 0 else q.QC_ROUND_STOCHASTIC
-        for w in range(self.M):
-            with timer(self.enc_name):
-                q.qc_encode_ef(self.g[w], None, self.n, self.bits, self.bucket, self.scheme, mode,
-                               self.seed | (w << 32), t, self.codes[w], self.scale[w],
-                               self.offset[w] if self.offset is not None else None,
-                               dtype=q.QC_DTYPE_BF16)
+        with timer(self.enc_name):
+            self.encode_all(q, t)
         with timer(self.dec_name):
             q.qc_reencode(self.codes, self.codes.stride(0), self.scale, self.offset,
                           self.scale.stride(0), self.M, self.n, self.bits, self.bucket,
@@ -516,7 +522,7 @@ class Reencode(Receiver):
         return {"compression_vs_fp32": round(32 / (self.bits + 8 * meta / self.bucket), 3)}
 
     def kernel_units(self):
-        return {self.enc_name: self.n, self.dec_name: self.M * self.n}
+        return {self.enc_name: self.M * self.n, self.dec_name: self.M * self.n}
 
     def oracle_sample(self, frac):
         import oracle as orc
@@ -530,18 +536,179 @@ class Reencode(Receiver):
             for w in range(self.M):
                 if self.scheme == 0:
                     c, s, o = orc.encode_uniform(gb[w, lo:hi], None, bits=8, bucket=self.bucket,
-                                                 index_base=lo)
+                                                 index_base=w * self.n + lo)
                     os_.append(o)
                 else:
                     c, s = orc.encode_ternary(gb[w, lo:hi], None, bucket=self.bucket,
-                                              mode=orc.ROUND_STOCHASTIC,
-                                              seed=self.seed | (w << 32), index_base=lo)
+                                              mode=orc.ROUND_STOCHASTIC, seed=self.seed,
+                                              index_base=w * self.n + lo)
                 cs.append(c)
                 ss.append(s)
             orc.reencode(np.stack(cs), np.stack(ss), np.stack(os_) if os_ else None, M=self.M,
                          n=hi - lo, bits=self.bits, bucket=self.bucket, scheme=self.scheme,
                          flags=orc.OUT_MEAN, err=err[lo:hi], mode=mode)
         return _split(go, n, self.bucket), self.units * n // self.n
+
+
+class VoteOnly(Component):
+    """The majority vote alone over M packed sign vectors of n bits (the vote's
+    streaming rate, at a size far above L2).  The sign words are seeded random
+    bits drawn on the device: the vote's work does not depend on their values."""
+
+    def __init__(self, name="vote_2p30", n=1 << 30, M=8, seed=3):
+        self.name, self.n, self.M, self.seed = name, n, M, seed
+        words = _words(n, 1)
+        self.kernels = {f"sign_vote_m{M}_{name.split('_')[-1]}": (1, (M + 1) * 4 * words)}
+        self.units = M * n
+
+    def setup(self, q, torch, shared=None):
+        gen = torch.Generator(device="cuda").manual_seed(self.seed)
+        words = _words(self.n, 1)
+        self.signs = torch.randint(-2 ** 31, 2 ** 31 - 1, (self.M, words), dtype=torch.int32,
+                                   device="cuda", generator=gen)
+        self.out = torch.empty(words, dtype=torch.int32, device="cuda")
+
+    def run(self, q, t, timer):
+        with timer(next(iter(self.kernels))):
+            q.qc_sign_vote(self.signs, self.signs.stride(0), self.M, self.n, self.out)
+
+    def kernel_units(self):
+        return {next(iter(self.kernels)): self.M * self.n}
+
+
+class ReencodeOnly(Component):
+    """The fused receiver re-encode alone, on the M payloads another component
+    (the 8-bit receiver workload) has just encoded: decode, MEAN, re-encode
+    with the receiver's own residual (seed 4 | 1 << 40)."""
+
+    def __init__(self, name="rx_reencode_u8_m16", src=None):
+        self.name, self.src = name, src
+        n, M, b = src.n, src.M, src.bucket
+        words, nb = _words(n, 8), _nb(n, b)
+        self.kernels = {"reencode_u8_m16": (1, M * (4 * words + 8 * nb) + 8 * n + 4 * words + 8 * nb)}
+        self.units = M * n
+
+    def setup(self, q, torch, shared=None):
+        r = self.src
+        self.err = torch.zeros(r.n, device="cuda")
+        self.codes2, self.scale2, self.offset2 = q.alloc_payload(r.n, 8, r.bucket, 0)
+
+    def run(self, q, t, timer):
+        r = self.src
+        with timer("reencode_u8_m16"):
+            q.qc_reencode(r.codes, r.codes.stride(0), r.scale, r.offset, r.scale.stride(0), r.M,
+                          r.n, 8, r.bucket, 0, q.QC_OUT_MEAN, self.err, q.QC_ROUND_NEAREST,
+                          r.seed | (1 << 40), t, self.codes2, self.scale2, self.offset2, None)
+
+    def kernel_units(self):
+        return {"reencode_u8_m16": self.src.M * self.src.n}
+
+
+SUPPLEMENT_TEXT = {
+    "u8_ef_2p20": "uniform 8-bit EF encode + M=1 decode, 2^20 fp32 (outlier recipe), B=2048, RN "
+                  "(13.6 MB: L2-resident; per-launch times from events and from a CUDA graph)",
+    "vote_2p30": "majority vote of 8 packed sign vectors of 2^30 bits",
+    "qsgd4_ef": "QSGD 4-bit SR + EF encode, M=1 decode, 250M fp32 (per-bucket sigma), B=512",
+    "log4_ef": "logarithmic levels 4-bit SR + EF encode, M=1 decode, 250M fp32, B=512",
+    "clip8_ef_2p28": "percentile-clipped 8-bit RN + EF encode, M=1 decode, 2^28 fp32 (outliers), "
+                     "B=2048",
+    "topk_ef": "top-k (10 of every 1024) 8-bit + EF encode x8 workers of 25.6M, scatter decode "
+               "MEAN M=8",
+    "rx_reencode_u8_m16": "fused decode MEAN + 8-bit re-encode with EF of 16 bf16-encoded payloads "
+                          "of 2^26",
+}
+
+
+def _kernel_stats(comp, timer, peak):
+    out = {}
+    per = timer.per_kernel_ms()
+    units = comp.kernel_units()
+    for name, (cnt, b) in comp.kernels.items():
+        ts = per.get(name, [])
+        if not ts:
+            continue
+        avg = sum(ts) / len(ts)
+        e = {"launches": len(ts), "avg_us": round(avg * 1e3, 2), "bytes_per_launch": b,
+             "gbs": round(b / (avg * 1e-3) / 1e9, 1), "frac_of_peak": round(b / (avg * 1e-3) / 1e9 / peak, 4)}
+        if units.get(name):
+            e["units_per_launch"] = units[name]
+            e["elements_per_s"] = float(f"{units[name] / (avg * 1e-3):.4g}")
+            e["fp32_equiv_gbs"] = round(4 * units[name] / (avg * 1e-3) / 1e9, 1)
+        out[name] = e
+    return out
+
+
+def _graph_us_per_launch(q, torch, comp, which, reps=64):
+    """Per-launch device time of one kernel of `comp` replayed back to back from
+    a CUDA graph (no host launch overhead between launches)."""
+    timer = KernelTimer(torch, enabled=False)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        comp.run(q, 1, timer)                  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for r in range(reps):
+            which(r)
+    graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(5):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return round(a.elapsed_time(b) * 1e3 / (5 * reps), 2)
+
+
+def run_supplements(q, torch, suite, peak, reps=10):
+    """The workloads outside the headline suite, each timed on its own after the
+    suite (CUDA events around every launch on the launching stream, 2 untimed
+    launches first): the 2^20 8-bit EF workload, the vote at 2^30, QSGD,
+    logarithmic levels, percentile clipping, top-k and the fused re-encode.
+    They reuse the suite's device data where the recipe is the same."""
+    by_name = {c.name: c for c in suite}
+    comps = [UniformEF("u8_ef_2p20", 1 << 20, 8, 2048, False, 0, "outlier"), VoteOnly()]
+    shared = {}
+    if "sr4_ef" in by_name:
+        comps += [UniformEF("qsgd4_ef", 250_000_000, 4, 512, True, 2, "bucket", scheme=3),
+                  UniformEF("log4_ef", 250_000_000, 4, 512, True, 2, "bucket", scheme=5)]
+        shared["qsgd4_ef"] = shared["log4_ef"] = by_name["sr4_ef"]
+    comps.append(UniformEF("clip8_ef_2p28", 1 << 28, 8, 2048, False, 0, "outlier", scheme=4))
+    if "sign_ef_vote" in by_name:
+        comps.append(TopkEF())
+        shared["topk_ef"] = by_name["sign_ef_vote"]
+    if "rx_u8" in by_name:
+        comps.append(ReencodeOnly(src=by_name["rx_u8"]))
+    out = {}
+    for c in comps:
+        c.setup(q, torch, shared=shared.get(c.name))
+        warm = KernelTimer(torch, enabled=False)
+        for t in range(2):
+            c.run(q, t, warm)
+        torch.cuda.synchronize()
+        timer = KernelTimer(torch, enabled=True)
+        for t in range(2, 2 + reps):
+            c.run(q, t, timer)
+        torch.cuda.synchronize()
+        entry = {"workload": SUPPLEMENT_TEXT.get(c.name, c.name), "kernels": _kernel_stats(c, timer, peak)}
+        if c.name == "u8_ef_2p20":
+            mode = q.QC_ROUND_NEAREST
+            enc = lambda r: q.qc_encode_ef(c.g, c.err, c.n, 8, c.bucket, 0, mode, 0, r, c.codes,
+                                           c.scale, c.offset)
+            dec = lambda r: q.qc_decode_accumulate(c.codes, 0, c.scale, c.offset, 0, 1, c.n, 8,
+                                                   c.bucket, 0, c.out, 0)
+            entry["graph_us_per_launch"] = {c.enc_name: _graph_us_per_launch(q, torch, c, enc),
+                                            c.dec_name: _graph_us_per_launch(q, torch, c, dec)}
+        out[c.name] = entry
+        for attr in list(vars(c)):
+            if attr not in ("src",) and hasattr(getattr(c, attr), "is_cuda"):
+                setattr(c, attr, None)
+        c.gs = None
+        torch.cuda.empty_cache()
+    return out
 
 
 def _split(fn, n, align):
@@ -602,6 +769,10 @@ def make_workload(name):
         "probe_ternary_bf16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 27, M=1)],
         "probe_decode_u8_m16": lambda: [Receiver("rx_u8", 0, 8, n=1 << 24, M=16)],
         "probe_decode_ternary_m16": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 24, M=16)],
+        "probe_decode_u8_m16_full": lambda: [Receiver("rx_u8", 0, 8, n=1 << 26, M=16)],
+        "probe_decode_ternary_m16_full": lambda: [Receiver("rx_ternary", 2, 2, n=1 << 26, M=16)],
+        "probe_vote": lambda: [VoteOnly("vote_2p28", n=1 << 28, M=8)],
+        "vote_2p30": lambda: [VoteOnly()],
         "probe_reencode_u8_m16": lambda: [Reencode("rx_reencode_u8", 0, 8, n=1 << 24, M=16)],
         "probe_fp8": lambda: [Fp8Rowwise(rows=1 << 19)],
     }
@@ -850,6 +1021,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
 
     e2e = run_e2e(args, comps, q, torch, world, units)
+    supplements = None
+    if not args.no_supplements and args.workload == "suite":
+        supplements = run_supplements(q, torch, comps, peak)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -871,6 +1045,8 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "quality": quality,
     }
+    if supplements is not None:
+        line["supplements"] = supplements
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(comps, args.cpu_seconds)
     if rank == 0:
@@ -1055,6 +1231,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-supplements", action="store_true",
+                    help="skip the workloads timed outside the headline suite")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

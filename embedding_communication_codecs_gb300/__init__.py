@@ -29,14 +29,16 @@ QC_DTYPE_F32, QC_DTYPE_BF16 = 0, 1
 QC_OUT_SUM, QC_OUT_MEAN, QC_ACCUMULATE_INTO_OUT = 0, 1, 2
 QC_MAX_WORKERS = 1024
 QC_MAX_FP8_DIM = 4096
+QC_MAX_SEGMENTS_PER_LAUNCH = 60
 
 STATUS_NAMES = {0: "QC_OK", 1: "QC_ERR_NULL", 2: "QC_ERR_INVALID_ARG", 3: "QC_ERR_ALIGNMENT",
                 4: "QC_ERR_UNSUPPORTED", 5: "QC_ERR_CUDA"}
 
 # Every symbol the C ABI exports, in header order.
-EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_decode_accumulate",
+EXPORTS = ("qc_code_words", "qc_num_buckets", "qc_encode_ef", "qc_encode_ef_segments",
+           "qc_decode_accumulate",
            "qc_reencode", "qc_topk_encode_ef", "qc_topk_decode_accumulate", "qc_sign_vote", "qc_rowwise_fp8", "qc_rowwise_fp8_dequant", "qc_take_device_errors",
-           "qc_selftest_wait_timeout",
+           "qc_set_status_word", "qc_selftest_wait_timeout",
            "qc_last_error", "qc_version")
 
 
@@ -44,6 +46,13 @@ class QCodecError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
         self.status = status
+
+
+class QcSegment(ctypes.Structure):
+    """One flat gradient of qc_encode_ef_segments (the C struct qc_segment)."""
+    _fields_ = [("grad", ctypes.c_void_p), ("err", ctypes.c_void_p), ("n", ctypes.c_size_t),
+                ("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("offset", ctypes.c_void_p)]
 
 
 def _load():
@@ -56,6 +65,7 @@ def _load():
     lib.qc_code_words.argtypes, lib.qc_code_words.restype = [S, I], S
     lib.qc_num_buckets.argtypes, lib.qc_num_buckets.restype = [S, S], S
     lib.qc_encode_ef.argtypes = [P, I, P, S, I, S, I, I, U64, U32, P, P, P, P]
+    lib.qc_encode_ef_segments.argtypes = [ctypes.POINTER(QcSegment), I, I, I, S, I, I, U64, U32, P]
     lib.qc_decode_accumulate.argtypes = [P, S, P, P, S, I, S, I, S, I, P, I, P]
     lib.qc_reencode.argtypes = [P, S, P, P, S, I, S, I, S, I, I, P, I, U64, U32, P, P, P, P, P]
     lib.qc_topk_encode_ef.argtypes = [P, I, P, S, S, U32, I, U64, U32, P, P, P, P, P]
@@ -63,13 +73,14 @@ def _load():
     lib.qc_sign_vote.argtypes = [P, S, I, S, P, P]
     lib.qc_rowwise_fp8.argtypes = [P, S, S, P, P, P]
     lib.qc_rowwise_fp8_dequant.argtypes = [P, P, S, S, P, P]
-    for name in ("qc_encode_ef", "qc_decode_accumulate", "qc_reencode", "qc_topk_encode_ef",
+    for name in ("qc_encode_ef", "qc_encode_ef_segments", "qc_decode_accumulate", "qc_reencode", "qc_topk_encode_ef",
                  "qc_topk_decode_accumulate", "qc_sign_vote",
                  "qc_rowwise_fp8",
                  "qc_rowwise_fp8_dequant"):
         getattr(lib, name).restype = I
     lib.qc_take_device_errors.argtypes, lib.qc_take_device_errors.restype = [P], I
     lib.qc_selftest_wait_timeout.argtypes, lib.qc_selftest_wait_timeout.restype = [U32, P], I
+    lib.qc_set_status_word.argtypes, lib.qc_set_status_word.restype = [P], I
     lib.qc_last_error.argtypes, lib.qc_last_error.restype = [], ctypes.c_char_p
     lib.qc_version.argtypes, lib.qc_version.restype = [], ctypes.c_char_p
     return lib
@@ -169,8 +180,18 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def qc_selftest_wait_timeout(rounds, stream=None):
-    _check(lib.qc_selftest_wait_timeout(rounds, _stream(stream)))
+def qc_selftest_wait_timeout(timeout_us, stream=None):
+    """One block whose bounded wait runs out after timeout_us microseconds."""
+    _check(lib.qc_selftest_wait_timeout(timeout_us, _stream(stream)))
+
+
+def qc_set_status_word(status):
+    """Launches from this thread report failures into the device word `status`
+    (a one-element int32 CUDA tensor or an address; None turns it off)."""
+    if status is not None and not isinstance(status, int):
+        _need(status, "status", 4, _words32())
+        _on_device(status=status)
+    _check(lib.qc_set_status_word(_ptr(status)))
 
 
 def qc_take_device_errors() -> int:
@@ -210,21 +231,63 @@ def qc_encode_ef(grad, err, n, bits, bucket, scheme, mode, seed, step, codes, sc
 
     ``err`` (fp32, in/out) may be None for no error feedback; ``offset`` may be
     None unless ``scheme`` is uniform.  Raises QCodecError on a non-OK status."""
-    if not isinstance(grad, int):
-        dt = _dtype_code(grad, dtype)
-        torch = _torch()
-        want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
-        _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
-    nb = qc_num_buckets(n, bucket) if bucket else 0
-    _need(err, "err", 4 * n, _f32())
-    _need(codes, "codes", 4 * qc_code_words(n, bits), _words32())
-    _need(scale, "scale", 4 * nb, _f32())
-    if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP):
-        _need(offset, "offset", 4 * nb, _f32())
-    _on_device(grad=grad, err=err, codes=codes, scale=scale, offset=offset)
+    if n:   # n == 0 is a no-op that reads and writes nothing
+        if not isinstance(grad, int):
+            dt = _dtype_code(grad, dtype)
+            torch = _torch()
+            want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
+            _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
+        nb = qc_num_buckets(n, bucket) if bucket else 0
+        _need(err, "err", 4 * n, _f32())
+        _need(codes, "codes", 4 * qc_code_words(n, bits), _words32())
+        _need(scale, "scale", 4 * nb, _f32())
+        if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP):
+            _need(offset, "offset", 4 * nb, _f32())
+        _on_device(grad=grad, err=err, codes=codes, scale=scale, offset=offset)
     _check(lib.qc_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bits, bucket,
                             scheme, mode, seed, step, _ptr(codes), _ptr(scale), _ptr(offset),
                             _stream(stream)))
+
+
+def segment_draw_bases(sizes):
+    """The draw index of element 0 of each segment of a qc_encode_ef_segments
+    call: the segments laid end to end, each padded to a multiple of 4."""
+    out, base = [], 0
+    for n in sizes:
+        out.append(base)
+        base += (int(n) + 3) & ~3
+    return out
+
+
+def qc_encode_ef_segments(segments, dtype, bits, bucket, scheme, mode, seed, step, stream=None):
+    """qc_encode_ef over a list of flat gradients in one launch.
+
+    ``segments`` holds (grad, err, n, codes, scale, offset) tuples, each as for
+    qc_encode_ef; element i of segment s draws with the index I_s + i, I_s the
+    sum of the earlier segments' n, each rounded up to a multiple of 4
+    (segment_draw_bases).  Every tensor is checked before anything runs."""
+    torch = _torch()
+    segs = []
+    for k, (grad, err, n, codes, scale, offset) in enumerate(segments):
+        if n:
+            if not isinstance(grad, int):
+                want = (torch.float32,) if dtype == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
+                _need(grad, f"segment {k} grad", n * (4 if dtype == QC_DTYPE_F32 else 2), want)
+            nb = qc_num_buckets(n, bucket) if bucket else 0
+            _need(err, f"segment {k} err", 4 * n, _f32())
+            _need(codes, f"segment {k} codes", 4 * qc_code_words(n, bits), _words32())
+            _need(scale, f"segment {k} scale", 4 * nb, _f32())
+            if scheme in (QC_SCHEME_UNIFORM, QC_SCHEME_UNIFORM_CLIP):
+                _need(offset, f"segment {k} offset", 4 * nb, _f32())
+        segs.append((grad, err, n, codes, scale, offset))
+    for grad, err, n, codes, scale, offset in segs:
+        if n:
+            _on_device(grad=grad, err=err, codes=codes, scale=scale, offset=offset)
+    arr = (QcSegment * max(1, len(segs)))()
+    for k, (grad, err, n, codes, scale, offset) in enumerate(segs):
+        arr[k] = QcSegment(_ptr(grad), _ptr(err), n, _ptr(codes), _ptr(scale), _ptr(offset))
+    _check(lib.qc_encode_ef_segments(arr, len(segs), dtype, bits, bucket, scheme, mode, seed, step,
+                                     _stream(stream)))
 
 
 def _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
@@ -245,10 +308,11 @@ def _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n,
 def qc_decode_accumulate(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits,
                          bucket, scheme, out, flags=QC_OUT_SUM, stream=None):
     """Receiver half: ``out`` = fixed-order fp32 sum (or mean) of M decoded payloads."""
-    _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
-                    scheme)
-    _need(out, "out", 4 * n, _f32())
-    _on_device(codes=codes, scale=scale, offset=offset, out=out)
+    if n:   # an empty call reads and writes nothing
+        _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                        scheme)
+        _need(out, "out", 4 * n, _f32())
+        _on_device(codes=codes, scale=scale, offset=offset, out=out)
     _check(lib.qc_decode_accumulate(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
                                     meta_stride, M, n, bits, bucket, scheme, _ptr(out), flags,
                                     _stream(stream)))
@@ -261,17 +325,18 @@ def qc_reencode(codes, codes_stride_words, scale, offset, meta_stride, M, n, bit
     QC_OUT_MEAN), then encode the result with the residual ``err`` (fp32,
     in/out, or None) in the same scheme, bits and bucket.  ``out`` (optional)
     receives the decoded result itself."""
-    _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
-                    scheme)
-    nb = qc_num_buckets(n, bucket) if bucket else 0
-    _need(err, "err", 4 * n, _f32())
-    _need(out, "out", 4 * n, _f32())
-    _need(codes_out, "codes_out", 4 * qc_code_words(n, bits), _words32())
-    _need(scale_out, "scale_out", 4 * nb, _f32())
-    if scheme == QC_SCHEME_UNIFORM:
-        _need(offset_out, "offset_out", 4 * nb, _f32())
-    _on_device(codes=codes, scale=scale, offset=offset, err=err, out=out, codes_out=codes_out,
-               scale_out=scale_out, offset_out=offset_out)
+    if n:   # an empty call reads and writes nothing
+        _check_payloads(codes, codes_stride_words, scale, offset, meta_stride, M, n, bits, bucket,
+                        scheme)
+        nb = qc_num_buckets(n, bucket) if bucket else 0
+        _need(err, "err", 4 * n, _f32())
+        _need(out, "out", 4 * n, _f32())
+        _need(codes_out, "codes_out", 4 * qc_code_words(n, bits), _words32())
+        _need(scale_out, "scale_out", 4 * nb, _f32())
+        if scheme == QC_SCHEME_UNIFORM:
+            _need(offset_out, "offset_out", 4 * nb, _f32())
+        _on_device(codes=codes, scale=scale, offset=offset, err=err, out=out, codes_out=codes_out,
+                   scale_out=scale_out, offset_out=offset_out)
     _check(lib.qc_reencode(_ptr(codes), codes_stride_words, _ptr(scale), _ptr(offset),
                            meta_stride, M, n, bits, bucket, scheme, flags, _ptr(err), mode, seed,
                            step, _ptr(codes_out), _ptr(scale_out), _ptr(offset_out), _ptr(out),
@@ -282,18 +347,19 @@ def qc_topk_encode_ef(grad, err, n, bucket, keep, mode, seed, step, idx, codes, 
                       stream=None, dtype=None):
     """Top-k sparsification per bucket with 8-bit codes of the kept values and
     error feedback (``err`` may be None); outputs keep slots per bucket."""
-    torch = _torch()
-    if not isinstance(grad, int):
-        dt = _dtype_code(grad, dtype)
-        want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
-        _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
-    nb = qc_num_buckets(n, bucket) if bucket else 0
-    _need(err, "err", 4 * n, _f32())
-    _need(idx, "idx", 4 * nb * keep, _words32())
-    _need(codes, "codes", nb * keep, (torch.uint8, torch.int8))
-    _need(scale, "scale", 4 * nb, _f32())
-    _need(offset, "offset", 4 * nb, _f32())
-    _on_device(grad=grad, err=err, idx=idx, codes=codes, scale=scale, offset=offset)
+    if n:   # an empty call reads and writes nothing
+        torch = _torch()
+        if not isinstance(grad, int):
+            dt = _dtype_code(grad, dtype)
+            want = (torch.float32,) if dt == QC_DTYPE_F32 else (torch.bfloat16, torch.int16)
+            _need(grad, "grad", n * (4 if dt == QC_DTYPE_F32 else 2), want)
+        nb = qc_num_buckets(n, bucket) if bucket else 0
+        _need(err, "err", 4 * n, _f32())
+        _need(idx, "idx", 4 * nb * keep, _words32())
+        _need(codes, "codes", nb * keep, (torch.uint8, torch.int8))
+        _need(scale, "scale", 4 * nb, _f32())
+        _need(offset, "offset", 4 * nb, _f32())
+        _on_device(grad=grad, err=err, idx=idx, codes=codes, scale=scale, offset=offset)
     _check(lib.qc_topk_encode_ef(_ptr(grad), _dtype_code(grad, dtype), _ptr(err), n, bucket, keep,
                                  mode, seed, step, _ptr(idx), _ptr(codes), _ptr(scale),
                                  _ptr(offset), _stream(stream)))
@@ -302,15 +368,16 @@ def qc_topk_encode_ef(grad, err, n, bucket, keep, mode, seed, step, idx, codes, 
 def qc_topk_decode_accumulate(idx, codes, pair_stride, scale, offset, meta_stride, M, n, bucket,
                               keep, out, flags=QC_OUT_SUM, stream=None):
     """Scatter M workers' top-k pairs into a dense fp32 vector in worker order."""
-    torch = _torch()
-    nb = qc_num_buckets(n, bucket) if bucket else 0
-    ps, ms = (pair_stride, meta_stride) if M > 1 else (0, 0)
-    _need(idx, "idx", 4 * ((M - 1) * ps + nb * keep), _words32(), flat=False)
-    _need(codes, "codes", (M - 1) * ps + nb * keep, (torch.uint8, torch.int8), flat=False)
-    _need(scale, "scale", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
-    _need(offset, "offset", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
-    _need(out, "out", 4 * n, _f32())
-    _on_device(idx=idx, codes=codes, scale=scale, offset=offset, out=out)
+    if n:   # an empty call reads and writes nothing
+        torch = _torch()
+        nb = qc_num_buckets(n, bucket) if bucket else 0
+        ps, ms = (pair_stride, meta_stride) if M > 1 else (0, 0)
+        _need(idx, "idx", 4 * ((M - 1) * ps + nb * keep), _words32(), flat=False)
+        _need(codes, "codes", (M - 1) * ps + nb * keep, (torch.uint8, torch.int8), flat=False)
+        _need(scale, "scale", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+        _need(offset, "offset", 4 * ((M - 1) * ms + nb), _f32(), flat=False)
+        _need(out, "out", 4 * n, _f32())
+        _on_device(idx=idx, codes=codes, scale=scale, offset=offset, out=out)
     _check(lib.qc_topk_decode_accumulate(_ptr(idx), _ptr(codes), pair_stride, _ptr(scale),
                                          _ptr(offset), meta_stride, M, n, bucket, keep, _ptr(out),
                                          flags, _stream(stream)))
@@ -318,32 +385,35 @@ def qc_topk_decode_accumulate(idx, codes, pair_stride, scale, offset, meta_strid
 
 def qc_sign_vote(signs, stride_words, M, n, out, stream=None):
     """Majority vote over M packed sign vectors."""
-    words = qc_code_words(n, 1)
-    _need(signs, "signs", 4 * ((M - 1) * (stride_words if M > 1 else 0) + words), _words32(),
-          flat=False)
-    _row_stride(signs, "signs", stride_words, M)
-    _need(out, "out", 4 * words, _words32())
-    _on_device(signs=signs, out=out)
+    if n:   # an empty call reads and writes nothing
+        words = qc_code_words(n, 1)
+        _need(signs, "signs", 4 * ((M - 1) * (stride_words if M > 1 else 0) + words), _words32(),
+              flat=False)
+        _row_stride(signs, "signs", stride_words, M)
+        _need(out, "out", 4 * words, _words32())
+        _on_device(signs=signs, out=out)
     _check(lib.qc_sign_vote(_ptr(signs), stride_words, M, n, _ptr(out), _stream(stream)))
 
 
 def qc_rowwise_fp8(x, rows, dim, codes, row_scale, stream=None):
     """FP32 rows -> E4M3 codes + per-row fp32 scale."""
-    torch = _torch()
-    _need(x, "x", 4 * rows * dim, _f32())
-    _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
-    _need(row_scale, "row_scale", 4 * rows, _f32())
-    _on_device(x=x, codes=codes, row_scale=row_scale)
+    if rows:   # an empty call reads and writes nothing
+        torch = _torch()
+        _need(x, "x", 4 * rows * dim, _f32())
+        _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
+        _need(row_scale, "row_scale", 4 * rows, _f32())
+        _on_device(x=x, codes=codes, row_scale=row_scale)
     _check(lib.qc_rowwise_fp8(_ptr(x), rows, dim, _ptr(codes), _ptr(row_scale), _stream(stream)))
 
 
 def qc_rowwise_fp8_dequant(codes, row_scale, rows, dim, out, stream=None):
     """E4M3 codes + per-row scale -> fp32 rows."""
-    torch = _torch()
-    _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
-    _need(row_scale, "row_scale", 4 * rows, _f32())
-    _need(out, "out", 4 * rows * dim, _f32())
-    _on_device(codes=codes, row_scale=row_scale, out=out)
+    if rows:   # an empty call reads and writes nothing
+        torch = _torch()
+        _need(codes, "codes", rows * dim, (torch.uint8, torch.int8))
+        _need(row_scale, "row_scale", 4 * rows, _f32())
+        _need(out, "out", 4 * rows * dim, _f32())
+        _on_device(codes=codes, row_scale=row_scale, out=out)
     _check(lib.qc_rowwise_fp8_dequant(_ptr(codes), _ptr(row_scale), rows, dim, _ptr(out),
                                       _stream(stream)))
 

@@ -5,7 +5,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
+#include <algorithm>
 #include <unordered_map>
+#include <vector>
 
 #include "../../include/qcodec.h"
 #include "qc_internal.h"
@@ -14,10 +16,13 @@ static_assert(int{QC_SCHEME_UNIFORM} == qc::kUniform && int{QC_SCHEME_SIGN} == q
                   int{QC_SCHEME_TERNARY} == qc::kTernary && int{QC_SCHEME_QSGD} == qc::kQsgd &&
                   int{QC_SCHEME_UNIFORM_CLIP} == qc::kClip && int{QC_SCHEME_LOG} == qc::kLog,
               "the public scheme numbers are the kernels' template arguments");
+static_assert(QC_MAX_SEGMENTS_PER_LAUNCH == qc::kMaxSegments, "one segment table per launch");
 
 namespace {
 
 thread_local char g_last_error[512] = "";
+// The status word that launches from this thread report failures into.
+thread_local uint32_t *g_status_word = nullptr;
 
 qc_status fail(qc_status st, const char *fmt, ...) {
     va_list ap;
@@ -133,7 +138,9 @@ bool decode_tiles_for(const qc::DecodeParams &p, int bits, qc::DecodeTiles &t) {
     if (!aligned(p.codes, 16) || p.codes_stride % 4 != 0) return false;
     const uint64_t unit = static_cast<uint64_t>(p.bucket) / gcd_u64(p.bucket, 128) * 128;
     const uint64_t bytes_per_elem_x8 = static_cast<uint64_t>(p.M) * bits;  // code bits per element
-    const uint64_t target = 32 * 1024;
+    // 2-bit payloads take half-size stages, four of them, so that three blocks
+    // share an SM (their consumers are the shorter-latency part of the kernel)
+    const uint64_t target = bits <= 2 ? 16 * 1024 : 32 * 1024;
     uint64_t te = (target * 8 / bytes_per_elem_x8) / unit * unit;
     if (te < unit) te = unit;
     const uint64_t worker_bytes = te * bits / 8;
@@ -146,7 +153,7 @@ bool decode_tiles_for(const qc::DecodeParams &p, int bits, qc::DecodeTiles &t) {
     t.worker_bytes = static_cast<uint32_t>(worker_bytes);
     t.meta_offset = static_cast<uint32_t>(p.M * worker_bytes);
     t.stage_bytes = static_cast<uint32_t>(stage);
-    t.stages = stage <= 36 * 1024 ? 3u : 2u;
+    t.stages = stage <= 18 * 1024 ? 4u : stage <= 36 * 1024 ? 3u : 2u;
     int sh = -1;
     if ((p.bucket & (p.bucket - 1)) == 0) {
         sh = 0;
@@ -297,112 +304,274 @@ const char *qc_last_error(void) { return g_last_error; }
 
 const char *qc_version(void) { return "libqcodec 0.2.0 (sm_103a)"; }
 
-qc_status qc_selftest_wait_timeout(uint32_t rounds, qc_stream_t stream) {
-    if (rounds < 1 || rounds > (1u << 20))
-        return fail(QC_ERR_INVALID_ARG, "qc_selftest_wait_timeout: rounds must be in [1, 2^20] (got %u)", rounds);
-    return from_cuda(qc::launch_wait_timeout_selftest(rounds, reinterpret_cast<cudaStream_t>(stream)),
+qc_status qc_set_status_word(uint32_t *status) {
+    if (status && !aligned(status, 4))
+        return fail(QC_ERR_ALIGNMENT, "qc_set_status_word: the status word must be 4-byte aligned");
+    g_status_word = status;
+    return ok();
+}
+
+qc_status qc_selftest_wait_timeout(uint32_t timeout_us, qc_stream_t stream) {
+    if (timeout_us < 1 || timeout_us > 10000000u)
+        return fail(QC_ERR_INVALID_ARG, "qc_selftest_wait_timeout: timeout_us must be in [1, 10^7] (got %u)",
+                    timeout_us);
+    return from_cuda(qc::launch_wait_timeout_selftest(timeout_us, g_status_word,
+                                                      reinterpret_cast<cudaStream_t>(stream)),
                      "qc_selftest_wait_timeout");
 }
 
 qc_status qc_take_device_errors(uint32_t *flags) {
     if (!flags) return fail(QC_ERR_NULL, "qc_take_device_errors: flags must be non-NULL");
     *flags = 0;
-    const cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
-    *flags = qc::take_encode_errors() | qc::take_encode_clip_errors() |
-             qc::take_encode_clip_bf16_errors() | qc::take_reencode_other_errors() |
-             qc::take_encode_log_errors() | qc::take_reencode_log_errors() |
-             qc::take_selftest_errors() |
-             qc::take_topk_errors() |
-             qc::take_encode_bf16_errors() | qc::take_encode_bf16_fast_errors() | qc::take_decode_errors() | qc::take_reencode_errors();
-    return from_cuda(cudaGetLastError(), "qc_take_device_errors");
+    cudaError_t (*const takes[])(uint32_t *) = {
+        qc::take_encode_errors,          qc::take_encode_clip_errors, qc::take_encode_clip_bf16_errors,
+        qc::take_reencode_other_errors,  qc::take_encode_log_errors,  qc::take_reencode_log_errors,
+        qc::take_selftest_errors,        qc::take_topk_errors,        qc::take_encode_bf16_errors,
+        qc::take_encode_bf16_fast_errors, qc::take_decode_errors,     qc::take_reencode_errors};
+    uint32_t all = 0;
+    for (auto take : takes) {
+        uint32_t v = 0;
+        e = take(&v);
+        if (e != cudaSuccess) return from_cuda(e, "qc_take_device_errors");
+        all |= v;
+    }
+    *flags = all;
+    return ok();
 }
 
-qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
-                       size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
-                       uint32_t step, uint32_t *codes, float *scale, float *offset,
-                       qc_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The call-wide arguments of an encode: QC_OK or the failure status.
+qc_status check_encode_args(const char *fn, qc_dtype dtype, int bits, size_t bucket,
+                            qc_scheme scheme, qc_round mode) {
     if (dtype != QC_DTYPE_F32 && dtype != QC_DTYPE_BF16)
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: dtype %d is not F32 or BF16", dtype);
-    const qc_status sc = check_scheme("qc_encode_ef", scheme, bits);
+        return fail(QC_ERR_INVALID_ARG, "%s: dtype %d is not F32 or BF16", fn, dtype);
+    const qc_status sc = check_scheme(fn, scheme, bits);
     if (sc != QC_OK) return sc;
     if (scheme == QC_SCHEME_SIGN && mode != QC_ROUND_NEAREST)
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: sign scheme is deterministic; mode must be NEAREST");
+        return fail(QC_ERR_INVALID_ARG, "%s: sign scheme is deterministic; mode must be NEAREST", fn);
     if (mode != QC_ROUND_NEAREST && mode != QC_ROUND_STOCHASTIC)
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: unknown rounding mode %d", mode);
+        return fail(QC_ERR_INVALID_ARG, "%s: unknown rounding mode %d", fn, mode);
     if (!valid_bucket(bucket))
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: bucket must be a multiple of 32 in [32, 2^24] (got %zu)", bucket);
-    if (n == 0) return ok();
+        return fail(QC_ERR_INVALID_ARG, "%s: bucket must be a multiple of 32 in [32, 2^24] (got %zu)",
+                    fn, bucket);
+    return QC_OK;
+}
+
+// The buffers of one flat gradient (n > 0): pointers, alignment, overlaps.
+qc_status check_encode_buffers(const char *fn, const void *grad, qc_dtype dtype, const float *err,
+                               size_t n, int bits, size_t bucket, qc_scheme scheme,
+                               const uint32_t *codes, const float *scale, const float *offset) {
     if (n > (static_cast<size_t>(1) << 40))
-        return fail(QC_ERR_UNSUPPORTED, "qc_encode_ef: n = %zu exceeds 2^40 elements", n);
-    if (!grad || !codes || !scale) return fail(QC_ERR_NULL, "qc_encode_ef: grad, codes and scale must be non-NULL");
+        return fail(QC_ERR_UNSUPPORTED, "%s: n = %zu exceeds 2^40 elements", fn, n);
+    if (!grad || !codes || !scale) return fail(QC_ERR_NULL, "%s: grad, codes and scale must be non-NULL", fn);
     const bool uni = scheme == QC_SCHEME_UNIFORM || scheme == QC_SCHEME_UNIFORM_CLIP;
-    if (uni && !offset)
-        return fail(QC_ERR_NULL, "qc_encode_ef: the uniform schemes need an offset array");
+    if (uni && !offset) return fail(QC_ERR_NULL, "%s: the uniform schemes need an offset array", fn);
     const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
     if (!aligned(grad, dtype == QC_DTYPE_F32 ? 16 : 8))
-        return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: grad must be %d-byte aligned", dtype == QC_DTYPE_F32 ? 16 : 8);
-    if (err && !aligned(err, 16)) return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: err must be 16-byte aligned");
+        return fail(QC_ERR_ALIGNMENT, "%s: grad must be %d-byte aligned", fn, dtype == QC_DTYPE_F32 ? 16 : 8);
+    if (err && !aligned(err, 16)) return fail(QC_ERR_ALIGNMENT, "%s: err must be 16-byte aligned", fn);
     if (!aligned(codes, 4) || !aligned(scale, 4) || (offset && !aligned(offset, 4)))
-        return fail(QC_ERR_ALIGNMENT, "qc_encode_ef: codes, scale and offset must be 4-byte aligned");
+        return fail(QC_ERR_ALIGNMENT, "%s: codes, scale and offset must be 4-byte aligned", fn);
     const size_t nb = qc_num_buckets(n, bucket);
     const size_t cbytes = qc_code_words(n, bits) * 4, mbytes = nb * 4;
     const void *outs[3] = {codes, scale, uni ? offset : nullptr};
     const size_t osz[3] = {cbytes, mbytes, mbytes};
     for (int a = 0; a < 3; ++a) {
         if (overlaps(outs[a], osz[a], grad, n * esize) || overlaps(outs[a], osz[a], err, n * 4))
-            return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: an output overlaps grad or err");
+            return fail(QC_ERR_INVALID_ARG, "%s: an output overlaps grad or err", fn);
         for (int b = a + 1; b < 3; ++b)
             if (overlaps(outs[a], osz[a], outs[b], osz[b]))
-                return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: outputs overlap each other");
+                return fail(QC_ERR_INVALID_ARG, "%s: outputs overlap each other", fn);
     }
-    if (overlaps(err, n * 4, grad, n * esize))
-        return fail(QC_ERR_INVALID_ARG, "qc_encode_ef: err overlaps grad");
+    if (overlaps(err, n * 4, grad, n * esize)) return fail(QC_ERR_INVALID_ARG, "%s: err overlaps grad", fn);
+    return QC_OK;
+}
 
+// The call-wide part of the kernel parameters (the per-array fields are the
+// caller's to fill).
+qc::EncodeParams encode_params(size_t bucket, uint64_t seed, uint32_t step) {
     qc::EncodeParams p{};
-    p.grad = grad;
-    p.err = err;
-    p.n = n;
     p.bucket = static_cast<uint32_t>(bucket);
-    p.nbuckets = nb;
     p.team_warps = team_warps_for(bucket);
     p.two_pass = bucket > static_cast<size_t>(qc::kWindowPerWarp) * p.team_warps ? 1 : 0;
     p.seed = seed;
     p.step = step;
     p.keys = qc::philox_round_keys(seed);
-    p.codes = codes;
-    p.scale = scale;
-    p.offset = offset;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    p.status = g_status_word;
+    return p;
+}
+
+// One flat gradient (validated), on the kernel its layout suits.
+qc_status encode_one(const char *fn, const qc::EncodeParams &p, qc_dtype dtype, int bits,
+                     qc_scheme scheme, qc_round mode, cudaStream_t st) {
+    const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
+    const bool grad16 = aligned(p.grad, 16), sr = mode == QC_ROUND_STOCHASTIC;
+    const bool bf16 = dtype == QC_DTYPE_BF16;
     qc::EncodeTiles tiles{};
     if (scheme == QC_SCHEME_UNIFORM_CLIP) {
         // the percentile selection runs over a bucket held in registers by one team
         const size_t teams = (qc::kBlock / 32) / p.team_warps;
-        if (!encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles,
+        if (!encode_tiles_for(p, esize, p.err != nullptr, grad16, tiles,
                               teams * qc::sel_region_words(p.bucket) * 4))
             return fail(QC_ERR_UNSUPPORTED,
-                        "qc_encode_ef: percentile clipping needs a bucket of at most 4096 elements "
-                        "and a 16-byte aligned gradient");
-        return from_cuda(qc::launch_encode_clip(p, tiles, bits, mode == QC_ROUND_STOCHASTIC,
-                                                dtype == QC_DTYPE_BF16, st),
-                         "qc_encode_ef");
+                        "%s: percentile clipping needs a bucket of at most 4096 elements "
+                        "and a 16-byte aligned gradient", fn);
+        return from_cuda(qc::launch_encode_clip(p, tiles, bits, sr, bf16, st), fn);
     }
-    if (dtype == QC_DTYPE_BF16 &&
-        qc::encode_bf16_fast_applies(p, scheme, bits, mode == QC_ROUND_STOCHASTIC, aligned(grad, 16),
-                                     aligned(codes, 8)))
-        return from_cuda(qc::launch_encode_bf16_fast(p, scheme, st), "qc_encode_ef");
+    if (bf16 && qc::encode_bf16_fast_applies(p, scheme, bits, sr, grad16, aligned(p.codes, 8)))
+        return from_cuda(qc::launch_encode_bf16_fast(p, scheme, st), fn);
     // the bf16 kernel stores 8-bit codes eight bytes at a time
-    if (dtype == QC_DTYPE_BF16 && (bits != 8 || aligned(codes, 8)) &&
-        bf16_tiles_for(p, aligned(grad, 16), tiles))
-        return from_cuda(qc::launch_encode_bf16(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC, st),
-                         "qc_encode_ef");
-    if (encode_tiles_for(p, esize, err != nullptr, aligned(grad, 16), tiles))
-        return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, mode == QC_ROUND_STOCHASTIC,
-                                               dtype == QC_DTYPE_BF16, st),
-                         "qc_encode_ef");
-    return from_cuda(qc::launch_encode(p, scheme, bits, mode == QC_ROUND_STOCHASTIC,
-                                       dtype == QC_DTYPE_BF16, st),
-                     "qc_encode_ef");
+    if (bf16 && (bits != 8 || aligned(p.codes, 8)) && bf16_tiles_for(p, grad16, tiles))
+        return from_cuda(qc::launch_encode_bf16(p, tiles, scheme, bits, sr, st), fn);
+    if (encode_tiles_for(p, esize, p.err != nullptr, grad16, tiles))
+        return from_cuda(qc::launch_encode_tma(p, tiles, scheme, bits, sr, bf16, st), fn);
+    return from_cuda(qc::launch_encode(p, scheme, bits, sr, bf16, st), fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, int bits,
+                       size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
+                       uint32_t step, uint32_t *codes, float *scale, float *offset,
+                       qc_stream_t stream) {
+    static const char *fn = "qc_encode_ef";
+    qc_status sc = check_encode_args(fn, dtype, bits, bucket, scheme, mode);
+    if (sc != QC_OK) return sc;
+    if (n == 0) return ok();
+    sc = check_encode_buffers(fn, grad, dtype, err, n, bits, bucket, scheme, codes, scale, offset);
+    if (sc != QC_OK) return sc;
+    qc::EncodeParams p = encode_params(bucket, seed, step);
+    p.grad = grad;
+    p.err = err;
+    p.n = n;
+    p.nbuckets = qc_num_buckets(n, bucket);
+    p.codes = codes;
+    p.scale = scale;
+    p.offset = offset;
+    return encode_one(fn, p, dtype, bits, scheme, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qc_status qc_encode_ef_segments(const qc_segment *segs, int nseg, qc_dtype dtype, int bits,
+                                size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
+                                uint32_t step, qc_stream_t stream) {
+    static const char *fn = "qc_encode_ef_segments";
+    qc_status sc = check_encode_args(fn, dtype, bits, bucket, scheme, mode);
+    if (sc != QC_OK) return sc;
+    if (nseg < 0) return fail(QC_ERR_INVALID_ARG, "%s: nseg must be >= 0 (got %d)", fn, nseg);
+    if (nseg == 0) return ok();
+    if (!segs) return fail(QC_ERR_NULL, "%s: segs must be non-NULL", fn);
+    const bool uni = scheme == QC_SCHEME_UNIFORM || scheme == QC_SCHEME_UNIFORM_CLIP;
+    const size_t esize = dtype == QC_DTYPE_F32 ? 4 : 2;
+    bool any_err = false, all_err = true;
+    uint64_t total = 0;
+    for (int a = 0; a < nseg; ++a) {
+        const qc_segment &g = segs[a];
+        if (g.n == 0) continue;
+        any_err |= g.err != nullptr;
+        all_err &= g.err != nullptr;
+        sc = check_encode_buffers(fn, g.grad, dtype, g.err, g.n, bits, bucket, scheme, g.codes,
+                                  g.scale, g.offset);
+        if (sc != QC_OK) {
+            char msg[400];
+            snprintf(msg, sizeof msg, "%s", g_last_error);
+            return fail(sc, "%s (segment %d)", msg, a);
+        }
+        total += g.n;
+        if (total > (static_cast<uint64_t>(1) << 40))
+            return fail(QC_ERR_UNSUPPORTED, "%s: the segments hold more than 2^40 elements", fn);
+    }
+    if (any_err && !all_err)
+        return fail(QC_ERR_INVALID_ARG, "%s: err must be given for every segment or for none", fn);
+    // no output of one segment may overlap any buffer of another
+    for (int a = 0; a < nseg; ++a) {
+        const qc_segment &x = segs[a];
+        if (x.n == 0) continue;
+        const size_t nb = qc_num_buckets(x.n, bucket);
+        const void *outs[4] = {x.codes, x.scale, uni ? x.offset : nullptr, x.err};
+        const size_t osz[4] = {qc_code_words(x.n, bits) * 4, nb * 4, nb * 4, x.n * 4};
+        for (int b = 0; b < nseg; ++b) {
+            const qc_segment &y = segs[b];
+            if (b == a || y.n == 0) continue;
+            const size_t mb = qc_num_buckets(y.n, bucket);
+            const void *bufs[5] = {y.grad, y.err, y.codes, y.scale, uni ? y.offset : nullptr};
+            const size_t bsz[5] = {y.n * esize, y.n * 4, qc_code_words(y.n, bits) * 4, mb * 4, mb * 4};
+            for (int i = 0; i < 4; ++i)
+                for (int j = 0; j < 5; ++j)
+                    if (overlaps(outs[i], osz[i], bufs[j], bsz[j]))
+                        return fail(QC_ERR_INVALID_ARG,
+                                    "%s: an output of segment %d overlaps a buffer of segment %d", fn, a, b);
+        }
+    }
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const qc::EncodeParams base = encode_params(bucket, seed, step);
+    const bool sr = mode == QC_ROUND_STOCHASTIC, bf16 = dtype == QC_DTYPE_BF16;
+    // the segment's own parameters, with its draw index base
+    std::vector<qc::EncodeParams> ps;
+    ps.reserve(static_cast<size_t>(nseg));
+    uint64_t base_index = 0;
+    for (int a = 0; a < nseg; ++a) {
+        const qc_segment &g = segs[a];
+        if (g.n == 0) continue;
+        qc::EncodeParams p = base;
+        p.grad = g.grad;
+        p.err = g.err;
+        p.n = g.n;
+        p.nbuckets = qc_num_buckets(g.n, bucket);
+        p.codes = g.codes;
+        p.scale = g.scale;
+        p.offset = g.offset;
+        p.index_base = base_index;
+        base_index += (g.n + 3u) & ~static_cast<uint64_t>(3);  // each segment starts a Philox block
+        ps.push_back(p);
+    }
+    // Which one-launch kernel takes every segment: the receiver's bf16 kernel, or
+    // the pipelined encode; otherwise each segment takes its own launch.
+    bool fast = bf16, tma = scheme != QC_SCHEME_UNIFORM_CLIP;
+    qc::EncodeTiles tiles{};
+    for (const auto &p : ps) {
+        fast = fast && qc::encode_bf16_fast_applies(p, scheme, bits, sr, aligned(p.grad, 16),
+                                                    aligned(p.codes, 8));
+        qc::EncodeTiles t{};
+        tma = tma && encode_tiles_for(p, esize, any_err, aligned(p.grad, 16), t);
+        if (tma) tiles = t;
+    }
+    if (fast || tma) {
+        for (size_t first = 0; first < ps.size(); first += qc::kMaxSegments) {
+            const size_t cnt = std::min(ps.size() - first, static_cast<size_t>(qc::kMaxSegments));
+            qc::EncodeSegs S;
+            S.nseg = static_cast<uint32_t>(cnt);
+            uint64_t tile0 = 0;
+            for (size_t i = 0; i < cnt; ++i) {
+                const qc::EncodeParams &p = ps[first + i];
+                S.s[i] = qc::EncodeSeg{p.grad, p.err, p.n, p.codes, p.scale, p.offset, tile0, p.index_base};
+                tile0 += fast ? qc::encode_bf16_fast_tiles(p.n) : (p.n + tiles.te - 1) / tiles.te;
+            }
+            cudaError_t e;
+            if (fast) {
+                e = qc::launch_encode_bf16_fast(base, scheme, st, &S);
+            } else {
+                qc::EncodeTiles g = tiles;
+                g.ntiles = tile0;
+                qc::EncodeParams p = base;
+                p.err = any_err ? ps[first].err : nullptr;  // selects the error-feedback kernel
+                e = qc::launch_encode_tma(p, g, scheme, bits, sr, bf16, st, &S);
+            }
+            if (e != cudaSuccess) return from_cuda(e, fn);
+        }
+        return ok();
+    }
+    for (const auto &p : ps) {
+        sc = encode_one(fn, p, dtype, bits, scheme, mode, st);
+        if (sc != QC_OK) return sc;
+    }
+    return ok();
 }
 
 qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
@@ -452,6 +621,7 @@ qc_status qc_decode_accumulate(const uint32_t *codes, size_t codes_stride_words,
     p.flags = flags;
     // x / M and x * (1 / M) round the same exact value when M is a power of two.
     p.inv_m = (M & (M - 1)) == 0 ? 1.0f / static_cast<float>(M) : 0.0f;
+    p.status = g_status_word;
     qc::DecodeTiles tiles{};
     if (decode_tiles_for(p, bits, tiles))
         return from_cuda(qc::launch_decode_tma(p, tiles, scheme, bits, reinterpret_cast<cudaStream_t>(stream)),
@@ -533,6 +703,7 @@ qc_status qc_reencode(const uint32_t *codes, size_t codes_stride_words, const fl
     p.codes_out = codes_out;
     p.scale_out = scale_out;
     p.offset_out = offset_out;
+    p.status = g_status_word;
     qc::ReencodeTiles tiles{};
     if (!reencode_tiles_for(p, bits, tiles))
         return fail(QC_ERR_UNSUPPORTED,
@@ -595,6 +766,7 @@ qc_status qc_topk_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t
     t.e.keys = qc::philox_round_keys(seed);
     t.e.scale = scale;
     t.e.offset = offset;
+    t.e.status = g_status_word;
     t.keep = keep;
     t.idx = idx;
     t.codes8 = codes;

@@ -91,6 +91,57 @@ __device__ __forceinline__ float accumulate16(float acc, const uint32_t (&f)[4],
     return accumulate_code<SCHEME, BITS>(acc, f[c / kPerWord], c % kPerWord, sc, of);
 }
 
+// ---------------------------------------------------- packed pairs (f32x2)
+//
+// Two fp32 lanes in one 64-bit register, low half first: add.rn.f32x2 and
+// fma.rn.f32x2 round each half exactly as the scalar instructions would, in one
+// issue slot for both.
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Sixteen ternary codes of one word f (code c in bits 2c, 2c+1) accumulated into
+// eight packed pairs: acc = fl(acc + (c - 1) * s) per element.  Code j of a
+// half word h becomes an exact float without shifting it down: (h & 3 << 2j)
+// OR'd under the exponent of 2^(23 - 2j) is 2^(23 - 2j) + c, so subtracting
+// 2^(23 - 2j) + 1 (exact) gives c - 1, and (c - 1) * s is exact, so one fma
+// rounds acc + d once, as the scalar accumulate_code does.
+__device__ __forceinline__ void accumulate_ternary16(unsigned long long (&acc)[8], uint32_t f,
+                                                     unsigned long long s2) {
+    const uint32_t half[2] = {f & 0xFFFFu, f >> 16};
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint32_t h = half[p >> 2];
+        const int j0 = 2 * (p & 3), j1 = j0 + 1;
+        const float m0 = __uint_as_float((h & (3u << (2 * j0))) | ((150u - 2u * j0) << 23));
+        const float m1 = __uint_as_float((h & (3u << (2 * j1))) | ((150u - 2u * j1) << 23));
+        const unsigned long long k2 =
+            pack2(-(static_cast<float>(1u << (23 - 2 * j0)) + 1.0f),
+                  -(static_cast<float>(1u << (23 - 2 * j1)) + 1.0f));
+        acc[p] = fma2(add2(pack2(m0, m1), k2), s2, acc[p]);
+    }
+}
+
 // The 4*BITS-bit field of the four codes of tile element e (e % 4 == 0) of one
 // worker: from the stage when staged, else from global memory (tile tail).
 template <int BITS>

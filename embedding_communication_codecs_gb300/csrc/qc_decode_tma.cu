@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __gri
         }
         cp_async_wait_all();
         if (!ok) {
-            if (lane == 0) atomicOr(&g_decode_errors, kErrPipelineTimeout);
+            if (lane == 0) report_failure(&g_decode_errors, P.status, kErrPipelineTimeout);
             // let copies already issued land (bounded)
             for (uint32_t d = 0; d < G.stages; ++d) {
                 const uint32_t j = it >= G.stages ? it - G.stages + d : d;
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __gri
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
         if (!mbar_wait(&full[s], (it / G.stages) & 1u)) {
-            if (lane == 0) atomicOr(&g_decode_errors, kErrPipelineTimeout);
+            if (lane == 0) report_failure(&g_decode_errors, P.status, kErrPipelineTimeout);
             break;
         }
         const unsigned char *stage = smem + s * G.stage_bytes;
@@ -118,17 +118,33 @@ __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __gri
                 const float2 *meta = reinterpret_cast<const float2 *>(msc) + kb;
                 const unsigned char *wst = stage + (e * BITS) / 8u;
                 float a[16];
+                if constexpr (SCHEME == kTernary) {
+                    // eight packed pairs; one word holds a worker's 16 codes
+                    unsigned long long a2[8];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) a[c] = 0.0f;
+                    for (int c = 0; c < 8; ++c) a2[c] = 0ull;  // +0, +0
 #pragma unroll 4
-                for (int w = 0; w < P.M; ++w) {
-                    uint32_t f[4];
-                    load_codes16<BITS>(wst, f);
-                    const float2 m = meta[w * G.tb];
+                    for (int w = 0; w < P.M; ++w) {
+                        const uint32_t f = *reinterpret_cast<const uint32_t *>(wst);
+                        const float sw = meta[w * G.tb].x;
+                        accumulate_ternary16(a2, f, pack2(sw, sw));
+                        wst += G.worker_bytes;
+                    }
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        a[c] = accumulate16<SCHEME, BITS>(a[c], f, c, m.x, m.y);
-                    wst += G.worker_bytes;
+                    for (int c = 0; c < 8; ++c) unpack2(a2[c], a[2 * c], a[2 * c + 1]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) a[c] = 0.0f;
+#pragma unroll 4
+                    for (int w = 0; w < P.M; ++w) {
+                        uint32_t f[4];
+                        load_codes16<BITS>(wst, f);
+                        const float2 m = meta[w * G.tb];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            a[c] = accumulate16<SCHEME, BITS>(a[c], f, c, m.x, m.y);
+                        wst += G.worker_bytes;
+                    }
                 }
                 float4 *o = reinterpret_cast<float4 *>(P.out + t0 + e);
 #pragma unroll
@@ -232,11 +248,6 @@ cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int s
     }
 }
 
-uint32_t take_decode_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_decode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_decode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_decode_errors, g_decode_errors)
 
 }  // namespace qc

@@ -339,13 +339,13 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                         store_codes8<BITS>(P.codes, i0, true, lane, f0, f1);
                     } else if constexpr (SCHEME == kTernary && SR) {
                         bool near;
-                        const uint32_t f16 = ternary_sr_field8(v, philox_words(i0, P.step, keys),
-                                                               philox_words(i0 + 4, P.step, keys),
+                        const uint32_t f16 = ternary_sr_field8(v, philox_words(P.index_base + i0, P.step, keys),
+                                                               philox_words(P.index_base + i0 + 4, P.step, keys),
                                                                fq.rinv, fq.delta2, near);
                         uint32_t f0 = f16 & 0xFFu, f1 = f16 >> 8;
                         if (near) {  // rare: recompute the slot with the division
-                            uniform4(i0, P.step, keys, u);
-                            uniform4(i0 + 4, P.step, keys, u + 4);
+                            uniform4(P.index_base + i0, P.step, keys, u);
+                            uniform4(P.index_base + i0 + 4, P.step, keys, u + 4);
                             f0 = f1 = 0;
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
 #pragma unroll
                         for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
                         if constexpr (SR) {
-                            uniform4(i0, P.step, keys, u);
-                            uniform4(i0 + 4, P.step, keys, u + 4);
+                            uniform4(P.index_base + i0, P.step, keys, u);
+                            uniform4(P.index_base + i0 + 4, P.step, keys, u + 4);
                         }
                         uint32_t f0 = 0, f1 = 0;
                         bool any = false;
@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
                     for (int c = 0; c < kEps; ++c) u[c] = 0.0f;
                     if constexpr (SR) {
                         if (j < cnt) {
-                            uniform4(b0 + j, P.step, keys, u);
-                            uniform4(b0 + j + 4, P.step, keys, u + 4);
+                            uniform4(P.index_base + b0 + j, P.step, keys, u);
+                            uniform4(P.index_base + b0 + j + 4, P.step, keys, u + 4);
                         }
                     }
                     uint32_t f0 = 0, f1 = 0;
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_kernel(const __grid_con
             }
         }
     }
-    if (failed && lane == 0) atomicOr(&g_encode_bf16_errors, kErrPipelineTimeout);
+    if (failed && lane == 0) report_failure(&g_encode_bf16_errors, P.status, kErrPipelineTimeout);
     // A team that gave up leaves its stages unrefilled, so the other teams' waits
     // run out too; every warp gets here.  Copies still in flight (only after a
     // failure) must land before the block's shared memory goes away.
@@ -495,11 +495,6 @@ cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int 
     }
 }
 
-uint32_t take_encode_bf16_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_bf16_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_bf16_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_bf16_errors, g_encode_bf16_errors)
 
 }  // namespace qc

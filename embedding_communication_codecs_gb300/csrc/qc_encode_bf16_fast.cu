@@ -36,10 +36,21 @@ constexpr uint32_t kB = 1024;                        // bucket
 constexpr int kWarps = kBlock / 32;                  // one bucket per warp
 constexpr uint32_t kTile = kB * kWarps;              // elements per tile
 constexpr uint32_t kStageBytes = kTile * 2u;         // 16 KB of bf16
-constexpr uint32_t kStages = 3;
 
 constexpr int kU8 = 0;       // 8-bit uniform, round to nearest
 constexpr int kTern = 1;     // ternary, stochastic rounding
+
+constexpr uint32_t kStages = 3;
+constexpr size_t kSmem = kStages * kStageBytes + kStages * 8u + 2u * kStages * 4u;
+
+// A 16-byte shared-memory load the compiler may not merge with an earlier one.
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return r;
+}
 
 // ------------------------------------------------------------------ helpers
 
@@ -114,6 +125,25 @@ __device__ __forceinline__ uint4 philox_blk(uint32_t blk, const PhiloxStep &k) {
     return c;
 }
 
+// min(m, |a|, |b|) in one three-input minimum.
+__device__ __forceinline__ float min_abs3(float m, float a, float b) {
+    float r;
+    asm("{\n\t.reg .f32 x, y;\n\tabs.f32 x, %2;\n\tabs.f32 y, %3;\n\tmin.f32 %0, %1, x, y;\n\t}"
+        : "=f"(r)
+        : "f"(m), "f"(a), "f"(b));
+    return r;
+}
+
+// max(|a|, |b|, |c|) in one three-input maximum.
+__device__ __forceinline__ float max_abs3(float a, float b, float c) {
+    float r;
+    asm("{\n\t.reg .f32 x, y, z;\n\tabs.f32 x, %1;\n\tabs.f32 y, %2;\n\tabs.f32 z, %3;\n\t"
+        "max.f32 %0, x, y, z;\n\t}"
+        : "=f"(r)
+        : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 1 / d within one ulp for d in [2^-125, 2^125]: the hardware approximation and
 // one Newton-Raphson step (the decisions below allow for one ulp).
 __device__ __forceinline__ float recip(float d) {
@@ -143,71 +173,111 @@ __device__ __forceinline__ uint32_t ternary_field8(const uint4 &raw, const uint4
     constexpr float kNear = 0x1p-20f;
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
     const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t field = 0u, far = 0xFFFFFFFFu;
+    uint32_t field = 0u;
+    float m = 1.0f;  // min |d| over the slot (|d| < 1)
 #pragma unroll
-    for (int c = 7; c >= 0; --c) {
-        const float v = (c & 1) ? bf16_sub<1>(h[c >> 1], 0.0f) : bf16_sub<0>(h[c >> 1], 0.0f);
-        const float pa1 = __fmaf_rn(fabsf(v), rinv, 1.0f);
-        const float f = __uint_as_float(__funnelshift_r(w[c], 0x7Fu, 9));  // 0x3F800000 | w >> 9
-        const float d = __fsub_rn(f, pa1);
-        const float e = __fadd_rn(d, 2.0f);
-        const uint32_t y = __float_as_uint(e) | (__float_as_uint(d) & ~__float_as_uint(v));
-        field = __funnelshift_l(y, field, 2);
-        far &= __float_as_uint(__fsub_rn(kNear, fabsf(d)));  // sign bit kept while |d| > 2^-20
+    for (int c = 7; c >= 0; c -= 2) {
+        float d2[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int cc = c - t;
+            const float v = (cc & 1) ? bf16_sub<1>(h[cc >> 1], 0.0f) : bf16_sub<0>(h[cc >> 1], 0.0f);
+            const float pa1 = __fmaf_rn(fabsf(v), rinv, 1.0f);
+            const float f = __uint_as_float(__funnelshift_r(w[cc], 0x7Fu, 9));  // 0x3F800000 | w >> 9
+            const float d = __fsub_rn(f, pa1);
+            const float e = __fadd_rn(d, 2.0f);
+            const uint32_t y = __float_as_uint(e) | (__float_as_uint(d) & ~__float_as_uint(v));
+            field = __funnelshift_l(y, field, 2);
+            d2[t] = d;
+        }
+        m = min_abs3(m, d2[0], d2[1]);
     }
-    near = (far >> 31) == 0u;
+    near = m <= kNear;
     return field;
 }
 
 // ------------------------------------------------------------------- 8 bit
 
-// Codes of the 8 elements of a lane slot, four per word.  ta = fl(fl(v - mn) *
-// rinv) is within 2^-22 t (t <= 255 (1 + 2^-22)) of the IEEE quotient t =
-// fl(fl(v - mn) / scale), so rint(ta) = rint(t) unless ta lies within 2^-13 of a
-// half-integer.  y = ta + 1.5 * 2^23 holds rint(ta) in its low mantissa bits,
-// so the low byte of y's pattern is the code: three byte permutes pack four.
-// `near` is set when some |ta - rint(ta)| >= 1/2 - 2^-12.
+__device__ __forceinline__ float bf16_at(uint32_t w, int c) {
+    return __uint_as_float(c ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// Codes of the 8 elements of a lane slot, four per word.  With d = fl(v - mn),
+// the exact product d * rinv is within 2^-22 t (t <= 255 (1 + 2^-22)) of the
+// IEEE quotient t = fl(d / scale) (rinv's ulp and t's own rounding), so its
+// nearest integer is rint(t) unless it lies within 2^-13 of a half-integer.
+// y = fl(d * rinv + 1.5 * 2^23), one fma, is that nearest integer (ties to
+// even) in its low mantissa bits, so the low byte of y's pattern is the code:
+// three byte permutes pack four.  The distance to it, fl(d * rinv - (y - 1.5 *
+// 2^23)), is one more fma; `near` is set when some distance reaches
+// 1/2 - 2^-12.
 __device__ __forceinline__ void u8_fields(const uint4 &raw, float mn, float rinv, uint32_t &f0,
                                           uint32_t &f1, bool &near) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t y[8];
-    float worst = 0.0f;
+    float dist[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         const float d = (c & 1) ? bf16_sub<1>(h[c >> 1], mn) : bf16_sub<0>(h[c >> 1], mn);
-        const float ta = __fmul_rn(d, rinv);
-        const float yf = __fadd_rn(ta, kMagic);
+        const float yf = __fmaf_rn(d, rinv, kMagic);
         y[c] = __float_as_uint(yf);
-        worst = fmaxf(worst, fabsf(__fsub_rn(ta, __fsub_rn(yf, kMagic))));
+        dist[c] = __fmaf_rn(d, rinv, -__fsub_rn(yf, kMagic));
     }
+    float worst = max_abs3(max_abs3(dist[0], dist[1], dist[2]), dist[3], dist[4]);
+    worst = max_abs3(worst, dist[5], dist[6]);
+    worst = fmaxf(worst, fabsf(dist[7]));
     f0 = __byte_perm(__byte_perm(y[0], y[1], 0x0040), __byte_perm(y[2], y[3], 0x0040), 0x5410);
     f1 = __byte_perm(__byte_perm(y[4], y[5], 0x0040), __byte_perm(y[6], y[7], 0x0040), 0x5410);
     near = worst >= 0.5f - 0x1p-12f;
 }
 
-// ------------------------------------------------------------------ kernel
-
-__device__ __forceinline__ float bf16_at(uint32_t w, int c) {
-    return __uint_as_float(c ? (w & 0xFFFF0000u) : (w << 16));
+// The ternary codes of a lane slot with the IEEE division (the slot that the
+// division-free decision could not settle); out of line, so that its registers
+// do not count against the common path's.
+__device__ __noinline__ uint32_t ternary_slot_exact(uint4 raw, float s, uint64_t i0,
+                                                    const EncodeParams &P) {
+    float u[8];
+    uniform4(i0, P.step, P.keys, u);
+    uniform4(i0 + 4, P.step, P.keys, u + 4);
+    const BucketParams bp{s, 0.0f};
+    const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t field = 0u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        field |= code_exact<kTernary, 2, true>(bf16_at(h[c >> 1], c & 1), u[c], bp) << (2 * c);
+    return field;
 }
 
-__device__ __forceinline__ void issue_tile(const EncodeParams &P, uint64_t ntiles, uint64_t tile,
-                                           unsigned char *stage, uint64_t *bar) {
-    const uint64_t t0 = tile * kTile;
-    const uint64_t tcnt = min(static_cast<uint64_t>(kTile), P.n - t0);
+// ------------------------------------------------------------------ kernel
+
+// The segment that owns launch tile `tile` (the segments' first tiles ascend).
+__device__ __forceinline__ uint32_t segment_of(const EncodeSegs &S, uint64_t tile) {
+    uint32_t lo = 0, hi = S.nseg;
+    while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (S.s[mid].tile0 <= tile) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void issue_tile(const EncodeSegs &S, uint64_t tile, unsigned char *stage,
+                                           uint64_t *bar) {
+    const EncodeSeg &sg = S.s[segment_of(S, tile)];
+    const uint64_t t0 = (tile - sg.tile0) * kTile;
+    const uint64_t tcnt = min(static_cast<uint64_t>(kTile), sg.n - t0);
     const uint32_t gb = floor16(tcnt * 2u);
     mbar_arrive_expect_tx(bar, gb);
-    if (gb) bulk_load(stage, static_cast<const uint16_t *>(P.grad) + t0, gb, bar);
-    (void)ntiles;
+    if (gb) bulk_load(stage, static_cast<const uint16_t *>(sg.grad) + t0, gb, bar);
 }
 
 // A bucket that is not whole and staged (the array's last one): element-wise
 // from global memory with the exact division; every lane writes whole code words.
 template <int KIND>
-__device__ __noinline__ void encode_partial_bucket(const EncodeParams &P, uint64_t k, uint64_t b0,
-                                                   uint32_t cnt, int lane) {
-    const uint16_t *g = static_cast<const uint16_t *>(P.grad);
+__device__ __noinline__ void encode_partial_bucket(const EncodeParams &P, const EncodeSeg &sg,
+                                                   uint64_t k, uint64_t b0, uint32_t cnt, int lane) {
+    const uint16_t *g = static_cast<const uint16_t *>(sg.grad);
     constexpr int SCHEME = KIND == kU8 ? kUniform : kTernary;
     constexpr int BITS = KIND == kU8 ? 8 : 2;
     constexpr bool SR = KIND == kTern;
@@ -223,18 +293,19 @@ __device__ __noinline__ void encode_partial_bucket(const EncodeParams &P, uint64
         for (uint32_t c = 0; c < per; ++c) {
             const uint32_t j = wi * per + c;
             if (j < cnt) {
-                const float u = SR ? uniform1(b0 + j, P.step, P.keys) : 0.0f;
+                const float u = SR ? uniform1(sg.index_base + b0 + j, P.step, P.keys) : 0.0f;
                 word |= code_exact<SCHEME, BITS, SR>(bf16_bits_to_float(g[b0 + j]), u, bp) << (c * BITS);
             }
         }
-        P.codes[b0 / per + wi] = word;
+        sg.codes[b0 / per + wi] = word;
     }
-    if (lane == 0) store_meta<SCHEME>(P.scale, P.offset, k, bp);
+    if (lane == 0) store_meta<SCHEME>(sg.scale, sg.offset, k, bp);
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __grid_constant__ EncodeParams P,
                                                                    const __grid_constant__ PhiloxStep K,
+                                                                   const __grid_constant__ EncodeSegs S,
                                                                    const uint64_t ntiles) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
@@ -255,7 +326,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
         for (uint32_t s = 0; s < kStages; ++s) {
             const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
             if (tile < ntiles) {
-                issue_tile(P, ntiles, tile, smem + s * kStageBytes, &full[s]);
+                issue_tile(S, tile, smem + s * kStageBytes, &full[s]);
                 issued[s] = 1u;
             }
         }
@@ -272,59 +343,57 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
             failed = true;
             break;
         }
-        const uint64_t t0 = tile * kTile;
-        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(kTile), P.n - t0));
+        const EncodeSeg &sg = S.s[segment_of(S, tile)];
+        const uint64_t lt = tile - sg.tile0;  // the tile within its segment
+        const uint64_t t0 = lt * kTile;
+        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(kTile), sg.n - t0));
         const uint32_t staged = floor16(static_cast<uint64_t>(tcnt) * 2u) / 2u;
         const uint32_t b_off = static_cast<uint32_t>(warp) * kB;
         const uint32_t cnt = b_off < tcnt ? min(kB, tcnt - b_off) : 0u;
-        const uint64_t b0 = t0 + b_off;
-        const uint64_t k = tile * kWarps + warp;
+        const uint64_t b0 = t0 + b_off;            // the bucket's first element in its segment
+        const uint64_t d0 = sg.index_base + b0;    // ... and its draw index
+        const uint64_t k = lt * kWarps + warp;
 
         if (cnt == kB && b_off + kB <= staged) {
-            uint4 raw[4];
-#pragma unroll
-            for (int sl = 0; sl < 4; ++sl)
-                raw[sl] = *reinterpret_cast<const uint4 *>(stage + (b_off + (sl * 32 + lane) * 8u) * 2u);
+            auto slot = [&](int sl) {
+                return *reinterpret_cast<const uint4 *>(stage + (b_off + (sl * 32 + lane) * 8u) * 2u);
+            };
             if constexpr (KIND == kTern) {
                 // ---- s = max |x|, on packed pairs (only the magnitudes count)
-                uint32_t a = absmax_bf16x2(raw[0].x, raw[0].y);
-                a = absmax_bf16x2(a, absmax_bf16x2(raw[0].z, raw[0].w));
+                uint32_t a = 0u;
 #pragma unroll
-                for (int sl = 1; sl < 4; ++sl) {
-                    a = absmax_bf16x2(a, absmax_bf16x2(raw[sl].x, raw[sl].y));
-                    a = absmax_bf16x2(a, absmax_bf16x2(raw[sl].z, raw[sl].w));
+                for (int sl = 0; sl < 4; ++sl) {
+                    const uint4 r = slot(sl);
+                    a = absmax_bf16x2(a, absmax_bf16x2(r.x, r.y));
+                    a = absmax_bf16x2(a, absmax_bf16x2(r.z, r.w));
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) a = absmax_bf16x2(a, __shfl_xor_sync(kFull, a, o));
                 a &= 0x7FFF7FFFu;
                 const float s_ = fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-                const BucketParams bp{s_, 0.0f};
                 const bool fast = s_ >= 0x1p-125f && s_ <= 0x1p125f;
                 const float rinv = fast ? recip(s_) : 0.0f;
-                // ---- codes, 8 elements per slot, two lanes per code word
+                // ---- codes, 8 elements per slot, two lanes per code word; the slot
+                // is read from the stage again rather than kept in registers
 #pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint32_t j = (sl * 32 + lane) * 8u;
                     const uint64_t i0 = b0 + j;
-                    const uint32_t blk = static_cast<uint32_t>(i0 >> 2);  // n < 2^34: fits
-                    uint32_t field;
+                    const uint32_t blk = static_cast<uint32_t>((d0 + j) >> 2);  // draws < 2^34
+                    const uint4 da = philox_blk(blk, K), db = philox_blk(blk + 1u, K);
+                    const uint4 r = lds128(stage + (b_off + j) * 2u);
+                    uint32_t field = 0u;
                     bool near = true;
-                    if (fast) field = ternary_field8(raw[sl], philox_blk(blk, K), philox_blk(blk | 1u, K), rinv, near);
-                    if (near) {  // rare: recompute the slot with the division
-                        float u[8];
-                        uniform4(i0, P.step, P.keys, u);
-                        uniform4(i0 + 4, P.step, P.keys, u + 4);
-                        const uint32_t h[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
-                        field = 0u;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            field |= code_exact<kTernary, 2, true>(bf16_at(h[c >> 1], c & 1), u[c], bp) << (2 * c);
-                    }
+                    if (fast) field = ternary_field8(r, da, db, rinv, near);
+                    if (near) field = ternary_slot_exact(r, s_, d0 + j, P);  // rare
                     field |= __shfl_down_sync(kFull, field, 1) << 16;
-                    if ((lane & 1) == 0) __stcs(P.codes + i0 / 16u, field);
+                    if ((lane & 1) == 0) __stcs(sg.codes + i0 / 16u, field);
                 }
-                if (lane == 0) P.scale[k] = s_;
+                if (lane == 0) sg.scale[k] = s_;
             } else {
+                uint4 raw[4];
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) raw[sl] = slot(sl);
                 // ---- min and max, on packed pairs
                 uint32_t lo = min_bf16x2(raw[0].x, raw[0].y), hi = max_bf16x2(raw[0].x, raw[0].y);
                 lo = min_bf16x2(lo, min_bf16x2(raw[0].z, raw[0].w));
@@ -363,15 +432,15 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                             f1 |= code_exact<kUniform, 8, false>(bf16_at(h[2 + (c >> 1)], c & 1), 0.0f, bp) << (8 * c);
                         }
                     }
-                    __stcs(reinterpret_cast<uint2 *>(P.codes + i0 / 4u), make_uint2(f0, f1));
+                    __stcs(reinterpret_cast<uint2 *>(sg.codes + i0 / 4u), make_uint2(f0, f1));
                 }
                 if (lane == 0) {
-                    P.scale[k] = bp.scale;
-                    P.offset[k] = bp.a;
+                    sg.scale[k] = bp.scale;
+                    sg.offset[k] = bp.a;
                 }
             }
         } else if (cnt) {
-            encode_partial_bucket<KIND>(P, k, b0, cnt, lane);
+            encode_partial_bucket<KIND>(P, sg, k, b0, cnt, lane);
         }
         // this warp is done with the stage (its reads have returned: their values
         // are used above); the warp that completes the count refills the stage
@@ -384,13 +453,13 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                 fence_proxy_async_shared();  // generic reads before the bulk copy's writes
                 const uint64_t next = tile + static_cast<uint64_t>(kStages) * gridDim.x;
                 if (next < ntiles) {
-                    issue_tile(P, ntiles, next, smem + s * kStageBytes, &full[s]);
+                    issue_tile(S, next, smem + s * kStageBytes, &full[s]);
                     issued[s] += 1u;
                 }
             }
         }
     }
-    if (failed && lane == 0) atomicOr(&g_encode_bf16_fast_errors, kErrPipelineTimeout);
+    if (failed && lane == 0) report_failure(&g_encode_bf16_fast_errors, P.status, kErrPipelineTimeout);
     // A warp that gave up leaves its stages unrefilled, so the other warps' waits
     // run out too; every warp gets here.  Copies still in flight (only after a
     // failure) must land before the block's shared memory goes away.
@@ -418,36 +487,40 @@ PhiloxStep philox_step(const EncodeParams &p) {
 }
 
 template <int KIND>
-cudaError_t launch_one(const EncodeParams &p, cudaStream_t stream) {
+cudaError_t launch_one(const EncodeParams &p, const EncodeSegs &S, uint64_t ntiles,
+                       cudaStream_t stream) {
     auto fn = &encode_bf16_fast_kernel<KIND>;
-    const size_t smem = kStages * kStageBytes + kStages * 8u + 2u * kStages * 4u;
+    const size_t smem = kSmem;
     cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
     if (e != cudaSuccess) return e;
-    const uint64_t ntiles = (p.n + kTile - 1) / kTile;
     const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kBlock, ntiles, smem);
-    fn<<<grid, kBlock, smem, stream>>>(p, philox_step(p), ntiles);
+    fn<<<grid, kBlock, smem, stream>>>(p, philox_step(p), S, ntiles);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+uint64_t encode_bf16_fast_tiles(uint64_t n) { return (n + kTile - 1) / kTile; }
+
 bool encode_bf16_fast_applies(const EncodeParams &p, int scheme, int bits, int stochastic,
                               bool grad16, bool codes8) {
-    if (!grad16 || p.err != nullptr || p.bucket != kB || p.n >= (static_cast<uint64_t>(1) << 34))
+    // draws are indexed in 32-bit Philox blocks of four: index_base + n < 2^34
+    if (!grad16 || p.err != nullptr || p.bucket != kB ||
+        p.index_base + p.n >= (static_cast<uint64_t>(1) << 34))
         return false;
     if (scheme == kTernary) return stochastic != 0;
     return scheme == kUniform && bits == 8 && !stochastic && codes8;
 }
 
-cudaError_t launch_encode_bf16_fast(const EncodeParams &p, int scheme, cudaStream_t stream) {
-    return scheme == kTernary ? launch_one<kTern>(p, stream) : launch_one<kU8>(p, stream);
+cudaError_t launch_encode_bf16_fast(const EncodeParams &p, int scheme, cudaStream_t stream,
+                                    const EncodeSegs *segs) {
+    const EncodeSegs S = segs ? *segs : single_segment(p);
+    uint64_t ntiles = 0;
+    for (uint32_t i = 0; i < S.nseg; ++i) ntiles = S.s[i].tile0 + encode_bf16_fast_tiles(S.s[i].n);
+    return scheme == kTernary ? launch_one<kTern>(p, S, ntiles, stream)
+                              : launch_one<kU8>(p, S, ntiles, stream);
 }
 
-uint32_t take_encode_bf16_fast_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_bf16_fast_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_bf16_fast_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_bf16_fast_errors, g_encode_bf16_fast_errors)
 
 }  // namespace qc

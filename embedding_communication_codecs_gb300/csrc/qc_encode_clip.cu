@@ -19,8 +19,8 @@ namespace {
 
 template <int BITS, bool SR>
 cudaError_t launch_f32(const EncodeParams &p, const EncodeTiles &g, cudaStream_t stream) {
-    return p.err ? launch_one<kClip, BITS, SR, float, true>(p, g, stream)
-                 : launch_one<kClip, BITS, SR, float, false>(p, g, stream);
+    return p.err ? launch_one<kClip, BITS, SR, float, true>(p, g, stream, nullptr)
+                 : launch_one<kClip, BITS, SR, float, false>(p, g, stream, nullptr);
 }
 
 template <int BITS>
@@ -44,11 +44,6 @@ cudaError_t launch_encode_clip(const EncodeParams &p, const EncodeTiles &g, int 
     }
 }
 
-uint32_t take_encode_clip_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_clip_errors, g_encode_errors)
 
 }  // namespace qc

@@ -9,8 +9,8 @@ namespace {
 
 template <int BITS, bool SR>
 cudaError_t launch_b16(const EncodeParams &p, const EncodeTiles &g, cudaStream_t stream) {
-    return p.err ? launch_one<kClip, BITS, SR, uint16_t, true>(p, g, stream)
-                 : launch_one<kClip, BITS, SR, uint16_t, false>(p, g, stream);
+    return p.err ? launch_one<kClip, BITS, SR, uint16_t, true>(p, g, stream, nullptr)
+                 : launch_one<kClip, BITS, SR, uint16_t, false>(p, g, stream, nullptr);
 }
 
 template <int BITS>
@@ -31,11 +31,6 @@ cudaError_t launch_encode_clip_bf16(const EncodeParams &p, const EncodeTiles &g,
     }
 }
 
-uint32_t take_encode_clip_bf16_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_clip_bf16_errors, g_encode_errors)
 
 }  // namespace qc

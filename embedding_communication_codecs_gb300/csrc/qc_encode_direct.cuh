@@ -115,13 +115,13 @@ __global__ void __launch_bounds__(kBlock) encode_kernel(const __grid_constant__ 
 
         if (!P.two_pass) {
             quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, b0, cnt, tt, team_threads,
-                                                       lane, p, bp, P.step, keys);
+                                                       lane, p, bp, P.step, keys, P.index_base);
         } else {
             for (uint32_t w0 = 0; w0 < cnt; w0 += window) {
                 load_slots<TIn, EF>(P, b0 + w0, cnt - w0, tt, team_threads, p);
                 quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, b0 + w0, cnt - w0, tt,
                                                            team_threads, lane, p, bp, P.step,
-                                                           keys);
+                                                           keys, P.index_base);
             }
         }
         if (active && tt == 0) store_meta<SCHEME>(P.scale, P.offset, k, bp);

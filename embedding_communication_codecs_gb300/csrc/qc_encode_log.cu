@@ -12,17 +12,13 @@
 namespace qc {
 
 cudaError_t launch_encode_log(const EncodeParams &p, const EncodeTiles &g, int bits,
-                              int stochastic, int bf16, cudaStream_t stream) {
-    if (bits == 2) return launch_round<kLog, 2>(p, g, stochastic, bf16, stream);
-    if (bits == 4) return launch_round<kLog, 4>(p, g, stochastic, bf16, stream);
-    return launch_round<kLog, 8>(p, g, stochastic, bf16, stream);
+                              int stochastic, int bf16, cudaStream_t stream,
+                              const EncodeSegs *segs) {
+    if (bits == 2) return launch_round<kLog, 2>(p, g, stochastic, bf16, stream, segs);
+    if (bits == 4) return launch_round<kLog, 4>(p, g, stochastic, bf16, stream, segs);
+    return launch_round<kLog, 8>(p, g, stochastic, bf16, stream, segs);
 }
 
-uint32_t take_encode_log_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_log_errors, g_encode_errors)
 
 }  // namespace qc

@@ -648,7 +648,8 @@ __device__ __forceinline__ float team_exact_norm(WideSum &acc, Stats<SCHEME> (*r
 }
 
 // Quantizes the lane's slots of bucket [b0, b0 + cnt), packs and stores the code
-// words, and (with error feedback) stores the new residual.  All 32 lanes of the
+// words, and (with error feedback) stores the new residual.  Element i draws
+// with the index draw_base + i (a segment's place in a multi-segment call).  All 32 lanes of the
 // warp must call this together (the packing uses shuffles).  FULL as for
 // accumulate_slots.
 template <int SCHEME, int BITS, bool SR, bool EF, bool FULL = false>
@@ -656,7 +657,7 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
                                                      uint32_t cnt, int tt, int team_threads,
                                                      int lane, const float4 (&p)[kSlots],
                                                      const BucketParams &bp, uint32_t step,
-                                                     const PhiloxKeys &keys) {
+                                                     const PhiloxKeys &keys, uint64_t draw_base = 0) {
     const FastQ fq = fast_params<SCHEME, BITS>(bp);
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
@@ -664,7 +665,7 @@ __device__ __forceinline__ void quantize_store_slots(uint32_t *codes, float *err
         const uint64_t i = b0 + j;
         float u[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (SR) {
-            if (FULL || j < cnt) uniform4(i, step, keys, u);
+            if (FULL || j < cnt) uniform4(draw_base + i, step, keys, u);
         }
         uint32_t field = 0;
         float4 e;

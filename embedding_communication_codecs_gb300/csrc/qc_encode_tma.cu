@@ -19,28 +19,24 @@
 namespace qc {
 
 cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
-                              int stochastic, int bf16, cudaStream_t stream) {
-    if (scheme == kLog) return launch_encode_log(p, g, bits, stochastic, bf16, stream);
-    if (scheme == kSign) return launch_dtype<kSign, 1, false>(p, g, bf16, stream);
-    if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, bf16, stream);
+                              int stochastic, int bf16, cudaStream_t stream,
+                              const EncodeSegs *segs) {
+    if (scheme == kLog) return launch_encode_log(p, g, bits, stochastic, bf16, stream, segs);
+    if (scheme == kSign) return launch_dtype<kSign, 1, false>(p, g, bf16, stream, segs);
+    if (scheme == kTernary) return launch_round<kTernary, 2>(p, g, stochastic, bf16, stream, segs);
     if (scheme == kQsgd) {
-        if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, bf16, stream);
-        if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, bf16, stream);
-        return launch_round<kQsgd, 8>(p, g, stochastic, bf16, stream);
+        if (bits == 2) return launch_round<kQsgd, 2>(p, g, stochastic, bf16, stream, segs);
+        if (bits == 4) return launch_round<kQsgd, 4>(p, g, stochastic, bf16, stream, segs);
+        return launch_round<kQsgd, 8>(p, g, stochastic, bf16, stream, segs);
     }
     switch (bits) {
-        case 1: return launch_round<kUniform, 1>(p, g, stochastic, bf16, stream);
-        case 2: return launch_round<kUniform, 2>(p, g, stochastic, bf16, stream);
-        case 4: return launch_round<kUniform, 4>(p, g, stochastic, bf16, stream);
-        default: return launch_round<kUniform, 8>(p, g, stochastic, bf16, stream);
+        case 1: return launch_round<kUniform, 1>(p, g, stochastic, bf16, stream, segs);
+        case 2: return launch_round<kUniform, 2>(p, g, stochastic, bf16, stream, segs);
+        case 4: return launch_round<kUniform, 4>(p, g, stochastic, bf16, stream, segs);
+        default: return launch_round<kUniform, 8>(p, g, stochastic, bf16, stream, segs);
     }
 }
 
-uint32_t take_encode_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_encode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_encode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_encode_errors, g_encode_errors)
 
 }  // namespace qc

@@ -26,16 +26,36 @@ static __device__ unsigned int g_encode_errors;
 
 namespace {
 
+// The segment that owns launch tile `tile` (binary search on the segments'
+// first tiles, which ascend).
+__device__ __forceinline__ uint32_t segment_of(const EncodeSegs &S, uint64_t tile) {
+    uint32_t lo = 0, hi = S.nseg;
+    while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (S.s[mid].tile0 <= tile) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// The bulk copies of tile `lt` of one segment (lt counted within the segment).
 template <typename TIn, bool EF>
-__device__ __forceinline__ void issue_tile(const EncodeParams &P, const EncodeTiles &G,
-                                           uint64_t tile, unsigned char *stage, uint64_t *bar) {
-    const uint64_t t0 = tile * G.te;
-    const uint64_t tcnt = min(static_cast<uint64_t>(G.te), P.n - t0);
+__device__ __forceinline__ void issue_seg_tile(const EncodeSeg &sg, const EncodeTiles &G,
+                                               uint64_t lt, unsigned char *stage, uint64_t *bar) {
+    const uint64_t t0 = lt * G.te;
+    const uint64_t tcnt = min(static_cast<uint64_t>(G.te), sg.n - t0);
     const uint32_t gb = floor16(tcnt * sizeof(TIn));
     const uint32_t eb = EF ? floor16(tcnt * 4u) : 0u;
     mbar_arrive_expect_tx(bar, gb + eb);
-    if (gb) bulk_load(stage, static_cast<const TIn *>(P.grad) + t0, gb, bar);
-    if (EF && eb) bulk_load(stage + G.e_offset, P.err + t0, eb, bar);
+    if (gb) bulk_load(stage, static_cast<const TIn *>(sg.grad) + t0, gb, bar);
+    if (EF && eb) bulk_load(stage + G.e_offset, sg.err + t0, eb, bar);
+}
+
+template <typename TIn, bool EF>
+__device__ __forceinline__ void issue_tile(const EncodeSegs &S, const EncodeTiles &G,
+                                           uint64_t tile, unsigned char *stage, uint64_t *bar) {
+    const EncodeSeg &sg = S.s[segment_of(S, tile)];
+    issue_seg_tile<TIn, EF>(sg, G, tile - sg.tile0, stage, bar);
 }
 
 // Elements of the tile that the bulk copies brought into shared memory.
@@ -67,7 +87,7 @@ __device__ __forceinline__ float smem_grad1(const unsigned char *stage, uint32_t
 // p = e + g for the lane's slots of the bucket at tile offset b_off.  FULL: every
 // slot is valid and staged.
 template <typename TIn, bool EF, bool FULL = false>
-__device__ __forceinline__ void load_slots_staged(const EncodeParams &P, const EncodeTiles &G,
+__device__ __forceinline__ void load_slots_staged(const EncodeSeg &P, const EncodeTiles &G,
                                                   const unsigned char *stage, uint64_t t0,
                                                   uint32_t b_off, uint32_t cnt, uint32_t staged,
                                                   int tt, int team_threads,
@@ -108,7 +128,8 @@ __device__ __forceinline__ void load_slots_staged(const EncodeParams &P, const E
 
 template <int SCHEME, int BITS, bool SR, typename TIn, bool EF>
 __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constant__ EncodeParams P,
-                                                            const __grid_constant__ EncodeTiles G) {
+                                                            const __grid_constant__ EncodeTiles G,
+                                                            const __grid_constant__ EncodeSegs S) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
     auto red = reinterpret_cast<Stats<SCHEME>(*)[kBlock / 32]>(full + G.stages);
@@ -134,10 +155,9 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
         for (uint32_t s = 0; s < G.stages; ++s) {
             const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
             if (tile < G.ntiles)
-                issue_tile<TIn, EF>(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+                issue_tile<TIn, EF>(S, G, tile, smem + s * G.stage_bytes, &full[s]);
         }
     }
-    const PhiloxKeys &keys = P.keys;
 
     int buf = 0;
     uint32_t sel_parity = 0;  // CLIP: which histogram set the team's next bucket uses
@@ -147,10 +167,19 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
         const uint32_t s = it % G.stages;
         const uint32_t parity = (it / G.stages) & 1u;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        const bool ok = mbar_wait(&full[s], parity);
+        // The block agrees on the wait's outcome before anything is computed or
+        // stored: after a timeout no thread touches the residual, codes or
+        // metadata of a tile whose stage may be only partly filled.
+        if (!__syncthreads_and(mbar_wait(&full[s], parity))) {
+            failed = true;
+            break;
+        }
 
-        const uint64_t t0 = tile * G.te;
-        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
+        const EncodeSeg &sg = S.s[segment_of(S, tile)];
+        const uint64_t lt = tile - sg.tile0;  // the tile within its segment
+        const PhiloxKeys &keys = P.keys;
+        const uint64_t t0 = lt * G.te;
+        const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), sg.n - t0));
         const uint32_t staged = staged_elems<TIn, EF>(tcnt);
         for (uint32_t kb0 = 0; kb0 < G.tb; kb0 += teams) {
             const uint32_t kb = kb0 + team;
@@ -163,11 +192,11 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
             Stats<SCHEME> st;
             st.init();
             if (whole) {
-                load_slots_staged<TIn, EF, true>(P, G, stage, t0, b_off, cnt, staged, tt,
+                load_slots_staged<TIn, EF, true>(sg, G, stage, t0, b_off, cnt, staged, tt,
                                                  team_threads, p);
                 if constexpr (SCHEME != kClip) accumulate_slots<SCHEME, true>(st, p, tt, team_threads, cnt);
             } else {
-                load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+                load_slots_staged<TIn, EF>(sg, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
                 if constexpr (SCHEME != kClip) accumulate_slots<SCHEME>(st, p, tt, team_threads, cnt);
             }
             if constexpr (SCHEME == kClip) {
@@ -189,28 +218,25 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                 }
             }
             if (whole)
-                quantize_store_slots<SCHEME, BITS, SR, EF, true>(P.codes, P.err, t0 + b_off, cnt, tt,
+                quantize_store_slots<SCHEME, BITS, SR, EF, true>(sg.codes, sg.err, t0 + b_off, cnt, tt,
                                                                  team_threads, lane, p, bp, P.step,
-                                                                 keys);
+                                                                 keys, sg.index_base);
             else
-                quantize_store_slots<SCHEME, BITS, SR, EF>(P.codes, P.err, t0 + b_off, cnt, tt,
-                                                           team_threads, lane, p, bp, P.step, keys);
-            if (cnt && tt == 0) store_meta<SCHEME>(P.scale, P.offset, tile * G.tb + kb, bp);
+                quantize_store_slots<SCHEME, BITS, SR, EF>(sg.codes, sg.err, t0 + b_off, cnt, tt,
+                                                           team_threads, lane, p, bp, P.step, keys,
+                                                           sg.index_base);
+            if (cnt && tt == 0) store_meta<SCHEME>(sg.scale, sg.offset, lt * G.tb + kb, bp);
         }
-        // Every thread is done with this stage (and agrees the wait succeeded)
-        // before it is refilled.
-        if (!__syncthreads_and(ok)) {
-            failed = true;
-            break;
-        }
+        // Every thread is done with this stage before it is refilled.
+        __syncthreads();
         if (threadIdx.x == 0) {
             const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
             if (next < G.ntiles)
-                issue_tile<TIn, EF>(P, G, next, smem + s * G.stage_bytes, &full[s]);
+                issue_tile<TIn, EF>(S, G, next, smem + s * G.stage_bytes, &full[s]);
         }
     }
     if (failed && threadIdx.x == 0) {
-        atomicOr(&g_encode_errors, kErrPipelineTimeout);
+        report_failure(&g_encode_errors, P.status, kErrPipelineTimeout);
         // Let every copy this block may still have in flight land (bounded).
         for (uint32_t d = 0; d < G.stages; ++d) {
             const uint32_t j = it + d;
@@ -221,7 +247,8 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
 }
 
 template <int SCHEME, int BITS, bool SR, typename TIn, bool EF>
-cudaError_t launch_one(const EncodeParams &p, const EncodeTiles &g, cudaStream_t stream) {
+cudaError_t launch_one(const EncodeParams &p, const EncodeTiles &g, cudaStream_t stream,
+                       const EncodeSegs *segs) {
     auto fn = &encode_tma_kernel<SCHEME, BITS, SR, TIn, EF>;
     size_t smem = encode_tiles_smem(g, sizeof(Stats<SCHEME>));
     if (SCHEME == kClip)
@@ -229,26 +256,27 @@ cudaError_t launch_one(const EncodeParams &p, const EncodeTiles &g, cudaStream_t
     cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
     if (e != cudaSuccess) return e;
     const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kBlock, g.ntiles, smem);
-    fn<<<grid, kBlock, smem, stream>>>(p, g);
+    if (segs) fn<<<grid, kBlock, smem, stream>>>(p, g, *segs);
+    else fn<<<grid, kBlock, smem, stream>>>(p, g, single_segment(p));
     return cudaGetLastError();
 }
 
 template <int SCHEME, int BITS, bool SR>
 cudaError_t launch_dtype(const EncodeParams &p, const EncodeTiles &g, int bf16,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const EncodeSegs *segs) {
     const bool ef = p.err != nullptr;
     if (bf16)
-        return ef ? launch_one<SCHEME, BITS, SR, uint16_t, true>(p, g, stream)
-                  : launch_one<SCHEME, BITS, SR, uint16_t, false>(p, g, stream);
-    return ef ? launch_one<SCHEME, BITS, SR, float, true>(p, g, stream)
-              : launch_one<SCHEME, BITS, SR, float, false>(p, g, stream);
+        return ef ? launch_one<SCHEME, BITS, SR, uint16_t, true>(p, g, stream, segs)
+                  : launch_one<SCHEME, BITS, SR, uint16_t, false>(p, g, stream, segs);
+    return ef ? launch_one<SCHEME, BITS, SR, float, true>(p, g, stream, segs)
+              : launch_one<SCHEME, BITS, SR, float, false>(p, g, stream, segs);
 }
 
 template <int SCHEME, int BITS>
 cudaError_t launch_round(const EncodeParams &p, const EncodeTiles &g, int stochastic, int bf16,
-                         cudaStream_t stream) {
-    return stochastic ? launch_dtype<SCHEME, BITS, true>(p, g, bf16, stream)
-                      : launch_dtype<SCHEME, BITS, false>(p, g, bf16, stream);
+                         cudaStream_t stream, const EncodeSegs *segs = nullptr) {
+    return stochastic ? launch_dtype<SCHEME, BITS, true>(p, g, bf16, stream, segs)
+                      : launch_dtype<SCHEME, BITS, false>(p, g, bf16, stream, segs);
 }
 
 }  // namespace

@@ -46,7 +46,43 @@ struct EncodeParams {
     uint32_t *codes;
     float *scale;
     float *offset;
+    uint32_t *status;  // the caller's status word (qc_set_status_word), or null
+    uint64_t index_base = 0;  // draw index of element 0 (a segment's place in its call)
 };
+
+// Several flat gradients encoded by one launch ("segments"): each with its own
+// arrays and length, its buckets starting at its own element 0; tiles never
+// straddle two segments, and segment s owns the launch's tiles [tile0, tile0 +
+// its tile count).  Stochastic draws of element i of a segment use the index
+// index_base + i (with the call's one seed; index_base is a multiple of 4, so a
+// segment's groups of four draws are whole Philox blocks).  A single array is
+// one segment at index 0.
+// Passed by value as a kernel parameter (60 segments: about 3.4 KB).
+constexpr int kMaxSegments = 60;  // QC_MAX_SEGMENTS_PER_LAUNCH
+
+struct EncodeSeg {
+    const void *grad;
+    float *err;
+    uint64_t n;
+    uint32_t *codes;
+    float *scale;
+    float *offset;
+    uint64_t tile0;
+    uint64_t index_base;
+};
+
+struct EncodeSegs {
+    uint32_t nseg;
+    EncodeSeg s[kMaxSegments];
+};
+
+// The segment table of a single-array call.
+inline EncodeSegs single_segment(const EncodeParams &p) {
+    EncodeSegs t;
+    t.nseg = 1;
+    t.s[0] = EncodeSeg{p.grad, p.err, p.n, p.codes, p.scale, p.offset, 0, p.index_base};
+    return t;
+}
 
 // Tiling of the TMA-pipelined encode: TB whole buckets per tile (TE elements),
 // `stages` shared-memory stages of stage_bytes each; the residual's part of a
@@ -83,6 +119,7 @@ struct DecodeParams {
     float *out;
     int flags;
     float inv_m;  // 1 / M when M is a power of two (an exact multiply), else 0
+    uint32_t *status;  // the caller's status word, or null
 };
 
 // Tiling of the pipelined decode: TB whole buckets (TE elements) per tile; a
@@ -174,6 +211,7 @@ struct ReencodeParams {
     uint32_t *codes_out;
     float *scale_out;
     float *offset_out;
+    uint32_t *status;       // the caller's status word, or null
 };
 
 // Tiling of the re-encode: TB whole buckets (TE elements) per tile, the M
@@ -216,7 +254,8 @@ struct Fp8Params {
 cudaError_t launch_encode(const EncodeParams &p, int scheme, int bits, int stochastic,
                           int bf16, cudaStream_t stream);
 cudaError_t launch_encode_tma(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
-                              int stochastic, int bf16, cudaStream_t stream);
+                              int stochastic, int bf16, cudaStream_t stream,
+                              const EncodeSegs *segs = nullptr);
 // The percentile-clipped uniform scheme (its own translation unit).
 cudaError_t launch_encode_clip(const EncodeParams &p, const EncodeTiles &g, int bits,
                                int stochastic, int bf16, cudaStream_t stream);
@@ -224,14 +263,18 @@ cudaError_t launch_encode_clip_bf16(const EncodeParams &p, const EncodeTiles &g,
                                     int stochastic, cudaStream_t stream);
 // The logarithmic-level scheme in the pipelined kernel (its own translation unit).
 cudaError_t launch_encode_log(const EncodeParams &p, const EncodeTiles &g, int bits,
-                              int stochastic, int bf16, cudaStream_t stream);
+                              int stochastic, int bf16, cudaStream_t stream,
+                              const EncodeSegs *segs = nullptr);
 cudaError_t launch_encode_bf16(const EncodeParams &p, const EncodeTiles &g, int scheme, int bits,
                                int stochastic, cudaStream_t stream);
 // The receiver's bf16 encodes without error feedback for buckets of 1024
 // (8-bit nearest, ternary stochastic): whether they apply, and the launch.
 bool encode_bf16_fast_applies(const EncodeParams &p, int scheme, int bits, int stochastic,
                               bool grad16, bool codes8);
-cudaError_t launch_encode_bf16_fast(const EncodeParams &p, int scheme, cudaStream_t stream);
+cudaError_t launch_encode_bf16_fast(const EncodeParams &p, int scheme, cudaStream_t stream,
+                                    const EncodeSegs *segs = nullptr);
+// Tiles of the receiver kernel over n elements (a segment's share of a launch).
+uint64_t encode_bf16_fast_tiles(uint64_t n);
 cudaError_t launch_decode(const DecodeParams &p, int scheme, int bits, cudaStream_t stream);
 cudaError_t launch_decode_tma(const DecodeParams &p, const DecodeTiles &g, int scheme, int bits,
                               cudaStream_t stream);
@@ -255,22 +298,23 @@ int persistent_grid(const void *kernel, int block, uint64_t units, size_t smem =
 // Raises the kernel's dynamic shared memory limit to `bytes` (once per device).
 cudaError_t prepare_dynamic_smem(const void *kernel, size_t bytes);
 
-// Device-side error flags of the pipelined kernels (read and cleared).
-uint32_t take_encode_errors();
-uint32_t take_encode_clip_errors();
-uint32_t take_encode_clip_bf16_errors();
-uint32_t take_encode_log_errors();
-uint32_t take_reencode_other_errors();
-uint32_t take_reencode_log_errors();
-uint32_t take_selftest_errors();
+// Device-side error flags of the pipelined kernels: each stores its flag in
+// *flags and clears it (one atomic exchange), returning the CUDA status.
+cudaError_t take_encode_errors(uint32_t *flags);
+cudaError_t take_encode_clip_errors(uint32_t *flags);
+cudaError_t take_encode_clip_bf16_errors(uint32_t *flags);
+cudaError_t take_encode_log_errors(uint32_t *flags);
+cudaError_t take_reencode_other_errors(uint32_t *flags);
+cudaError_t take_reencode_log_errors(uint32_t *flags);
+cudaError_t take_selftest_errors(uint32_t *flags);
 
-// One block waits on a barrier nothing completes, `rounds` tries, and records
-// the pipeline-timeout flag (qc_selftest.cu).
-cudaError_t launch_wait_timeout_selftest(uint32_t rounds, cudaStream_t stream);
-uint32_t take_topk_errors();
-uint32_t take_encode_bf16_errors();
-uint32_t take_encode_bf16_fast_errors();
-uint32_t take_decode_errors();
-uint32_t take_reencode_errors();
+// One block waits on a barrier nothing completes for timeout_us microseconds,
+// and records the pipeline-timeout flag (and *status, if given) (qc_selftest.cu).
+cudaError_t launch_wait_timeout_selftest(uint32_t timeout_us, uint32_t *status, cudaStream_t stream);
+cudaError_t take_topk_errors(uint32_t *flags);
+cudaError_t take_encode_bf16_errors(uint32_t *flags);
+cudaError_t take_encode_bf16_fast_errors(uint32_t *flags);
+cudaError_t take_decode_errors(uint32_t *flags);
+cudaError_t take_reencode_errors(uint32_t *flags);
 
 }  // namespace qc

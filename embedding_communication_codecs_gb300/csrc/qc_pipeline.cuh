@@ -7,10 +7,13 @@
 // no 16-byte alignment guarantee is fetched with 4-byte cp.async copies whose
 // completion is tracked on the same barrier (cp.async.mbarrier.arrive.noinc).
 //
-// Every wait is bounded: after kWaitRounds unsuccessful try_wait rounds the wait
-// gives up and reports failure, the block stops at its next block-wide
-// agreement point, and the kernel records the failure in a device flag that the
-// host reads with qc_take_device_errors().  Nothing spins forever.
+// Every wait is bounded in time: a wait that has not completed after
+// kWaitNs nanoseconds of the GPU's global timer (or, as a backstop should that
+// timer not advance, after kWaitRoundsBackstop tries) gives up and reports
+// failure; the block stops at its next agreement point, and the kernel records
+// the failure in a device flag that the host reads with
+// qc_take_device_errors(), and in the caller's status word if one was set
+// (qc_set_status_word).  Nothing spins forever.
 #pragma once
 
 #include <cstdint>
@@ -18,9 +21,11 @@
 
 namespace qc {
 
-// An unsuccessful try_wait returns after about 6 us on GB300 (measured through
-// qc_selftest_wait_timeout), so a stalled pipeline gives up after about 1.5 s.
-constexpr uint32_t kWaitRounds = 1u << 18;
+// A stalled pipeline gives up after 2 s.  An unsuccessful try_wait may return
+// early or late (the suspend time is the implementation's choice), so the limit
+// is kept on the global timer; the round count is only a backstop.
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kWaitRoundsBackstop = 1u << 26;
 
 // Named barrier 1 over the first `threads` threads of the block (the consumer
 // warps of a warp-specialised block; the producer warp never takes part).
@@ -114,17 +119,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase with the given parity, at most `rounds` tries; false if it
-// never completed.
-__device__ __forceinline__ bool mbar_wait_rounds(uint64_t *bar, uint32_t parity, uint32_t rounds) {
-    for (uint32_t r = 0; r < rounds; ++r)
+// The GPU's global timer, in nanoseconds.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity for at most limit_ns nanoseconds (the
+// timer is read every 16 tries); false if it never completed.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t r = 1; r < kWaitRoundsBackstop; ++r) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((r & 15u) == 0u && global_ns() - t0 > limit_ns) return false;
+    }
     return false;
 }
 
 // The pipelines' bounded wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    return mbar_wait_rounds(bar, parity, kWaitRounds);
+    return mbar_wait_ns(bar, parity, kWaitNs);
+}
+
+// Records failure bits in a translation unit's device flag and, if the launch
+// carries one, in the caller's status word.
+__device__ __forceinline__ void report_failure(unsigned int *flag, uint32_t *status, uint32_t bits) {
+    atomicOr(flag, bits);
+    if (status) atomicOr(status, bits);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -136,5 +159,23 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __host__ __device__ constexpr uint32_t floor16(uint64_t bytes) {
     return static_cast<uint32_t>(bytes & ~static_cast<uint64_t>(15));
 }
+
+// Defines FN (cudaError_t FN(uint32_t *flags)): stores FLAG's value in *flags
+// and clears it in one atomic exchange on the device (a one-thread kernel on the
+// legacy stream, then a copy of the exchanged value), so a bit that a kernel
+// sets at any moment is reported exactly once.  For use at namespace qc scope.
+#define QC_DEFINE_TAKE_FLAG(FN, FLAG)                                               \
+    static __device__ unsigned int FLAG##_taken;                                    \
+    static __global__ void FLAG##_exchange() { FLAG##_taken = atomicExch(&FLAG, 0u); } \
+    cudaError_t FN(uint32_t *flags) {                                               \
+        *flags = 0u;                                                                \
+        FLAG##_exchange<<<1, 1>>>();                                                \
+        cudaError_t e = cudaGetLastError();                                         \
+        if (e != cudaSuccess) return e;                                             \
+        unsigned int v = 0u;                                                        \
+        e = cudaMemcpyFromSymbol(&v, FLAG##_taken, sizeof v);                       \
+        *flags = v;                                                                 \
+        return e;                                                                   \
+    }
 
 }  // namespace qc

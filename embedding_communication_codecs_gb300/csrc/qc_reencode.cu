@@ -38,11 +38,6 @@ cudaError_t launch_reencode(const ReencodeParams &p, const ReencodeTiles &g, int
     }
 }
 
-uint32_t take_reencode_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_reencode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_reencode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_reencode_errors, g_reencode_errors)
 
 }  // namespace qc

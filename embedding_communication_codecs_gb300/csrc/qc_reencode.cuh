@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kReBlock, 2) reencode_kernel(const __grid_cons
         }
         cp_async_wait_all();
         if (!ok) {
-            if (lane == 0) atomicOr(&g_reencode_errors, kErrPipelineTimeout);
+            if (lane == 0) report_failure(&g_reencode_errors, P.status, kErrPipelineTimeout);
             // let copies already issued land (bounded)
             for (uint32_t d = 0; d < G.stages; ++d) {
                 const uint32_t j = it >= G.stages ? it - G.stages + d : d;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kReBlock, 2) reencode_kernel(const __grid_cons
 
         // ---- phase 2: every consumer agrees the tile's sums are complete
         if (!consumer_sync_and<kConsumers>(ok)) {
-            if (ct == 0) atomicOr(&g_reencode_errors, kErrPipelineTimeout);
+            if (ct == 0) report_failure(&g_reencode_errors, P.status, kErrPipelineTimeout);
             break;
         }
         for (uint32_t kb0 = 0; kb0 < G.tb; kb0 += teams) {

@@ -13,11 +13,6 @@ cudaError_t launch_reencode_log(const ReencodeParams &p, const ReencodeTiles &g,
     return launch_round<kLog, 8>(p, g, stochastic, stream);
 }
 
-uint32_t take_reencode_log_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_reencode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_reencode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_reencode_log_errors, g_reencode_errors)
 
 }  // namespace qc

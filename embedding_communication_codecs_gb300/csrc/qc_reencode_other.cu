@@ -15,11 +15,6 @@ cudaError_t launch_reencode_other(const ReencodeParams &p, const ReencodeTiles &
     return launch_round<kQsgd, 8>(p, g, stochastic, stream);
 }
 
-uint32_t take_reencode_other_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_reencode_errors, sizeof v);
-    cudaMemcpyToSymbol(g_reencode_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_reencode_other_errors, g_reencode_errors)
 
 }  // namespace qc

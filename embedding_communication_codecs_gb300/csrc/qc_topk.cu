@@ -207,10 +207,12 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
     }
     for (int i = threadIdx.x; i < teams * region_words; i += kBlock) teamwords[i] = 0u;
     __syncthreads();
+    // the whole gradient is one segment of the pipelined encode's tiling
+    const EncodeSeg seg{P.grad, P.err, P.n, nullptr, P.scale, P.offset, 0, 0};
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < G.stages; ++s) {
             const uint64_t tile = blockIdx.x + static_cast<uint64_t>(s) * gridDim.x;
-            if (tile < G.ntiles) issue_tile<TIn, EF>(P, G, tile, smem + s * G.stage_bytes, &full[s]);
+            if (tile < G.ntiles) issue_seg_tile<TIn, EF>(seg, G, tile, smem + s * G.stage_bytes, &full[s]);
         }
     }
 
@@ -220,7 +222,11 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        const bool ok = mbar_wait(&full[s], (it / G.stages) & 1u);
+        // the block agrees on the wait's outcome before computing or storing anything
+        if (!__syncthreads_and(mbar_wait(&full[s], (it / G.stages) & 1u))) {
+            failed = true;
+            break;
+        }
         const uint64_t t0 = tile * G.te;
         const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
         const uint32_t staged = staged_elems<TIn, EF>(tcnt);
@@ -232,26 +238,23 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
             const uint64_t k = tile * G.tb + kb;
             float4 p[kSlots];
             if (cnt == window && b_off + cnt <= staged) {
-                load_slots_staged<TIn, EF, true>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+                load_slots_staged<TIn, EF, true>(seg, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
                 topk_bucket<EF, SR, true>(T, p, cnt, b0, k, tt, team_threads, W, team, warp, lane,
                                           region, tot, red, buf, parity);
             } else if (cnt) {
-                load_slots_staged<TIn, EF>(P, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
+                load_slots_staged<TIn, EF>(seg, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
                 topk_bucket<EF, SR, false>(T, p, cnt, b0, k, tt, team_threads, W, team, warp, lane,
                                            region, tot, red, buf, parity);
             }
         }
-        if (!__syncthreads_and(ok)) {
-            failed = true;
-            break;
-        }
+        __syncthreads();  // every thread is done with this stage before it is refilled
         if (threadIdx.x == 0) {
             const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
-            if (next < G.ntiles) issue_tile<TIn, EF>(P, G, next, smem + s * G.stage_bytes, &full[s]);
+            if (next < G.ntiles) issue_seg_tile<TIn, EF>(seg, G, next, smem + s * G.stage_bytes, &full[s]);
         }
     }
     if (failed && threadIdx.x == 0) {
-        atomicOr(&g_topk_errors, kErrPipelineTimeout);
+        report_failure(&g_topk_errors, T.e.status, kErrPipelineTimeout);
         for (uint32_t d = 0; d < G.stages; ++d) {
             const uint32_t j = it + d;
             const uint64_t tile = blockIdx.x + static_cast<uint64_t>(j) * gridDim.x;
@@ -354,11 +357,6 @@ cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-uint32_t take_topk_errors() {
-    unsigned int v = 0, zero = 0;
-    cudaMemcpyFromSymbol(&v, g_topk_errors, sizeof v);
-    cudaMemcpyToSymbol(g_topk_errors, &zero, sizeof zero);
-    return v;
-}
+QC_DEFINE_TAKE_FLAG(take_topk_errors, g_topk_errors)
 
 }  // namespace qc

@@ -20,7 +20,8 @@
  *   - Every buffer pointer is a DEVICE pointer on the current CUDA device.  The
  *     caller allocates and frees every buffer; the library never allocates,
  *     frees, or synchronises, and keeps no device state between calls apart from
- *     the error flags that qc_take_device_errors() reads.
+ *     the error flags that qc_take_device_errors() reads (and, per host
+ *     thread, the status word address of qc_set_status_word).
  *   - Every compute call is asynchronous on `stream` (0 = legacy default stream).
  *     Arguments are validated on the host before any launch; on a non-OK status
  *     nothing was launched and nothing was written, and qc_last_error() holds a
@@ -38,6 +39,10 @@
  *   - Arithmetic is IEEE-754 binary32 with round-to-nearest-even, one rounding per
  *     operation as listed for each call; results are deterministic and do not
  *     depend on the launch shape.
+ *   - Inputs are expected finite.  A NaN or infinity in a gradient never faults
+ *     and never spills into another element's code: the codes of the non-finite
+ *     elements (and, for the uniform scheme, their bucket's scale when the first
+ *     element is one) are unspecified, the other elements' outputs are as stated.
  */
 #ifndef QCODEC_H
 #define QCODEC_H
@@ -124,11 +129,8 @@ size_t qc_num_buckets(size_t n, size_t bucket);
  *       NEAREST:    l_i = min(rint(t_i), s)
  *       STOCHASTIC: l_i = min(floor(t_i) + [u_i < t_i - floor(t_i)], s)
  *     code_i = [p_i < 0] << (bits-1) | l_i; deq_i = +-fl(l_i * unit); scale[k] = unit.
- *     The norm is the square root of a double-word sum of exactly split squares:
- *     it is the correctly rounded norm unless that lies within about 2^-40
- *     (relative) of a rounding boundary.  Norms must stay below 2^63 (the
- *     squares are summed in binary32 range); below 2^-40 the squares of the
- *     smallest elements are no longer split exactly.
+ *     nrm is the binary32 value nearest (ties to even) to the square root of the
+ *     EXACT sum of the squares (non-finite elements left out of the sum).
  *   UNIFORM_CLIP ("Adaptive Quantization Strategies", Percentile Clipping; bits
  *     1, 2, 4 or 8): as UNIFORM, but mn and mx are the bucket's nearest-rank 1st
  *     and 99th percentiles (the elements of 0-based rank ceil(cnt/100) - 1 and
@@ -169,6 +171,52 @@ qc_status qc_encode_ef(const void *grad, qc_dtype dtype, float *err, size_t n, i
                        size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
                        uint32_t step, uint32_t *codes, float *scale, float *offset,
                        qc_stream_t stream);
+
+/*
+ * qc_encode_ef_segments -- qc_encode_ef over a list of flat gradients in one
+ * launch (or one per QC_MAX_SEGMENTS_PER_LAUNCH segments).
+ *
+ * "Gradient Compression and Quantised Collectives", "When it breaks": small
+ * tensors make the launch cost dominate, and bucketing many small tensors into
+ * one exchange is what makes the all-reduce efficient.  Here the tensors stay
+ * where they are: each segment keeps its own arrays and its buckets start at
+ * its own element 0, exactly as a separate qc_encode_ef call on it would, and
+ * every output is that call's, bit for bit, except for the stochastic draws:
+ * element i of segment s draws with the index I_s + i under the call's one seed
+ * and step, where I_s = the sum over the segments r before s of n_r rounded up
+ * to a multiple of 4.  That is the place of segment s when the segments are
+ * laid end to end, each padded to a whole Philox block of four draws (16 bytes
+ * of fp32), the way tensors are padded into a flat communication bucket; where
+ * every n is a multiple of 4 the draws are those of one call over the
+ * concatenation.  With one segment this is qc_encode_ef.
+ *
+ * segs   : nseg host-memory descriptors (nseg == 0 is a no-op); a segment with
+ *          n == 0 is skipped.  Every field is as for qc_encode_ef's argument of
+ *          the same name; err must be given for every segment or for none.
+ *          No output of a segment may overlap any buffer of another segment.
+ * dtype, bits, bucket, scheme, mode, seed, step : as for qc_encode_ef, shared by
+ *          every segment.
+ * One launch covers the segments when every one suits the same kernel: the
+ * receiver's bf16 encode (8-bit nearest or ternary stochastic, no residual,
+ * buckets of 1024) or the pipelined encode (16-byte aligned gradients, buckets
+ * of at most 4096 elements, any scheme but UNIFORM_CLIP); otherwise each
+ * segment takes its own launch, with the same results.  Validation of every
+ * segment precedes every launch.
+ */
+typedef struct {
+    const void *grad;   /* n elements of the call's dtype                          */
+    float *err;         /* n fp32 residual (in/out), or NULL                        */
+    size_t n;           /* elements                                                 */
+    uint32_t *codes;    /* out: qc_code_words(n, bits) words                        */
+    float *scale;       /* out: qc_num_buckets(n, bucket)                           */
+    float *offset;      /* out: qc_num_buckets(n, bucket) (uniform schemes), or NULL */
+} qc_segment;
+
+#define QC_MAX_SEGMENTS_PER_LAUNCH 60
+
+qc_status qc_encode_ef_segments(const qc_segment *segs, int nseg, qc_dtype dtype, int bits,
+                                size_t bucket, qc_scheme scheme, qc_round mode, uint64_t seed,
+                                uint32_t step, qc_stream_t stream);
 
 /*
  * qc_decode_accumulate -- receiver half: dequantize M workers' payloads and
@@ -336,25 +384,47 @@ qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, s
 /*
  * qc_take_device_errors -- device-side failures of the pipelined kernels.
  *
- * The kernels that stream tiles through shared memory wait on mbarriers with
- * an iteration limit; a wait that runs out stops its block and sets a flag in
- * device memory instead of spinning forever.  This call synchronises the
- * current device, stores the OR of the flags set since the previous call in
- * *flags (bit 0: a pipeline wait timed out; the outputs of that launch are
- * incomplete) and clears them.  It is a diagnostic call: it blocks the host and
- * must not be used inside stream capture.
+ * The kernels that stream tiles through shared memory wait on mbarriers for at
+ * most 2 s of the GPU's global timer; a wait that runs out stops its block and
+ * sets a flag in device memory instead of spinning forever.  This call
+ * synchronises the current device, stores the OR of the flags set since the
+ * previous call in *flags (bit 0: a pipeline wait timed out; the outputs of
+ * that launch are incomplete) and clears them, each flag in one atomic
+ * exchange, so a flag set concurrently is reported by this call or the next,
+ * never lost.  A CUDA error while reading them returns QC_ERR_CUDA.  It is a
+ * diagnostic call: it blocks the host and must not be used inside stream
+ * capture.  qc_set_status_word gives the same information per launch, in
+ * stream order, without a synchronisation.
  */
 qc_status qc_take_device_errors(uint32_t *flags);
 
 /*
- * qc_selftest_wait_timeout -- exercises the failure path that
- * qc_take_device_errors() reports, without a fault: one block waits on a
- * shared-memory barrier that nothing completes, with the pipelines' bounded
- * wait limited to `rounds` tries (1 .. 2^20, else QC_ERR_INVALID_ARG).  The wait
- * runs out, the block sets the pipeline-timeout flag (bit 0) and returns; the
- * context stays usable.  Asynchronous on `stream`.
+ * qc_set_status_word -- per-launch failure reporting in stream order.
+ *
+ * Every launch that the library issues from the calling host thread after this
+ * call carries `status` (a device address of one 32-bit word; NULL turns it
+ * off): if the launch's bounded waits run out, the kernel ORs the failure bits
+ * (bit 0: a pipeline wait timed out) into *status as well as into the flags of
+ * qc_take_device_errors.  The caller zeroes the word (for example with
+ * cudaMemsetAsync) before the launches it wants to watch and reads it back on
+ * the same stream after them; no synchronisation of the device is needed.  The
+ * word must stay valid until those launches have run.  Only the kernels that
+ * wait on a pipeline can fail this way; the others never write the word.
+ * status must be 4-byte aligned (else QC_ERR_ALIGNMENT).  The setting is
+ * per host thread and lasts until the next call.
  */
-qc_status qc_selftest_wait_timeout(uint32_t rounds, qc_stream_t stream);
+qc_status qc_set_status_word(uint32_t *status);
+
+/*
+ * qc_selftest_wait_timeout -- exercises the failure path that
+ * qc_take_device_errors() and the status word report, without a fault: one
+ * block waits on a shared-memory barrier that nothing completes, with the
+ * pipelines' time-bounded wait limited to `timeout_us` microseconds
+ * (1 .. 10^7, else QC_ERR_INVALID_ARG).  The wait runs out, the block sets the
+ * pipeline-timeout flag (bit 0), and the status word if one is set, and
+ * returns; the context stays usable.  Asynchronous on `stream`.
+ */
+qc_status qc_selftest_wait_timeout(uint32_t timeout_us, qc_stream_t stream);
 
 /* Message for the last non-OK status returned on the calling thread ("" if none). */
 const char *qc_last_error(void);

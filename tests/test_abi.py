@@ -193,9 +193,17 @@ def test_clip_rejects(q):
 
 
 def test_selftest_rejects(q):
-    for rounds in (0, (1 << 20) + 1):
-        assert q.lib.qc_selftest_wait_timeout(rounds, 0) == q.QC_ERR_INVALID_ARG
-    assert b"rounds" in q.lib.qc_last_error()
+    for us in (0, 10_000_001):
+        assert q.lib.qc_selftest_wait_timeout(us, 0) == q.QC_ERR_INVALID_ARG
+    assert b"timeout_us" in q.lib.qc_last_error()
+
+
+def test_status_word_setting(q):
+    """The status word is a host-side setting: it takes any 4-byte aligned
+    address (or NULL) without touching the device."""
+    assert q.lib.qc_set_status_word(0x1002) == q.QC_ERR_ALIGNMENT
+    assert q.lib.qc_set_status_word(0x1000) == q.QC_OK
+    assert q.lib.qc_set_status_word(None) == q.QC_OK
 
 
 def test_log_rejects(q):
@@ -242,3 +250,51 @@ def test_topk_rejects(q):
     assert dec(bucket=32768, n=1 << 16, ps=20, ms=2, keep=10) == q.QC_ERR_UNSUPPORTED
     assert dec(bucket=4096, keep=2000, ps=2000) == q.QC_ERR_UNSUPPORTED
     assert dec(n=0, idx=None, out=None) == q.QC_OK
+
+
+def _segs(q, *rows):
+    arr = (q.QcSegment * max(1, len(rows)))()
+    for k, (grad, err, n, codes, scale, offset) in enumerate(rows):
+        arr[k] = q.QcSegment(grad, err, n, codes, scale, offset)
+    return arr
+
+
+def _enc_segs(q, rows, dtype=None, bits=4, bucket=512, scheme=None, mode=None, nseg=None):
+    dtype = q.QC_DTYPE_F32 if dtype is None else dtype
+    scheme = q.QC_SCHEME_UNIFORM if scheme is None else scheme
+    mode = q.QC_ROUND_STOCHASTIC if mode is None else mode
+    return q.lib.qc_encode_ef_segments(_segs(q, *rows), len(rows) if nseg is None else nseg,
+                                       dtype, bits, bucket, scheme, mode, 1, 0, 0)
+
+
+MB = 0x100000
+
+
+def _seg(k, n=4096):
+    """Segment k's buffers, 16 MB apart from every other segment's."""
+    base = 0x1000000 * (k + 1)
+    return (base, base + 4 * MB, n, base + 8 * MB, base + 12 * MB, base + 14 * MB)
+
+
+def test_segments_reject(q):
+    assert _enc_segs(q, [], nseg=0) == q.QC_OK                      # nothing to do
+    assert _enc_segs(q, [_seg(0)], nseg=-1) == q.QC_ERR_INVALID_ARG
+    assert q.lib.qc_encode_ef_segments(None, 2, q.QC_DTYPE_F32, 4, 512, 0, 1, 1, 0, 0) == \
+        q.QC_ERR_NULL
+    assert _enc_segs(q, [_seg(0)], bits=3) == q.QC_ERR_INVALID_ARG   # arguments of the call
+    # a bad segment is named
+    g, e, n, c, s, o = _seg(1)
+    assert _enc_segs(q, [_seg(0), (g, e, n, c, s, 0)]) == q.QC_ERR_NULL
+    assert b"segment 1" in q.lib.qc_last_error()
+    assert _enc_segs(q, [_seg(0), (g + 2, e, n, c, s, o)]) == q.QC_ERR_ALIGNMENT
+    # residuals for every segment or for none
+    assert _enc_segs(q, [_seg(0), (g, 0, n, c, s, o)]) == q.QC_ERR_INVALID_ARG
+    assert b"every segment or for none" in q.lib.qc_last_error()
+    # an output of one segment over a buffer of another
+    g0, e0, n0, c0, s0, o0 = _seg(0)
+    assert _enc_segs(q, [_seg(0), (g, e, n, c0 + 256, s, o)]) == q.QC_ERR_INVALID_ARG
+    assert b"overlaps" in q.lib.qc_last_error()
+    assert _enc_segs(q, [_seg(0), (g, g0, n, c, s, o)]) == q.QC_ERR_INVALID_ARG  # err over grad
+    # empty segments take no buffers and are not checked
+    assert _enc_segs(q, [(0, 0, 0, 0, 0, 0)]) == q.QC_OK
+    assert q.QC_MAX_SEGMENTS_PER_LAUNCH == 60

@@ -1,11 +1,10 @@
 """GPU <-> oracle parity at the full sizes of the five workloads, through the same
-calls and launch configuration as the benchmark.
-
-Where the oracle would take minutes over a whole workload it computes sampled
-buckets one by one (its global-index slicing reproduces exactly the
-corresponding part of a whole-array call), and properties that hold at any size
-are checked on the GPU over the full arrays: the error-feedback identity over
-10 steps, and the vote being the majority of the GPU's own sign vectors.
+calls and launch configuration as the benchmark, every element of every
+output compared.  The oracle runs over bucket-aligned slices on every host
+core (tests/_par_oracle.py: its global-index slicing reproduces a whole-array
+call exactly).  Properties that hold at any size are checked on the GPU over
+the full arrays as well: the error-feedback identity over 10 steps, and the
+vote being the majority of the GPU's own sign vectors.
 """
 from __future__ import annotations
 
@@ -15,6 +14,7 @@ import torch
 
 import oracle as orc
 import workloads as wl
+from tests import _par_oracle as par
 from tests._gpu import assert_bits_equal, host, u32
 
 pytestmark = pytest.mark.gpu
@@ -26,16 +26,6 @@ def q():
     assert torch.cuda.is_available()
     yield q
     assert q.qc_take_device_errors() == 0
-
-
-def sample_buckets(nb, k=24, seed=0):
-    rng = np.random.default_rng(seed)
-    ks = {0, 1, nb // 2, nb - 2, nb - 1} | set(rng.integers(0, nb, k).tolist())
-    return sorted(x for x in ks if 0 <= x < nb)
-
-
-def word_range(lo, hi, bits):
-    return (lo * bits) // 32, (hi * bits + 31) // 32
 
 
 # ------------------------------------------------------- uniform 8-bit, n = 2^20
@@ -85,12 +75,13 @@ def test_fp8_rowwise_full(q):
 @pytest.mark.slow
 def test_sr4_ef_ten_steps_full(q):
     """250,000,000 elements (1 GB), buckets of 512, per-bucket std log-uniform in
-    [1e-5, 1e-2], a fresh draw each step, Philox (seed 2, step, index)."""
+    [1e-5, 1e-2], a fresh draw each step, Philox (seed 2, step, index).  The
+    oracle runs all 10 steps over the whole array with its own residual; codes,
+    scales and offsets are compared in full at every step, the residual and the
+    decoded gradient in full at steps 0, 4 and 9."""
     n, bucket, bits, seed, steps = 250_000_000, 512, 4, 2, 10
-    nb = (n + bucket - 1) // bucket
     sig = wl.bucket_sigmas(n, bucket, seed)
-    ks = sample_buckets(nb)
-    e_or = {k: np.zeros(min(n, (k + 1) * bucket) - k * bucket, dtype=np.float32) for k in ks}
+    e_or = np.zeros(n, dtype=np.float32)
     err = torch.zeros(n, device="cuda")
     codes, scale, offset = q.alloc_payload(n, bits, bucket, 0)
     out = torch.empty(n, device="cuda")
@@ -103,22 +94,17 @@ def test_sr4_ef_ten_steps_full(q):
         e_prev = err.abs()
         q.qc_encode_ef(gd, err, n, bits, bucket, 0, 1, seed, t, codes, scale, offset)
         q.qc_decode_accumulate(codes, 0, scale, offset, 0, 1, n, bits, bucket, 0, out, 0)
-        cw, sh, oh = u32(codes), host(scale), host(offset)
-        eh, dh = None, host(out)
-        eh = host(err)
-        for k in ks:
-            lo, hi = k * bucket, min(n, (k + 1) * bucket)
-            c, s, o = orc.encode_uniform(g[lo:hi], e_or[k], bits=bits, bucket=bucket, mode=1,
-                                         seed=seed, step=t, index_base=lo)
-            d = orc.decode_accumulate(c, s, o, M=1, n=hi - lo, bits=bits, bucket=bucket,
-                                      scheme=orc.SCHEME_UNIFORM)
-            w0, w1 = word_range(lo, hi, bits)
-            tag = f"step {t} bucket {k}"
-            assert_bits_equal(cw[w0:w1], c, tag + " codes")
-            assert_bits_equal(sh[k:k + 1], s, tag + " scale")
-            assert_bits_equal(oh[k:k + 1], o, tag + " offset")
-            assert_bits_equal(eh[lo:hi], e_or[k], tag + " residual")
-            assert_bits_equal(dh[lo:hi], d, tag + " decoded")
+        c, s_, o = par.encode(orc.encode_uniform, g, e_or, bucket=bucket, bits=bits, mode=1,
+                              seed=seed, step=t)
+        tag = f"step {t}"
+        assert_bits_equal(u32(codes), c, tag + " codes")
+        assert_bits_equal(host(scale), s_, tag + " scale")
+        assert_bits_equal(host(offset), o, tag + " offset")
+        if t in (0, 4, steps - 1):
+            d = par.decode(c, s_, o, M=1, n=n, bits=bits, bucket=bucket,
+                           scheme=orc.SCHEME_UNIFORM)
+            assert_bits_equal(host(err), e_or, tag + " residual")
+            assert_bits_equal(host(out), d, tag + " decoded")
         sent += out.double()
         gsum += gd.double()
         # each step rounds p = e + g once and e_new = p - deq once
@@ -174,20 +160,18 @@ def test_sign_ef_vote_full(q):
     q.qc_sign_vote(signs, words, M, n, vote)
     sh, vh, eh = u32(signs).reshape(M, words), u32(vote), host(err)
     sc = host(scale)
-    for k in sample_buckets(nb):
-        lo, hi = k * bucket, (k + 1) * bucket
-        w0, w1 = word_range(lo, hi, 1)
-        bits_or = []
-        for w in range(M):
-            e_or = np.zeros(hi - lo, dtype=np.float32)
-            c, s = orc.encode_sign(gw[w, lo:hi], e_or, bucket=bucket)
-            assert_bits_equal(sh[w, w0:w1], c, f"worker {w} bucket {k} bits")
-            pmax = float(np.abs(gw[w, lo:hi]).max())
-            assert abs(float(sc[w, k]) - float(s[0])) <= 1e-6 * pmax
-            assert np.all(np.abs(eh[w, lo:hi].astype(np.float64) - e_or) <= 1e-6 * pmax)
-            bits_or.append(c)
-        v = orc.sign_vote(np.stack(bits_or), M=M, n=hi - lo)
-        assert_bits_equal(vh[w0:w1], v, f"vote bucket {k}")
+    bits_or = np.empty((M, words), dtype=np.uint32)
+    for w in range(M):
+        e_or = np.zeros(n, dtype=np.float32)
+        c, s = par.encode(orc.encode_sign, gw[w], e_or, bucket=bucket, index=False)
+        bits_or[w] = c
+        assert_bits_equal(sh[w], c, f"worker {w} bits")
+        # the mean |p| may differ in the order of its sum only: within 1e-6 max|p|
+        pmax = np.abs(gw[w]).reshape(nb, bucket).max(axis=1).astype(np.float64)
+        assert np.all(np.abs(sc[w].astype(np.float64) - s) <= 1e-6 * pmax), f"worker {w} scale"
+        de = np.abs(eh[w].astype(np.float64) - e_or).reshape(nb, bucket).max(axis=1)
+        assert np.all(de <= 1e-6 * pmax), f"worker {w} residual"
+    assert_bits_equal(vh, par.sign_vote(bits_or, M=M, n=n), "vote")
     # the whole vote is the majority of the GPU's own sign vectors
     bitsum = torch.zeros((words, 32), dtype=torch.int32, device="cuda")
     shifts = torch.arange(32, device="cuda", dtype=torch.int64)
@@ -208,34 +192,30 @@ def test_allreduce_receiver_full(q, scheme):
     sch, bits, mode = (0, 8, 0) if scheme == "u8" else (2, 2, 1)
     codes, scale, offset = q.alloc_payload(n, bits, bucket, sch, workers=M)
     out = torch.empty(n, device="cuda")
-    for w in range(M):
-        q.qc_encode_ef(g[w], None, n, bits, bucket, sch, mode, seed | (w << 32), 0, codes[w],
-                       scale[w], offset[w] if offset is not None else None,
-                       dtype=q.QC_DTYPE_BF16)
+    # the benchmark's call: the 16 workers as the segments of one launch, worker
+    # w's draws indexed w * n + i under the one seed
+    q.qc_encode_ef_segments([(g[w], None, n, codes[w], scale[w],
+                              offset[w] if offset is not None else None) for w in range(M)],
+                            q.QC_DTYPE_BF16, bits, bucket, sch, mode, seed, 0)
     q.qc_decode_accumulate(codes, codes.stride(0), scale, offset, scale.stride(0), M, n, bits,
                            bucket, sch, out, q.QC_OUT_MEAN)
     ch = u32(codes).reshape(M, -1)
     sh = host(scale)
     oh = host(offset) if offset is not None else None
-    dh = host(out)
-    for k in sample_buckets(nb):
-        lo, hi = k * bucket, (k + 1) * bucket
-        w0, w1 = word_range(lo, hi, bits)
-        cs, ss, os_ = [], [], []
-        for w in range(M):
-            if sch == 0:
-                c, s, o = orc.encode_uniform(gb[w, lo:hi], None, bits=8, bucket=bucket,
-                                             index_base=lo)
-                assert_bits_equal(oh[w, k:k + 1], o)
-                os_.append(o)
-            else:
-                c, s = orc.encode_ternary(gb[w, lo:hi], None, bucket=bucket, mode=1,
-                                          seed=seed | (w << 32), step=0, index_base=lo)
-            assert_bits_equal(ch[w, w0:w1], c, f"{scheme} worker {w} bucket {k} codes")
-            assert_bits_equal(sh[w, k:k + 1], s, f"{scheme} worker {w} bucket {k} scale")
-            cs.append(c)
-            ss.append(s)
-        d = orc.decode_accumulate(np.stack(cs), np.stack(ss), np.stack(os_) if os_ else None,
-                                  M=M, n=hi - lo, bits=bits, bucket=bucket, scheme=sch,
-                                  flags=orc.OUT_MEAN)
-        assert_bits_equal(dh[lo:hi], d, f"{scheme} bucket {k} mean")
+    cs, ss, os_ = [], [], []
+    for w in range(M):
+        if sch == 0:
+            c, s, o = par.encode(orc.encode_uniform, gb[w], None, bucket=bucket, bits=8,
+                                 base=w * n)
+            assert_bits_equal(oh[w], o, f"{scheme} worker {w} offset")
+            os_.append(o)
+        else:
+            c, s = par.encode(orc.encode_ternary, gb[w], None, bucket=bucket, mode=1, seed=seed,
+                              step=0, base=w * n)
+        assert_bits_equal(ch[w], c, f"{scheme} worker {w} codes")
+        assert_bits_equal(sh[w], s, f"{scheme} worker {w} scale")
+        cs.append(c)
+        ss.append(s)
+    d = par.decode(np.stack(cs), np.stack(ss), np.stack(os_) if os_ else None, M=M, n=n,
+                   bits=bits, bucket=bucket, scheme=sch, flags=orc.OUT_MEAN)
+    assert_bits_equal(host(out), d, f"{scheme} mean")
