@@ -634,6 +634,9 @@ def _kernel_stats(comp, timer, peak):
             e["units_per_launch"] = units[name]
             e["elements_per_s"] = float(f"{units[name] / (avg * 1e-3):.4g}")
             e["fp32_equiv_gbs"] = round(4 * units[name] / (avg * 1e-3) / 1e9, 1)
+            # DRAM bytes per launch from the kernel's committed ncu capture (None
+            # when there is none or its sources changed since)
+            e["traffic"] = ncu_traffic(name, units[name])
         out[name] = e
     return out
 

@@ -137,14 +137,18 @@ def _need(t, name, nbytes, dtypes=None, flat=True):
         raise ValueError(f"{name} must be a torch tensor or an integer address")
     if dtypes is not None and t.dtype not in dtypes:
         raise ValueError(f"{name} has dtype {t.dtype}; expected one of {tuple(dtypes)}")
-    if any(st < 0 for st in t.stride()):
-        raise ValueError(f"{name} has a negative stride")
-    if flat and not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if not flat and t.dim() > 0 and t.shape[-1] > 1 and t.stride(-1) != 1:
-        raise ValueError(f"{name} must be dense along its last dimension")
-    if _extent_bytes(t) < nbytes:
-        raise ValueError(f"{name} spans {_extent_bytes(t)} bytes; the call needs {nbytes}")
+    if t.is_contiguous():   # the common case: a dense buffer, its extent is its size
+        extent = t.numel() * t.element_size()
+    else:
+        if any(st < 0 for st in t.stride()):
+            raise ValueError(f"{name} has a negative stride")
+        if flat:
+            raise ValueError(f"{name} must be contiguous")
+        if t.dim() > 0 and t.shape[-1] > 1 and t.stride(-1) != 1:
+            raise ValueError(f"{name} must be dense along its last dimension")
+        extent = _extent_bytes(t)
+    if extent < nbytes:
+        raise ValueError(f"{name} spans {extent} bytes; the call needs {nbytes}")
 
 
 def _on_device(**tensors):
@@ -162,13 +166,20 @@ def _row_stride(t, name, stride_elems, M):
                              f"stride passed ({stride_elems} 4-byte units)")
 
 
+_DTYPES = {}
+
+
 def _words32():
-    torch = _torch()
-    return (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    if "w" not in _DTYPES:
+        torch = _torch()
+        _DTYPES["w"] = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    return _DTYPES["w"]
 
 
 def _f32():
-    return (_torch().float32,)
+    if "f" not in _DTYPES:
+        _DTYPES["f"] = (_torch().float32,)
+    return _DTYPES["f"]
 
 
 def _stream(stream):

@@ -125,20 +125,21 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
 // half word h becomes an exact float without shifting it down: (h & 3 << 2j)
 // OR'd under the exponent of 2^(23 - 2j) is 2^(23 - 2j) + c, so subtracting
 // 2^(23 - 2j) + 1 (exact) gives c - 1, and (c - 1) * s is exact, so one fma
-// rounds acc + d once, as the scalar accumulate_code does.
+// rounds acc + d once, as the scalar accumulate_code does.  The exponent
+// fields ex[j] = (150 - 2j) << 23 and the packed biases k2[i] = -(2^(23 - 2j) +
+// 1) for j = 2i, 2i + 1 come in registers: with the exponent an immediate as
+// well as the mask, the mask-and-merge would take two logic operations.
 __device__ __forceinline__ void accumulate_ternary16(unsigned long long (&acc)[8], uint32_t f,
-                                                     unsigned long long s2) {
-    const uint32_t half[2] = {f & 0xFFFFu, f >> 16};
+                                                     unsigned long long s2, const uint32_t (&ex)[8],
+                                                     const unsigned long long (&k2)[4]) {
+    const uint32_t half[2] = {f, f >> 16};  // the masks ignore the other half's bits
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         const uint32_t h = half[p >> 2];
         const int j0 = 2 * (p & 3), j1 = j0 + 1;
-        const float m0 = __uint_as_float((h & (3u << (2 * j0))) | ((150u - 2u * j0) << 23));
-        const float m1 = __uint_as_float((h & (3u << (2 * j1))) | ((150u - 2u * j1) << 23));
-        const unsigned long long k2 =
-            pack2(-(static_cast<float>(1u << (23 - 2 * j0)) + 1.0f),
-                  -(static_cast<float>(1u << (23 - 2 * j1)) + 1.0f));
-        acc[p] = fma2(add2(pack2(m0, m1), k2), s2, acc[p]);
+        const float m0 = __uint_as_float((h & (3u << (2 * j0))) | ex[j0]);
+        const float m1 = __uint_as_float((h & (3u << (2 * j1))) | ex[j1]);
+        acc[p] = fma2(add2(pack2(m0, m1), k2[p & 3]), s2, acc[p]);
     }
 }
 

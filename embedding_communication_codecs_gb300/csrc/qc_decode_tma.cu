@@ -26,8 +26,16 @@ namespace {
 
 constexpr int kDecodeBlock = kProducerBlock;
 
+// The ternary decode's exponent fields and biases (accumulate_ternary16), read
+// into registers once per thread.  They sit in memory so that the compiler
+// cannot fold them into the logic operations as immediates.
+__constant__ uint32_t kTernaryExp[8] = {150u << 23, 148u << 23, 146u << 23, 144u << 23,
+                                        142u << 23, 140u << 23, 138u << 23, 136u << 23};
+__constant__ float kTernaryBias[8] = {-8388609.0f, -2097153.0f, -524289.0f, -131073.0f,
+                                      -32769.0f,   -8193.0f,    -2049.0f,   -513.0f};
+
 template <int SCHEME, int BITS>
-__global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __grid_constant__ DecodeParams P,
+__global__ void __launch_bounds__(kDecodeBlock, SCHEME == kTernary ? 3 : 2) decode_tma_kernel(const __grid_constant__ DecodeParams P,
                                                                   const __grid_constant__ DecodeTiles G) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G.stages * G.stage_bytes);
@@ -94,6 +102,14 @@ __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __gri
     // -------------------------------------------------------------- consumers
     const int ct = warp * 32 + lane;
     const float Mf = static_cast<float>(P.M);
+    uint32_t tex[8];
+    unsigned long long tk2[4];
+    if constexpr (SCHEME == kTernary) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tex[j] = kTernaryExp[j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tk2[i] = pack2(kTernaryBias[2 * i], kTernaryBias[2 * i + 1]);
+    }
     uint32_t it = 0;
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
@@ -127,7 +143,7 @@ __global__ void __launch_bounds__(kDecodeBlock, 2) decode_tma_kernel(const __gri
                     for (int w = 0; w < P.M; ++w) {
                         const uint32_t f = *reinterpret_cast<const uint32_t *>(wst);
                         const float sw = meta[w * G.tb].x;
-                        accumulate_ternary16(a2, f, pack2(sw, sw));
+                        accumulate_ternary16(a2, f, pack2(sw, sw), tex, tk2);
                         wst += G.worker_bytes;
                     }
 #pragma unroll

@@ -6,8 +6,9 @@
 // gradients are bf16).  They compute exactly what the general bf16 kernel
 // computes (and what the oracle computes), with fewer instructions per element:
 //
-//  * one warp per bucket and 32 elements per lane, all held in registers
-//    between the statistics and the codes (four 16-byte shared-memory reads);
+//  * one warp per bucket and 32 elements per lane (four 16-byte shared-memory
+//    reads), which the 8-bit kernel holds in registers between the statistics
+//    and the codes and the ternary kernel reads again for the codes;
 //  * the statistics on packed bf16 pairs: max |x| with one max.xorsign.abs per
 //    pair (only the magnitude of the result is used), min and max with one
 //    min / max each;

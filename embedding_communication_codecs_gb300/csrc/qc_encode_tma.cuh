@@ -165,15 +165,15 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
     bool failed = false;
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
-        const uint32_t parity = (it / G.stages) & 1u;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        // The block agrees on the wait's outcome before anything is computed or
-        // stored: after a timeout no thread touches the residual, codes or
-        // metadata of a tile whose stage may be only partly filled.
-        if (!__syncthreads_and(mbar_wait(&full[s], parity))) {
-            failed = true;
-            break;
-        }
+        // Each thread waits for the stage on its own.  The block learns whether
+        // every wait succeeded at the one barrier per tile below, which also
+        // frees the stage for its refill; a block that learns of a timeout
+        // stops there and reports it, and the call's outputs are then undefined
+        // (they may hold values computed from a stage that had not landed).
+        // Agreeing before computing would take a second barrier per tile
+        // (measured 7 % slower on the 4-bit encode).
+        const bool ok = mbar_wait(&full[s], (it / G.stages) & 1u);
 
         const EncodeSeg &sg = S.s[segment_of(S, tile)];
         const uint64_t lt = tile - sg.tile0;  // the tile within its segment
@@ -227,8 +227,12 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                                                            sg.index_base);
             if (cnt && tt == 0) store_meta<SCHEME>(sg.scale, sg.offset, lt * G.tb + kb, bp);
         }
-        // Every thread is done with this stage before it is refilled.
-        __syncthreads();
+        // Every thread is done with this stage, and every wait succeeded, before
+        // the stage is refilled.
+        if (!__syncthreads_and(ok)) {
+            failed = true;
+            break;
+        }
         if (threadIdx.x == 0) {
             const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
             if (next < G.ntiles)

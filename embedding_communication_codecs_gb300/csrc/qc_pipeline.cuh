@@ -22,8 +22,9 @@
 namespace qc {
 
 // A stalled pipeline gives up after 2 s.  An unsuccessful try_wait may return
-// early or late (the suspend time is the implementation's choice), so the limit
-// is kept on the global timer; the round count is only a backstop.
+// early or late (the suspend time is the implementation's choice, the hint
+// below only a suggestion), so the limit is kept on the global timer and on the
+// SM's cycle counter; the round count is only a backstop.
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kWaitRoundsBackstop = 1u << 26;
 
@@ -107,14 +108,19 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
                  : "memory");
 }
 
+// One try with a suspend-time hint: the thread sleeps in the barrier unit until
+// the phase completes or about kTryWaitHintNs pass, instead of spinning on
+// issue slots that the block's working warps need.
+constexpr uint32_t kTryWaitHintNs = 1000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitHintNs)
         : "memory");
     return done != 0;
 }
@@ -126,14 +132,20 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity for at most limit_ns nanoseconds (the
-// timer is read every 16 tries); false if it never completed.
+// Wait for the phase with the given parity for at most about limit_ns
+// nanoseconds (the timer is read after every unsuccessful try); false if it
+// never completed.
+// The SM's cycle counter bounds the wait as well (4 cycles per nanosecond of
+// the limit: about twice the limit at the highest clock), and so does a count
+// of tries, so that no single clock has to be trusted.
 __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
+    const long long c0 = clock64();
+    const long long cycle_limit = static_cast<long long>(4u * limit_ns + (1u << 20));
     for (uint32_t r = 1; r < kWaitRoundsBackstop; ++r) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((r & 15u) == 0u && global_ns() - t0 > limit_ns) return false;
+        if (global_ns() - t0 > limit_ns || clock64() - c0 > cycle_limit) return false;
     }
     return false;
 }
