@@ -749,6 +749,24 @@ __device__ __forceinline__ void team_reduce(Stats<SCHEME> &st, Stats<SCHEME> (*r
     }
 }
 
+// team_reduce for the pipelined kernels, which also tells the team whether every
+// thread's wait for the stage succeeded (ok): the warp's vote when a team is one
+// warp, else the block barrier that the exchange needs anyway (then block-wide).
+template <int SCHEME>
+__device__ __forceinline__ bool team_reduce_ok(Stats<SCHEME> &st, Stats<SCHEME> (*red)[kBlock / 32],
+                                               int &buf, int W, int warp, int lane, int team,
+                                               bool ok) {
+    st.warp_reduce();
+    if (W > 1) {
+        if (lane == 0) red[buf][warp] = st;
+        ok = __syncthreads_and(ok) != 0;
+        st = red[buf][team * W];
+        for (int w = 1; w < W; ++w) st.merge(red[buf][team * W + w]);
+        buf ^= 1;
+        return ok;
+    }
+    return __all_sync(kFull, ok);
+}
 
 // Team-wide reduction like team_reduce, synchronised only within the team
 // (team_sync), so teams proceed independently.  Every thread of the team calls

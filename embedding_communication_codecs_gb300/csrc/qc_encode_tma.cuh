@@ -166,13 +166,14 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        // Each thread waits for the stage on its own.  The block learns whether
-        // every wait succeeded at the one barrier per tile below, which also
-        // frees the stage for its refill; a block that learns of a timeout
-        // stops there and reports it, and the call's outputs are then undefined
-        // (they may hold values computed from a stage that had not landed).
-        // Agreeing before computing would take a second barrier per tile
-        // (measured 7 % slower on the 4-bit encode).
+        // Each thread waits for the stage on its own.  A team learns whether
+        // all of its waits succeeded from the reduction of its statistics (the
+        // warp's vote, or the block barrier that a multi-warp team's exchange
+        // takes anyway), before it stores anything: a team that learns of a
+        // timeout stores no codes, metadata or residual for the tile.  The
+        // block learns it at the one barrier per tile below, which also frees
+        // the stage for its refill, and stops there.  (A separate agreement
+        // barrier before the compute measured 7 % slower on the 4-bit encode.)
         const bool ok = mbar_wait(&full[s], (it / G.stages) & 1u);
 
         const EncodeSeg &sg = S.s[segment_of(S, tile)];
@@ -199,7 +200,9 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                 load_slots_staged<TIn, EF>(sg, G, stage, t0, b_off, cnt, staged, tt, team_threads, p);
                 if constexpr (SCHEME != kClip) accumulate_slots<SCHEME>(st, p, tt, team_threads, cnt);
             }
+            bool team_ok;
             if constexpr (SCHEME == kClip) {
+                team_ok = __syncthreads_and(ok) != 0;  // the selection has no block barrier of its own
                 uint32_t *region = hist + team * sel_region_words(P.bucket);
                 if (whole)
                     team_percentiles<true>(p, cnt, P.bucket, tt, team_threads, W, team, warp % W,
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                     team_percentiles<false>(p, cnt, P.bucket, tt, team_threads, W, team, warp % W,
                                             lane, region, sel_parity, st.mn, st.mx);
             } else {
-                team_reduce<SCHEME>(st, red, buf, W, warp, lane, team);
+                team_ok = team_reduce_ok<SCHEME>(st, red, buf, W, warp, lane, team, ok);
             }
             BucketParams bp = Finish<SCHEME, BITS>::run(st, cnt);
             if constexpr (SCHEME == kQsgd) {
@@ -217,6 +220,7 @@ __global__ void __launch_bounds__(kBlock) encode_tma_kernel(const __grid_constan
                                                                             red, W, warp, lane, team));
                 }
             }
+            if (!team_ok) continue;  // a wait timed out: store nothing (the block stops below)
             if (whole)
                 quantize_store_slots<SCHEME, BITS, SR, EF, true>(sg.codes, sg.err, t0 + b_off, cnt, tt,
                                                                  team_threads, lane, p, bp, P.step,

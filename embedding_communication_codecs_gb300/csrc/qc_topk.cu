@@ -222,10 +222,12 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
     for (uint64_t tile = blockIdx.x; tile < G.ntiles; tile += gridDim.x, ++it) {
         const uint32_t s = it % G.stages;
         const unsigned char *stage = smem + s * G.stage_bytes;
-        // as in the pipelined encode: one barrier per tile, after the tile,
-        // both frees the stage and tells the block whether every wait succeeded
-        // (after a reported timeout the call's outputs are undefined)
-        const bool ok = mbar_wait(&full[s], (it / G.stages) & 1u);
+        // the block agrees on the wait's outcome before computing or storing
+        // anything (the selection is the bound here, not this barrier)
+        if (!__syncthreads_and(mbar_wait(&full[s], (it / G.stages) & 1u))) {
+            failed = true;
+            break;
+        }
         const uint64_t t0 = tile * G.te;
         const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(G.te), P.n - t0));
         const uint32_t staged = staged_elems<TIn, EF>(tcnt);
@@ -246,10 +248,7 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
                                            region, tot, red, buf, parity);
             }
         }
-        if (!__syncthreads_and(ok)) {  // every thread is done with this stage; every wait succeeded
-            failed = true;
-            break;
-        }
+        __syncthreads();  // every thread is done with this stage before it is refilled
         if (threadIdx.x == 0) {
             const uint64_t next = tile + static_cast<uint64_t>(G.stages) * gridDim.x;
             if (next < G.ntiles) issue_seg_tile<TIn, EF>(seg, G, next, smem + s * G.stage_bytes, &full[s]);

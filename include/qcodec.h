@@ -385,11 +385,13 @@ qc_status qc_rowwise_fp8_dequant(const uint8_t *codes, const float *row_scale, s
  * qc_take_device_errors -- device-side failures of the pipelined kernels.
  *
  * The kernels that stream tiles through shared memory wait on mbarriers for at
- * most 2 s of the GPU's global timer; a wait that runs out stops its block and
+ * most 2 s (of the GPU's global timer, and of its SM cycle counter); a wait that runs out stops its block and
  * sets a flag in device memory instead of spinning forever.  This call
  * synchronises the current device, stores the OR of the flags set since the
  * previous call in *flags (bit 0: a pipeline wait timed out; the outputs of
- * that launch are incomplete) and clears them, each flag in one atomic
+ * that launch are incomplete: the tiles whose wait timed out, and the ones after
+ * them in that block, are not written, so an encode's residual keeps its old
+ * values there) and clears them, each flag in one atomic
  * exchange, so a flag set concurrently is reported by this call or the next,
  * never lost.  A CUDA error while reading them returns QC_ERR_CUDA.  It is a
  * diagnostic call: it blocks the host and must not be used inside stream
