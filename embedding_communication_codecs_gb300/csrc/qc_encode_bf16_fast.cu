@@ -424,13 +424,31 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                     uint32_t f0 = 0u, f1 = 0u;
                     bool near = true;
                     if (fast) u8_fields(raw[sl], bp.a, rinv, f0, f1, near);
-                    if (near) {  // rare: recompute the slot with the division
+                    if (near) {  // rare: the flagged elements with the division
                         const uint32_t h[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
-                        f0 = f1 = 0u;
+                        uint32_t redo = 0xFFu;  // scales outside the fast range: all eight
+                        if (fast) {
+                            // with bf16 data a flagged slot holds one or two elements
+                            // near a half-integer (often an exact tie of the quotient)
+                            constexpr float kMagic = 12582912.0f;
+                            redo = 0u;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            f0 |= code_exact<kUniform, 8, false>(bf16_at(h[c >> 1], c & 1), 0.0f, bp) << (8 * c);
-                            f1 |= code_exact<kUniform, 8, false>(bf16_at(h[2 + (c >> 1)], c & 1), 0.0f, bp) << (8 * c);
+                            for (int c = 0; c < 8; ++c) {
+                                const float d = (c & 1) ? bf16_sub<1>(h[c >> 1], bp.a) : bf16_sub<0>(h[c >> 1], bp.a);
+                                const float yf = __fmaf_rn(d, rinv, kMagic);
+                                const float dist = __fmaf_rn(d, rinv, -__fsub_rn(yf, kMagic));
+                                redo |= (fabsf(dist) >= 0.5f - 0x1p-12f ? 1u : 0u) << c;
+                            }
+                        }
+                        while (redo != 0u) {  // a loop, so the common path is not predicated with it
+                            const int c = __ffs(redo) - 1;
+                            redo &= redo - 1u;
+                            const uint32_t hw = c < 2 ? h[0] : c < 4 ? h[1] : c < 6 ? h[2] : h[3];
+                            const float v = __uint_as_float((c & 1) ? (hw & 0xFFFF0000u) : (hw << 16));
+                            const uint32_t code = code_exact<kUniform, 8, false>(v, 0.0f, bp);
+                            const uint32_t sh = 8u * static_cast<uint32_t>(c & 3);
+                            if (c < 4) f0 = (f0 & ~(0xFFu << sh)) | (code << sh);
+                            else f1 = (f1 & ~(0xFFu << sh)) | (code << sh);
                         }
                     }
                     __stcs(reinterpret_cast<uint2 *>(sg.codes + i0 / 4u), make_uint2(f0, f1));
