@@ -401,17 +401,19 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             qf = __fsub_rn(y, kMagic);
             redo = fabsf(__fsub_rn(ta, qf)) >= 0.5f - fq.delta2;
         } else {
-            // floor(ta) = rint(ta - 1/2) unless ta is an integer, which the
-            // check below sends to the exact path anyway.
-            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
-            q = __float_as_uint(y) - 0x4B400000u;
-            const float ff = __fsub_rn(y, kMagic);
-            const float fr = __fsub_rn(ta, ff);  // ta - floor(ta), exact
-            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
-                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
-            const bool up = u < fr;
-            q += up ? 1u : 0u;
-            qf = up ? __fadd_rn(ff, 1.0f) : ff;
+            // floor(t) + [u < t - floor(t)] = ceil(t - u): one decision instead
+            // of two.  x = fl(ta - u) is within delta2 of t - u (ta's bound and
+            // the subtraction's rounding, (L + 1) 2^-24 at most), so ceil(x) is
+            // the level unless x lies within delta2 of an integer (then the exact
+            // path decides).  x > -1, and rint(x) = -1 wraps to 0 with the +1.
+            const float x = __fsub_rn(ta, u);
+            const float y = __fadd_rn(x, kMagic);  // rint(x) in the low mantissa bits
+            const float rf = __fsub_rn(y, kMagic);
+            const float dx = __fsub_rn(x, rf);     // exact
+            const bool up = dx > 0.0f;             // ceil(x) = rint(x) + [x > rint(x)]
+            q = __float_as_uint(y) - 0x4B400000u + (up ? 1u : 0u);
+            qf = up ? __fadd_rn(rf, 1.0f) : rf;
+            redo = fabsf(dx) <= fq.delta2;
         }
         // no clamp: 0 <= ta <= L (1 + 2^-22), so a level above L needs ta within
         // reach of L + 1/2 (impossible) or of the integer L (flagged by redo).
@@ -429,16 +431,15 @@ __device__ __forceinline__ uint32_t quantize_fast(float p, float u, const Bucket
             q = __float_as_uint(y) - 0x4B400000u;
             qf = __fsub_rn(y, kMagic);
             redo = fabsf(__fsub_rn(ta, qf)) >= 0.5f - fq.delta2;
-        } else {
-            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
-            q = __float_as_uint(y) - 0x4B400000u;
-            const float ff = __fsub_rn(y, kMagic);
-            const float fr = __fsub_rn(ta, ff);
-            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
-                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
-            const bool up = u < fr;
-            q += up ? 1u : 0u;
-            qf = up ? __fadd_rn(ff, 1.0f) : ff;
+        } else {  // ceil(ta - u), as for the uniform levels
+            const float x = __fsub_rn(ta, u);
+            const float y = __fadd_rn(x, kMagic);
+            const float rf = __fsub_rn(y, kMagic);
+            const float dx = __fsub_rn(x, rf);
+            const bool up = dx > 0.0f;
+            q = __float_as_uint(y) - 0x4B400000u + (up ? 1u : 0u);
+            qf = up ? __fadd_rn(rf, 1.0f) : rf;
+            redo = fabsf(dx) <= fq.delta2;
         }
         // no clamp: t <= S (1 + 2^-22); a level above S would be flagged by redo
         // (the mask keeps a non-finite element's code inside its own field)
@@ -489,15 +490,12 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
             const float y = __fadd_rn(ta, kMagic);  // rint(ta) in the low mantissa bits
             q = __float_as_uint(y) - 0x4B400000u;
             redo = fabsf(__fsub_rn(ta, __fsub_rn(y, kMagic))) >= 0.5f - fq.delta2;
-        } else {
-            // floor(ta) = rint(ta - 1/2) unless ta is an integer, which the
-            // check below sends to the exact path anyway.
-            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
-            q = __float_as_uint(y) - 0x4B400000u;
-            const float fr = __fsub_rn(ta, __fsub_rn(y, kMagic));  // ta - floor(ta), exact
-            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
-                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
-            q += (u < fr) ? 1u : 0u;
+        } else {  // ceil(ta - u) (see quantize_fast)
+            const float x = __fsub_rn(ta, u);
+            const float y = __fadd_rn(x, kMagic);
+            const float dx = __fsub_rn(x, __fsub_rn(y, kMagic));
+            redo = fabsf(dx) <= fq.delta2;
+            q = __float_as_uint(y) - 0x4B400000u + (dx > 0.0f ? 1u : 0u);
         }
         return q & ((1u << BITS) - 1u);  // no clamp needed outside redo (see quantize_fast)
     } else if constexpr (SCHEME == kTernary) {
@@ -521,13 +519,12 @@ __device__ __forceinline__ uint32_t code_fast(float p, float u, const BucketPara
             const float y = __fadd_rn(ta, kMagic);
             q = __float_as_uint(y) - 0x4B400000u;
             redo = fabsf(__fsub_rn(ta, __fsub_rn(y, kMagic))) >= 0.5f - fq.delta2;
-        } else {
-            const float y = __fadd_rn(__fsub_rn(ta, 0.5f), kMagic);
-            q = __float_as_uint(y) - 0x4B400000u;
-            const float fr = __fsub_rn(ta, __fsub_rn(y, kMagic));
-            redo = (fabsf(__fsub_rn(fr, 0.5f)) >= 0.5f - fq.delta2) |
-                   (fabsf(__fsub_rn(u, fr)) <= fq.delta2);
-            q += (u < fr) ? 1u : 0u;
+        } else {  // ceil(ta - u)
+            const float x = __fsub_rn(ta, u);
+            const float y = __fadd_rn(x, kMagic);
+            const float dx = __fsub_rn(x, __fsub_rn(y, kMagic));
+            redo = fabsf(dx) <= fq.delta2;
+            q = __float_as_uint(y) - 0x4B400000u + (dx > 0.0f ? 1u : 0u);
         }
         return ((p < 0.0f ? 1u : 0u) << (BITS - 1)) | (q & ((1u << (BITS - 1)) - 1u));  // no clamp outside redo
     } else if constexpr (SCHEME == kLog) {
