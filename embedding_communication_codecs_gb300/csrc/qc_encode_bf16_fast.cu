@@ -35,13 +35,14 @@ namespace {
 
 constexpr uint32_t kB = 1024;                        // bucket
 constexpr int kWarps = kBlock / 32;                  // one bucket per warp
-constexpr uint32_t kTile = kB * kWarps;              // elements per tile
-constexpr uint32_t kStageBytes = kTile * 2u;         // 16 KB of bf16
+constexpr uint32_t kPerWarp = 2;                     // buckets per warp and tile
+constexpr uint32_t kTile = kB * kWarps * kPerWarp;   // elements per tile
+constexpr uint32_t kStageBytes = kTile * 2u;         // 32 KB of bf16
 
 constexpr int kU8 = 0;       // 8-bit uniform, round to nearest
 constexpr int kTern = 1;     // ternary, stochastic rounding
 
-constexpr uint32_t kStages = 3;
+constexpr uint32_t kStages = 2;
 constexpr size_t kSmem = kStages * kStageBytes + kStages * 8u + 2u * kStages * 4u;
 
 // A 16-byte shared-memory load the compiler may not merge with an earlier one.
@@ -349,117 +350,121 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
         const uint64_t t0 = lt * kTile;
         const uint32_t tcnt = static_cast<uint32_t>(min(static_cast<uint64_t>(kTile), sg.n - t0));
         const uint32_t staged = floor16(static_cast<uint64_t>(tcnt) * 2u) / 2u;
-        const uint32_t b_off = static_cast<uint32_t>(warp) * kB;
-        const uint32_t cnt = b_off < tcnt ? min(kB, tcnt - b_off) : 0u;
-        const uint64_t b0 = t0 + b_off;            // the bucket's first element in its segment
-        const uint64_t d0 = sg.index_base + b0;    // ... and its draw index
-        const uint64_t k = lt * kWarps + warp;
+        // the warp's buckets of the tile, kWarps apart, so that the tile's
+        // bookkeeping (wait, segment, counts, refill) is paid once for several
+        for (uint32_t bb = 0; bb < kPerWarp; ++bb) {
+            const uint32_t b_off = (bb * kWarps + static_cast<uint32_t>(warp)) * kB;
+            const uint32_t cnt = b_off < tcnt ? min(kB, tcnt - b_off) : 0u;
+            const uint64_t b0 = t0 + b_off;            // the bucket's first element in its segment
+            const uint64_t d0 = sg.index_base + b0;    // ... and its draw index
+            const uint64_t k = lt * (kWarps * kPerWarp) + bb * kWarps + warp;
 
-        if (cnt == kB && b_off + kB <= staged) {
-            auto slot = [&](int sl) {
-                return *reinterpret_cast<const uint4 *>(stage + (b_off + (sl * 32 + lane) * 8u) * 2u);
-            };
-            if constexpr (KIND == kTern) {
-                // ---- s = max |x|, on packed pairs (only the magnitudes count)
-                uint32_t a = 0u;
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const uint4 r = slot(sl);
-                    a = absmax_bf16x2(a, absmax_bf16x2(r.x, r.y));
-                    a = absmax_bf16x2(a, absmax_bf16x2(r.z, r.w));
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) a = absmax_bf16x2(a, __shfl_xor_sync(kFull, a, o));
-                a &= 0x7FFF7FFFu;
-                const float s_ = fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
-                const bool fast = s_ >= 0x1p-125f && s_ <= 0x1p125f;
-                const float rinv = fast ? recip(s_) : 0.0f;
-                // ---- codes, 8 elements per slot, two lanes per code word; the slot
-                // is read from the stage again rather than kept in registers
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const uint32_t j = (sl * 32 + lane) * 8u;
-                    const uint64_t i0 = b0 + j;
-                    const uint32_t blk = static_cast<uint32_t>((d0 + j) >> 2);  // draws < 2^34
-                    const uint4 da = philox_blk(blk, K), db = philox_blk(blk + 1u, K);
-                    const uint4 r = lds128(stage + (b_off + j) * 2u);
-                    uint32_t field = 0u;
-                    bool near = true;
-                    if (fast) field = ternary_field8(r, da, db, rinv, near);
-                    if (near) field = ternary_slot_exact(r, s_, d0 + j, P);  // rare
-                    field |= __shfl_down_sync(kFull, field, 1) << 16;
-                    if ((lane & 1) == 0) __stcs(sg.codes + i0 / 16u, field);
-                }
-                if (lane == 0) sg.scale[k] = s_;
-            } else {
-                uint4 raw[4];
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) raw[sl] = slot(sl);
-                // ---- min and max, on packed pairs
-                uint32_t lo = min_bf16x2(raw[0].x, raw[0].y), hi = max_bf16x2(raw[0].x, raw[0].y);
-                lo = min_bf16x2(lo, min_bf16x2(raw[0].z, raw[0].w));
-                hi = max_bf16x2(hi, max_bf16x2(raw[0].z, raw[0].w));
-#pragma unroll
-                for (int sl = 1; sl < 4; ++sl) {
-                    lo = min_bf16x2(lo, min_bf16x2(raw[sl].x, raw[sl].y));
-                    hi = max_bf16x2(hi, max_bf16x2(raw[sl].x, raw[sl].y));
-                    lo = min_bf16x2(lo, min_bf16x2(raw[sl].z, raw[sl].w));
-                    hi = max_bf16x2(hi, max_bf16x2(raw[sl].z, raw[sl].w));
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    lo = min_bf16x2(lo, __shfl_xor_sync(kFull, lo, o));
-                    hi = max_bf16x2(hi, __shfl_xor_sync(kFull, hi, o));
-                }
-                Stats<kUniform> st;
-                st.mn = fminf(__uint_as_float(lo << 16), __uint_as_float(lo & 0xFFFF0000u));
-                st.mx = fmaxf(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
-                const BucketParams bp = Finish<kUniform, 8>::run(st, kB);
-                const bool fast = bp.scale >= 0x1p-125f && bp.scale <= 0x1p125f;
-                const float rinv = fast ? recip(bp.scale) : 0.0f;
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const uint32_t j = (sl * 32 + lane) * 8u;
-                    const uint64_t i0 = b0 + j;
-                    uint32_t f0 = 0u, f1 = 0u;
-                    bool near = true;
-                    if (fast) u8_fields(raw[sl], bp.a, rinv, f0, f1, near);
-                    if (near) {  // rare: the flagged elements with the division
-                        const uint32_t h[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
-                        uint32_t redo = 0xFFu;  // scales outside the fast range: all eight
-                        if (fast) {
-                            // with bf16 data a flagged slot holds one or two elements
-                            // near a half-integer (often an exact tie of the quotient)
-                            constexpr float kMagic = 12582912.0f;
-                            redo = 0u;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const float d = (c & 1) ? bf16_sub<1>(h[c >> 1], bp.a) : bf16_sub<0>(h[c >> 1], bp.a);
-                                const float yf = __fmaf_rn(d, rinv, kMagic);
-                                const float dist = __fmaf_rn(d, rinv, -__fsub_rn(yf, kMagic));
-                                redo |= (fabsf(dist) >= 0.5f - 0x1p-12f ? 1u : 0u) << c;
+            if (cnt == kB && b_off + kB <= staged) {
+                auto slot = [&](int sl) {
+                    return *reinterpret_cast<const uint4 *>(stage + (b_off + (sl * 32 + lane) * 8u) * 2u);
+                };
+                if constexpr (KIND == kTern) {
+                    // ---- s = max |x|, on packed pairs (only the magnitudes count)
+                    uint32_t a = 0u;
+    #pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) {
+                        const uint4 r = slot(sl);
+                        a = absmax_bf16x2(a, absmax_bf16x2(r.x, r.y));
+                        a = absmax_bf16x2(a, absmax_bf16x2(r.z, r.w));
+                    }
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) a = absmax_bf16x2(a, __shfl_xor_sync(kFull, a, o));
+                    a &= 0x7FFF7FFFu;
+                    const float s_ = fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
+                    const bool fast = s_ >= 0x1p-125f && s_ <= 0x1p125f;
+                    const float rinv = fast ? recip(s_) : 0.0f;
+                    // ---- codes, 8 elements per slot, two lanes per code word; the slot
+                    // is read from the stage again rather than kept in registers
+    #pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) {
+                        const uint32_t j = (sl * 32 + lane) * 8u;
+                        const uint64_t i0 = b0 + j;
+                        const uint32_t blk = static_cast<uint32_t>((d0 + j) >> 2);  // draws < 2^34
+                        const uint4 da = philox_blk(blk, K), db = philox_blk(blk + 1u, K);
+                        const uint4 r = lds128(stage + (b_off + j) * 2u);
+                        uint32_t field = 0u;
+                        bool near = true;
+                        if (fast) field = ternary_field8(r, da, db, rinv, near);
+                        if (near) field = ternary_slot_exact(r, s_, d0 + j, P);  // rare
+                        field |= __shfl_down_sync(kFull, field, 1) << 16;
+                        if ((lane & 1) == 0) __stcs(sg.codes + i0 / 16u, field);
+                    }
+                    if (lane == 0) sg.scale[k] = s_;
+                } else {
+                    uint4 raw[4];
+    #pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) raw[sl] = slot(sl);
+                    // ---- min and max, on packed pairs
+                    uint32_t lo = min_bf16x2(raw[0].x, raw[0].y), hi = max_bf16x2(raw[0].x, raw[0].y);
+                    lo = min_bf16x2(lo, min_bf16x2(raw[0].z, raw[0].w));
+                    hi = max_bf16x2(hi, max_bf16x2(raw[0].z, raw[0].w));
+    #pragma unroll
+                    for (int sl = 1; sl < 4; ++sl) {
+                        lo = min_bf16x2(lo, min_bf16x2(raw[sl].x, raw[sl].y));
+                        hi = max_bf16x2(hi, max_bf16x2(raw[sl].x, raw[sl].y));
+                        lo = min_bf16x2(lo, min_bf16x2(raw[sl].z, raw[sl].w));
+                        hi = max_bf16x2(hi, max_bf16x2(raw[sl].z, raw[sl].w));
+                    }
+    #pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        lo = min_bf16x2(lo, __shfl_xor_sync(kFull, lo, o));
+                        hi = max_bf16x2(hi, __shfl_xor_sync(kFull, hi, o));
+                    }
+                    Stats<kUniform> st;
+                    st.mn = fminf(__uint_as_float(lo << 16), __uint_as_float(lo & 0xFFFF0000u));
+                    st.mx = fmaxf(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+                    const BucketParams bp = Finish<kUniform, 8>::run(st, kB);
+                    const bool fast = bp.scale >= 0x1p-125f && bp.scale <= 0x1p125f;
+                    const float rinv = fast ? recip(bp.scale) : 0.0f;
+    #pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) {
+                        const uint32_t j = (sl * 32 + lane) * 8u;
+                        const uint64_t i0 = b0 + j;
+                        uint32_t f0 = 0u, f1 = 0u;
+                        bool near = true;
+                        if (fast) u8_fields(raw[sl], bp.a, rinv, f0, f1, near);
+                        if (near) {  // rare: the flagged elements with the division
+                            const uint32_t h[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+                            uint32_t redo = 0xFFu;  // scales outside the fast range: all eight
+                            if (fast) {
+                                // with bf16 data a flagged slot holds one or two elements
+                                // near a half-integer (often an exact tie of the quotient)
+                                constexpr float kMagic = 12582912.0f;
+                                redo = 0u;
+    #pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const float d = (c & 1) ? bf16_sub<1>(h[c >> 1], bp.a) : bf16_sub<0>(h[c >> 1], bp.a);
+                                    const float yf = __fmaf_rn(d, rinv, kMagic);
+                                    const float dist = __fmaf_rn(d, rinv, -__fsub_rn(yf, kMagic));
+                                    redo |= (fabsf(dist) >= 0.5f - 0x1p-12f ? 1u : 0u) << c;
+                                }
+                            }
+                            while (redo != 0u) {  // a loop, so the common path is not predicated with it
+                                const int c = __ffs(redo) - 1;
+                                redo &= redo - 1u;
+                                const uint32_t hw = c < 2 ? h[0] : c < 4 ? h[1] : c < 6 ? h[2] : h[3];
+                                const float v = __uint_as_float((c & 1) ? (hw & 0xFFFF0000u) : (hw << 16));
+                                const uint32_t code = code_exact<kUniform, 8, false>(v, 0.0f, bp);
+                                const uint32_t sh = 8u * static_cast<uint32_t>(c & 3);
+                                if (c < 4) f0 = (f0 & ~(0xFFu << sh)) | (code << sh);
+                                else f1 = (f1 & ~(0xFFu << sh)) | (code << sh);
                             }
                         }
-                        while (redo != 0u) {  // a loop, so the common path is not predicated with it
-                            const int c = __ffs(redo) - 1;
-                            redo &= redo - 1u;
-                            const uint32_t hw = c < 2 ? h[0] : c < 4 ? h[1] : c < 6 ? h[2] : h[3];
-                            const float v = __uint_as_float((c & 1) ? (hw & 0xFFFF0000u) : (hw << 16));
-                            const uint32_t code = code_exact<kUniform, 8, false>(v, 0.0f, bp);
-                            const uint32_t sh = 8u * static_cast<uint32_t>(c & 3);
-                            if (c < 4) f0 = (f0 & ~(0xFFu << sh)) | (code << sh);
-                            else f1 = (f1 & ~(0xFFu << sh)) | (code << sh);
-                        }
+                        __stcs(reinterpret_cast<uint2 *>(sg.codes + i0 / 4u), make_uint2(f0, f1));
                     }
-                    __stcs(reinterpret_cast<uint2 *>(sg.codes + i0 / 4u), make_uint2(f0, f1));
+                    if (lane == 0) {
+                        sg.scale[k] = bp.scale;
+                        sg.offset[k] = bp.a;
+                    }
                 }
-                if (lane == 0) {
-                    sg.scale[k] = bp.scale;
-                    sg.offset[k] = bp.a;
-                }
+            } else if (cnt) {
+                encode_partial_bucket<KIND>(P, sg, k, b0, cnt, lane);
             }
-        } else if (cnt) {
-            encode_partial_bucket<KIND>(P, sg, k, b0, cnt, lane);
         }
         // this warp is done with the stage (its reads have returned: their values
         // are used above); the warp that completes the count refills the stage
