@@ -366,13 +366,13 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                 if constexpr (KIND == kTern) {
                     // ---- s = max |x|, on packed pairs (only the magnitudes count)
                     uint32_t a = 0u;
-    #pragma unroll
+#pragma unroll
                     for (int sl = 0; sl < 4; ++sl) {
                         const uint4 r = slot(sl);
                         a = absmax_bf16x2(a, absmax_bf16x2(r.x, r.y));
                         a = absmax_bf16x2(a, absmax_bf16x2(r.z, r.w));
                     }
-    #pragma unroll
+#pragma unroll
                     for (int o = 16; o > 0; o >>= 1) a = absmax_bf16x2(a, __shfl_xor_sync(kFull, a, o));
                     a &= 0x7FFF7FFFu;
                     const float s_ = fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xFFFF0000u));
@@ -380,37 +380,41 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                     const float rinv = fast ? recip(s_) : 0.0f;
                     // ---- codes, 8 elements per slot, two lanes per code word; the slot
                     // is read from the stage again rather than kept in registers
-    #pragma unroll
+                    // per-bucket bases: slot sl of the lane is element j = 256 sl + 8 lane,
+                    // its Philox blocks (d0 + j) / 4 (draws < 2^34; d0 % 4 == 0), its
+                    // code word (b0 + j) / 16
+                    const uint32_t blk0 = static_cast<uint32_t>(d0 >> 2) + 2u * static_cast<uint32_t>(lane);
+                    const unsigned char *src = stage + (b_off + 8u * static_cast<uint32_t>(lane)) * 2u;
+                    uint32_t *dst = sg.codes + (b0 >> 4) + (lane >> 1);
+#pragma unroll
                     for (int sl = 0; sl < 4; ++sl) {
-                        const uint32_t j = (sl * 32 + lane) * 8u;
-                        const uint64_t i0 = b0 + j;
-                        const uint32_t blk = static_cast<uint32_t>((d0 + j) >> 2);  // draws < 2^34
+                        const uint32_t blk = blk0 + 64u * sl;
                         const uint4 da = philox_blk(blk, K), db = philox_blk(blk + 1u, K);
-                        const uint4 r = lds128(stage + (b_off + j) * 2u);
+                        const uint4 r = lds128(src + 512u * sl);
                         uint32_t field = 0u;
                         bool near = true;
                         if (fast) field = ternary_field8(r, da, db, rinv, near);
-                        if (near) field = ternary_slot_exact(r, s_, d0 + j, P);  // rare
+                        if (near) field = ternary_slot_exact(r, s_, d0 + 256u * sl + 8u * lane, P);  // rare
                         field |= __shfl_down_sync(kFull, field, 1) << 16;
-                        if ((lane & 1) == 0) __stcs(sg.codes + i0 / 16u, field);
+                        if ((lane & 1) == 0) __stcs(dst + 16 * sl, field);
                     }
                     if (lane == 0) sg.scale[k] = s_;
                 } else {
                     uint4 raw[4];
-    #pragma unroll
+#pragma unroll
                     for (int sl = 0; sl < 4; ++sl) raw[sl] = slot(sl);
                     // ---- min and max, on packed pairs
                     uint32_t lo = min_bf16x2(raw[0].x, raw[0].y), hi = max_bf16x2(raw[0].x, raw[0].y);
                     lo = min_bf16x2(lo, min_bf16x2(raw[0].z, raw[0].w));
                     hi = max_bf16x2(hi, max_bf16x2(raw[0].z, raw[0].w));
-    #pragma unroll
+#pragma unroll
                     for (int sl = 1; sl < 4; ++sl) {
                         lo = min_bf16x2(lo, min_bf16x2(raw[sl].x, raw[sl].y));
                         hi = max_bf16x2(hi, max_bf16x2(raw[sl].x, raw[sl].y));
                         lo = min_bf16x2(lo, min_bf16x2(raw[sl].z, raw[sl].w));
                         hi = max_bf16x2(hi, max_bf16x2(raw[sl].z, raw[sl].w));
                     }
-    #pragma unroll
+#pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
                         lo = min_bf16x2(lo, __shfl_xor_sync(kFull, lo, o));
                         hi = max_bf16x2(hi, __shfl_xor_sync(kFull, hi, o));
@@ -421,10 +425,9 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                     const BucketParams bp = Finish<kUniform, 8>::run(st, kB);
                     const bool fast = bp.scale >= 0x1p-125f && bp.scale <= 0x1p125f;
                     const float rinv = fast ? recip(bp.scale) : 0.0f;
-    #pragma unroll
+                    uint2 *dst = reinterpret_cast<uint2 *>(sg.codes + (b0 >> 2)) + lane;  // slot sl: + 32 sl
+#pragma unroll
                     for (int sl = 0; sl < 4; ++sl) {
-                        const uint32_t j = (sl * 32 + lane) * 8u;
-                        const uint64_t i0 = b0 + j;
                         uint32_t f0 = 0u, f1 = 0u;
                         bool near = true;
                         if (fast) u8_fields(raw[sl], bp.a, rinv, f0, f1, near);
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                                 // near a half-integer (often an exact tie of the quotient)
                                 constexpr float kMagic = 12582912.0f;
                                 redo = 0u;
-    #pragma unroll
+#pragma unroll
                                 for (int c = 0; c < 8; ++c) {
                                     const float d = (c & 1) ? bf16_sub<1>(h[c >> 1], bp.a) : bf16_sub<0>(h[c >> 1], bp.a);
                                     const float yf = __fmaf_rn(d, rinv, kMagic);
@@ -455,7 +458,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
                                 else f1 = (f1 & ~(0xFFu << sh)) | (code << sh);
                             }
                         }
-                        __stcs(reinterpret_cast<uint2 *>(sg.codes + i0 / 4u), make_uint2(f0, f1));
+                        __stcs(dst + 32 * sl, make_uint2(f0, f1));
                     }
                     if (lane == 0) {
                         sg.scale[k] = bp.scale;
