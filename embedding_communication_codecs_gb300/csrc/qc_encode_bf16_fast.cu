@@ -6,6 +6,8 @@
 // gradients are bf16).  They compute exactly what the general bf16 kernel
 // computes (and what the oracle computes), with fewer instructions per element:
 //
+//  * tiles of 16 buckets in 32 KB stages, two buckets per warp, so that the
+//    tile's bookkeeping (wait, segment, counts, refill) is paid once for both;
 //  * one warp per bucket and 32 elements per lane (four 16-byte shared-memory
 //    reads), which the 8-bit kernel holds in registers between the statistics
 //    and the codes and the ternary kernel reads again for the codes;
@@ -20,8 +22,9 @@
 //    differences and shifted in with one funnel shift.
 //
 // The division-free decisions keep the exact fallback of the general kernels:
-// a lane slot of 8 elements with one element within reach of a decision
-// boundary is recomputed with the IEEE division.  A bucket that is not whole
+// in a lane slot of 8 elements with an element within reach of a decision
+// boundary, the ternary kernel recomputes the slot and the 8-bit kernel the
+// flagged elements with the IEEE division.  A bucket that is not whole
 // (the last one of the array) is encoded from global memory by the same warp
 // with the exact element-wise code.
 #include "qc_encode_math.cuh"
@@ -34,7 +37,7 @@ static __device__ unsigned int g_encode_bf16_fast_errors;
 namespace {
 
 constexpr uint32_t kB = 1024;                        // bucket
-constexpr int kWarps = kBlock / 32;                  // one bucket per warp
+constexpr int kWarps = kBlock / 32;                  // warps per block
 constexpr uint32_t kPerWarp = 2;                     // buckets per warp and tile
 constexpr uint32_t kTile = kB * kWarps * kPerWarp;   // elements per tile
 constexpr uint32_t kStageBytes = kTile * 2u;         // 32 KB of bf16
