@@ -308,7 +308,7 @@ __device__ __noinline__ void encode_partial_bucket(const EncodeParams &P, const 
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __grid_constant__ EncodeParams P,
+__global__ void __launch_bounds__(kBlock, 3) encode_bf16_fast_kernel(const __grid_constant__ EncodeParams P,
                                                                    const __grid_constant__ PhiloxStep K,
                                                                    const __grid_constant__ EncodeSegs S,
                                                                    const uint64_t ntiles) {
@@ -318,6 +318,10 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
     uint32_t *issued = done + kStages;                               // tiles issued into a stage
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the folded Philox keys in registers for the whole kernel (the smem limit
+    // leaves three blocks per SM, so registers are not what bounds occupancy)
+    PhiloxStep Kr;
+    if constexpr (KIND == kTern) Kr = K;
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kBlock, 4) encode_bf16_fast_kernel(const __gri
 #pragma unroll
                     for (int sl = 0; sl < 4; ++sl) {
                         const uint32_t blk = blk0 + 64u * sl;
-                        const uint4 da = philox_blk(blk, K), db = philox_blk(blk + 1u, K);
+                        const uint4 da = philox_blk(blk, Kr), db = philox_blk(blk + 1u, Kr);
                         const uint4 r = lds128(src + 512u * sl);
                         uint32_t field = 0u;
                         bool near = true;
