@@ -265,7 +265,7 @@ class SignVote(Component):
     def __init__(self, n=25_600_000, M=8, bucket=4096, seed=3):
         self.n, self.M, self.bucket, self.seed = n, M, bucket, seed
         words, nb = _words(n, 1), _nb(n, bucket)
-        self.kernels = {"encode_sign_ef": (M, 12 * n + 4 * words + 4 * nb),
+        self.kernels = {"encode_sign_ef": (1, M * (12 * n + 4 * words + 4 * nb)),
                         "sign_vote": (1, (M + 1) * 4 * words)}
         self.units = 2 * M * n
         self.h2d = 4 * M * n
@@ -281,10 +281,13 @@ class SignVote(Component):
         self.vote = torch.empty(words, dtype=torch.int32, device="cuda")
 
     def run(self, q, t, timer):
-        for w in range(self.M):
-            with timer("encode_sign_ef"):
-                q.qc_encode_ef(self.g[w], self.err[w], self.n, 1, self.bucket, q.QC_SCHEME_SIGN,
-                               q.QC_ROUND_NEAREST, 0, t, self.signs[w], self.scale[w], None)
+        # the M workers' encodes as the segments of one launch (each with its
+        # own residual; the sign scheme draws nothing)
+        with timer("encode_sign_ef"):
+            q.qc_encode_ef_segments([(self.g[w], self.err[w], self.n, self.signs[w], self.scale[w],
+                                      None) for w in range(self.M)],
+                                    q.QC_DTYPE_F32, 1, self.bucket, q.QC_SCHEME_SIGN,
+                                    q.QC_ROUND_NEAREST, 0, t)
         with timer("sign_vote"):
             q.qc_sign_vote(self.signs, self.words, self.M, self.n, self.vote)
 
@@ -295,7 +298,7 @@ class SignVote(Component):
         return [self.vote]
 
     def kernel_units(self):
-        return {"encode_sign_ef": self.n, "sign_vote": self.M * self.n}
+        return {"encode_sign_ef": self.M * self.n, "sign_vote": self.M * self.n}
 
     def quality(self, q, torch):
         self.run(q, 10_000, KernelTimer(torch, enabled=False))

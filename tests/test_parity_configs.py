@@ -145,7 +145,8 @@ def test_ef_resume_is_bit_identical(q):
 
 def test_sign_ef_vote_full(q):
     """8 workers x 25,600,000 elements ~ N(mu, 1e-3), shared mu ~ N(0, 5e-4),
-    buckets of 4096, scaled sign with error feedback, then the vote."""
+    buckets of 4096, scaled sign with error feedback (one multi-segment launch),
+    then the vote."""
     n, M, bucket = 25_600_000, 8, 4096
     nb = n // bucket
     gw = wl.shared_mean_gradients(n, M, seed=3)
@@ -155,8 +156,9 @@ def test_sign_ef_vote_full(q):
     signs = torch.empty((M, words), dtype=torch.int32, device="cuda")
     scale = torch.empty((M, nb), device="cuda")
     vote = torch.empty(words, dtype=torch.int32, device="cuda")
-    for w in range(M):
-        q.qc_encode_ef(g[w], err[w], n, 1, bucket, 1, 0, 0, 0, signs[w], scale[w], None)
+    # the benchmark's call: the 8 workers as the segments of one launch
+    q.qc_encode_ef_segments([(g[w], err[w], n, signs[w], scale[w], None) for w in range(M)],
+                            q.QC_DTYPE_F32, 1, bucket, 1, 0, 0, 0)
     q.qc_sign_vote(signs, words, M, n, vote)
     sh, vh, eh = u32(signs).reshape(M, words), u32(vote), host(err)
     sc = host(scale)
