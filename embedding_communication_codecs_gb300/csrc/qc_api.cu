@@ -479,9 +479,9 @@ qc_status qc_encode_ef_segments(const qc_segment *segs, int nseg, qc_dtype dtype
         sc = check_encode_buffers(fn, g.grad, dtype, g.err, g.n, bits, bucket, scheme, g.codes,
                                   g.scale, g.offset);
         if (sc != QC_OK) {
-            char msg[400];
+            char msg[sizeof g_last_error];  // the message is rewritten into g_last_error
             snprintf(msg, sizeof msg, "%s", g_last_error);
-            return fail(sc, "%s (segment %d)", msg, a);
+            return fail(sc, "%.480s (segment %d)", msg, a);
         }
         total += g.n;
         if (total > (static_cast<uint64_t>(1) << 40))
