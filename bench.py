@@ -1018,6 +1018,9 @@ def run_ours(args, world, rank, local):
         if u:
             kinfo[k]["units_per_launch"] = u
             kinfo[k]["elements_per_s"] = float(f"{u / (kinfo[k]['avg_us'] * 1e-6):.4g}")
+            # DRAM bytes per launch from the kernel's committed ncu capture (None
+            # when there is none or its sources changed since)
+            kinfo[k]["traffic"] = ncu_traffic(k, u)
 
     quality = {}
     for c in comps:
