@@ -31,11 +31,107 @@ __device__ __forceinline__ uint32_t load_field(const uint32_t *words, uint64_t i
     }
 }
 
+// The outputs of one window (4 per lane and slot) from the accumulated values:
+// MEAN and accumulate flags, then the stores.
+__device__ __forceinline__ void store_window(const DecodeParams &P, float (&acc)[kSlots][4],
+                                             uint64_t b0, uint32_t w0, uint32_t cnt, int lane,
+                                             float Mf) {
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        const uint32_t j = w0 + static_cast<uint32_t>(s * 32 + lane) * 4u;
+        if (j >= cnt) continue;
+        const uint64_t i = b0 + j;
+        float4 r = make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
+        if (P.flags & 1) {
+            r = P.inv_m != 0.0f
+                    ? make_float4(__fmul_rn(r.x, P.inv_m), __fmul_rn(r.y, P.inv_m),
+                                  __fmul_rn(r.z, P.inv_m), __fmul_rn(r.w, P.inv_m))
+                    : make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf),
+                                  __fdiv_rn(r.z, Mf), __fdiv_rn(r.w, Mf));
+        }
+        if (j + 4u <= cnt) {
+            float4 *o = reinterpret_cast<float4 *>(P.out + i);
+            if (P.flags & 2) {
+                const float4 prev = __ldcs(o);
+                r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
+                                __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
+            }
+            __stcs(o, r);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (j + c < cnt) {
+                    float v = get(r, c);
+                    if (P.flags & 2) v = __fadd_rn(P.out[i + c], v);
+                    P.out[i + c] = v;
+                }
+            }
+        }
+    }
+}
+
+// One worker (M = 1): a warp's items are (bucket, window) pairs, and the code
+// fields, scale and offset of its next item are loaded before the current one
+// is dequantized and stored, so that a load is in flight while the warp works.
+template <int SCHEME, int BITS>
+__device__ __forceinline__ void decode_single(const DecodeParams &P, int lane, uint64_t first,
+                                              uint64_t warps) {
+    const uint32_t wpb = (static_cast<uint32_t>(P.bucket) + kWindowPerWarp - 1u) / kWindowPerWarp;
+    const uint64_t items = P.nbuckets * wpb;
+    const float Mf = 1.0f;
+    uint32_t f[kSlots];
+    float sc = 0.0f, of = 0.0f;
+    uint64_t b0 = 0;
+    uint32_t w0 = 0, cnt = 0;
+    auto load = [&](uint64_t t, uint32_t (&fd)[kSlots], float &s_, float &o_, uint64_t &b0_,
+                    uint32_t &w0_, uint32_t &cnt_) {
+        const uint64_t k = t / wpb;
+        w0_ = static_cast<uint32_t>(t - k * wpb) * kWindowPerWarp;
+        b0_ = k * P.bucket;
+        cnt_ = static_cast<uint32_t>(min(static_cast<uint64_t>(P.bucket), P.n - b0_));
+        s_ = __ldg(P.scale + k);
+        o_ = 0.0f;
+        if constexpr (SCHEME == kUniform) o_ = __ldg(P.offset + k);
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            const uint32_t j = w0_ + static_cast<uint32_t>(s * 32 + lane) * 4u;
+            fd[s] = (j < cnt_) ? load_field<BITS>(P.codes, b0_ + j) : 0u;
+        }
+    };
+    if (first < items) load(first, f, sc, of, b0, w0, cnt);
+    for (uint64_t t = first; t < items; t += warps) {
+        uint32_t fn[kSlots];
+        float scn = 0.0f, ofn = 0.0f;
+        uint64_t b0n = 0;
+        uint32_t w0n = 0, cntn = 0;
+        if (t + warps < items) load(t + warps, fn, scn, ofn, b0n, w0n, cntn);
+        float acc[kSlots][4];
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[s][c] = accumulate_code<SCHEME, BITS>(0.0f, f[s], c, sc, of);
+        store_window(P, acc, b0, w0, cnt, lane, Mf);
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) f[s] = fn[s];
+        sc = scn;
+        of = ofn;
+        b0 = b0n;
+        w0 = w0n;
+        cnt = cntn;
+    }
+}
+
 template <int SCHEME, int BITS>
 __global__ void __launch_bounds__(kBlock) decode_kernel(const __grid_constant__ DecodeParams P) {
     const int lane = threadIdx.x & 31;
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kBlock / 32);
     const float Mf = static_cast<float>(P.M);
+    // (QSGD keeps the plain loop: measured slower with the prefetch)
+    if (SCHEME != kQsgd && P.M == 1) {
+        decode_single<SCHEME, BITS>(P, lane, static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5),
+                                    warps);
+        return;
+    }
 
     for (uint64_t k = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
          k < P.nbuckets; k += warps) {
@@ -68,38 +164,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const __grid_constant__ 
                         acc[s][c] = accumulate_code<SCHEME, BITS>(acc[s][c], field[s], c, sc, of);
             }
 
-#pragma unroll
-            for (int s = 0; s < kSlots; ++s) {
-                const uint32_t j = w0 + static_cast<uint32_t>(s * 32 + lane) * 4u;
-                if (j >= cnt) continue;
-                const uint64_t i = b0 + j;
-                float4 r = make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
-                if (P.flags & 1) {
-                    r = P.inv_m != 0.0f
-                            ? make_float4(__fmul_rn(r.x, P.inv_m), __fmul_rn(r.y, P.inv_m),
-                                          __fmul_rn(r.z, P.inv_m), __fmul_rn(r.w, P.inv_m))
-                            : make_float4(__fdiv_rn(r.x, Mf), __fdiv_rn(r.y, Mf),
-                                          __fdiv_rn(r.z, Mf), __fdiv_rn(r.w, Mf));
-                }
-                if (j + 4u <= cnt) {
-                    float4 *o = reinterpret_cast<float4 *>(P.out + i);
-                    if (P.flags & 2) {
-                        const float4 prev = __ldcs(o);
-                        r = make_float4(__fadd_rn(prev.x, r.x), __fadd_rn(prev.y, r.y),
-                                        __fadd_rn(prev.z, r.z), __fadd_rn(prev.w, r.w));
-                    }
-                    __stcs(o, r);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (j + c < cnt) {
-                            float v = get(r, c);
-                            if (P.flags & 2) v = __fadd_rn(P.out[i + c], v);
-                            P.out[i + c] = v;
-                        }
-                    }
-                }
-            }
+            store_window(P, acc, b0, w0, cnt, lane, Mf);
         }
     }
 }
