@@ -343,45 +343,32 @@ __device__ __forceinline__ FastQ fast_params(const BucketParams &bp) {
 // edge of its binade, where x and xa may sit in neighbouring binades and the
 // position jumps from 1 to 0 (for nearest rounding both sides of that jump give
 // the same level).  Those elements set redo.  |p| == s is the top level exactly;
-// any other |p| has x < 1.
+// any other |p| has x < 1.  Both positions are formed and one is selected, so
+// the element takes no branch; the edge test also flags positions below delta2
+// under the smallest level, which only sends a few more elements to the
+// division.
 template <int BITS, bool SR>
 __device__ __forceinline__ uint32_t log_level_fast(float ap, float s, float u, const FastQ &fq,
                                                    bool &redo) {
     constexpr int J = (1 << (BITS - 1)) - 1;
-    if (ap == s) {
-        redo = false;
-        return J;
-    }
     const float xa = __fmul_rn(ap, fq.rinv);
     const uint32_t xb = __float_as_uint(xa);
-    const int e = static_cast<int>(xb >> 23) - 127;
-    if (xa >= 1.0f) {  // x < 1 here: leave it to the division
-        redo = true;
-        return J;
-    }
-    if (e >= 1 - J) {
-        const uint32_t j0 = static_cast<uint32_t>(e + J);
-        const float m = __fsub_rn(__uint_as_float((xb & 0x7FFFFFu) | 0x3F800000u), 1.0f);
-        bool up;
-        if constexpr (SR) {
-            up = u < m;
-            redo = (fabsf(__fsub_rn(u, m)) <= fq.delta2) | (fminf(m, __fsub_rn(1.0f, m)) <= fq.delta2);
-        } else {
-            up = m > 0.5f;  // a tie is within delta2 and recomputed
-            redo = fabsf(__fsub_rn(m, 0.5f)) <= fq.delta2;
-        }
-        return j0 + (up ? 1u : 0u);
-    }
-    const float f = __fmul_rn(xa, __uint_as_float(static_cast<uint32_t>(127 + J - 1) << 23));
+    const bool binade = xb >= (static_cast<uint32_t>(128 - J) << 23);  // e >= 1 - J
+    const float pos = binade ? __fsub_rn(__uint_as_float((xb & 0x7FFFFFu) | 0x3F800000u), 1.0f)
+                             : __fmul_rn(xa, __uint_as_float(static_cast<uint32_t>(127 + J - 1) << 23));
+    const uint32_t j0 = binade ? (xb >> 23) - static_cast<uint32_t>(127 - J) : 0u;
     bool up;
     if constexpr (SR) {
-        up = u < f;
-        redo = (fabsf(__fsub_rn(u, f)) <= fq.delta2) | (f >= __fsub_rn(1.0f, fq.delta2));
+        up = u < pos;
+        redo = (fabsf(__fsub_rn(u, pos)) <= fq.delta2) |
+               (fabsf(__fsub_rn(pos, 0.5f)) >= 0.5f - fq.delta2) | (xa >= 1.0f);
     } else {
-        up = f > 0.5f;
-        redo = fabsf(__fsub_rn(f, 0.5f)) <= fq.delta2;
+        up = pos > 0.5f;  // a tie is within delta2 and recomputed
+        redo = (fabsf(__fsub_rn(pos, 0.5f)) <= fq.delta2) | (xa >= 1.0f);
     }
-    return up ? 1u : 0u;
+    const bool top = ap == s;
+    redo = redo && !top;
+    return top ? static_cast<uint32_t>(J) : j0 + (up ? 1u : 0u);
 }
 
 // Code and dequantized value of one element from ta; sets redo when the
