@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <mutex>
 #include <algorithm>
+#include <map>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -233,12 +235,12 @@ namespace qc {
 
 int persistent_grid(const void *kernel, int block, uint64_t units, size_t smem) {
     static std::mutex mu;
-    static std::unordered_map<uint64_t, int> cache;  // (device, kernel, smem) -> blocks per SM
+    // (device, kernel, block size, smem) -> blocks per SM
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
     static std::unordered_map<int, int> sms;
     int dev = 0;
     cudaGetDevice(&dev);
-    const uint64_t key = (static_cast<uint64_t>(dev) << 56) ^ (static_cast<uint64_t>(smem) << 40) ^
-                         reinterpret_cast<uintptr_t>(kernel);
+    const auto key = std::make_tuple(dev, kernel, block, smem);
     int per_sm = 0, nsm = 0;
     {
         std::lock_guard<std::mutex> lock(mu);

@@ -24,11 +24,11 @@
 // every element whether it is kept (all keys > T, and the first `need` ties)
 // and its output slot.
 //
-// Decode: a block per bucket stages the workers' pairs for the bucket in shared
-// memory, accumulates them into a shared-memory copy of the bucket's output,
-// worker by worker with a barrier in between (a worker's indices within a
-// bucket are distinct, so each step is race-free and the fixed worker order
-// holds), then writes the dense result.
+// Decode: a warp per bucket accumulates the workers' pairs into its own
+// shared-memory copy of the bucket's output, worker by worker with a warp
+// barrier in between (a worker's indices within a bucket are distinct, so each
+// step is race-free and the fixed worker order holds), then writes the dense
+// result.
 #include "qc_encode_tma.cuh"
 
 namespace qc {
@@ -264,59 +264,123 @@ __global__ void __launch_bounds__(kBlock) topk_kernel(const __grid_constant__ To
     }
 }
 
-constexpr int kDecodeThreads = 128;
-constexpr int kDecodePairs = 1024;  // pairs of one bucket staged in shared memory at a time
+constexpr int kDecodeMaxWarps = 8;
+constexpr int kDecodeBatch = 8;  // workers whose pairs a lane holds in registers at once
 
-// One bucket per block iteration: zero the bucket's accumulators in shared
-// memory and stage the workers' pairs for the bucket (all of them when they fit,
-// so their loads overlap), then add them worker by worker with a barrier in
-// between, and write the dense result with the MEAN / accumulate flags.
-__global__ void __launch_bounds__(kDecodeThreads) topk_decode_kernel(const __grid_constant__ TopkDecodeParams D) {
-    extern __shared__ float acc[];
-    uint32_t *pidx = reinterpret_cast<uint32_t *>(acc + D.bucket);
-    uint32_t *pcode = pidx + kDecodePairs;
-    float *pmeta = reinterpret_cast<float *>(pcode + kDecodePairs);  // (scale, offset) per worker
+// Dequantized value of one kept code (the uniform 8-bit level q * s + o, one
+// rounding).
+__device__ __forceinline__ float topk_level(uint32_t q, float s, float o) {
+    return __fmaf_rn(__fsub_rn(__uint_as_float(q | 0x4B000000u), 8388608.0f), s, o);
+}
+
+// The warp's dense output pass over its bucket: finish, store, and zero the
+// accumulators for the warp's next bucket.  MEAN: 0 none, 1 times inv_m (M a
+// power of two, exact), 2 divided by M; ACC: add into the output's old value.
+template <int MEAN, bool ACC>
+__device__ __forceinline__ float topk_finish(float r, float prev, const TopkDecodeParams &D, float Mf) {
+    if constexpr (MEAN == 1) r = __fmul_rn(r, D.inv_m);
+    if constexpr (MEAN == 2) r = __fdiv_rn(r, Mf);
+    if constexpr (ACC) r = __fadd_rn(prev, r);
+    return r;
+}
+
+template <int MEAN, bool ACC>
+__device__ __forceinline__ void topk_write_bucket(const TopkDecodeParams &D, float *acc, uint64_t lo,
+                                                  uint32_t cnt, int lane, float Mf, bool vec) {
+    uint32_t j0 = 0;
+    if (vec) {  // bucket and output rows 16-byte aligned
+        for (uint32_t j = 4u * static_cast<uint32_t>(lane); j + 4u <= cnt; j += 128u) {
+            float4 *a4 = reinterpret_cast<float4 *>(acc + j);
+            const float4 v = *a4;
+            *a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 *o4 = reinterpret_cast<float4 *>(D.out + lo + j);
+            float4 prev = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (ACC) prev = *o4;
+            __stcs(o4, make_float4(topk_finish<MEAN, ACC>(v.x, prev.x, D, Mf),
+                                   topk_finish<MEAN, ACC>(v.y, prev.y, D, Mf),
+                                   topk_finish<MEAN, ACC>(v.z, prev.z, D, Mf),
+                                   topk_finish<MEAN, ACC>(v.w, prev.w, D, Mf)));
+        }
+        j0 = cnt & ~3u;
+    }
+    for (uint32_t j = j0 + static_cast<uint32_t>(lane); j < cnt; j += 32u) {
+        const float v = acc[j];
+        acc[j] = 0.0f;
+        float *o = D.out + lo + j;
+        *o = topk_finish<MEAN, ACC>(v, ACC ? *o : 0.0f, D, Mf);
+    }
+}
+
+// One bucket per warp: the bucket's accumulators live in the warp's part of
+// shared memory; workers are added in their fixed order, a lane per kept pair,
+// with only a warp barrier between workers (a worker's indices within a bucket
+// are distinct, so the lanes of one step never touch the same accumulator).
+// With keep <= 32 a lane loads its pair of the next kDecodeBatch workers ahead
+// of adding them, so the loads of a batch overlap.  Pairs outside the bucket
+// (the sentinel included) are skipped.
+template <int MEAN, bool ACC>
+__global__ void __launch_bounds__(kDecodeMaxWarps * 32) topk_decode_kernel(const __grid_constant__ TopkDecodeParams D) {
+    extern __shared__ float sacc[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    float *acc = sacc + static_cast<size_t>(warp) * D.bucket;
     const float Mf = static_cast<float>(D.M);
-    const int per = static_cast<int>(kDecodePairs / D.keep);     // workers per staging round (>= 1)
-    for (uint64_t k = blockIdx.x; k < D.nbuckets; k += gridDim.x) {
+    const bool vec = (D.bucket & 3u) == 0u && (reinterpret_cast<uintptr_t>(D.out) & 15u) == 0u;
+    for (uint32_t j = static_cast<uint32_t>(lane); j < D.bucket; j += 32u) acc[j] = 0.0f;
+    __syncwarp();
+    for (uint64_t k = static_cast<uint64_t>(blockIdx.x) * wpb + warp; k < D.nbuckets;
+         k += static_cast<uint64_t>(gridDim.x) * wpb) {
         const uint64_t lo = k * D.bucket;
         const uint32_t cnt = static_cast<uint32_t>(min(static_cast<uint64_t>(D.bucket), D.n - lo));
-        for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) acc[j] = 0.0f;
-        for (int w0 = 0; w0 < D.M; w0 += per) {
-            const int nw = min(per, D.M - w0);
-            const uint32_t np = static_cast<uint32_t>(nw) * D.keep;
-            for (uint32_t t = threadIdx.x; t < np; t += kDecodeThreads) {
-                const uint32_t w = t / D.keep, s = t - w * D.keep;
-                const uint64_t at = static_cast<uint64_t>(w0 + w) * D.pair_stride + k * D.keep + s;
-                pidx[t] = __ldg(D.idx + at);
-                pcode[t] = __ldg(D.codes8 + at);
-            }
-            for (int w = threadIdx.x; w < nw; w += kDecodeThreads) {
-                const uint64_t at = static_cast<uint64_t>(w0 + w) * D.meta_stride + k;
-                pmeta[2 * w] = __ldg(D.scale + at);
-                pmeta[2 * w + 1] = __ldg(D.offset + at);
-            }
-            __syncthreads();
-            for (int w = 0; w < nw; ++w) {
-                const float s = pmeta[2 * w], o = pmeta[2 * w + 1];
-                for (uint32_t t = threadIdx.x; t < D.keep; t += kDecodeThreads) {
-                    const uint32_t i = pidx[w * D.keep + t];
-                    if (i >= lo && i < lo + cnt) {
-                        const uint32_t q = pcode[w * D.keep + t];
-                        const float d = __fmaf_rn(__fsub_rn(__uint_as_float(q | 0x4B000000u), 8388608.0f), s, o);
-                        acc[i - lo] = __fadd_rn(acc[i - lo], d);
+        if (D.keep <= 32u) {
+            const bool mine = static_cast<uint32_t>(lane) < D.keep;
+            for (int w0 = 0; w0 < D.M; w0 += kDecodeBatch) {
+                uint32_t iv[kDecodeBatch], qv[kDecodeBatch];
+                float sv[kDecodeBatch], ov[kDecodeBatch];
+#pragma unroll
+                for (int b = 0; b < kDecodeBatch; ++b) {
+                    const int w = w0 + b;
+                    iv[b] = kNoIndex;
+                    qv[b] = 0u;
+                    sv[b] = ov[b] = 0.0f;
+                    if (w < D.M) {
+                        const uint64_t at = static_cast<uint64_t>(w) * D.pair_stride + k * D.keep + lane;
+                        if (mine) {
+                            iv[b] = __ldg(D.idx + at);
+                            qv[b] = __ldg(D.codes8 + at);
+                        }
+                        const uint64_t m = static_cast<uint64_t>(w) * D.meta_stride + k;
+                        sv[b] = __ldg(D.scale + m);
+                        ov[b] = __ldg(D.offset + m);
                     }
                 }
-                __syncthreads();
+#pragma unroll
+                for (int b = 0; b < kDecodeBatch; ++b) {
+                    if (w0 + b >= D.M) break;  // uniform across the warp
+                    if (iv[b] >= lo && iv[b] < lo + cnt) {
+                        float *a = acc + (iv[b] - lo);
+                        *a = __fadd_rn(*a, topk_level(qv[b], sv[b], ov[b]));
+                    }
+                    __syncwarp();
+                }
+            }
+        } else {
+            for (int w = 0; w < D.M; ++w) {
+                const uint64_t base = static_cast<uint64_t>(w) * D.pair_stride + k * D.keep;
+                const uint64_t m = static_cast<uint64_t>(w) * D.meta_stride + k;
+                const float s = __ldg(D.scale + m), o = __ldg(D.offset + m);
+                for (uint32_t t = static_cast<uint32_t>(lane); t < D.keep; t += 32u) {
+                    const uint32_t i = __ldg(D.idx + base + t);
+                    if (i >= lo && i < lo + cnt) {
+                        float *a = acc + (i - lo);
+                        *a = __fadd_rn(*a, topk_level(__ldg(D.codes8 + base + t), s, o));
+                    }
+                }
+                __syncwarp();
             }
         }
-        for (uint32_t j = threadIdx.x; j < cnt; j += kDecodeThreads) {
-            float r = acc[j];
-            if (D.flags & 1) r = D.inv_m != 0.0f ? __fmul_rn(r, D.inv_m) : __fdiv_rn(r, Mf);
-            if (D.flags & 2) r = __fadd_rn(D.out[lo + j], r);
-            D.out[lo + j] = r;
-        }
-        __syncthreads();
+        topk_write_bucket<MEAN, ACC>(D, acc, lo, cnt, lane, Mf, vec);
+        __syncwarp();
     }
 }
 
@@ -347,15 +411,36 @@ cudaError_t launch_topk_encode(const TopkParams &p, const EncodeTiles &g, int st
     return stochastic ? launch_dtype<true>(p, g, bf16, stream) : launch_dtype<false>(p, g, bf16, stream);
 }
 
-cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(p.bucket) * 4u + 2u * kDecodePairs * 4u +
-                        2u * (kDecodePairs / p.keep) * 4u;
-    auto fn = &topk_decode_kernel;
+namespace {
+
+template <int MEAN, bool ACC>
+cudaError_t launch_decode_flags(const TopkDecodeParams &p, cudaStream_t stream) {
+    // a warp per bucket, as many warps per block as keep the block's
+    // accumulators within 64 KB
+    const uint64_t bucket_bytes = static_cast<uint64_t>(p.bucket) * 4u;
+    uint64_t fit = 65536u / bucket_bytes;
+    if (fit < 1) fit = 1;
+    const int wpb = static_cast<int>(fit < kDecodeMaxWarps ? fit : kDecodeMaxWarps);
+    const size_t smem = static_cast<size_t>(wpb) * bucket_bytes;
+    auto fn = &topk_decode_kernel<MEAN, ACC>;
     cudaError_t e = prepare_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
     if (e != cudaSuccess) return e;
-    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), kDecodeThreads, p.nbuckets, smem);
-    fn<<<grid, kDecodeThreads, smem, stream>>>(p);
+    const uint64_t blocks = (p.nbuckets + wpb - 1) / wpb;
+    const int grid = persistent_grid(reinterpret_cast<const void *>(fn), wpb * 32, blocks, smem);
+    fn<<<grid, wpb * 32, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <bool ACC>
+cudaError_t launch_decode_acc(const TopkDecodeParams &p, cudaStream_t stream) {
+    if (!(p.flags & 1)) return launch_decode_flags<0, ACC>(p, stream);
+    return p.inv_m != 0.0f ? launch_decode_flags<1, ACC>(p, stream) : launch_decode_flags<2, ACC>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_decode(const TopkDecodeParams &p, cudaStream_t stream) {
+    return (p.flags & 2) ? launch_decode_acc<true>(p, stream) : launch_decode_acc<false>(p, stream);
 }
 
 QC_DEFINE_TAKE_FLAG(take_topk_errors, g_topk_errors)

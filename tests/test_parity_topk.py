@@ -96,10 +96,14 @@ def test_topk_ties_and_degenerate(q, keep):
         _check(q, g, np.zeros(n, np.float32), n, bucket, keep, mode, f"topk ties K={keep} m={mode}")
 
 
-@pytest.mark.parametrize("M", [1, 3, 16])
-def test_topk_decode(q, M):
-    bucket, keep = 512, 12
-    n = 40 * bucket + 100                        # short last bucket
+@pytest.mark.parametrize("M,bucket,keep,tail,shift", [(1, 512, 12, 100, 0), (3, 512, 12, 101, 0),
+                                                      (16, 512, 12, 100, 0), (8, 1024, 32, 101, 1),
+                                                      (5, 992, 45, 101, 1), (9, 4096, 300, 100, 0)])
+def test_topk_decode(q, M, bucket, keep, tail, shift):
+    """keep <= 32 (a lane per pair, workers batched) and above; an output that
+    starts one float past a 16-byte boundary, and a ragged last bucket, take the
+    scalar output path."""
+    n = 40 * bucket + tail                       # short last bucket
     idxs, codes, scales, offsets = [], [], [], []
     for w in range(M):
         i, c, s, o = orc.topk_encode(wl.outlier_gradient(n, seed=200 + w), bucket=bucket, keep=keep)
@@ -115,7 +119,9 @@ def test_topk_decode(q, M):
     idx[-1, keep + 1] = 5                         # belongs to bucket 0, sits in bucket 1: skipped
     prior = np.random.default_rng(M).standard_normal(n).astype(np.float32)
     for flags in (0, 1, 3):
-        out = torch.from_numpy(prior.copy()).cuda()
+        buf = torch.zeros(n + shift, dtype=torch.float32, device="cuda")
+        out = buf[shift:]
+        out.copy_(torch.from_numpy(prior))
         q.qc_topk_decode_accumulate(dev(idx), dev(cod), idx.shape[1], dev(sc), dev(of), sc.shape[1],
                                     M, n, bucket, keep, out, flags)
         want = orc.topk_decode(idx, cod, sc, of, M=M, n=n, bucket=bucket, keep=keep, flags=flags,
