@@ -311,6 +311,70 @@ __device__ __forceinline__ void topk_write_bucket(const TopkDecodeParams &D, flo
     }
 }
 
+// M <= kDecodeBatch and keep <= 32: a lane holds its pair of every worker, and
+// lane w holds worker w's scale and offset; the warp loads the pairs and
+// metadata of its next bucket before it adds and writes the current one, so a
+// bucket's loads are in flight while the previous bucket is processed.
+template <int MEAN, bool ACC>
+__device__ __forceinline__ void topk_decode_prefetched(const TopkDecodeParams &D, float *acc, int lane,
+                                                       uint64_t first, uint64_t stride, float Mf,
+                                                       bool vec) {
+    const bool mine = static_cast<uint32_t>(lane) < D.keep;
+    auto fetch = [&](uint64_t k, uint32_t (&iv)[kDecodeBatch], uint32_t (&qv)[kDecodeBatch], float &sl,
+                     float &ol) {
+#pragma unroll
+        for (int b = 0; b < kDecodeBatch; ++b) {
+            iv[b] = kNoIndex;
+            qv[b] = 0u;
+            if (b < D.M && mine) {
+                const uint64_t at = static_cast<uint64_t>(b) * D.pair_stride + k * D.keep + lane;
+                iv[b] = __ldg(D.idx + at);
+                qv[b] = __ldg(D.codes8 + at);
+            }
+        }
+        sl = ol = 0.0f;
+        if (lane < D.M) {
+            const uint64_t m = static_cast<uint64_t>(lane) * D.meta_stride + k;
+            sl = __ldg(D.scale + m);
+            ol = __ldg(D.offset + m);
+        }
+    };
+    uint32_t iv[kDecodeBatch], qv[kDecodeBatch];
+    float sl = 0.0f, ol = 0.0f;
+    if (first < D.nbuckets) fetch(first, iv, qv, sl, ol);
+    for (uint64_t k = first; k < D.nbuckets; k += stride) {
+        uint32_t in[kDecodeBatch], qn[kDecodeBatch];
+        float sn = 0.0f, on = 0.0f;
+#pragma unroll
+        for (int b = 0; b < kDecodeBatch; ++b) {
+            in[b] = kNoIndex;
+            qn[b] = 0u;
+        }
+        if (k + stride < D.nbuckets) fetch(k + stride, in, qn, sn, on);
+        const uint64_t lo = k * D.bucket;
+        const uint32_t cnt = static_cast<uint32_t>(min(static_cast<uint64_t>(D.bucket), D.n - lo));
+#pragma unroll
+        for (int b = 0; b < kDecodeBatch; ++b) {
+            if (b >= D.M) break;  // uniform across the warp
+            const float s = __shfl_sync(kFull, sl, b), o = __shfl_sync(kFull, ol, b);
+            if (iv[b] >= lo && iv[b] < lo + cnt) {
+                float *a = acc + (iv[b] - lo);
+                *a = __fadd_rn(*a, topk_level(qv[b], s, o));
+            }
+            __syncwarp();
+        }
+        topk_write_bucket<MEAN, ACC>(D, acc, lo, cnt, lane, Mf, vec);
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < kDecodeBatch; ++b) {
+            iv[b] = in[b];
+            qv[b] = qn[b];
+        }
+        sl = sn;
+        ol = on;
+    }
+}
+
 // One bucket per warp: the bucket's accumulators live in the warp's part of
 // shared memory; workers are added in their fixed order, a lane per kept pair,
 // with only a warp barrier between workers (a worker's indices within a bucket
@@ -328,6 +392,11 @@ __global__ void __launch_bounds__(kDecodeMaxWarps * 32) topk_decode_kernel(const
     const bool vec = (D.bucket & 3u) == 0u && (reinterpret_cast<uintptr_t>(D.out) & 15u) == 0u;
     for (uint32_t j = static_cast<uint32_t>(lane); j < D.bucket; j += 32u) acc[j] = 0.0f;
     __syncwarp();
+    if (D.M <= kDecodeBatch && D.keep <= 32u) {
+        topk_decode_prefetched<MEAN, ACC>(D, acc, lane, static_cast<uint64_t>(blockIdx.x) * wpb + warp,
+                                          static_cast<uint64_t>(gridDim.x) * wpb, Mf, vec);
+        return;
+    }
     for (uint64_t k = static_cast<uint64_t>(blockIdx.x) * wpb + warp; k < D.nbuckets;
          k += static_cast<uint64_t>(gridDim.x) * wpb) {
         const uint64_t lo = k * D.bucket;
