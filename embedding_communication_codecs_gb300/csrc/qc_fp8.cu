@@ -54,6 +54,14 @@ __device__ __forceinline__ float absmax4(const float4 &v) {
     return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 }
 
+// max over the warp's lanes of m >= +0, NaN lanes left out (+0 when every lane
+// is NaN), as the row maximum ignores NaN elements.  Non-negative floats order
+// like their bit patterns, so one integer max reduction replaces the
+// five-step shuffle tree.
+__device__ __forceinline__ float warp_absmax(float m) {
+    return __uint_as_float(__reduce_max_sync(kFull, m == m ? __float_as_uint(m) : 0u));
+}
+
 constexpr int kRowsPerWarp = kSlots;  // dim <= 128: one row per slot
 
 __global__ void __launch_bounds__(kBlock) fp8_quant_narrow(const Fp8Params P) {
@@ -81,7 +89,7 @@ __global__ void __launch_bounds__(kBlock) fp8_quant_narrow(const Fp8Params P) {
 #pragma unroll
         for (int s = 0; s < kRowsPerWarp; ++s) {
             const uint64_t r = g * kRowsPerWarp + s;
-            const float sc = __fdiv_rn(positive_zero(warp_max(absmax4(cur[s]))), 448.0f);
+            const float sc = __fdiv_rn(warp_absmax(absmax4(cur[s])), 448.0f);
             if (col_ok && r < P.rows) {
                 __stcs(reinterpret_cast<uint32_t *>(P.codes + r * P.dim) + lane, encode4(cur[s], sc));
                 if (lane == 0) P.row_scale[r] = sc;
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kBlock) fp8_quant_wide(const Fp8Params P) {
                        : make_float4(0.f, 0.f, 0.f, 0.f);
             m = fmaxf(m, absmax4(v[s]));
         }
-        m = warp_max(m);
+        m = warp_absmax(m);
         if (W > 1) {
             if (lane == 0) red[buf][warp] = m;
             __syncthreads();

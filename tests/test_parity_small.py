@@ -364,6 +364,9 @@ def test_rowwise_fp8(q, dim):
             x[2, dim // 2] = np.float32(1e30)                 # one huge value
             x[3] *= np.float32(1e-38)                         # subnormal scale
             x[4] = -np.abs(x[4])                              # all negative
+        if rows > 6:
+            x[5] = np.float32(np.nan)                         # NaN row: its maximum is +0
+            x[6, : (dim + 1) // 2] = np.float32(np.nan)       # NaN elements are left out of the maximum
         codes = Guarded(rows * dim, torch.uint8, fill=0xA5)
         sc = Guarded(rows, torch.float32)
         q.qc_rowwise_fp8(dev(x), rows, dim, codes.t, sc.t)
@@ -377,8 +380,11 @@ def test_rowwise_fp8(q, dim):
         q.qc_rowwise_fp8_dequant(dev(c_or), dev(s_or), rows, dim, out.t)
         torch.cuda.synchronize()
         out.check()
-        want = orc.rowwise_fp8_dequant(c_or, s_or)
-        assert_bits_equal(host(out.t), want.reshape(-1), f"fp8 dequant dim={dim} rows={rows}")
+        want = orc.rowwise_fp8_dequant(c_or, s_or).reshape(-1)
+        got = host(out.t)
+        nan = np.isnan(want)                                  # NaN codes: any NaN pattern
+        assert np.array_equal(np.isnan(got), nan), f"fp8 dequant NaNs dim={dim} rows={rows}"
+        assert_bits_equal(got[~nan], want[~nan], f"fp8 dequant dim={dim} rows={rows}")
 
 
 def test_fp8_dequant_all_codes(q):
