@@ -13,7 +13,8 @@
 //
 // Layout: for dim <= 128 each warp takes four rows per step, one per float4
 // slot, lane l covering columns 4l .. 4l+3 (four independent warp reductions,
-// four 512-byte loads in flight per warp).  For wider rows a team of W warps
+// four 512-byte loads in flight per warp); both directions load the warp's next
+// four rows before they process the current ones.  For wider rows a team of W warps
 // owns a row with up to 4 float4 slots per lane.
 #include "qc_device.cuh"
 #include "qc_internal.h"
@@ -148,17 +149,25 @@ __global__ void __launch_bounds__(kBlock) fp8_dequant_narrow(const Fp8Params P) 
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kBlock / 32);
     const uint64_t groups = (P.rows + kRowsPerWarp - 1) / kRowsPerWarp;
     const bool col_ok = static_cast<uint32_t>(lane) * 4u < P.dim;
-    for (uint64_t g = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
-         g < groups; g += warps) {
-        uint32_t cw[kRowsPerWarp];
-        float sc[kRowsPerWarp];
+    // the code words and scales of the warp's next group are loaded before the
+    // current group is converted and stored, so loads stay in flight
+    auto load = [&](uint64_t g, uint32_t (&cw)[kRowsPerWarp], float (&sc)[kRowsPerWarp]) {
 #pragma unroll
         for (int s = 0; s < kRowsPerWarp; ++s) {
             const uint64_t r = g * kRowsPerWarp + s;
-            const bool ok = col_ok && r < P.rows;
+            const bool ok = g < groups && col_ok && r < P.rows;
             cw[s] = ok ? __ldcs(reinterpret_cast<const uint32_t *>(P.codes_in + r * P.dim) + lane) : 0u;
             sc[s] = ok ? __ldg(P.scale_in + r) : 0.0f;
         }
+    };
+    uint64_t g = static_cast<uint64_t>(blockIdx.x) * (kBlock / 32) + (threadIdx.x >> 5);
+    uint32_t cw[kRowsPerWarp];
+    float sc[kRowsPerWarp];
+    load(g, cw, sc);
+    for (; g < groups; g += warps) {
+        uint32_t cn[kRowsPerWarp];
+        float sn[kRowsPerWarp];
+        load(g + warps, cn, sn);
 #pragma unroll
         for (int s = 0; s < kRowsPerWarp; ++s) {
             const uint64_t r = g * kRowsPerWarp + s;
@@ -168,6 +177,11 @@ __global__ void __launch_bounds__(kBlock) fp8_dequant_narrow(const Fp8Params P) 
                        make_float4(__fmul_rn(f.x, sc[s]), __fmul_rn(f.y, sc[s]),
                                    __fmul_rn(f.z, sc[s]), __fmul_rn(f.w, sc[s])));
             }
+        }
+#pragma unroll
+        for (int s = 0; s < kRowsPerWarp; ++s) {
+            cw[s] = cn[s];
+            sc[s] = sn[s];
         }
     }
 }
